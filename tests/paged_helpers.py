@@ -1,0 +1,79 @@
+"""Test-side helpers: build paged pools from logical per-sequence K/V with the oracle.
+
+Everything here runs on the CPU through ``oracle`` (the fp64 reference); the CUDA
+library is never used to build an expected value.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0}
+TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round float data to fp16/bf16 (round-to-nearest-even) and return the raw bits."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(TORCH_DT[dtype])
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_to_f64(b: np.ndarray, dtype: str) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(TORCH_DT[dtype])
+    return t.to(torch.float64).numpy()
+
+
+class Paged:
+    """Logical K/V for S sequences written into a NaN-filled paged pool."""
+
+    def __init__(self, rng, S, Hq, Hkv, D, bs, ctx, dtype="f16", num_blocks=None,
+                 values="normal", width=None, perm=None):
+        self.S, self.Hq, self.Hkv, self.D, self.bs, self.dtype = S, Hq, Hkv, D, bs, dtype
+        self.ctx = np.asarray(ctx, dtype=np.int32)
+        nblk = (self.ctx + bs - 1) // bs
+        need = int(nblk.sum())
+        self.num_blocks = num_blocks or max(need + 3, 1)
+        self.width = width or max(int(nblk.max()) if S else 1, 1)
+        self.geom = oracle.Geom(self.num_blocks, bs, Hkv, D, dtype)
+        draw = (lambda *s: rng.uniform(-1, 1, s)) if values == "uniform" else (lambda *s: rng.standard_normal(s))
+        # logical data, already rounded to the storage type
+        self.K = [bits_to_f64(to_bits(draw(c, Hkv, D), dtype), dtype) for c in self.ctx]
+        self.V = [bits_to_f64(to_bits(draw(c, Hkv, D), dtype), dtype) for c in self.ctx]
+        self.q_bits = to_bits(draw(S, Hq, D), dtype)
+        self.q = bits_to_f64(self.q_bits, dtype)
+        perm = rng.permutation(self.num_blocks) if perm is None else np.asarray(perm)
+        self.tables = np.full((S, self.width), -1, dtype=np.int32)
+        nxt = 0
+        for s in range(S):
+            self.tables[s, :nblk[s]] = perm[nxt:nxt + nblk[s]]
+            nxt += nblk[s]
+        self.pool = np.full(self.geom.layer_elems, NAN_BITS[dtype], dtype=np.uint16)
+        self.write_all()
+
+    def write_all(self):
+        for s in range(self.S):
+            c = int(self.ctx[s])
+            if c == 0:
+                continue
+            t = np.arange(c)
+            slots = self.tables[s, t // self.bs].astype(np.int64) * self.bs + t % self.bs
+            err = oracle.reshape_and_cache(self.pool, self.geom, to_bits(self.K[s], self.dtype),
+                                           to_bits(self.V[s], self.dtype), slots)
+            assert err == 0
+
+    def expected_contiguous(self, scale):
+        """Reference via torch's fp64 scaled_dot_product_attention on the logical arrays
+        (kv head of query head h is h // (Hq // Hkv))."""
+        G = self.Hq // self.Hkv
+        out = np.zeros((self.S, self.Hq, self.D))
+        for s in range(self.S):
+            if self.ctx[s] == 0:
+                continue
+            q = torch.from_numpy(self.q[s]).unsqueeze(1)                       # [Hq, 1, D]
+            K = torch.from_numpy(self.K[s]).permute(1, 0, 2).repeat_interleave(G, 0)   # [Hq, ctx, D]
+            V = torch.from_numpy(self.V[s]).permute(1, 0, 2).repeat_interleave(G, 0)
+            o = torch.nn.functional.scaled_dot_product_attention(q, K, V, scale=scale)
+            out[s] = o[:, 0, :].numpy()
+        return out

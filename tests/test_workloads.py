@@ -1,0 +1,49 @@
+"""The seeded workload generator: shapes, determinism and table/slot consistency."""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_168_gb300.workloads import CONFIGS, make_workload
+
+
+def test_tiny_shapes_and_determinism():
+    a = make_workload("tiny")
+    b = make_workload("tiny")
+    assert a.q.shape == (4, 4, 64) and a.kv_cache.shape == (64, 4, 2 * 16 * 64)
+    assert torch.equal(a.kv_cache, b.kv_cache) and np.array_equal(a.block_tables_np, b.block_tables_np)
+    assert a.kv_cache.dtype == torch.float16 and float(a.kv_cache.abs().max()) <= 1.0
+    assert 1 <= a.context_lens_np.min() and a.context_lens_np.max() <= 100
+
+
+@pytest.mark.parametrize("name", ["tiny", "7b", "8b", "beam"])
+def test_tables_slots_and_pool_sizing(name):
+    cfg = CONFIGS[name]
+    w = make_workload(name, num_seqs=None if name in ("tiny", "beam") else 16)
+    S, bs = w.cfg.num_seqs, cfg.block_size
+    ctx, bt = w.context_lens_np, w.block_tables_np
+    nblk = -(-ctx // bs)
+    for s in range(S):
+        assert np.all(bt[s, :nblk[s]] >= 0) and np.all(bt[s, nblk[s]:] == -1)
+        pos = ctx[s] - 1
+        assert w.slot_mapping_np[s] == bt[s, pos // bs] * bs + pos % bs
+    if name != "beam":
+        used = bt[bt >= 0]
+        assert len(np.unique(used)) == used.size           # no block shared
+    else:
+        # 4 beams of a group share their 128 prompt blocks, and nothing else
+        for g in range(S // 4):
+            rows = bt[4 * g:4 * g + 4]
+            assert np.all(rows[:, :128] == rows[0, :128])
+        assert len(np.unique(bt[:, 128:][bt[:, 128:] >= 0])) == (bt[:, 128:] >= 0).sum()
+        assert w.copy_pairs.shape == (S, 2)
+        assert np.array_equal(w.copy_pairs[:, 1], bt[np.arange(S), nblk - 1])
+        assert abs(w.swap_out_pairs.shape[0] - 0.1 * w.used_blocks.size) <= 1
+        assert np.array_equal(w.swap_in_pairs, w.swap_out_pairs[:, ::-1])
+    assert w.num_blocks >= len(np.unique(bt[bt >= 0]))
+
+
+def test_nan_unused_blocks():
+    w = make_workload("tiny", nan_unused=True)
+    used = set(w.used_blocks.tolist())
+    for b in range(w.num_blocks):
+        assert bool(torch.isnan(w.kv_cache[b]).all()) == (b not in used)

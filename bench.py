@@ -1,0 +1,386 @@
+"""Benchmark: one paged-attention decode step of the Llama-2-7B-shaped layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 7b] [--impl reference]
+
+A step = swap_out -> swap_in -> copy_blocks -> reshape_and_cache -> paged decode
+(+ log-sum-exp merge) for one layer of the workload (the 7B workload has no
+swaps or copies).  The KV pool (2.9 GB, > L2) stays resident; per-step inputs are
+already in HBM when the timed region starts.  Prints one JSON line.
+
+value  = algorithmic bytes of the step / device time of the step, GB/s (whole job).
+e2e    = the same, through the C ABI with host buffers: every step copies the
+         step's inputs (q, new K/V, block tables, context lengths, slot mapping)
+         from pinned host memory and the output back, inside the timed region.
+roofline = the decode launch (pa_decode: decode kernel + merge kernel) against the
+         measured HBM copy bandwidth.
+--impl reference times the fp64 CPU oracle (the correctness reference) on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "paged-attn decode KV-read HBM GB/s (frac of peak); seq-steps/s at 7B shape"
+SPEC_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DESCRIPTIONS = {
+    "tiny": "tiny paged decode: 4 seqs, MHA 4 heads, head_size 64, block_size 16, fp16, ctx U[1,100]",
+    "7b": "Llama-2-7B-shaped decode layer: 64 seqs, 32 q/32 kv heads, head_size 128, block_size 16, fp16 "
+          "K/V/Q ~N(0,1), context_lens ~U[512,4096], pool 1.2x needed blocks, random block_tables, "
+          "reshape_and_cache of 1 token/seq",
+    "8b": "Llama-3-8B-shaped GQA decode: 256 seqs, 32 q/8 kv heads, head_size 128, block_size 16, bf16, "
+          "context_lens lognormal(median 1024, sigma 0.8) capped at 8192",
+    "70b": "long-context 70B-shaped GQA decode: 8 seqs, 64 q/8 kv heads, head_size 128, block_size 32, bf16, "
+           "context_lens ~U[32768,131072]",
+    "beam": "beam/shared-prefix decode: 32 groups x 4 beams, 32 q/8 kv heads, head_size 128, block_size 16, "
+            "bf16, 2048-token shared prompt, tails ~U[0,256], CoW copy_blocks + 10% swap_blocks",
+}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_168_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_src = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    m_val = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m_src and m_val) or m_src.group(1) != source_digest():
+        return None
+    return float(m_val.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    """Max over ranks (identity on one process)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+_ORACLE_INPUTS = {}
+
+
+def oracle_inputs(w):
+    """Host copies (raw 16-bit bits) of the workload for the oracle, made once."""
+    import oracle
+    from paged_kv_cache_168_gb300.workloads import as_u16
+    key = id(w)
+    if key not in _ORACLE_INPUTS:
+        cfg = w.cfg
+        g = oracle.Geom(w.num_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_size, cfg.dtype)
+        _ORACLE_INPUTS[key] = (g, as_u16(w.kv_cache).reshape(-1), as_u16(w.q))
+    return _ORACLE_INPUTS[key]
+
+
+def oracle_sample(w, budget_s: float, max_items: int | None = None, start: int = 0):
+    """Time the fp64 oracle on the workload sequence by sequence (all query heads
+    of a sequence together) until ~budget_s seconds of wall time.  Returns
+    (GB/s of algorithmic KV bytes, seq-steps/s, description, cores, seconds)."""
+    import oracle
+    cfg = w.cfg
+    g, pool, q = oracle_inputs(w)
+    kv_tok = 2 * cfg.num_kv_heads * cfg.head_size * 2
+    done_bytes, done_seqs, t_total = 0, 0, 0.0
+    order = np.random.default_rng(start).permutation(cfg.num_seqs)
+    for s in order:
+        sel = np.array([[s, h] for h in range(cfg.num_q_heads)], dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.decode(q, pool, g, w.block_tables_np, w.context_lens_np, w.scale,
+                      max_context_len=w.max_context_len, sel=sel)
+        t_total += time.perf_counter() - t0
+        done_bytes += int(w.context_lens_np[s]) * kv_tok
+        done_seqs += 1
+        if t_total >= budget_s or (max_items and done_seqs >= max_items):
+            break
+    cores = oracle.max_threads()
+    desc = (f"{done_seqs} of {cfg.num_seqs} sequences (all {cfg.num_q_heads} query heads each, "
+            f"{done_bytes / 1e9:.3f} GB of KV) of the {cfg.name} workload, fp64 oracle, {cores} OpenMP threads")
+    return done_bytes / t_total / 1e9, done_seqs / t_total, desc, cores, t_total
+
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    from paged_kv_cache_168_gb300.workloads import make_workload
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = make_workload(args.workload, device=dev)
+    cfg = w.cfg
+    # each step is a bounded sample: a few sequences of the workload
+    per_step = max(1.0, args.reference_seconds / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step / 4, max_items=1)
+    vals, seqs, secs, desc, cores = [], [], [], "", 1
+    for i in range(args.steps):
+        v, sps, desc, cores, t = oracle_sample(w, per_step, start=i + 1)
+        vals.append(v)
+        seqs.append(sps)
+        secs.append(t)
+    value = float(np.median(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * float(np.median(secs)), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[args.workload], "global_batch": cfg.num_seqs,
+                   "max_context_len": w.max_context_len},
+        "seq_steps_per_s": round(float(np.median(seqs)), 4),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU benchmark
+
+def run_gpu(args):
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    from paged_kv_cache_168_gb300 import _lib
+    from paged_kv_cache_168_gb300.build import build
+    from paged_kv_cache_168_gb300.step import DecodeStep
+    from paged_kv_cache_168_gb300.workloads import CONFIGS, make_workload
+    build()
+    _lib.load()
+
+    cfg = CONFIGS[args.workload]
+    w = make_workload(args.workload, device=device, seed=cfg.seed + 1000 * rank)
+    stream = torch.cuda.Stream(device)
+    step = DecodeStep(w, partition_size=args.partition_size, stream=stream)
+    nbytes = step.algorithmic_bytes()
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    assert _lib.read_device_errors(step.dev_err, stream=stream) == 0, "device error during warm-up"
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                ev[i][0].record(stream)
+                step.cache_ops()
+                ev[i][1].record(stream)
+                step.attention()
+                ev[i][2].record(stream)
+                ev[i][3].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][3])
+    decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    total_ms = reduce_max(total_ms, world, device)
+    assert _lib.read_device_errors(step.dev_err, stream=stream) == 0, "device error during timed steps"
+
+    # ---- end to end through the C ABI with host buffers
+    host_in = {k: getattr(w, k).cpu().pin_memory() for k in
+               ("q", "key", "value", "block_tables", "context_lens", "slot_mapping")}
+    dev_in = {k: torch.empty_like(getattr(w, k)) for k in host_in}
+    host_out = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    saved = {k: getattr(w, k) for k in host_in}
+    for k in host_in:
+        setattr(w, k, dev_in[k])
+
+    def e2e_step():
+        for k in host_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        step()
+        host_out.copy_(step.out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world, device)
+    for k, v in saved.items():
+        setattr(w, k, v)
+
+    ms = total_ms / K
+    value = world * nbytes["total"] / (ms * 1e-3) / 1e9
+    dec_ms = float(np.mean(decode_ms))
+    achieved = nbytes["decode"] / (dec_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if args.cpu_baseline_seconds > 0:
+            v, sps, desc, cores, _ = oracle_sample(w, args.cpu_baseline_seconds)
+            cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc,
+                   "seq_steps_per_s": round(sps, 4)}
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.cfg.dtype, "data": "synthetic",
+            "config": {"workload": DESCRIPTIONS[args.workload], "global_batch": w.cfg.num_seqs * world,
+                       "max_context_len": w.max_context_len, "tokens_in_context": int(w.context_lens_np.sum()),
+                       "partition_size": _lib.decode_partition_size(args.partition_size),
+                       "parallelism": f"replicas{world}",
+                       "l2": f"inputs larger than L2: {w.kv_cache.numel() * 2 / 1e9:.2f} GB pool, "
+                             f"{nbytes['decode_kv'] / 1e9:.2f} GB of KV read per step"},
+            "seq_steps_per_s": round(world * w.cfg.num_seqs / (ms * 1e-3), 1),
+            "decode_kv_gbs": round(nbytes["decode_kv"] / (dec_ms * 1e-3) / 1e9, 2),
+            "frac_of_spec_8tbs": round(achieved / SPEC_HBM_GBS, 4),
+            "bytes_per_step": nbytes,
+            "roofline": {"bound": "hbm", "kernel": "pa_decode (decode + log-sum-exp merge)",
+                         "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                         "traffic": recorded_traffic(args.workload),
+                         "decode_ms": round(dec_ms, 4)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(world * nbytes["total"] / (e2e_ms / K * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms / K, 4)},
+            "gpu_launches": K * step.kernel_launches() * world,
+            "clocks": clocks.summary(),
+            "source_digest": source_digest(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="7b", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=60.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

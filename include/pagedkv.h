@@ -1,0 +1,199 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) paged KV-cache decode library.
+ *
+ * The library implements the hot path of paged-attention decoding as the vLLM
+ * and nano-vLLM write-ups describe it:
+ *
+ *   pa_reshape_and_cache  scatter each step's new K/V into cache slots
+ *                         (nano-vLLM article, section 5.2.3 "KV Cache 写入":
+ *                         store_kvcache writes token i to slot_mapping[i],
+ *                         -1 means "skip").
+ *   pa_decode             one query token per sequence attends over its
+ *                         non-contiguous KV blocks found through a block table
+ *                         ("vLLM" page, section "PageAttention": softmax(QK^T /
+ *                         sqrt(d_k)) V; mlqm.cn article, section 二.2.2: block
+ *                         table maps logical to physical blocks).  Long contexts
+ *                         are split into partitions merged by log-sum-exp
+ *                         ("vLLM" page, "Prefill vs decoding" item 5,
+ *                         FlashDecoding).
+ *   pa_copy_blocks        copy-on-write block copies ("vLLM" page, section
+ *                         "CacheEngine": copy / copy_blocks; mlqm.cn article,
+ *                         Copy-on-Write example).
+ *   pa_swap_blocks        whole-block moves between the GPU cache and a pinned
+ *                         CPU cache ("vLLM" page, section "CacheEngine":
+ *                         swap_in = CPU->GPU, swap_out = GPU->CPU; section
+ *                         "Preemption").
+ *
+ * Conventions
+ *   Ownership:  the caller allocates every buffer (cache pools, workspace,
+ *               error word).  The library allocates no memory and keeps no
+ *               per-call state.
+ *   Streams:    every call except pa_read_device_errors is asynchronous on the
+ *               given CUDA stream (a cudaStream_t passed as void*; NULL = the
+ *               legacy default stream) and performs no host synchronisation.
+ *   Errors:     problems visible on the host (null or misaligned pointers,
+ *               unsupported shapes, bad pair lists, small workspace) return a
+ *               status synchronously and launch nothing; pa_last_error_message()
+ *               then names the argument.  Problems only visible on the device
+ *               (a block id or slot out of range, a context longer than the
+ *               block table) set bits in the optional device error word
+ *               `dev_err`; the affected item is skipped (its output zeroed).
+ *               Kernels never trap.
+ *   Types:      cache, query, key, value and output elements are fp16 or bf16
+ *               (one dtype per call); arithmetic is fp32.
+ *
+ * Cache layout (one layer; a pool may hold several layers `layer_stride_bytes`
+ * apart).  The pool is num_blocks blocks; block b holds, for each kv head h,
+ * one contiguous chunk of 2 * block_size * head_size elements at element offset
+ * (b * num_kv_heads + h) * 2 * block_size * head_size.  Inside a chunk the
+ * block's token slots are grouped by R = min(block_size, 8); group g holds the K
+ * rows of its R slots and then their V rows; each is head_size / 64 "atoms" of
+ * R rows x 64 dims (128-byte rows); inside an atom the 16-byte piece c (dims
+ * 8c..8c+7) of row r is stored at piece position c XOR r.  This is the
+ * 128-byte-swizzled K-major operand layout of the sm_100-family tensor cores,
+ * so one bulk copy per chunk stages a block ready for both CUDA-core and
+ * tensor-core consumers.  pa_cache_element_offset() computes the position of
+ * any element.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,        /* bad pointer, size, id or pair list */
+    PA_ERR_UNSUPPORTED = 2,        /* valid but not implemented (head_size, block_size, group) */
+    PA_ERR_CUDA = 3,               /* a CUDA runtime call failed (launch, copy, attribute query) */
+    PA_ERR_WORKSPACE_TOO_SMALL = 4 /* workspace_bytes < pa_decode_workspace_bytes(...) */
+} pa_status;
+
+typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Bits of the device error word. */
+#define PA_DEVERR_BLOCK_ID 0x1u  /* a block-table entry that must be read is < 0 or >= num_blocks */
+#define PA_DEVERR_SLOT 0x2u      /* a slot_mapping entry is not -1 and not in [0, num_blocks*block_size) */
+#define PA_DEVERR_CONTEXT 0x4u   /* context_lens[s] > block_table_stride*block_size or > max_context_len */
+#define PA_DEVERR_TIMEOUT 0x8u   /* a bounded wait inside a kernel ran out (the item was abandoned) */
+
+/* Geometry of a cache pool.  head_size in {64, 128}; block_size in {8, 16, 32};
+ * dtype a pa_dtype.  layer_stride_bytes = distance between consecutive layers
+ * (0 means layers are packed: pa_cache_bytes(desc)). */
+typedef struct pa_cache_desc {
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_size;
+    int32_t dtype;
+    int32_t num_layers;
+    int64_t layer_stride_bytes;
+} pa_cache_desc;
+
+/* Bytes of one layer of the pool: num_blocks * num_kv_heads * 2 * block_size *
+ * head_size * 2 (the KV-size formula of the mlqm.cn article, section 二.2.1,
+ * rounded up to whole blocks).  Returns 0 for an invalid descriptor. */
+size_t pa_cache_bytes(const pa_cache_desc* desc);
+
+/* Element offset (in 16-bit elements from the start of a layer) of dim `dim` of
+ * the K (part = 0) or V (part = 1) vector stored in slot `slot` of block `block`
+ * for kv head `kv_head`.  Returns -1 for out-of-range arguments.  Host only. */
+int64_t pa_cache_element_offset(const pa_cache_desc* desc, int64_t block, int32_t kv_head,
+                                int32_t part, int32_t slot, int32_t dim);
+
+/* Write each new token's K and V into the cache.
+ * Follows store_kvcache (nano-vLLM article, section 5.2.3): for token i with
+ * slot = slot_mapping[i] != -1, block = slot / block_size and offset =
+ * slot % block_size, the num_kv_heads x head_size K and V elements are copied
+ * bit for bit into that slot of layer `layer`.
+ *   kv_cache     device pool (see layout above), 16-byte aligned.
+ *   key, value   device [num_tokens, num_kv_heads, head_size], heads and dims
+ *                contiguous; token strides key_token_stride / value_token_stride
+ *                in elements (multiples of 8); 16-byte aligned.
+ *   slot_mapping device int64 [num_tokens].
+ *   dev_err      optional device uint32; PA_DEVERR_SLOT is OR-ed in for a slot
+ *                out of range (that token is skipped).
+ * num_tokens == 0 launches nothing. */
+pa_status pa_reshape_and_cache(void* kv_cache, const pa_cache_desc* desc, int32_t layer,
+                               const void* key, int64_t key_token_stride, const void* value,
+                               int64_t value_token_stride, const int64_t* slot_mapping,
+                               int32_t num_tokens, uint32_t* dev_err, void* stream);
+
+/* Workspace bytes pa_decode needs for these shapes (0 when no sequence can span
+ * more than one partition).  partition_size 0 selects the default (512 tokens). */
+size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
+                                 int32_t max_context_len, int32_t partition_size);
+
+/* The partition size pa_decode uses for `partition_size` (0 -> default). */
+int32_t pa_decode_partition_size(int32_t partition_size);
+
+/* Paged decode attention: one query token per sequence.
+ * For sequence s and query head h (kv head = h / (num_q_heads / num_kv_heads)):
+ *   z_t = scale * q[s,h,:] . K_t   for t < ctx = context_lens[s], where token t
+ *         lives in slot t % block_size of block block_tables[s*block_table_stride + t/block_size];
+ *   out[s,h,:] = sum_t softmax(z)_t V_t     (fp32 accumulation, rounded to the
+ *                                            dtype of q, round-to-nearest-even).
+ * context_lens counts the new token, so pa_reshape_and_cache must run first.
+ * ctx <= 0 gives a zero output row.  Contexts longer than partition_size are
+ * split into partitions of partition_size tokens, each producing (max, sum,
+ * unnormalised output) in the workspace, merged by log-sum-exp in a second
+ * kernel on the same stream.
+ *   out           device [num_seqs, num_q_heads, head_size], q's dtype, contiguous.
+ *   q             device [num_seqs, num_q_heads, head_size]; sequence stride
+ *                 q_seq_stride elements (multiple of 8); 16-byte aligned.
+ *   block_tables  device int32 [num_seqs, block_table_stride]; entries past
+ *                 ceil(ctx / block_size) are never read.
+ *   context_lens  device int32 [num_seqs].
+ *   max_context_len  an upper bound of context_lens (sizes the launch and the
+ *                 workspace); a longer context sets PA_DEVERR_CONTEXT.
+ *   partition_size   0 (default) or a multiple of 128 in [128, 8192].
+ *   workspace     device, 16-byte aligned, >= pa_decode_workspace_bytes(...);
+ *                 may be NULL when that is 0.  Contents need no initialisation.
+ *   dev_err       optional device uint32 error word (PA_DEVERR_* bits).
+ * Supported: head_size 64 or 128, block_size 8/16/32, num_q_heads a multiple of
+ * num_kv_heads with group size 1, 2, 4 or 8 (PA_ERR_UNSUPPORTED otherwise). */
+pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,
+                    const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
+                    int32_t block_table_stride, const int32_t* context_lens, int32_t num_seqs,
+                    int32_t num_q_heads, int32_t max_context_len, float scale,
+                    int32_t partition_size, void* workspace, size_t workspace_bytes,
+                    uint32_t* dev_err, void* stream);
+
+/* Copy whole blocks inside one pool (every kv head, K and V, every layer):
+ * for each pair i, block pairs[2i+1] receives block pairs[2i].  All pairs act
+ * at once ("vLLM" page, CacheEngine copy; used for copy-on-write).
+ *   pairs   HOST int64 [num_pairs][2] (src, dst), read before the call returns.
+ * Rejected with PA_ERR_INVALID_ARG: an id out of range, a repeated dst, a dst
+ * that is also a src.  num_pairs == 0 launches nothing. */
+pa_status pa_copy_blocks(void* kv_cache, const pa_cache_desc* desc, const int64_t* pairs,
+                         int32_t num_pairs, void* stream);
+
+/* Move whole blocks (every layer) between the device pool and a pinned host
+ * pool of the same geometry (num_blocks and layer stride may differ).
+ *   direction 0 = swap_out (src device pool -> dst pinned host pool),
+ *             1 = swap_in  (src pinned host pool -> dst device pool).
+ *   pairs   HOST int64 [num_pairs][2] (src block, dst block); dst ids unique.
+ * The host pool must be page-locked (cudaHostAlloc / pin_memory). */
+pa_status pa_swap_blocks(void* dst_pool, const pa_cache_desc* dst_desc, const void* src_pool,
+                         const pa_cache_desc* src_desc, int32_t direction, const int64_t* pairs,
+                         int32_t num_pairs, void* stream);
+
+/* Synchronise `stream`, copy the device error word into *host_bits, and reset
+ * it to 0 when `clear` is non-zero. */
+pa_status pa_read_device_errors(uint32_t* dev_err, uint32_t* host_bits, int32_t clear, void* stream);
+
+/* Static description of a status code. */
+const char* pa_status_string(pa_status status);
+
+/* Detail of the last failed call on this thread ("" if none). */
+const char* pa_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

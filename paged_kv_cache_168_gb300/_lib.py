@@ -1,0 +1,192 @@
+"""Thin ctypes binding over libpagedkv.so (argument marshalling only).
+
+Every entry point of ``include/pagedkv.h`` is exposed under the same name
+without the ``pa_`` prefix.  Tensors are torch tensors used only as device (or
+pinned host) memory; pointers, sizes and the current CUDA stream are passed to
+the C ABI, which does all the work in its CUDA kernels.  There is no fallback:
+if the library is not built, importing the binding's functions raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedkv.so")
+_lib = None
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_WORKSPACE_TOO_SMALL = range(5)
+PA_F16, PA_BF16 = 0, 1
+DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_CONTEXT, DEVERR_TIMEOUT = 1, 2, 4, 8
+DTYPE_CODE = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+
+EXPORTED = [
+    "pa_cache_bytes", "pa_cache_element_offset", "pa_reshape_and_cache", "pa_decode_workspace_bytes",
+    "pa_decode_partition_size", "pa_decode", "pa_copy_blocks", "pa_swap_blocks", "pa_read_device_errors",
+    "pa_status_string", "pa_last_error_message",
+]
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [
+        ("num_blocks", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_size", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("num_layers", ctypes.c_int32),
+        ("layer_stride_bytes", ctypes.c_int64),
+    ]
+
+
+@dataclass
+class CacheDesc:
+    """Geometry of a cache pool (mirrors pa_cache_desc)."""
+    num_blocks: int
+    block_size: int
+    num_kv_heads: int
+    head_size: int
+    dtype: torch.dtype = torch.float16
+    num_layers: int = 1
+    layer_stride_bytes: int = 0
+
+    def c(self) -> _Desc:
+        return _Desc(self.num_blocks, self.block_size, self.num_kv_heads, self.head_size,
+                     DTYPE_CODE[self.dtype], self.num_layers, self.layer_stride_bytes)
+
+
+def load():
+    """Load libpagedkv.so; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is not built; run paged_kv_cache_168_gb300.build.build()")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    D = ctypes.POINTER(_Desc)
+    lib.pa_cache_bytes.argtypes = [D]
+    lib.pa_cache_bytes.restype = sz
+    lib.pa_cache_element_offset.argtypes = [D, i64, i32, i32, i32, i32]
+    lib.pa_cache_element_offset.restype = i64
+    lib.pa_reshape_and_cache.argtypes = [P, D, i32, P, i64, P, i64, P, i32, P, P]
+    lib.pa_reshape_and_cache.restype = ctypes.c_int
+    lib.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    lib.pa_decode_workspace_bytes.restype = sz
+    lib.pa_decode_partition_size.argtypes = [i32]
+    lib.pa_decode_partition_size.restype = i32
+    lib.pa_decode.argtypes = [P, P, i64, P, D, i32, P, i32, P, i32, i32, i32, ctypes.c_float, i32, P, sz, P, P]
+    lib.pa_decode.restype = ctypes.c_int
+    lib.pa_copy_blocks.argtypes = [P, D, P, i32, P]
+    lib.pa_copy_blocks.restype = ctypes.c_int
+    lib.pa_swap_blocks.argtypes = [P, D, P, D, i32, P, i32, P]
+    lib.pa_swap_blocks.restype = ctypes.c_int
+    lib.pa_read_device_errors.argtypes = [P, P, i32, P]
+    lib.pa_read_device_errors.restype = ctypes.c_int
+    lib.pa_status_string.argtypes = [ctypes.c_int]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_last_error_message.argtypes = []
+    lib.pa_last_error_message.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != PA_OK:
+        lib = load()
+        raise PagedKVError(status, f"{lib.pa_status_string(status).decode()}: "
+                                   f"{lib.pa_last_error_message().decode()}")
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _pairs(pairs) -> np.ndarray:
+    arr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    return arr
+
+
+def cache_bytes(desc: CacheDesc) -> int:
+    return load().pa_cache_bytes(ctypes.byref(desc.c()))
+
+
+def cache_element_offset(desc: CacheDesc, block: int, kv_head: int, part: int, slot: int, dim: int) -> int:
+    return load().pa_cache_element_offset(ctypes.byref(desc.c()), block, kv_head, part, slot, dim)
+
+
+def reshape_and_cache(kv_cache: torch.Tensor, desc: CacheDesc, key: torch.Tensor, value: torch.Tensor,
+                      slot_mapping: torch.Tensor, layer: int = 0, dev_err: torch.Tensor | None = None,
+                      stream=None) -> None:
+    """pa_reshape_and_cache: key/value [N, Hkv, D] (token stride = stride(0))."""
+    n = key.shape[0]
+    _check(load().pa_reshape_and_cache(_ptr(kv_cache), ctypes.byref(desc.c()), layer, _ptr(key), key.stride(0),
+                                       _ptr(value), value.stride(0), _ptr(slot_mapping), n, _ptr(dev_err),
+                                       _stream(stream)))
+
+
+def decode_partition_size(partition_size: int = 0) -> int:
+    return load().pa_decode_partition_size(partition_size)
+
+
+def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_size: int, max_context_len: int,
+                           partition_size: int = 0) -> int:
+    return load().pa_decode_workspace_bytes(num_seqs, num_q_heads, head_size, max_context_len, partition_size)
+
+
+def decode(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor, desc: CacheDesc,
+           block_tables: torch.Tensor, context_lens: torch.Tensor, max_context_len: int, scale: float,
+           workspace: torch.Tensor | None = None, partition_size: int = 0, layer: int = 0,
+           dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """pa_decode: out/q [S, Hq, D]; block_tables int32 [S, W]; context_lens int32 [S]."""
+    S, Hq = q.shape[0], q.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pa_decode(_ptr(out), _ptr(q), q.stride(0), _ptr(kv_cache), ctypes.byref(desc.c()), layer,
+                            _ptr(block_tables), block_tables.stride(0), _ptr(context_lens), S, Hq,
+                            max_context_len, scale, partition_size, _ptr(workspace), ws_bytes, _ptr(dev_err),
+                            _stream(stream)))
+
+
+def copy_blocks(kv_cache: torch.Tensor, desc: CacheDesc, pairs, stream=None) -> None:
+    """pa_copy_blocks: pairs = host (src, dst) list / array [n, 2]."""
+    arr = _pairs(pairs)
+    _check(load().pa_copy_blocks(_ptr(kv_cache), ctypes.byref(desc.c()), arr.ctypes.data_as(ctypes.c_void_p),
+                                 arr.shape[0], _stream(stream)))
+
+
+def swap_blocks(dst_pool: torch.Tensor, dst_desc: CacheDesc, src_pool: torch.Tensor, src_desc: CacheDesc,
+                direction: int, pairs, stream=None) -> None:
+    """pa_swap_blocks: direction 0 = device -> pinned host, 1 = pinned host -> device."""
+    arr = _pairs(pairs)
+    _check(load().pa_swap_blocks(_ptr(dst_pool), ctypes.byref(dst_desc.c()), _ptr(src_pool),
+                                 ctypes.byref(src_desc.c()), direction, arr.ctypes.data_as(ctypes.c_void_p),
+                                 arr.shape[0], _stream(stream)))
+
+
+def read_device_errors(dev_err: torch.Tensor, clear: bool = True, stream=None) -> int:
+    host = ctypes.c_uint32(0)
+    _check(load().pa_read_device_errors(_ptr(dev_err), ctypes.byref(host), int(clear), _stream(stream)))
+    return host.value
+
+
+def status_string(status: int) -> str:
+    return load().pa_status_string(status).decode()

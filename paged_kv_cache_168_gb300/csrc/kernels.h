@@ -1,0 +1,55 @@
+// kernels.h -- internal launch interface between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+constexpr int kMaxPairsPerLaunch = 1024;
+
+// Block pairs passed by value in kernel parameter space (16 KiB).
+struct PairList {
+  int64_t src[kMaxPairsPerLaunch];
+  int64_t dst[kMaxPairsPerLaunch];
+};
+
+struct DecodeParams {
+  void* out;                  // [S, Hq, D] q dtype
+  const void* q;              // [S, Hq, D] with sequence stride q_seq_stride
+  int64_t q_seq_stride;       // elements
+  const uint8_t* cache;       // this layer's pool
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  const int32_t* block_tables;
+  int32_t bt_stride;
+  const int32_t* context_lens;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t max_context_len;
+  int32_t partition_size;     // tokens per partition (multiple of 128)
+  int32_t max_parts;          // ceil(max_context_len / partition_size)
+  float scale_log2;           // scale * log2(e): scores are kept in base-2 units
+  float* ws_o;                // [S, Hq, max_parts, D] unnormalised partition outputs
+  float* ws_ml;               // [S, Hq, max_parts, 2] (running max in base-2 units, sum)
+  uint32_t* dev_err;
+};
+
+cudaError_t launch_reshape_and_cache(uint8_t* layer_base, int32_t num_blocks, int32_t block_size,
+                                     int32_t num_kv_heads, int32_t head_size, const void* key,
+                                     int64_t key_stride, const void* value, int64_t value_stride,
+                                     const int64_t* slot_mapping, int32_t n, uint32_t* dev_err,
+                                     cudaStream_t stream);
+
+// Copies `pairs.n` whole blocks of `block_bytes` for each of `layers` layers.
+cudaError_t launch_block_copy(uint8_t* dst, int64_t dst_layer_stride, const uint8_t* src,
+                              int64_t src_layer_stride, int64_t block_bytes, int32_t layers,
+                              const PairList& pairs, int32_t n, cudaStream_t stream);
+
+// Paged decode on CUDA cores (all supported shapes).  Returns cudaErrorInvalidValue
+// for an unsupported (dtype, head_size, group) combination.
+cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, int head_size, int group,
+                               cudaStream_t stream);
+
+}  // namespace pkv

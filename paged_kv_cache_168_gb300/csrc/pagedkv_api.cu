@@ -1,0 +1,293 @@
+// pagedkv_api.cu -- the C ABI: argument validation on the host, then kernel
+// dispatch on the caller's stream.  No memory is allocated and no state is kept
+// between calls (the per-thread error message aside).
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "pagedkv.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+pa_status fail(pa_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+pa_status fail(pa_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+pa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+constexpr int kDefaultPartition = 512;
+
+int64_t block_bytes(const pa_cache_desc* d) {
+  return (int64_t)d->num_kv_heads * 2 * d->block_size * d->head_size * 2;
+}
+
+pa_status check_desc(const pa_cache_desc* d) {
+  if (!d) return fail(PA_ERR_INVALID_ARG, "desc is NULL");
+  if (d->num_blocks <= 0 || d->num_kv_heads <= 0 || d->num_layers <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_blocks, num_kv_heads and num_layers must be > 0");
+  if (d->dtype != PA_F16 && d->dtype != PA_BF16) return fail(PA_ERR_INVALID_ARG, "dtype %d", d->dtype);
+  if (d->head_size != 64 && d->head_size != 128)
+    return fail(PA_ERR_UNSUPPORTED, "head_size %d (supported: 64, 128)", d->head_size);
+  if (d->block_size != 8 && d->block_size != 16 && d->block_size != 32)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", d->block_size);
+  const int64_t lb = block_bytes(d) * d->num_blocks;
+  if (d->layer_stride_bytes != 0 && (d->layer_stride_bytes < lb || d->layer_stride_bytes % 16 != 0))
+    return fail(PA_ERR_INVALID_ARG, "layer_stride_bytes %lld must be 0 or >= %lld and a multiple of 16",
+                (long long)d->layer_stride_bytes, (long long)lb);
+  return PA_OK;
+}
+
+int64_t layer_stride(const pa_cache_desc* d) {
+  return d->layer_stride_bytes ? d->layer_stride_bytes : block_bytes(d) * d->num_blocks;
+}
+
+// Validate a host list of (src, dst) pairs.  Destinations must be distinct; when
+// `same_pool`, no destination may also be a source (all pairs act at once).
+pa_status check_pairs(const int64_t* pairs, int32_t n, int32_t src_blocks, int32_t dst_blocks,
+                      bool same_pool) {
+  if (n < 0) return fail(PA_ERR_INVALID_ARG, "num_pairs %d < 0", n);
+  if (n > 0 && !pairs) return fail(PA_ERR_INVALID_ARG, "pairs is NULL");
+  std::vector<int64_t> dst(n), src(n);
+  for (int32_t i = 0; i < n; ++i) {
+    src[i] = pairs[2 * i];
+    dst[i] = pairs[2 * i + 1];
+    if (src[i] < 0 || src[i] >= src_blocks)
+      return fail(PA_ERR_INVALID_ARG, "pair %d: src block %lld out of range [0, %d)", i, (long long)src[i],
+                  src_blocks);
+    if (dst[i] < 0 || dst[i] >= dst_blocks)
+      return fail(PA_ERR_INVALID_ARG, "pair %d: dst block %lld out of range [0, %d)", i, (long long)dst[i],
+                  dst_blocks);
+  }
+  std::sort(dst.begin(), dst.end());
+  for (int32_t i = 1; i < n; ++i)
+    if (dst[i] == dst[i - 1]) return fail(PA_ERR_INVALID_ARG, "dst block %lld repeated", (long long)dst[i]);
+  if (same_pool) {
+    for (int32_t i = 0; i < n; ++i)
+      if (std::binary_search(dst.begin(), dst.end(), src[i]))
+        return fail(PA_ERR_INVALID_ARG, "block %lld is both a src and a dst", (long long)src[i]);
+  }
+  return PA_OK;
+}
+
+pa_status run_pairs(uint8_t* dst, int64_t dst_ls, const uint8_t* src, int64_t src_ls, int64_t bb,
+                    int32_t layers, const int64_t* pairs, int32_t n, cudaStream_t stream) {
+  pkv::PairList list;
+  for (int32_t i0 = 0; i0 < n; i0 += pkv::kMaxPairsPerLaunch) {
+    const int32_t cnt = std::min<int32_t>(pkv::kMaxPairsPerLaunch, n - i0);
+    for (int32_t i = 0; i < cnt; ++i) {
+      list.src[i] = pairs[2 * (i0 + i)];
+      list.dst[i] = pairs[2 * (i0 + i) + 1];
+    }
+    cudaError_t e = pkv::launch_block_copy(dst, dst_ls, src, src_ls, bb, layers, list, cnt, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "block copy launch");
+  }
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_cache_bytes(const pa_cache_desc* desc) {
+  if (check_desc(desc) != PA_OK) return 0;
+  return (size_t)(block_bytes(desc) * desc->num_blocks);
+}
+
+int64_t pa_cache_element_offset(const pa_cache_desc* desc, int64_t block, int32_t kv_head, int32_t part,
+                                int32_t slot, int32_t dim) {
+  if (check_desc(desc) != PA_OK) return -1;
+  if (block < 0 || block >= desc->num_blocks || kv_head < 0 || kv_head >= desc->num_kv_heads || part < 0 ||
+      part > 1 || slot < 0 || slot >= desc->block_size || dim < 0 || dim >= desc->head_size)
+    return -1;
+  pkv::Layout L{desc->block_size, desc->head_size, desc->num_kv_heads};
+  return L.offset(block, kv_head, part, slot, dim);
+}
+
+pa_status pa_reshape_and_cache(void* kv_cache, const pa_cache_desc* desc, int32_t layer, const void* key,
+                               int64_t key_token_stride, const void* value, int64_t value_token_stride,
+                               const int64_t* slot_mapping, int32_t num_tokens, uint32_t* dev_err,
+                               void* stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (layer < 0 || layer >= desc->num_layers) return fail(PA_ERR_INVALID_ARG, "layer %d", layer);
+  if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens %d < 0", num_tokens);
+  if (num_tokens == 0) return PA_OK;
+  if (!kv_cache || !key || !value || !slot_mapping)
+    return fail(PA_ERR_INVALID_ARG, "kv_cache, key, value and slot_mapping must be non-NULL");
+  if (!aligned16(kv_cache) || !aligned16(key) || !aligned16(value))
+    return fail(PA_ERR_INVALID_ARG, "kv_cache, key and value must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7) != 0)
+    return fail(PA_ERR_INVALID_ARG, "slot_mapping must be 8-byte aligned");
+  const int64_t row = (int64_t)desc->num_kv_heads * desc->head_size;
+  if (key_token_stride < row || value_token_stride < row || key_token_stride % 8 || value_token_stride % 8)
+    return fail(PA_ERR_INVALID_ARG, "token strides must be >= num_kv_heads*head_size and multiples of 8");
+  uint8_t* base = static_cast<uint8_t*>(kv_cache) + layer * layer_stride(desc);
+  cudaError_t e = pkv::launch_reshape_and_cache(base, desc->num_blocks, desc->block_size, desc->num_kv_heads,
+                                                desc->head_size, key, key_token_stride, value,
+                                                value_token_stride, slot_mapping, num_tokens, dev_err,
+                                                static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e, "reshape_and_cache launch");
+}
+
+int32_t pa_decode_partition_size(int32_t partition_size) {
+  return partition_size > 0 ? partition_size : kDefaultPartition;
+}
+
+size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
+                                 int32_t max_context_len, int32_t partition_size) {
+  const int64_t P = pa_decode_partition_size(partition_size);
+  if (num_seqs <= 0 || num_q_heads <= 0 || head_size <= 0 || max_context_len <= 0 || P <= 0) return 0;
+  const int64_t parts = (max_context_len + P - 1) / P;
+  if (parts <= 1) return 0;
+  return (size_t)((int64_t)num_seqs * num_q_heads * parts * (head_size + 2) * 4);
+}
+
+pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,
+                    const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
+                    int32_t block_table_stride, const int32_t* context_lens, int32_t num_seqs,
+                    int32_t num_q_heads, int32_t max_context_len, float scale, int32_t partition_size,
+                    void* workspace, size_t workspace_bytes, uint32_t* dev_err, void* stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (layer < 0 || layer >= desc->num_layers) return fail(PA_ERR_INVALID_ARG, "layer %d", layer);
+  if (num_seqs < 0 || num_seqs > 65535) return fail(PA_ERR_INVALID_ARG, "num_seqs %d not in [0, 65535]", num_seqs);
+  if (num_seqs == 0) return PA_OK;
+  if (num_q_heads <= 0 || num_q_heads % desc->num_kv_heads)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
+                num_q_heads, desc->num_kv_heads);
+  const int group = num_q_heads / desc->num_kv_heads;
+  if (group != 1 && group != 2 && group != 4 && group != 8)
+    return fail(PA_ERR_UNSUPPORTED, "query heads per kv head %d (supported: 1, 2, 4, 8)", group);
+  if (desc->num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads > 65535");
+  if (!out || !q || !kv_cache || !block_tables || !context_lens)
+    return fail(PA_ERR_INVALID_ARG, "out, q, kv_cache, block_tables and context_lens must be non-NULL");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(kv_cache))
+    return fail(PA_ERR_INVALID_ARG, "out, q and kv_cache must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3) || (reinterpret_cast<uintptr_t>(context_lens) & 3))
+    return fail(PA_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
+  if (q_seq_stride < (int64_t)num_q_heads * desc->head_size || q_seq_stride % 8)
+    return fail(PA_ERR_INVALID_ARG, "q_seq_stride must be >= num_q_heads*head_size and a multiple of 8");
+  if (block_table_stride <= 0) return fail(PA_ERR_INVALID_ARG, "block_table_stride %d", block_table_stride);
+  if (max_context_len <= 0) return fail(PA_ERR_INVALID_ARG, "max_context_len %d", max_context_len);
+  const int32_t P = pa_decode_partition_size(partition_size);
+  if (P % 128 || P < 128 || P > 8192)
+    return fail(PA_ERR_INVALID_ARG, "partition_size %d must be a multiple of 128 in [128, 8192]", P);
+  if (!(scale > 0.f) || scale != scale) return fail(PA_ERR_INVALID_ARG, "scale must be a positive number");
+  const size_t need = pa_decode_workspace_bytes(num_seqs, num_q_heads, desc->head_size, max_context_len, P);
+  if (workspace_bytes < need)
+    return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+  if (need && (!workspace || !aligned16(workspace)))
+    return fail(PA_ERR_INVALID_ARG, "workspace must be non-NULL and 16-byte aligned");
+
+  pkv::DecodeParams p{};
+  p.out = out;
+  p.q = q;
+  p.q_seq_stride = q_seq_stride;
+  p.cache = static_cast<const uint8_t*>(kv_cache) + layer * layer_stride(desc);
+  p.num_blocks = desc->num_blocks;
+  p.block_size = desc->block_size;
+  p.num_kv_heads = desc->num_kv_heads;
+  p.block_tables = block_tables;
+  p.bt_stride = block_table_stride;
+  p.context_lens = context_lens;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.max_context_len = max_context_len;
+  p.partition_size = P;
+  p.max_parts = (max_context_len + P - 1) / P;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const int64_t parts = p.max_parts;
+  p.ws_o = need ? static_cast<float*>(workspace) : nullptr;
+  p.ws_ml = need ? static_cast<float*>(workspace) + (int64_t)num_seqs * num_q_heads * parts * desc->head_size
+                 : nullptr;
+  p.dev_err = dev_err;
+  cudaError_t e = pkv::launch_decode_simt(p, desc->dtype, desc->head_size, group, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e, "decode launch");
+}
+
+pa_status pa_copy_blocks(void* kv_cache, const pa_cache_desc* desc, const int64_t* pairs, int32_t num_pairs,
+                         void* stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  st = check_pairs(pairs, num_pairs, desc->num_blocks, desc->num_blocks, true);
+  if (st != PA_OK) return st;
+  if (num_pairs == 0) return PA_OK;
+  if (!kv_cache || !aligned16(kv_cache)) return fail(PA_ERR_INVALID_ARG, "kv_cache NULL or not 16-byte aligned");
+  uint8_t* base = static_cast<uint8_t*>(kv_cache);
+  return run_pairs(base, layer_stride(desc), base, layer_stride(desc), block_bytes(desc), desc->num_layers, pairs,
+                   num_pairs, static_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_swap_blocks(void* dst_pool, const pa_cache_desc* dst_desc, const void* src_pool,
+                         const pa_cache_desc* src_desc, int32_t direction, const int64_t* pairs,
+                         int32_t num_pairs, void* stream) {
+  pa_status st = check_desc(dst_desc);
+  if (st != PA_OK) return st;
+  st = check_desc(src_desc);
+  if (st != PA_OK) return st;
+  if (dst_desc->block_size != src_desc->block_size || dst_desc->num_kv_heads != src_desc->num_kv_heads ||
+      dst_desc->head_size != src_desc->head_size || dst_desc->dtype != src_desc->dtype ||
+      dst_desc->num_layers != src_desc->num_layers)
+    return fail(PA_ERR_INVALID_ARG, "src and dst pools differ in geometry");
+  if (direction != 0 && direction != 1) return fail(PA_ERR_INVALID_ARG, "direction %d (0 = out, 1 = in)", direction);
+  st = check_pairs(pairs, num_pairs, src_desc->num_blocks, dst_desc->num_blocks, false);
+  if (st != PA_OK) return st;
+  if (num_pairs == 0) return PA_OK;
+  if (!dst_pool || !src_pool || !aligned16(dst_pool) || !aligned16(src_pool))
+    return fail(PA_ERR_INVALID_ARG, "pools must be non-NULL and 16-byte aligned");
+  const void* host = direction == 0 ? dst_pool : src_pool;
+  const void* devp = direction == 0 ? src_pool : dst_pool;
+  cudaPointerAttributes ah, ad;
+  cudaError_t e = cudaPointerGetAttributes(&ah, host);
+  if (e != cudaSuccess) return cuda_fail(e, "host pool attributes");
+  if (ah.type != cudaMemoryTypeHost || ah.devicePointer == nullptr)
+    return fail(PA_ERR_INVALID_ARG, "the host pool must be page-locked host memory mapped for the device");
+  e = cudaPointerGetAttributes(&ad, devp);
+  if (e != cudaSuccess) return cuda_fail(e, "device pool attributes");
+  if (ad.type != cudaMemoryTypeDevice) return fail(PA_ERR_INVALID_ARG, "the device pool must be device memory");
+  // the host pool is addressed through its device mapping
+  const uint8_t* src = static_cast<const uint8_t*>(direction == 0 ? src_pool : ah.devicePointer);
+  uint8_t* dst = static_cast<uint8_t*>(direction == 0 ? ah.devicePointer : dst_pool);
+  return run_pairs(dst, layer_stride(dst_desc), src, layer_stride(src_desc), block_bytes(src_desc),
+                   src_desc->num_layers, pairs, num_pairs, static_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_read_device_errors(uint32_t* dev_err, uint32_t* host_bits, int32_t clear, void* stream) {
+  if (!dev_err || !host_bits) return fail(PA_ERR_INVALID_ARG, "dev_err and host_bits must be non-NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(host_bits, dev_err, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(dev_err, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? PA_OK : cuda_fail(e, "read device errors");
+}
+
+const char* pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case PA_ERR_CUDA: return "CUDA runtime error";
+    case PA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+const char* pa_last_error_message(void) { return g_msg; }
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+"""One decode step of one layer over a workload, through the C ABI.
+
+Order within a step (what a scheduler's output asks the cache engine for, then
+the attention layer): swap_out -> swap_in -> copy_blocks (copy-on-write) ->
+reshape_and_cache (the new token's K/V) -> paged decode.  All buffers (output,
+workspace, pinned host pool, error word) are allocated once here, outside the
+step; the step itself only launches kernels on one stream.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from .workloads import Workload
+
+
+class DecodeStep:
+    def __init__(self, w: Workload, partition_size: int = 0, stream: torch.cuda.Stream | None = None):
+        cfg = w.cfg
+        dev = w.q.device
+        self.w = w
+        self.stream = stream or torch.cuda.current_stream(dev)
+        self.desc = _lib.CacheDesc(w.num_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_size, w.dtype)
+        self.partition_size = partition_size
+        self.out = torch.empty_like(w.q)
+        nbytes = _lib.decode_workspace_bytes(cfg.num_seqs, cfg.num_q_heads, cfg.head_size, w.max_context_len,
+                                             partition_size)
+        self.workspace = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device=dev)
+        self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.host_pool = None
+        if w.host_blocks:
+            self.host_desc = _lib.CacheDesc(w.host_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_size,
+                                            w.dtype)
+            self.host_pool = torch.empty(w.host_blocks * w.kv_cache[0].numel(), dtype=w.dtype).pin_memory()
+
+    def cache_ops(self):
+        w, s = self.w, self.stream
+        if self.host_pool is not None:
+            _lib.swap_blocks(self.host_pool, self.host_desc, w.kv_cache, self.desc, 0, w.swap_out_pairs, stream=s)
+            _lib.swap_blocks(w.kv_cache, self.desc, self.host_pool, self.host_desc, 1, w.swap_in_pairs, stream=s)
+        if w.copy_pairs.shape[0]:
+            _lib.copy_blocks(w.kv_cache, self.desc, w.copy_pairs, stream=s)
+        _lib.reshape_and_cache(w.kv_cache, self.desc, w.key, w.value, w.slot_mapping, dev_err=self.dev_err,
+                               stream=s)
+
+    def attention(self, q=None, out=None):
+        w = self.w
+        _lib.decode(self.out if out is None else out, w.q if q is None else q, w.kv_cache, self.desc,
+                    w.block_tables, w.context_lens, w.max_context_len, w.scale, self.workspace,
+                    self.partition_size, dev_err=self.dev_err, stream=self.stream)
+
+    def __call__(self):
+        self.cache_ops()
+        self.attention()
+        return self.out
+
+    def kernel_launches(self) -> int:
+        """Kernels one step launches."""
+        w, cfg = self.w, self.w.cfg
+        n = 1                                                   # reshape_and_cache
+        per = 1024                                              # pairs per copy launch
+        if self.host_pool is not None:
+            n += -(-w.swap_out_pairs.shape[0] // per) + -(-w.swap_in_pairs.shape[0] // per)
+        if w.copy_pairs.shape[0]:
+            n += -(-w.copy_pairs.shape[0] // per)
+        P = _lib.decode_partition_size(self.partition_size)
+        n += 1 + (1 if -(-w.max_context_len // P) > 1 else 0)   # decode (+ merge)
+        return n
+
+    def algorithmic_bytes(self) -> dict:
+        """Bytes the method must move per step (what each kernel reads + writes)."""
+        w, cfg = self.w, self.w.cfg
+        esz = 2
+        kv_tok = 2 * cfg.num_kv_heads * cfg.head_size * esz
+        ctx = w.context_lens_np.astype("int64")
+        nblk = -(-ctx // cfg.block_size)
+        decode = int(ctx.sum()) * kv_tok + 2 * cfg.num_seqs * cfg.num_q_heads * cfg.head_size * esz \
+            + 4 * int(nblk.sum()) + 4 * cfg.num_seqs
+        reshape = 2 * cfg.num_seqs * kv_tok + 8 * cfg.num_seqs
+        block_bytes = w.kv_cache[0].numel() * esz
+        copy = 2 * w.copy_pairs.shape[0] * block_bytes
+        swap = (w.swap_out_pairs.shape[0] + w.swap_in_pairs.shape[0]) * block_bytes * 2
+        return {"decode": decode, "decode_kv": int(ctx.sum()) * kv_tok, "reshape": reshape, "copy": copy,
+                "swap": swap, "total": decode + reshape + copy + swap}

@@ -1,0 +1,143 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every entry
+point the header declares, and its host-side logic (sizes, layout, argument
+validation) behaves as documented.  No call here reaches a kernel launch."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_168_gb300 import _lib, build as build_mod
+from paged_kv_cache_168_gb300._lib import CacheDesc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return _lib.load()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(_lib.EXPORTED) == names
+
+
+def test_cache_bytes(lib):
+    d = CacheDesc(num_blocks=8192 // 16, block_size=16, num_kv_heads=40, head_size=128)
+    # one LLaMA-13B layer for an 8192-token request: 2 x 8192 x 40 x 128 x 2 bytes
+    assert _lib.cache_bytes(d) == 2 * 8192 * 40 * 128 * 2
+    assert _lib.cache_bytes(CacheDesc(10, 16, 2, 96)) == 0          # unsupported head size
+    assert _lib.cache_bytes(CacheDesc(0, 16, 2, 128)) == 0
+
+
+@pytest.mark.parametrize("bs,D,dtype", [(8, 64, torch.float16), (16, 128, torch.bfloat16), (32, 128, torch.float16)])
+def test_library_layout_agrees_with_oracle_layout(lib, bs, D, dtype):
+    d = CacheDesc(3, bs, 2, D, dtype)
+    g = oracle.Geom(3, bs, 2, D)
+    for b in range(3):
+        for h in range(2):
+            for part in range(2):
+                for t in range(bs):
+                    for dim in range(0, D, 3):
+                        assert _lib.cache_element_offset(d, b, h, part, t, dim) == \
+                            oracle.cache_offset(g, b, h, part, t, dim)
+    assert _lib.cache_element_offset(d, 3, 0, 0, 0, 0) == -1
+    assert _lib.cache_element_offset(d, 0, 0, 2, 0, 0) == -1
+
+
+def test_workspace_sizing(lib):
+    assert _lib.decode_partition_size(0) == 512
+    assert _lib.decode_workspace_bytes(64, 32, 128, 512) == 0        # one partition: no workspace
+    assert _lib.decode_workspace_bytes(64, 32, 128, 4096) == 64 * 32 * 8 * 130 * 4
+    assert _lib.decode_workspace_bytes(8, 64, 128, 131072, 1024) == 8 * 64 * 128 * 130 * 4
+
+
+def test_status_strings(lib):
+    assert _lib.status_string(0) == "ok"
+    assert "workspace" in _lib.status_string(4)
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def _desc(**kw):
+    base = dict(num_blocks=16, block_size=16, num_kv_heads=2, head_size=128, dtype=torch.float16)
+    base.update(kw)
+    return CacheDesc(**base).c()
+
+
+def _copy(lib, pairs, desc=None):
+    arr = np.ascontiguousarray(np.asarray(pairs, np.int64).reshape(-1, 2))
+    return lib.pa_copy_blocks(ctypes.c_void_p(FAKE), ctypes.byref(desc or _desc()),
+                              arr.ctypes.data_as(ctypes.c_void_p), arr.shape[0], None)
+
+
+def test_copy_blocks_rejects_bad_pair_lists(lib):
+    assert _copy(lib, [[0, 1], [2, 1]]) == _lib.PA_ERR_INVALID_ARG       # repeated dst
+    assert b"repeated" in lib.pa_last_error_message()
+    assert _copy(lib, [[0, 1], [1, 2]]) == _lib.PA_ERR_INVALID_ARG       # dst is also a src
+    assert _copy(lib, [[0, 16]]) == _lib.PA_ERR_INVALID_ARG              # out of range
+    assert _copy(lib, [[-1, 3]]) == _lib.PA_ERR_INVALID_ARG
+    assert _copy(lib, [[0, 1]], _desc(head_size=96)) == _lib.PA_ERR_UNSUPPORTED
+    assert _copy(lib, [[0, 1]], _desc(block_size=12)) == _lib.PA_ERR_UNSUPPORTED
+    assert _copy(lib, np.zeros((0, 2))) == _lib.PA_OK                     # nothing to do
+
+
+def _decode(lib, desc=None, S=2, Hq=4, max_ctx=100, P=0, ws=0, q=FAKE, scale=0.1, bt_stride=8):
+    return lib.pa_decode(ctypes.c_void_p(FAKE), ctypes.c_void_p(q), Hq * 128, ctypes.c_void_p(FAKE),
+                         ctypes.byref(desc or _desc()), 0, ctypes.c_void_p(FAKE), bt_stride,
+                         ctypes.c_void_p(FAKE), S, Hq, max_ctx, scale, P, None, ws, None, None)
+
+
+def test_decode_rejects_bad_arguments(lib):
+    assert _decode(lib, Hq=3) == _lib.PA_ERR_INVALID_ARG                  # not a multiple of Hkv
+    assert _decode(lib, Hq=6) == _lib.PA_ERR_UNSUPPORTED                  # group of 3
+    assert _decode(lib, desc=_desc(head_size=80)) == _lib.PA_ERR_UNSUPPORTED
+    assert _decode(lib, max_ctx=4096) == _lib.PA_ERR_WORKSPACE_TOO_SMALL
+    assert _decode(lib, P=100) == _lib.PA_ERR_INVALID_ARG                 # not a multiple of 128
+    assert _decode(lib, q=FAKE + 8) == _lib.PA_ERR_INVALID_ARG            # misaligned q
+    assert _decode(lib, scale=0.0) == _lib.PA_ERR_INVALID_ARG
+    assert _decode(lib, scale=float("nan")) == _lib.PA_ERR_INVALID_ARG
+    assert _decode(lib, bt_stride=0) == _lib.PA_ERR_INVALID_ARG
+    assert _decode(lib, S=70000) == _lib.PA_ERR_INVALID_ARG
+    assert _decode(lib, S=0) == _lib.PA_OK                                 # nothing to do
+
+
+def test_reshape_rejects_bad_arguments(lib):
+    call = lambda stride, n=4, key=FAKE, layer=0: lib.pa_reshape_and_cache(
+        ctypes.c_void_p(FAKE), ctypes.byref(_desc()), layer, ctypes.c_void_p(key), stride,
+        ctypes.c_void_p(FAKE), 256, ctypes.c_void_p(FAKE), n, None, None)
+    assert call(255) == _lib.PA_ERR_INVALID_ARG          # stride below one token row
+    assert call(260) == _lib.PA_ERR_INVALID_ARG          # not a multiple of 8
+    assert call(256, key=FAKE + 2) == _lib.PA_ERR_INVALID_ARG
+    assert call(256, layer=1) == _lib.PA_ERR_INVALID_ARG
+    assert call(256, n=-1) == _lib.PA_ERR_INVALID_ARG
+    assert call(256, n=0) == _lib.PA_OK
+
+
+def test_swap_rejects_mismatched_pools(lib):
+    arr = np.array([[0, 1]], np.int64)
+    st = lib.pa_swap_blocks(ctypes.c_void_p(FAKE), ctypes.byref(_desc()), ctypes.c_void_p(FAKE),
+                            ctypes.byref(_desc(num_kv_heads=4)), 0, arr.ctypes.data_as(ctypes.c_void_p), 1, None)
+    assert st == _lib.PA_ERR_INVALID_ARG
+    st = lib.pa_swap_blocks(ctypes.c_void_p(FAKE), ctypes.byref(_desc()), ctypes.c_void_p(FAKE),
+                            ctypes.byref(_desc()), 2, arr.ctypes.data_as(ctypes.c_void_p), 1, None)
+    assert st == _lib.PA_ERR_INVALID_ARG
+
+
+def test_read_device_errors_rejects_null(lib):
+    assert lib.pa_read_device_errors(None, None, 0, None) == _lib.PA_ERR_INVALID_ARG

@@ -204,7 +204,7 @@ def run_reference(args):
         return 0
     from paged_kv_cache_168_gb300.workloads import make_workload
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    w = make_workload(args.workload, device=dev)
+    w = make_workload(args.workload, device=dev, num_seqs=args.seqs)
     cfg = w.cfg
     # each step is a bounded sample: a few sequences of the workload
     per_step = max(1.0, args.reference_seconds / max(args.steps + args.warmup, 1))
@@ -252,7 +252,7 @@ def run_gpu(args):
     _lib.load()
 
     cfg = CONFIGS[args.workload]
-    w = make_workload(args.workload, device=device, seed=cfg.seed + 1000 * rank)
+    w = make_workload(args.workload, device=device, seed=cfg.seed + 1000 * rank, num_seqs=args.seqs)
     stream = torch.cuda.Stream(device)
     step = DecodeStep(w, partition_size=args.partition_size, stream=stream)
     nbytes = step.algorithmic_bytes()
@@ -334,7 +334,8 @@ def run_gpu(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.cfg.dtype, "data": "synthetic",
-            "config": {"workload": DESCRIPTIONS[args.workload], "global_batch": w.cfg.num_seqs * world,
+            "config": {"workload": DESCRIPTIONS[args.workload] + (f" (first {args.seqs} sequences)" if args.seqs else ""),
+                       "global_batch": w.cfg.num_seqs * world,
                        "max_context_len": w.max_context_len, "tokens_in_context": int(w.context_lens_np.sum()),
                        "partition_size": _lib.decode_partition_size(args.partition_size),
                        "parallelism": f"replicas{world}",
@@ -367,11 +368,12 @@ def run_gpu(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="7b", choices=sorted(DESCRIPTIONS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--seqs", type=int, default=None, help="use only the first N sequences (small profiling runs)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     args = ap.parse_args(argv)

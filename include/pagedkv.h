@@ -27,7 +27,8 @@
  * Conventions
  *   Ownership:  the caller allocates every buffer (cache pools, workspace,
  *               error word).  The library allocates no memory and keeps no
- *               per-call state.
+ *               per-call state (pa_decode_static_workspace alone uses a fixed
+ *               array the library carries; see its comment).
  *   Streams:    every call except pa_read_device_errors is asynchronous on the
  *               given CUDA stream (a cudaStream_t passed as void*; NULL = the
  *               legacy default stream) and performs no host synchronisation.
@@ -162,6 +163,35 @@ pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* 
                     int32_t num_q_heads, int32_t max_context_len, float scale,
                     int32_t partition_size, void* workspace, size_t workspace_bytes,
                     uint32_t* dev_err, void* stream);
+
+/* Size of the workspace the library carries for pa_decode_static_workspace
+ * (32 MiB on every device that loads the library, held until the process exits). */
+#define PA_STATIC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+
+/* pa_decode for callers that cannot allocate device memory.  The pages describe
+ * no such entry point; it exists for this library's users.  Some callers cannot
+ * call cudaMalloc where they call decode: a plugin inside a framework whose
+ * allocator owns all device memory, a serving loop that forbids allocation once
+ * it runs, or a binding from another language that cannot keep a device buffer
+ * between calls.  This call takes the same arguments as pa_decode minus the
+ * workspace, and uses instead a fixed array of PA_STATIC_WORKSPACE_BYTES in the
+ * library's own device memory.
+ *   - Shapes whose pa_decode_workspace_bytes(...) exceeds
+ *     PA_STATIC_WORKSPACE_BYTES are rejected with PA_ERR_WORKSPACE_TOO_SMALL
+ *     (pa_last_error_message explains); nothing is launched.  A larger
+ *     partition_size shrinks the need.
+ *   - It allocates nothing.  The first call on a device that needs the array
+ *     looks up its device address (cudaGetSymbolAddress) with that device
+ *     current and caches it; make that first call before any stream capture.
+ *   - The array is shared by every call on a device and keeps the last call's
+ *     contents (decode needs none of it zeroed).  Calls that may overlap on the
+ *     GPU -- on different streams, or from different threads -- race on it:
+ *     serialise them, or give each its own workspace through pa_decode. */
+pa_status pa_decode_static_workspace(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,
+                                     const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
+                                     int32_t block_table_stride, const int32_t* context_lens,
+                                     int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                                     float scale, int32_t partition_size, uint32_t* dev_err, void* stream);
 
 /* Copy whole blocks inside one pool (every kv head, K and V, every layer):
  * for each pair i, block pairs[2i+1] receives block pairs[2i].  All pairs act

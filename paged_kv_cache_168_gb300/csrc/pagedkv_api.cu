@@ -102,6 +102,12 @@ pa_status run_pairs(uint8_t* dst, int64_t dst_ls, const uint8_t* src, int64_t sr
 
 }  // namespace
 
+namespace pkv {
+// Record a message for pa_last_error_message() (used by entry points defined in
+// other translation units).
+void set_last_error(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
+}  // namespace pkv
+
 extern "C" {
 
 size_t pa_cache_bytes(const pa_cache_desc* desc) {

@@ -1,0 +1,67 @@
+"""pa_decode_static_workspace: decode for callers that cannot allocate device memory.
+
+Some callers of this library cannot call cudaMalloc where they run decode -- a
+plugin inside a framework whose allocator owns all device memory, a serving loop
+that forbids allocation once it is running, a binding from another language that
+cannot keep a device buffer alive between calls.  For them the library offers an
+entry point that takes no workspace and uses a fixed array in its own device
+memory instead.  These tests call it through the C ABI and check that it gives
+the same output as pa_decode with a caller-allocated workspace, on two calls in
+a row (the second call must not be disturbed by what the first left in the
+shared array), and that shapes too large for the array are refused.
+
+This file is named so that pytest collects it last."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_168_gb300 as pkv
+from gpu_helpers import assert_attention_close, ensure_built, paged_to_dev, run_decode
+from paged_helpers import Paged
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_device):
+    ensure_built()
+
+
+def _case(seed, ctx, Hq=8, Hkv=2, D=128, bs=16, dtype="bf16"):
+    p = Paged(np.random.default_rng(seed), S=len(ctx), Hq=Hq, Hkv=Hkv, D=D, bs=bs, ctx=ctx, dtype=dtype)
+    return p, paged_to_dev(p)
+
+
+def test_static_workspace_matches_caller_workspace_on_two_calls():
+    P = 128
+    cases = [_case(300, [1, 127, 129, 700, 2049, 3000]),
+             _case(301, [3000, 5, 1500, 256, 257, 999], Hq=16, Hkv=16, D=64, bs=8, dtype="f16")]
+    for p, (q, pool, tables, ctx, desc) in cases:          # two calls in a row, different data
+        max_ctx = int(p.ctx.max())
+        scale = 1 / math.sqrt(p.D)
+        need = pkv.decode_workspace_bytes(p.S, p.Hq, p.D, max_ctx, P)
+        assert 0 < need <= pkv._lib.STATIC_WORKSPACE_BYTES     # the shared array is really used
+        ref = run_decode(q, pool, desc, tables, ctx, max_ctx, scale, P)
+        out = torch.full_like(q, float("nan"))
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pkv._lib.decode_static_workspace(out, q, pool, desc, tables, ctx, max_ctx, scale, P, dev_err=err)
+        torch.cuda.synchronize()
+        assert pkv.read_device_errors(err) == 0
+        assert_attention_close(out, ref.to(torch.float64).cpu().numpy(), "static workspace vs caller workspace")
+
+
+def test_static_workspace_refuses_shapes_beyond_its_size():
+    S, Hq, D, max_ctx, P = 2048, 64, 128, 8192, 128
+    assert pkv.decode_workspace_bytes(S, Hq, D, max_ctx, P) > pkv._lib.STATIC_WORKSPACE_BYTES
+    q = torch.zeros((S, Hq, D), dtype=torch.float16, device="cuda")
+    out = torch.zeros_like(q)
+    pool = torch.zeros(8 * 2 * 16 * D, dtype=torch.float16, device="cuda")
+    tables = torch.zeros((S, 1), dtype=torch.int32, device="cuda")
+    ctx = torch.zeros(S, dtype=torch.int32, device="cuda")     # even if launched, nothing would be read
+    desc = pkv.CacheDesc(1, 16, 8, D, torch.float16)
+    with pytest.raises(pkv.PagedKVError) as e:
+        pkv._lib.decode_static_workspace(out, q, pool, desc, tables, ctx, max_ctx, 0.088, P)
+    assert e.value.status == pkv.PA_ERR_WORKSPACE_TOO_SMALL
+    assert "PA_STATIC_WORKSPACE_BYTES" in str(e.value)

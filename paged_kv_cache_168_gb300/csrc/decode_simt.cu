@@ -410,6 +410,17 @@ static cudaError_t launch_typed(const DecodeParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_merge(const DecodeParams& p, int dtype, int head_size, cudaStream_t stream) {
+  if (p.max_parts <= 1) return cudaSuccess;
+  const dim3 grid((unsigned)p.num_q_heads, (unsigned)p.num_seqs);
+  if (dtype == PA_F16 && head_size == 128) merge_partitions_kernel<__half, 128><<<grid, 128, 0, stream>>>(p);
+  else if (dtype == PA_F16 && head_size == 64) merge_partitions_kernel<__half, 64><<<grid, 64, 0, stream>>>(p);
+  else if (dtype == PA_BF16 && head_size == 128) merge_partitions_kernel<__nv_bfloat16, 128><<<grid, 128, 0, stream>>>(p);
+  else if (dtype == PA_BF16 && head_size == 64) merge_partitions_kernel<__nv_bfloat16, 64><<<grid, 64, 0, stream>>>(p);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
 template <typename T, int D>
 static cudaError_t launch_group(const DecodeParams& p, int group, cudaStream_t stream) {
   switch (group) {

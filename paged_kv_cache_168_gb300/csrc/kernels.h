@@ -52,4 +52,13 @@ cudaError_t launch_block_copy(uint8_t* dst, int64_t dst_layer_stride, const uint
 cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, int head_size, int group,
                                cudaStream_t stream);
 
+// Log-sum-exp merge of partition results in the workspace (items whose context
+// spans more than one partition); no-op launch when max_parts <= 1.
+cudaError_t launch_merge(const DecodeParams& p, int dtype, int head_size, cudaStream_t stream);
+
+// Paged decode on the tensor cores (tcgen05): head_size 128, group size 1-16,
+// at most kTcMaxSeqs sequences.  Launches the decode kernel and the merge.
+constexpr int kTcMaxSeqs = 8192;
+cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, int group, int num_sms, cudaStream_t stream);
+
 }  // namespace pkv

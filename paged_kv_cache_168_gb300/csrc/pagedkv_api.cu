@@ -3,6 +3,7 @@
 // between calls (the per-thread error message aside).
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -32,6 +33,17 @@ pa_status cuda_fail(cudaError_t e, const char* what) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 constexpr int kDefaultPartition = 512;
+
+// Kernel choice: the tensor-core kernel serves head_size 128 (group sizes 1-16,
+// up to pkv::kTcMaxSeqs sequences); the CUDA-core kernel serves the rest.  The
+// environment variable PAGEDKV_DECODE_KERNEL=simt selects the CUDA-core kernel
+// wherever it applies (used to test both kernels on the same inputs).
+bool use_tensor_cores(int head_size, int group, int num_seqs) {
+  if (head_size != 128 || num_seqs > pkv::kTcMaxSeqs) return false;
+  if (group > 8) return true;
+  const char* env = getenv("PAGEDKV_DECODE_KERNEL");
+  return !(env && strcmp(env, "simt") == 0);
+}
 
 int64_t block_bytes(const pa_cache_desc* d) {
   return (int64_t)d->num_kv_heads * 2 * d->block_size * d->head_size * 2;
@@ -178,8 +190,9 @@ pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* 
     return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
                 num_q_heads, desc->num_kv_heads);
   const int group = num_q_heads / desc->num_kv_heads;
-  if (group != 1 && group != 2 && group != 4 && group != 8)
-    return fail(PA_ERR_UNSUPPORTED, "query heads per kv head %d (supported: 1, 2, 4, 8)", group);
+  if (group != 1 && group != 2 && group != 4 && group != 8 && !(group == 16 && desc->head_size == 128))
+    return fail(PA_ERR_UNSUPPORTED, "query heads per kv head %d (supported: 1, 2, 4, 8; 16 at head_size 128)",
+                group);
   if (desc->num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads > 65535");
   if (!out || !q || !kv_cache || !block_tables || !context_lens)
     return fail(PA_ERR_INVALID_ARG, "out, q, kv_cache, block_tables and context_lens must be non-NULL");
@@ -223,7 +236,15 @@ pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* 
   p.ws_ml = need ? static_cast<float*>(workspace) + (int64_t)num_seqs * num_q_heads * parts * desc->head_size
                  : nullptr;
   p.dev_err = dev_err;
-  cudaError_t e = pkv::launch_decode_simt(p, desc->dtype, desc->head_size, group, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (use_tensor_cores(desc->head_size, group, num_seqs)) {
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = pkv::launch_decode_tc(p, desc->dtype, group, sms, static_cast<cudaStream_t>(stream));
+  } else {
+    e = pkv::launch_decode_simt(p, desc->dtype, desc->head_size, group, static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? PA_OK : cuda_fail(e, "decode launch");
 }
 

@@ -40,20 +40,46 @@ def ctx_cases(bs, P):
     return [1, bs - 1, bs, bs + 1, P - 1, P, P + 1, 2 * P + 7, 3]
 
 
+@pytest.fixture(params=["tc", "simt"])
+def kernel(request, monkeypatch):
+    """Which decode kernel serves head_size 128: the tensor-core one (default) or
+    the CUDA-core one (selected through PAGEDKV_DECODE_KERNEL=simt)."""
+    if request.param == "simt":
+        monkeypatch.setenv("PAGEDKV_DECODE_KERNEL", "simt")
+    else:
+        monkeypatch.delenv("PAGEDKV_DECODE_KERNEL", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("bs", [8, 16, 32])
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 1), (32, 8), (64, 8), (4, 2)])
-def test_decode_sweep(dtype, bs, D, Hq, Hkv):
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 1), (32, 8), (64, 8), (4, 2), (16, 1)])
+def test_decode_sweep(dtype, bs, D, Hq, Hkv, kernel):
+    if D == 64 and kernel == "tc":
+        pytest.skip("head_size 64 is served by the CUDA-core kernel only")
+    if Hq // Hkv == 16 and (D != 128 or kernel != "tc"):
+        pytest.skip("16 query heads per kv head: tensor-core kernel (head_size 128) only")
     rng = np.random.default_rng(zlib.crc32(repr((dtype, bs, D, Hq, Hkv)).encode()))
     P = 128
     ctx = ctx_cases(bs, P)
     p = Paged(rng, S=len(ctx), Hq=Hq, Hkv=Hkv, D=D, bs=bs, ctx=ctx, dtype=dtype)
-    check(p, P=P, what=f"{dtype} bs{bs} D{D} {Hq}/{Hkv}")
+    check(p, P=P, what=f"{kernel} {dtype} bs{bs} D{D} {Hq}/{Hkv}")
+
+
+def test_both_kernels_agree_on_many_sequences(monkeypatch):
+    # more items than SMs, so every persistent CTA walks several items and tiles
+    rng = np.random.default_rng(210)
+    ctx = list(rng.integers(1, 700, size=300))
+    p = Paged(rng, S=len(ctx), Hq=8, Hkv=2, D=128, bs=16, ctx=ctx, dtype="bf16")
+    out_tc = check(p, P=256, what="tc many")
+    monkeypatch.setenv("PAGEDKV_DECODE_KERNEL", "simt")
+    out_simt = check(p, P=256, what="simt many")
+    assert_attention_close(out_tc, out_simt.to(torch.float64).cpu().numpy(), "tc vs simt")
 
 
 @pytest.mark.parametrize("P", [128, 256, 512, 8192])
-def test_partition_size_does_not_change_the_result(P):
+def test_partition_size_does_not_change_the_result(P, kernel):
     rng = np.random.default_rng(200)
     ctx = [1, 127, 128, 129, 700, 2049, 3000]
     p = Paged(rng, S=len(ctx), Hq=8, Hkv=2, D=128, bs=16, ctx=ctx, dtype="bf16")
@@ -79,7 +105,7 @@ def test_tiny_config_end_to_end():
     assert_attention_close(out, ref, "tiny")
 
 
-def test_physical_placement_gives_bit_identical_output():
+def test_physical_placement_gives_bit_identical_output(kernel):
     outs = []
     for perm in (None, np.arange(40)[::-1].copy(), np.random.default_rng(9).permutation(40)):
         rng = np.random.default_rng(201)
@@ -97,7 +123,7 @@ def test_block_size_gives_matching_output():
         check(p, P=256, what=f"bs={bs}")
 
 
-def test_shared_prefix_blocks_equal_unshared_copies():
+def test_shared_prefix_blocks_equal_unshared_copies(kernel):
     rng = np.random.default_rng(203)
     p = Paged(rng, S=2, Hq=8, Hkv=8, D=128, bs=16, ctx=[300, 300], num_blocks=48, dtype="f16")
     p.K[1][:256] = p.K[0][:256]
@@ -112,14 +138,15 @@ def test_shared_prefix_blocks_equal_unshared_copies():
     assert torch.equal(a, b)
 
 
-def test_zero_context_rows_are_zero():
+@pytest.mark.parametrize("D", [64, 128])
+def test_zero_context_rows_are_zero(D, kernel):
     rng = np.random.default_rng(204)
-    p = Paged(rng, S=3, Hq=4, Hkv=4, D=64, bs=16, ctx=[0, 20, 0], dtype="f16")
+    p = Paged(rng, S=3, Hq=4, Hkv=4, D=D, bs=16, ctx=[0, 20, 0], dtype="f16")
     out = check(p, P=128)
     assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
 
 
-def test_device_errors_skip_the_item_and_zero_its_output():
+def test_device_errors_skip_the_item_and_zero_its_output(kernel):
     rng = np.random.default_rng(205)
     p = Paged(rng, S=4, Hq=8, Hkv=2, D=128, bs=16, ctx=[40, 600, 50, 300], dtype="bf16", width=40)
     scale = 0.088
@@ -144,9 +171,10 @@ def test_device_errors_skip_the_item_and_zero_its_output():
     assert pkv.read_device_errors(err) == pkv.DEVERR_CONTEXT and torch.all(out[1] == 0)
 
 
-def test_entries_past_the_context_are_never_read():
+@pytest.mark.parametrize("D", [64, 128])
+def test_entries_past_the_context_are_never_read(D, kernel):
     # table padding of -1 (already in every Paged case) plus garbage ids past ceil(ctx/bs)
     rng = np.random.default_rng(206)
-    p = Paged(rng, S=2, Hq=4, Hkv=4, D=64, bs=16, ctx=[17, 100], dtype="f16", width=12)
+    p = Paged(rng, S=2, Hq=4, Hkv=4, D=D, bs=16, ctx=[17, 100], dtype="f16", width=12)
     p.tables[0, 2:] = 10 ** 6
     check(p, P=128)

@@ -84,52 +84,62 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling in the background during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle sampling in the background; only samples taken
+    inside the timed window (mark_start / mark_end, host clock) are summarised."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, index: int):
-        self.index, self.proc, self.lines = index, None, []
+    def __init__(self, index: int, interval_ms: int = 50):
+        self.index, self.interval_ms, self.proc, self.lines = index, interval_ms, None, []
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
-                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms",
+                 str(self.interval_ms), "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         time.sleep(0.3)
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
     def __exit__(self, *exc):
         if self.proc is not None:
-            time.sleep(0.25)
+            time.sleep(0.2)
             self.proc.terminate()
             out, _ = self.proc.communicate(timeout=10)
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
+    @staticmethod
+    def _parse(line):
+        import datetime
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 10:
+            return None
+        try:
+            ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            return ts, float(f[2]), float(f[3]), f[6:10]
+        except ValueError:
+            return None
+
     def summary(self):
-        if not self.lines:
+        samples = [x for x in (self._parse(ln) for ln in self.lines) if x]
+        if not samples:
             return None
-        sm, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = max(mx, float(f[2]))
-            except ValueError:
-                continue
-            for name, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        inside = [x for x in samples if self.t0 is not None and self.t0 <= x[0] <= (self.t1 or x[0])]
+        used = inside or [min(samples, key=lambda x: abs(x[0] - (self.t0 or x[0])))]
+        reasons = sorted({name for x in used for name, v in zip(self.REASONS, x[3]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([x[1] for x in used])), "sm_max_mhz": max(x[2] for x in used),
+                "reasons": reasons, "samples": len(used), "samples_in_timed_region": len(inside)}
 
 
 def dist_env():
@@ -269,6 +279,7 @@ def run_gpu(args):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        clocks.mark_start()
         with torch.cuda.stream(stream):
             for i in range(K):
                 ev[i][0].record(stream)
@@ -278,6 +289,7 @@ def run_gpu(args):
                 ev[i][2].record(stream)
                 ev[i][3].record(stream)
         torch.cuda.synchronize()
+        clocks.mark_end()
         barrier(world)
     total_ms = ev[0][0].elapsed_time(ev[K - 1][3])
     decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
@@ -368,7 +380,7 @@ def run_gpu(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="7b", choices=sorted(DESCRIPTIONS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])

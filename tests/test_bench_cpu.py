@@ -1,0 +1,80 @@
+"""Host-side logic of bench.py without a GPU: clock-sample parsing, the traffic
+record, the oracle CPU baseline on the tiny workload, and the cross-rank
+aggregation with two gloo ranks."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_clock_summary_keeps_samples_inside_the_timed_window():
+    c = bench.ClockSampler(0)
+    c.lines = [
+        "2026/12/02 08:00:00.000, 0, 1980, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 08:00:01.000, 0, 1440, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 08:00:01.500, 0, 1500, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 08:00:03.000, 0, 2070, 2070, 300.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    import datetime
+    t = lambda s: datetime.datetime.strptime(s, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+    c.t0, c.t1 = t("2026/12/02 08:00:00.900"), t("2026/12/02 08:00:02.000")
+    s = c.summary()
+    assert s["samples_in_timed_region"] == 2 and s["sm_mhz"] == 1470.0
+    assert s["reasons"] == ["sw_power_cap"] and s["sm_max_mhz"] == 2070.0
+    c.lines = ["garbage"]
+    assert c.summary() is None
+
+
+def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_digest", lambda: "abc123")
+    (tmp_path / "profiles" / "decode_7b_traffic.md").write_text(
+        "traffic_bytes_per_launch: 2.5e9\nsource_digest: abc123\n")
+    assert bench.recorded_traffic("7b") == 2.5e9
+    monkeypatch.setattr(bench, "source_digest", lambda: "changed")
+    assert bench.recorded_traffic("7b") is None
+    assert bench.recorded_traffic("8b") is None
+
+
+def test_oracle_baseline_on_tiny_workload():
+    from paged_kv_cache_168_gb300.workloads import make_workload
+    w = make_workload("tiny")
+    gbs, sps, desc, cores, secs = bench.oracle_sample(w, 0.05)
+    assert gbs > 0 and sps > 0 and cores >= 1 and "tiny" in desc
+
+
+def _rank(rank, world, port, out):
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        bench.barrier(world)
+        out[rank] = bench.reduce_max(10.0 + rank, world, torch.device("cpu"))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_max_over_ranks_with_gloo():
+    with socket.socket() as sck:
+        sck.bind(("127.0.0.1", 0))
+        port = sck.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert dict(out) == {0: 11.0, 1: 11.0}
+
+
+def test_dist_env_defaults(monkeypatch):
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.dist_env() == (1, 0, 0)
+    assert bench.reduce_max(3.5, 1, None) == 3.5

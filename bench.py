@@ -349,7 +349,7 @@ def run_gpu(args):
             "config": {"workload": DESCRIPTIONS[args.workload] + (f" (first {args.seqs} sequences)" if args.seqs else ""),
                        "global_batch": w.cfg.num_seqs * world,
                        "max_context_len": w.max_context_len, "tokens_in_context": int(w.context_lens_np.sum()),
-                       "partition_size": _lib.decode_partition_size(args.partition_size),
+                       "partition_size": _lib.decode_partition_size(args.partition_size, w.max_context_len),
                        "parallelism": f"replicas{world}",
                        "l2": f"inputs larger than L2: {w.kv_cache.numel() * 2 / 1e9:.2f} GB pool, "
                              f"{nbytes['decode_kv'] / 1e9:.2f} GB of KV read per step"},

@@ -125,12 +125,14 @@ pa_status pa_reshape_and_cache(void* kv_cache, const pa_cache_desc* desc, int32_
                                int32_t num_tokens, uint32_t* dev_err, void* stream);
 
 /* Workspace bytes pa_decode needs for these shapes (0 when no sequence can span
- * more than one partition).  partition_size 0 selects the default (512 tokens). */
+ * more than one partition).  partition_size 0 selects the default
+ * (pa_decode_partition_size). */
 size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
                                  int32_t max_context_len, int32_t partition_size);
 
-/* The partition size pa_decode uses for `partition_size` (0 -> default). */
-int32_t pa_decode_partition_size(int32_t partition_size);
+/* The partition size pa_decode uses: `partition_size` itself when > 0, else the
+ * default for this max_context_len (512 tokens, or 1024 above 32768 tokens). */
+int32_t pa_decode_partition_size(int32_t partition_size, int32_t max_context_len);
 
 /* Paged decode attention: one query token per sequence.
  * For sequence s and query head h (kv head = h / (num_q_heads / num_kv_heads)):

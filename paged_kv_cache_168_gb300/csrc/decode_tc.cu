@@ -25,13 +25,16 @@
 //               per-stage metadata travels with the stage's mbarrier.
 //   warp 1      MMA issuer (one lane): QK(t) and PV(t) each issued as soon as
 //               their inputs are ready (polled, bounded).
-//   warps 2-5   softmax (thread = TMEM lane): tile max across the 128 rows,
-//               p = 2^(s - m) in fp32, written as two operands in the cache type,
-//               p_hi = round(p) and p_lo = round(p - p_hi); the PV product is
-//               issued for both into the same accumulator, so the weights reach
-//               the tensor core with ~16 significant bits even for bf16.  Then
-//               O^T of the previous tile is folded into registers with the
-//               online-softmax correction.
+//   warps 2-5   softmax (thread = TMEM lane = token row): tile max across the
+//               128 rows, p = 2^(s - m) in fp32, written in the cache type as
+//               p_hi = round(p) and p_lo = round(p - p_hi) side by side in one
+//               P^T operand (N = 16, or 32 at 16 heads), so one PV product gives
+//               O_hi and O_lo and the weights reach the tensor core with ~16
+//               significant bits even for bf16.  At an item's end they also
+//               reduce the normaliser.
+//   warps 6-9   output (thread = TMEM lane = head dim): fold O_hi + O_lo of
+//               each tile into registers with the online-softmax correction the
+//               softmax warps hand over, and write the item's result.
 // Every wait is bounded; a timeout sets PA_DEVERR_TIMEOUT and ends the CTA.
 #include <math.h>
 
@@ -50,9 +53,9 @@ constexpr int kTileBytes = kTile * 2 * kD * 2;     // K + V of 128 tokens: 64 Ki
 constexpr int kGroupBytes = 8 * 2 * kD * 2;        // one 8-token group: 4 KiB
 constexpr int kN = 16;                             // MMA N: query heads, zero-padded
 constexpr int kQBytes = kN * kD * 2;               // 4 KiB
-constexpr int kPBytes = kTile * kN * 2;            // 4 KiB per P^T operand (hi or lo)
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 64;                 // S0 S1 | O0 O1, 16 columns each
+constexpr int kPBytes = kTile * 32 * 2;            // P^T operand: 128 tokens x up to 32 columns (8 KiB)
+constexpr int kThreads = 320;                      // producer, MMA, 4 softmax warps, 4 output warps
+constexpr uint32_t kTmemCols = 128;                // S0 S1 (16 columns each) | O0 O1 (32 columns each)
 constexpr uint32_t kFull = 0xffffffffu;
 
 struct TileMeta {
@@ -65,7 +68,13 @@ struct Shared {
   uint64_t full[NS], empty[NS];
   uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2], q_free[2];
   uint64_t max_bar[2], sum_bar;   // softmax-warp exchanges (bounded waits, unlike bar.sync)
+  uint64_t c_full[2], c_free[2];  // softmax -> output warps: per-tile hand-off ring
   TileMeta meta[NS];
+  struct Handoff {                // what the output warps need for tile t (ring slot t & 1)
+    TileMeta meta;
+    float corr[kN];               // 2^(m_{t-1} - m_t) per head
+    float m_fin[kN], L[kN];       // item maximum and normaliser, valid when meta.last
+  } hand[2];
   float red_max[2][4][kN];
   float red_sum[4][kN];
   uint32_t tmem_base;
@@ -90,6 +99,10 @@ __device__ void warp_zero_rows(const DecodeParams& p, int s, int kvh, int lane) 
 
 template <typename T, int G, int NS>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
+  // P^T holds p_hi for the G heads in columns [0, HG) and p_lo in [HG, 2 HG):
+  // one PV product (N = 2 HG) yields both halves of O^T.
+  constexpr int HG = G < 8 ? 8 : G;
+  constexpr int NPV = 2 * HG;
   __shared__ Shared<NS> sh;
   extern __shared__ __align__(1024) uint8_t dyn_raw[];
   const uint32_t raw_s = smem_u32(dyn_raw);
@@ -97,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   uint8_t* stages = dyn;
   uint8_t* qbuf = dyn + NS * kTileBytes;
   uint8_t* pbuf = qbuf + 2 * kQBytes;
-  int* pre = reinterpret_cast<int*>(pbuf + 4 * kPBytes);   // pbuf: 2 x (p_hi, p_lo)
+  int* pre = reinterpret_cast<int*>(pbuf + 2 * kPBytes);   // pbuf: 2 buffers of [p_hi | p_lo]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.num_seqs, Hkv = p.num_kv_heads, bs = p.block_size;
@@ -118,6 +131,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       mbar_init(&sh.o_free[i], 4);
       mbar_init(&sh.q_free[i], 1);
       mbar_init(&sh.max_bar[i], 4);
+      mbar_init(&sh.c_full[i], 4);
+      mbar_init(&sh.c_free[i], 4);
     }
     mbar_init(&sh.sum_bar, 4);
     sh.abort_flag = 0;
@@ -150,32 +165,48 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     if (lane == 0) pre[0] = 0;
     __syncwarp();
     const int total = carry * Hkv;
-    int tile_seq = 0, item_seq = 0;
-    bool aborted = false;
-    for (int it = blockIdx.x; it < total && !aborted; it += gridDim.x) {
-      const int j = it / Hkv, kvh = it - (it / Hkv) * Hkv;
+    const int P = p.partition_size;
+    constexpr int kQChunks = (G * 16 + 31) / 32;
+    // The next item's independent loads (context length, its first 32 block ids,
+    // the query rows) are issued while the current item streams, so an item's
+    // set-up never waits on a global-memory round trip.
+    struct Item {
+      int s, kvh, part, ctx, id_lane;
+      uint4 qv[kQChunks];
+    };
+    auto fetch = [&](int it) {
+      Item r;
+      const int j = it / Hkv;
+      r.kvh = it - j * Hkv;
       int lo = 0, hi = S - 1;   // last sequence whose first item index is <= j
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (pre[mid] <= j) lo = mid;
         else hi = mid - 1;
       }
-      const int s = lo, part = j - pre[s];
-      const int P = p.partition_size;
-      const int jb = part * (P / bs);                      // first logical block of the partition
-      const int32_t* row = p.block_tables + (int64_t)s * p.bt_stride + jb;
-      // issue the item's independent loads together: context length, the first
-      // 32 block ids of the partition, and the query rows
-      const int ctx = p.context_lens[s];
-      const int id_lane = (lane < P / bs && jb + lane < p.bt_stride) ? row[lane] : 0;
-      constexpr int kQChunks = (G * 16 + 31) / 32;
-      const T* qsrc = static_cast<const T*>(p.q) + (int64_t)s * p.q_seq_stride + (int64_t)kvh * G * kD;
-      uint4 qv[kQChunks];
+      r.s = lo;
+      r.part = j - pre[lo];
+      const int jb = r.part * (P / bs);
+      r.ctx = p.context_lens[r.s];
+      r.id_lane = (lane < P / bs && jb + lane < p.bt_stride) ? p.block_tables[(int64_t)r.s * p.bt_stride + jb + lane] : 0;
+      const T* qsrc = static_cast<const T*>(p.q) + (int64_t)r.s * p.q_seq_stride + (int64_t)r.kvh * G * kD;
 #pragma unroll
       for (int k = 0; k < kQChunks; ++k) {
         const int c = lane + 32 * k;
-        if (c < G * 16) qv[k] = *reinterpret_cast<const uint4*>(qsrc + (c >> 4) * kD + (c & 15) * 8);
+        r.qv[k] = (c < G * 16) ? *reinterpret_cast<const uint4*>(qsrc + (c >> 4) * kD + (c & 15) * 8)
+                               : make_uint4(0, 0, 0, 0);
       }
+      return r;
+    };
+    int tile_seq = 0, item_seq = 0;
+    bool aborted = false;
+    Item nxt;
+    if (blockIdx.x < total) nxt = fetch(blockIdx.x);
+    for (int it = blockIdx.x; it < total && !aborted; it += gridDim.x) {
+      const Item cur = nxt;
+      if (it + (int)gridDim.x < total) nxt = fetch(it + gridDim.x);
+      const int s = cur.s, kvh = cur.kvh, part = cur.part, ctx = cur.ctx, id_lane = cur.id_lane;
+      const int32_t* row = p.block_tables + (int64_t)s * p.bt_stride + part * (P / bs);
       if (ctx_invalid(p, ctx)) {
         warp_zero_rows<T, G>(p, s, kvh, lane);
         if (lane == 0) report(p.dev_err, PA_DEVERR_CONTEXT);
@@ -218,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           if (c < G * 16) {
             const int n = c >> 4, cc = c & 15, atom = cc >> 3, piece = cc & 7;
             *reinterpret_cast<uint4*>(qb + (atom * 2 + (n >> 3)) * 1024 + (n & 7) * 128 + ((piece ^ (n & 7)) << 4)) =
-                qv[k];
+                cur.qv[k];
           }
         }
         tc::fence_proxy_async_smem();
@@ -276,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     // for the other stream, so a stage is released right after its own PV.
     if (lane == 0) {
       const uint32_t id_qk = tc::idesc_f16(128, kN, kBF16, false, false);
-      const uint32_t id_pv = tc::idesc_f16(128, kN, kBF16, true, true);
+      const uint32_t id_pv = tc::idesc_f16(128, NPV, kBF16, true, true);
       int qk = 0, pv = 0, end = 0x7fffffff;
       uint32_t idle = 0;
       bool ok = true;
@@ -312,14 +343,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             tc::fence_after_sync();
             const int slot = pv % NS;
             const int valid = sh.meta[slot].valid;   // the stage is not refilled before this PV completes
-            const uint32_t st = smem_u32(stages + slot * kTileBytes), pa = smem_u32(pbuf + pb * 2 * kPBytes);
+            const uint32_t st = smem_u32(stages + slot * kTileBytes), pa = smem_u32(pbuf + pb * kPBytes);
             const int nsteps = (valid + 15) >> 4;
-            for (int half = 0; half < 2; ++half)      // p_hi, then p_lo into the same accumulator
-              for (int kk = 0; kk < nsteps; ++kk)
-                tc::mma_f16(tmem + 32 + pb * 16,
-                            tc::smem_desc(st + kk * 8192 + 2048, 1024, kGroupBytes, tc::kSwizzle128B),
-                            tc::smem_desc(pa + half * kPBytes + kk * 512, 256, 128, tc::kSwizzleNone), id_pv,
-                            (half | kk) > 0);
+            for (int kk = 0; kk < nsteps; ++kk)
+              tc::mma_f16(tmem + 32 + pb * 32,
+                          tc::smem_desc(st + kk * 8192 + 2048, 1024, kGroupBytes, tc::kSwizzle128B),
+                          tc::smem_desc(pa + kk * (NPV / 8) * 256, (NPV / 8) * 128, 128, tc::kSwizzleNone), id_pv,
+                          kk > 0);
             tc::commit(&sh.o_full[pb]);
             tc::commit(&sh.empty[slot]);
             ++pv;
@@ -339,161 +369,203 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       }
     }
     __syncwarp();
-  } else {
-    // =================================================================== softmax warps
-    // Iteration t: probabilities of tile t first (so the tensor core can run
-    // PV(t-1) meanwhile), then fold O^T of tile t-1 into the accumulators and,
-    // if t-1 ended its item, write that item's result.
+  } else if (warp < 6) {
+    // =================================================================== softmax warps (2-5)
+    // Tile t: S^T -> tile maxima -> P^T (hi, lo) for the PV product; at the end
+    // of an item, the normaliser.  Hands per-tile factors to the output warps.
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;   // TMEM lane: token row of S^T, dim row of O^T
+    const int row = quarter * 32 + lane;   // TMEM lane = token row of S^T
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-    float m[G], lp[G], acc[G], corr[G], corr_prev[G], m_fin[G], lp_fin[G];
+    float m[G], lp[G];
 #pragma unroll
     for (int n = 0; n < G; ++n) {
       m[n] = -INFINITY;
       lp[n] = 0.f;
-      acc[n] = 0.f;
-      corr[n] = 0.f;
-      corr_prev[n] = 0.f;
-      m_fin[n] = -INFINITY;
-      lp_fin[n] = 0.f;
     }
-    TileMeta prev;
-    prev.s = -1;
     int tile_seq = 0, sum_uses = 0;
     bool ok = true;
     while (true) {
       const int slot = tile_seq % NS;
       if (!mbar_wait(&sh.full[slot], (tile_seq / NS) & 1)) { ok = false; break; }
       const TileMeta mt = sh.meta[slot];
-      // state of the item that tile t-1 finishes (if it does)
+      const int hb = tile_seq & 1;
+      if (mt.s < 0 || sh.abort_flag) {
+        // tell the output warps there is no more work
+        if (tile_seq >= 2 && !mbar_wait(&sh.c_free[hb], ((tile_seq >> 1) - 1) & 1)) { ok = false; break; }
+        if (row == 0) sh.hand[hb].meta.s = -1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.c_full[hb]);
+        break;
+      }
+      const int sb = tile_seq & 1;
+      if (!mbar_wait(&sh.s_full[sb], (tile_seq >> 1) & 1)) { ok = false; break; }
+      tc::fence_after_sync();
+      float sv[16];
+      tc::tmem_ld16(lane_addr + sb * 16, sv);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.s_free[sb]);
+      const bool rv = row < mt.valid;
+      float x[G], corr[G];
 #pragma unroll
-      for (int n = 0; n < G; ++n) corr_prev[n] = corr[n];
-      if (prev.s >= 0 && (prev.last || mt.s < 0)) {
+      for (int n = 0; n < G; ++n) {
+        x[n] = rv ? sv[n] * p.scale_log2 : -INFINITY;
+        float v = x[n];
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o2));
+        if (lane == 0) sh.red_max[hb][quarter][n] = v;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.max_bar[hb]);
+      if (!mbar_wait(&sh.max_bar[hb], (tile_seq >> 1) & 1)) { ok = false; break; }
+#pragma unroll
+      for (int n = 0; n < G; ++n) {
+        const float (*rm)[kN] = sh.red_max[hb];
+        const float mx = fmaxf(fmaxf(rm[0][n], rm[1][n]), fmaxf(rm[2][n], rm[3][n]));
+        const float mn = fmaxf(m[n], mx);
+        corr[n] = (m[n] == -INFINITY) ? 0.f : exp2f(m[n] - mn);
+        m[n] = mn;
+      }
+      float pr[G];
+#pragma unroll
+      for (int n = 0; n < G; ++n) {
+        pr[n] = rv ? exp2f(x[n] - m[n]) : 0.f;
+        lp[n] = fmaf(lp[n], corr[n], pr[n]);
+      }
+      uint32_t pk[NPV / 2];   // [p_hi of heads 0..HG-1 | p_lo of heads 0..HG-1], two per word
+#pragma unroll
+      for (int n2 = 0; n2 < HG; n2 += 2) {
+        const float a = (n2 < G) ? pr[n2] : 0.f, b = (n2 + 1 < G) ? pr[n2 + 1] : 0.f;
+        pk[n2 >> 1] = Elem<T>::pack2(a, b);
+        const float2 r = Elem<T>::to_float2(pk[n2 >> 1]);
+        pk[(HG + n2) >> 1] = Elem<T>::pack2(a - r.x, b - r.y);
+      }
+      // P^T buffer hb was last read by PV(t - 2): wait for it to complete
+      if (tile_seq >= 2 && !mbar_wait(&sh.o_full[hb], ((tile_seq - 2) >> 1) & 1)) { ok = false; break; }
+      // MN-major without swizzle: core matrix = 8 tokens x 8 columns (128 B);
+      // column chunks 128 B apart, 8-token groups (NPV / 8) * 128 B apart
+      uint8_t* prow = pbuf + hb * kPBytes + (row >> 3) * (NPV / 8) * 128 + (row & 7) * 16;
+#pragma unroll
+      for (int c = 0; c < NPV / 8; ++c)
+        *reinterpret_cast<uint4*>(prow + c * 128) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      // V rows of tokens past the context inside the last 16-token MMA step
+      // must not hold NaN/Inf (0 * NaN = NaN): zero them.
+      if (!rv && row < ((mt.valid + 15) & ~15)) {
+        uint8_t* vrow = stages + slot * kTileBytes + (row >> 3) * kGroupBytes + 2048 + (row & 7) * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vrow + 1024 + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.p_full[hb]);
+      // item end: normaliser L = sum over the 128 rows of the running sums
+      float L[G];
+      if (mt.last) {
 #pragma unroll
         for (int n = 0; n < G; ++n) {
-          m_fin[n] = m[n];
-          lp_fin[n] = lp[n];
+          float v = lp[n];
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) v += __shfl_xor_sync(kFull, v, o2);
+          if (lane == 0) sh.red_sum[quarter][n] = v;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.sum_bar);
+        if (!mbar_wait(&sh.sum_bar, sum_uses & 1)) { ok = false; break; }
+        ++sum_uses;
+#pragma unroll
+        for (int n = 0; n < G; ++n)
+          L[n] = sh.red_sum[0][n] + sh.red_sum[1][n] + sh.red_sum[2][n] + sh.red_sum[3][n];
+      }
+      // hand-off to the output warps
+      if (tile_seq >= 2 && !mbar_wait(&sh.c_free[hb], ((tile_seq >> 1) - 1) & 1)) { ok = false; break; }
+      if (row == 0) {
+        sh.hand[hb].meta = mt;
+#pragma unroll
+        for (int n = 0; n < G; ++n) {
+          sh.hand[hb].corr[n] = corr[n];
+          if (mt.last) {
+            sh.hand[hb].m_fin[n] = m[n];
+            sh.hand[hb].L[n] = L[n];
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.c_full[hb]);
+      if (mt.last) {
+#pragma unroll
+        for (int n = 0; n < G; ++n) {
           m[n] = -INFINITY;
           lp[n] = 0.f;
         }
       }
-
-      // ---- 1. S^T of tile t -> probabilities P^T (hi and lo parts)
-      if (mt.s >= 0) {
-        const int sb = tile_seq & 1;
-        if (!mbar_wait(&sh.s_full[sb], (tile_seq >> 1) & 1)) { ok = false; break; }
-        tc::fence_after_sync();
-        float sv[16];
-        tc::tmem_ld16(lane_addr + sb * 16, sv);
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.s_free[sb]);
-        const bool rv = row < mt.valid;
-        float x[G];
+      ++tile_seq;
+    }
+    if (!ok && lane == 0) {
+      report(p.dev_err, PA_DEVERR_TIMEOUT);
+      sh.abort_flag = 1;
+    }
+  } else {
+    // =================================================================== output warps (6-9)
+    // Tile t: O^T -> acc = acc * corr_t + O_t (thread = TMEM lane = head dim);
+    // at the end of an item, write out = acc / L (or the partition's partials).
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    float acc[G];
 #pragma unroll
-        for (int n = 0; n < G; ++n) {
-          x[n] = rv ? sv[n] * p.scale_log2 : -INFINITY;
-          float v = x[n];
+    for (int n = 0; n < G; ++n) acc[n] = 0.f;
+    int tile_seq = 0;
+    bool ok = true;
+    while (true) {
+      const int hb = tile_seq & 1;
+      if (!mbar_wait(&sh.c_full[hb], (tile_seq >> 1) & 1)) { ok = false; break; }
+      const TileMeta mt = sh.hand[hb].meta;
+      if (mt.s < 0) break;
+      float corr[G], m_fin[G], L[G];
 #pragma unroll
-          for (int o2 = 16; o2 > 0; o2 >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o2));
-          if (lane == 0) sh.red_max[tile_seq & 1][quarter][n] = v;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.max_bar[tile_seq & 1]);
-        if (!mbar_wait(&sh.max_bar[tile_seq & 1], (tile_seq >> 1) & 1)) { ok = false; break; }
-#pragma unroll
-        for (int n = 0; n < G; ++n) {
-          const float (*rm)[kN] = sh.red_max[tile_seq & 1];
-          const float mx = fmaxf(fmaxf(rm[0][n], rm[1][n]), fmaxf(rm[2][n], rm[3][n]));
-          const float mn = fmaxf(m[n], mx);
-          corr[n] = (m[n] == -INFINITY) ? 0.f : exp2f(m[n] - mn);
-          m[n] = mn;
-        }
-        float pr[G];
-#pragma unroll
-        for (int n = 0; n < G; ++n) {
-          pr[n] = rv ? exp2f(x[n] - m[n]) : 0.f;
-          lp[n] = fmaf(lp[n], corr[n], pr[n]);
-        }
-        uint32_t hi[kN / 2], lo[kN / 2];
-#pragma unroll
-        for (int n2 = 0; n2 < kN; n2 += 2) {
-          const float a = (n2 < G) ? pr[n2] : 0.f, b = (n2 + 1 < G) ? pr[n2 + 1] : 0.f;
-          hi[n2 >> 1] = Elem<T>::pack2(a, b);
-          const float2 r = Elem<T>::to_float2(hi[n2 >> 1]);
-          lo[n2 >> 1] = Elem<T>::pack2(a - r.x, b - r.y);
-        }
-        uint8_t* prow = pbuf + (tile_seq & 1) * 2 * kPBytes + (row >> 3) * 256 + (row & 7) * 16;
-        *reinterpret_cast<uint4*>(prow) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(prow + 128) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-        *reinterpret_cast<uint4*>(prow + kPBytes) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        *reinterpret_cast<uint4*>(prow + kPBytes + 128) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-        // V rows of tokens past the context inside the last 16-token MMA step
-        // must not hold NaN/Inf (0 * NaN = NaN): zero them.
-        if (!rv && row < ((mt.valid + 15) & ~15)) {
-          uint8_t* vrow = stages + slot * kTileBytes + (row >> 3) * kGroupBytes + 2048 + (row & 7) * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(vrow + 1024 + c * 16) = make_uint4(0, 0, 0, 0);
-          }
-        }
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.p_full[tile_seq & 1]);
+      for (int n = 0; n < G; ++n) {
+        corr[n] = sh.hand[hb].corr[n];
+        m_fin[n] = sh.hand[hb].m_fin[n];
+        L[n] = sh.hand[hb].L[n];
       }
-
-      // ---- 2. O^T of tile t-1: online-softmax correction; finish its item
-      if (prev.s >= 0) {
-        const int seq = tile_seq - 1, pb = seq & 1;
-        if (!mbar_wait(&sh.o_full[pb], (seq >> 1) & 1)) { ok = false; break; }
-        tc::fence_after_sync();
-        float o[16];
-        tc::tmem_ld16(lane_addr + 32 + pb * 16, o);
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.o_free[pb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.c_free[hb]);
+      if (!mbar_wait(&sh.o_full[hb], (tile_seq >> 1) & 1)) { ok = false; break; }
+      tc::fence_after_sync();
+      float o[2][16];
+      tc::tmem_ld16(lane_addr + 32 + hb * 32, o[0]);
+      if (NPV > 16) tc::tmem_ld16(lane_addr + 32 + hb * 32 + 16, o[1]);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.o_free[hb]);
 #pragma unroll
-        for (int n = 0; n < G; ++n) acc[n] = fmaf(acc[n], corr_prev[n], o[n]);
-        if (prev.last) {
-          float L[G];
+      for (int n = 0; n < G; ++n) {
+        const float hi_part = o[n >> 4][n & 15], lo_part = o[(HG + n) >> 4][(HG + n) & 15];
+        acc[n] = fmaf(acc[n], corr[n], hi_part + lo_part);
+      }
+      if (mt.last) {
+        const int64_t h0 = (int64_t)mt.s * p.num_q_heads + mt.kvh * G;
+        if (mt.n_parts == 1) {
+          T* out = static_cast<T*>(p.out);
+#pragma unroll
+          for (int n = 0; n < G; ++n) out[(h0 + n) * kD + row] = Elem<T>::from_float(acc[n] / L[n]);
+        } else {
 #pragma unroll
           for (int n = 0; n < G; ++n) {
-            float v = lp_fin[n];
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) v += __shfl_xor_sync(kFull, v, o2);
-            if (lane == 0) sh.red_sum[quarter][n] = v;
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.sum_bar);
-          if (!mbar_wait(&sh.sum_bar, sum_uses & 1)) { ok = false; break; }
-          ++sum_uses;
-#pragma unroll
-          for (int n = 0; n < G; ++n)
-            L[n] = sh.red_sum[0][n] + sh.red_sum[1][n] + sh.red_sum[2][n] + sh.red_sum[3][n];
-          const int64_t h0 = (int64_t)prev.s * p.num_q_heads + prev.kvh * G;
-          if (prev.n_parts == 1) {
-            T* out = static_cast<T*>(p.out);
-#pragma unroll
-            for (int n = 0; n < G; ++n) out[(h0 + n) * kD + row] = Elem<T>::from_float(acc[n] / L[n]);
-          } else {
-#pragma unroll
-            for (int n = 0; n < G; ++n) {
-              const int64_t r = (h0 + n) * p.max_parts + prev.part;
-              p.ws_o[r * kD + row] = acc[n];
-              if (row == 0) {
-                p.ws_ml[r * 2 + 0] = m_fin[n];
-                p.ws_ml[r * 2 + 1] = L[n];
-              }
+            const int64_t r = (h0 + n) * p.max_parts + mt.part;
+            p.ws_o[r * kD + row] = acc[n];
+            if (row == 0) {
+              p.ws_ml[r * 2 + 0] = m_fin[n];
+              p.ws_ml[r * 2 + 1] = L[n];
             }
           }
-#pragma unroll
-          for (int n = 0; n < G; ++n) acc[n] = 0.f;
         }
+#pragma unroll
+        for (int n = 0; n < G; ++n) acc[n] = 0.f;
       }
-      if (mt.s < 0 || sh.abort_flag) break;
-      prev = mt;
       ++tile_seq;
     }
     if (!ok && lane == 0) {
@@ -513,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 
 template <typename T, int G, int NS>
 cudaError_t launch_typed(const DecodeParams& p, int num_sms, cudaStream_t stream) {
-  const size_t smem = 1024 + (size_t)NS * kTileBytes + 2 * kQBytes + 4 * kPBytes + (size_t)(p.num_seqs + 1) * 4;
+  const size_t smem = 1024 + (size_t)NS * kTileBytes + 2 * kQBytes + 2 * kPBytes + (size_t)(p.num_seqs + 1) * 4;
   auto kern = decode_tc_kernel<T, G, NS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -163,13 +163,16 @@ pa_status pa_reshape_and_cache(void* kv_cache, const pa_cache_desc* desc, int32_
   return e == cudaSuccess ? PA_OK : cuda_fail(e, "reshape_and_cache launch");
 }
 
-int32_t pa_decode_partition_size(int32_t partition_size) {
-  return partition_size > 0 ? partition_size : kDefaultPartition;
+int32_t pa_decode_partition_size(int32_t partition_size, int32_t max_context_len) {
+  if (partition_size > 0) return partition_size;
+  // Long contexts use longer partitions: each partition writes (D + 2) floats per
+  // query head, which at 8 query heads per kv head is 2G/P of the KV bytes.
+  return max_context_len > 32768 ? 2 * kDefaultPartition : kDefaultPartition;
 }
 
 size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
                                  int32_t max_context_len, int32_t partition_size) {
-  const int64_t P = pa_decode_partition_size(partition_size);
+  const int64_t P = pa_decode_partition_size(partition_size, max_context_len);
   if (num_seqs <= 0 || num_q_heads <= 0 || head_size <= 0 || max_context_len <= 0 || P <= 0) return 0;
   const int64_t parts = (max_context_len + P - 1) / P;
   if (parts <= 1) return 0;
@@ -204,7 +207,7 @@ pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* 
     return fail(PA_ERR_INVALID_ARG, "q_seq_stride must be >= num_q_heads*head_size and a multiple of 8");
   if (block_table_stride <= 0) return fail(PA_ERR_INVALID_ARG, "block_table_stride %d", block_table_stride);
   if (max_context_len <= 0) return fail(PA_ERR_INVALID_ARG, "max_context_len %d", max_context_len);
-  const int32_t P = pa_decode_partition_size(partition_size);
+  const int32_t P = pa_decode_partition_size(partition_size, max_context_len);
   if (P % 128 || P < 128 || P > 8192)
     return fail(PA_ERR_INVALID_ARG, "partition_size %d must be a multiple of 128 in [128, 8192]", P);
   if (!(scale > 0.f) || scale != scale) return fail(PA_ERR_INVALID_ARG, "scale must be a positive number");

@@ -63,7 +63,7 @@ class DecodeStep:
             n += -(-w.swap_out_pairs.shape[0] // per) + -(-w.swap_in_pairs.shape[0] // per)
         if w.copy_pairs.shape[0]:
             n += -(-w.copy_pairs.shape[0] // per)
-        P = _lib.decode_partition_size(self.partition_size)
+        P = _lib.decode_partition_size(self.partition_size, w.max_context_len)
         n += 1 + (1 if -(-w.max_context_len // P) > 1 else 0)   # decode (+ merge)
         return n
 

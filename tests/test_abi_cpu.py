@@ -60,10 +60,12 @@ def test_library_layout_agrees_with_oracle_layout(lib, bs, D, dtype):
 
 
 def test_workspace_sizing(lib):
-    assert _lib.decode_partition_size(0) == 512
+    assert _lib.decode_partition_size(0, 4096) == 512 and _lib.decode_partition_size(0, 131072) == 1024
+    assert _lib.decode_partition_size(256, 131072) == 256
     assert _lib.decode_workspace_bytes(64, 32, 128, 512) == 0        # one partition: no workspace
     assert _lib.decode_workspace_bytes(64, 32, 128, 4096) == 64 * 32 * 8 * 130 * 4
     assert _lib.decode_workspace_bytes(8, 64, 128, 131072, 1024) == 8 * 64 * 128 * 130 * 4
+    assert _lib.decode_workspace_bytes(8, 64, 128, 131072) == 8 * 64 * 128 * 130 * 4
 
 
 def test_status_strings(lib):

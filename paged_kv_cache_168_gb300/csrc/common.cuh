@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "pagedkv.h"
 
 namespace pkv {
@@ -56,6 +58,28 @@ template <> struct Elem<__nv_bfloat16> {
     return *reinterpret_cast<uint32_t*>(&h);
   }
 };
+
+// ------------------------------------------------------------------ launch set-up
+// Raise kernel Kern's dynamic shared-memory limit once per device (the
+// attribute is per function and device).  Doing it once keeps later launches
+// free of non-stream runtime calls, so they can be captured into CUDA graphs.
+// The size recorded is the largest requested so far.
+template <auto Kern>
+cudaError_t set_smem_attribute_once(size_t bytes) {
+  static std::atomic<size_t> done[64];   // one set per kernel (Kern is a template argument)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (done[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) {
+    size_t cur = done[dev].load();
+    while (cur < bytes && !done[dev].compare_exchange_weak(cur, bytes)) {
+    }
+  }
+  return e;
+}
 
 // ------------------------------------------------------------------ error word
 __device__ __forceinline__ void report(uint32_t* dev_err, uint32_t bits) {

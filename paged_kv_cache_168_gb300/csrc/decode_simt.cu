@@ -400,7 +400,7 @@ static cudaError_t launch_typed(const DecodeParams& p, cudaStream_t stream) {
   const int max_blk = (p.partition_size + p.block_size - 1) / p.block_size + 1;
   const size_t smem = (size_t)C::kStages * C::kStageBytes + (size_t)C::kRedFloats * 4 + (size_t)max_blk * 4;
   auto kern = decode_simt_kernel<T, D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_attribute_once<decode_simt_kernel<T, D, G>>(smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.max_parts, (unsigned)p.num_kv_heads, (unsigned)p.num_seqs);
   kern<<<grid, C::kThreads, smem, stream>>>(p);

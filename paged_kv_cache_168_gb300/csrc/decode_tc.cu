@@ -587,7 +587,7 @@ template <typename T, int G, int NS>
 cudaError_t launch_typed(const DecodeParams& p, int num_sms, cudaStream_t stream) {
   const size_t smem = 1024 + (size_t)NS * kTileBytes + 2 * kQBytes + 2 * kPBytes + (size_t)(p.num_seqs + 1) * 4;
   auto kern = decode_tc_kernel<T, G, NS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_attribute_once<decode_tc_kernel<T, G, NS>>(smem);
   if (e != cudaSuccess) return e;
   kern<<<num_sms, kThreads, smem, stream>>>(p);
   return cudaGetLastError();

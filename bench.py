@@ -48,6 +48,8 @@ DESCRIPTIONS = {
            "context_lens ~U[32768,131072]",
     "beam": "beam/shared-prefix decode: 32 groups x 4 beams, 32 q/8 kv heads, head_size 128, block_size 16, "
             "bf16, 2048-token shared prompt, tails ~U[0,256], CoW copy_blocks + 10% swap_blocks",
+    "7b_bs1": "Llama-2-7B-shaped decode layer with token-granular paging (block_size 1): 64 seqs, 32/32 heads, "
+              "head_size 128, fp16, context_lens ~U[512,4096]",
 }
 
 

@@ -82,7 +82,8 @@ typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
 #define PA_DEVERR_CONTEXT 0x4u   /* context_lens[s] > block_table_stride*block_size or > max_context_len */
 #define PA_DEVERR_TIMEOUT 0x8u   /* a bounded wait inside a kernel ran out (the item was abandoned) */
 
-/* Geometry of a cache pool.  head_size in {64, 128}; block_size in {8, 16, 32};
+/* Geometry of a cache pool.  head_size in {64, 128}; block_size in {1, 2, 4, 8, 16, 32}
+ * (block_size 1 is token-granular paging);
  * dtype a pa_dtype.  layer_stride_bytes = distance between consecutive layers
  * (0 means layers are packed: pa_cache_bytes(desc)). */
 typedef struct pa_cache_desc {
@@ -157,8 +158,9 @@ int32_t pa_decode_partition_size(int32_t partition_size, int32_t max_context_len
  *   workspace     device, 16-byte aligned, >= pa_decode_workspace_bytes(...);
  *                 may be NULL when that is 0.  Contents need no initialisation.
  *   dev_err       optional device uint32 error word (PA_DEVERR_* bits).
- * Supported: head_size 64 or 128, block_size 8/16/32, num_q_heads a multiple of
- * num_kv_heads with group size 1, 2, 4 or 8 (PA_ERR_UNSUPPORTED otherwise). */
+ * Supported: head_size 64 or 128, block_size 1/2/4/8/16/32, num_q_heads a
+ * multiple of num_kv_heads with group size 1, 2, 4 or 8, and 16 at head_size 128
+ * with block_size >= 8 (PA_ERR_UNSUPPORTED otherwise). */
 pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,
                     const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
                     int32_t block_table_stride, const int32_t* context_lens, int32_t num_seqs,

@@ -100,6 +100,8 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
   const int nblk = (t1 - t0 + bs - 1) / bs;
   const int64_t chunk_bytes = 2LL * bs * D * 2;
   const int blocks_per_stage = C::kStageTokens / bs;
+  const int R = bs < 8 ? bs : 8;              // token rows per atom (8, or the whole block)
+  const int atom_bytes = R * 128;
   const int n_stages = (t1 - t0 + C::kStageTokens - 1) / C::kStageTokens;
 
   if (threadIdx.x == 0) {
@@ -133,32 +135,38 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
   }
 
   if (warp == C::kConsumerWarps) {
-    // ---------------- producer: one lane issues the bulk copies
+    // ---------------- producer: lane 0 arms each stage, all lanes issue its copies
+    int issued = 0;
+    bool aborted = false;
+    for (int st = 0; st < n_stages && !aborted; ++st) {
+      const int slot = st % C::kStages;
+      if (st >= C::kStages && !mbar_wait(&empty_bar[slot], ((st / C::kStages) - 1) & 1)) {
+        aborted = true;
+        break;
+      }
+      if (flag_abort) {
+        aborted = true;
+        break;
+      }
+      const int jb = st * blocks_per_stage;
+      const int je = min(nblk, jb + blocks_per_stage);
+      if (lane == 0) mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)((je - jb) * chunk_bytes));
+      __syncwarp();
+      uint8_t* dst = stages + slot * C::kStageBytes;
+      for (int j = jb + lane; j < je; j += 32)
+        bulk_g2s(dst + (j - jb) * chunk_bytes, p.cache + ((int64_t)ids[j] * p.num_kv_heads + kvh) * chunk_bytes,
+                 (uint32_t)chunk_bytes, &full_bar[slot]);
+      issued = st + 1;
+    }
     if (lane == 0) {
-      int issued = 0;
-      for (int st = 0; st < n_stages; ++st) {
-        const int slot = st % C::kStages;
-        if (st >= C::kStages && !mbar_wait(&empty_bar[slot], ((st / C::kStages) - 1) & 1)) {
-          report(p.dev_err, PA_DEVERR_TIMEOUT);
-          flag_abort = 1;
-          break;
-        }
-        if (flag_abort) break;
-        const int jb = st * blocks_per_stage;
-        const int je = min(nblk, jb + blocks_per_stage);
-        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)((je - jb) * chunk_bytes));
-        uint8_t* dst = stages + slot * C::kStageBytes;
-        for (int j = jb; j < je; ++j)
-          bulk_g2s(dst + (j - jb) * chunk_bytes,
-                   p.cache + ((int64_t)ids[j] * p.num_kv_heads + kvh) * chunk_bytes,
-                   (uint32_t)chunk_bytes, &full_bar[slot]);
-        issued = st + 1;
+      if (aborted) {
+        report(p.dev_err, PA_DEVERR_TIMEOUT);
+        flag_abort = 1;
       }
       // never leave the CTA with copies in flight: wait (bounded) for the last
       // phase issued on every stage
       for (int st = max(0, issued - C::kStages); st < issued; ++st)
-        if (!mbar_wait(&full_bar[st % C::kStages], (st / C::kStages) & 1))
-          report(p.dev_err, PA_DEVERR_TIMEOUT);
+        if (!mbar_wait(&full_bar[st % C::kStages], (st / C::kStages) & 1)) report(p.dev_err, PA_DEVERR_TIMEOUT);
     }
     return;   // the CTA's shared memory lives until every thread has exited
   }
@@ -212,12 +220,12 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
 #pragma unroll
       for (int i = 0; i < HPW; ++i) part_dot[i] = 0.f;
       if (pos < valid) {
-        const int blk = pos / bs, tb = pos % bs, g8 = tb >> 3, r = tb & 7;
-        const uint8_t* kb = buf + blk * chunk_bytes + (g8 * 2 * A) * 1024 + r * 128 + ((j ^ r) << 4);
+        const int blk = pos / bs, tb = pos % bs, g8 = tb / R, r = tb % R;
+        const uint8_t* kb = buf + blk * chunk_bytes + (g8 * 2 * A) * atom_bytes + r * 128 + ((j ^ r) << 4);
 #pragma unroll
         for (int a = 0; a < A; ++a) {
           float kf[8];
-          load_row8<T>(kb + a * 1024, kf);
+          load_row8<T>(kb + a * atom_bytes, kf);
 #pragma unroll
           for (int i = 0; i < HPW; ++i)
 #pragma unroll
@@ -253,8 +261,8 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
     for (int k = 0; k < TPG; ++k) {
       const int pos = tw * 4 + gi + k * 4 * C::TW;
       if (pos < valid) {
-        const int blk = pos / bs, tb = pos % bs, g8 = tb >> 3, r = tb & 7;
-        const uint8_t* vb = buf + blk * chunk_bytes + ((g8 * 2 + 1) * A) * 1024 + r * 128 + ((j ^ r) << 4);
+        const int blk = pos / bs, tb = pos % bs, g8 = tb / R, r = tb % R;
+        const uint8_t* vb = buf + blk * chunk_bytes + ((g8 * 2 + 1) * A) * atom_bytes + r * 128 + ((j ^ r) << 4);
         float w[HPW];
 #pragma unroll
         for (int i = 0; i < HPW; ++i) {
@@ -264,7 +272,7 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
 #pragma unroll
         for (int a = 0; a < A; ++a) {
           float vf[8];
-          load_row8<T>(vb + a * 1024, vf);
+          load_row8<T>(vb + a * atom_bytes, vf);
 #pragma unroll
           for (int i = 0; i < HPW; ++i)
 #pragma unroll

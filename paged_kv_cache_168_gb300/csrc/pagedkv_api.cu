@@ -38,8 +38,9 @@ constexpr int kDefaultPartition = 512;
 // up to pkv::kTcMaxSeqs sequences); the CUDA-core kernel serves the rest.  The
 // environment variable PAGEDKV_DECODE_KERNEL=simt selects the CUDA-core kernel
 // wherever it applies (used to test both kernels on the same inputs).
-bool use_tensor_cores(int head_size, int group, int num_seqs) {
-  if (head_size != 128 || num_seqs > pkv::kTcMaxSeqs) return false;
+bool use_tensor_cores(int head_size, int block_size, int group, int num_seqs) {
+  // the tensor-core operands need whole 8-token swizzle atoms: block_size >= 8
+  if (head_size != 128 || block_size < 8 || num_seqs > pkv::kTcMaxSeqs) return false;
   if (group > 8) return true;
   const char* env = getenv("PAGEDKV_DECODE_KERNEL");
   return !(env && strcmp(env, "simt") == 0);
@@ -56,8 +57,9 @@ pa_status check_desc(const pa_cache_desc* d) {
   if (d->dtype != PA_F16 && d->dtype != PA_BF16) return fail(PA_ERR_INVALID_ARG, "dtype %d", d->dtype);
   if (d->head_size != 64 && d->head_size != 128)
     return fail(PA_ERR_UNSUPPORTED, "head_size %d (supported: 64, 128)", d->head_size);
-  if (d->block_size != 8 && d->block_size != 16 && d->block_size != 32)
-    return fail(PA_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", d->block_size);
+  if (d->block_size != 1 && d->block_size != 2 && d->block_size != 4 && d->block_size != 8 &&
+      d->block_size != 16 && d->block_size != 32)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d (supported: 1, 2, 4, 8, 16, 32)", d->block_size);
   const int64_t lb = block_bytes(d) * d->num_blocks;
   if (d->layer_stride_bytes != 0 && (d->layer_stride_bytes < lb || d->layer_stride_bytes % 16 != 0))
     return fail(PA_ERR_INVALID_ARG, "layer_stride_bytes %lld must be 0 or >= %lld and a multiple of 16",
@@ -193,9 +195,10 @@ pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* 
     return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
                 num_q_heads, desc->num_kv_heads);
   const int group = num_q_heads / desc->num_kv_heads;
-  if (group != 1 && group != 2 && group != 4 && group != 8 && !(group == 16 && desc->head_size == 128))
-    return fail(PA_ERR_UNSUPPORTED, "query heads per kv head %d (supported: 1, 2, 4, 8; 16 at head_size 128)",
-                group);
+  if (group != 1 && group != 2 && group != 4 && group != 8 &&
+      !(group == 16 && desc->head_size == 128 && desc->block_size >= 8))
+    return fail(PA_ERR_UNSUPPORTED,
+                "query heads per kv head %d (supported: 1, 2, 4, 8; 16 at head_size 128 with block_size >= 8)", group);
   if (desc->num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads > 65535");
   if (!out || !q || !kv_cache || !block_tables || !context_lens)
     return fail(PA_ERR_INVALID_ARG, "out, q, kv_cache, block_tables and context_lens must be non-NULL");
@@ -240,7 +243,7 @@ pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* 
                  : nullptr;
   p.dev_err = dev_err;
   cudaError_t e;
-  if (use_tensor_cores(desc->head_size, group, num_seqs)) {
+  if (use_tensor_cores(desc->head_size, desc->block_size, group, num_seqs)) {
     int dev = 0, sms = 0;
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

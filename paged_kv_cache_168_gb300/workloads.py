@@ -67,6 +67,8 @@ CONFIGS = {
         Config("70b", 3, 8, 64, 8, 128, 32, "bf16", "normal", ("uniform", 32768, 131072)),
         Config("beam", 4, 128, 32, 8, 128, 16, "bf16", "normal", ("beam", 2048, 256), beams=4,
                swap_fraction=0.10),
+        # token-granular paging (block_size 1) on the Llama-2-7B-shaped layer
+        Config("7b_bs1", 5, 64, 32, 32, 128, 1, "f16", "normal", ("uniform", 512, 4096)),
     ]
 }
 

@@ -41,10 +41,13 @@ def test_cache_bytes(lib):
     # one LLaMA-13B layer for an 8192-token request: 2 x 8192 x 40 x 128 x 2 bytes
     assert _lib.cache_bytes(d) == 2 * 8192 * 40 * 128 * 2
     assert _lib.cache_bytes(CacheDesc(10, 16, 2, 96)) == 0          # unsupported head size
+    assert _lib.cache_bytes(CacheDesc(10, 1, 2, 128)) == 10 * 2 * 2 * 128 * 2   # token-granular blocks
+    assert _lib.cache_bytes(CacheDesc(10, 3, 2, 128)) == 0          # block size must be a power of two <= 32
     assert _lib.cache_bytes(CacheDesc(0, 16, 2, 128)) == 0
 
 
-@pytest.mark.parametrize("bs,D,dtype", [(8, 64, torch.float16), (16, 128, torch.bfloat16), (32, 128, torch.float16)])
+@pytest.mark.parametrize("bs,D,dtype", [(1, 128, torch.float16), (4, 64, torch.bfloat16), (8, 64, torch.float16),
+                                        (16, 128, torch.bfloat16), (32, 128, torch.float16)])
 def test_library_layout_agrees_with_oracle_layout(lib, bs, D, dtype):
     d = CacheDesc(3, bs, 2, D, dtype)
     g = oracle.Geom(3, bs, 2, D)

@@ -37,7 +37,7 @@ def check(p, P=0, max_ctx=None, what=""):
 
 
 def ctx_cases(bs, P):
-    return [1, bs - 1, bs, bs + 1, P - 1, P, P + 1, 2 * P + 7, 3]
+    return [1, max(bs - 1, 2), bs, bs + 1, P - 1, P, P + 1, 2 * P + 7, 3]
 
 
 @pytest.fixture(params=["tc", "simt"])
@@ -52,14 +52,14 @@ def kernel(request, monkeypatch):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("bs", [1, 2, 4, 8, 16, 32])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 1), (32, 8), (64, 8), (4, 2), (16, 1)])
 def test_decode_sweep(dtype, bs, D, Hq, Hkv, kernel):
-    if D == 64 and kernel == "tc":
-        pytest.skip("head_size 64 is served by the CUDA-core kernel only")
+    if (D == 64 or bs < 8) and kernel == "tc":
+        pytest.skip("head_size 64 and block sizes below 8 are served by the CUDA-core kernel only")
     if Hq // Hkv == 16 and (D != 128 or kernel != "tc"):
-        pytest.skip("16 query heads per kv head: tensor-core kernel (head_size 128) only")
+        pytest.skip("16 query heads per kv head: tensor-core kernel (head_size 128, block_size >= 8) only")
     rng = np.random.default_rng(zlib.crc32(repr((dtype, bs, D, Hq, Hkv)).encode()))
     P = 128
     ctx = ctx_cases(bs, P)
@@ -117,7 +117,7 @@ def test_physical_placement_gives_bit_identical_output(kernel):
 
 
 def test_block_size_gives_matching_output():
-    for bs in (8, 16, 32):
+    for bs in (1, 2, 4, 8, 16, 32):
         rng = np.random.default_rng(202)
         p = Paged(rng, S=3, Hq=8, Hkv=2, D=64, bs=bs, ctx=[1, 200, 513], dtype="f16")
         check(p, P=256, what=f"bs={bs}")

@@ -102,6 +102,10 @@ def _load():
     lib.oracle_contiguous_attention.restype = None
     lib.oracle_decode.argtypes = [P, P, i64, P, G, P, i32, P, i32, i32, i32, dbl, P, i32, i32]
     lib.oracle_decode.restype = ctypes.c_int
+    lib.oracle_decode_window.argtypes = [P, P, i64, P, G, P, i32, P, i32, i32, i32, dbl, i32, i32, P, i32, i32]
+    lib.oracle_decode_window.restype = ctypes.c_int
+    lib.oracle_window_start.argtypes = [i32, i32, i32, i32]
+    lib.oracle_window_start.restype = i32
     lib.oracle_partition_stats.argtypes = [P, P, G, P, i32, i32, dbl, i32, P, P, P]
     lib.oracle_partition_stats.restype = ctypes.c_int
     lib.oracle_merge_partitions.argtypes = [P, P, P, i32, i32, P]
@@ -175,11 +179,13 @@ def contiguous_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: flo
 
 def decode(q: np.ndarray, layer: np.ndarray, geom: Geom, block_tables: np.ndarray,
            context_lens: np.ndarray, scale: float, max_context_len: int | None = None,
-           sel: np.ndarray | None = None, nthreads: int = 0):
+           sel: np.ndarray | None = None, nthreads: int = 0, window: int = 0, ring: int = 0):
     """Paged decode attention in fp64.
 
     q: uint16 [S, Hq, D].  Returns (out float64 [S, Hq, D] or [len(sel), D], error bits).
     sel: optional int32 [n, 2] list of (sequence, query head) pairs to compute.
+    window > 0 attends only positions >= ctx - window; ring > 0 reads the table
+    row as a ring of that many blocks (logical block j at entry j % ring).
     """
     q = _u16(q)
     S, Hq, D = q.shape
@@ -194,10 +200,15 @@ def decode(q: np.ndarray, layer: np.ndarray, geom: Geom, block_tables: np.ndarra
     else:
         out = np.zeros((S, Hq, D))
         nsel = 0
-    err = _load().oracle_decode(_ptr(out), _ptr(q), Hq * D, _ptr(layer), ctypes.byref(geom.c()),
-                                _ptr(bt), bt.shape[1], _ptr(cl), S, Hq, max_context_len, scale,
-                                _ptr(sel), nsel, nthreads)
+    err = _load().oracle_decode_window(_ptr(out), _ptr(q), Hq * D, _ptr(layer), ctypes.byref(geom.c()),
+                                       _ptr(bt), bt.shape[1], _ptr(cl), S, Hq, max_context_len, scale, window,
+                                       ring, _ptr(sel), nsel, nthreads)
     return out, err
+
+
+def window_start(ctx: int, block_size: int, window: int, ring: int) -> int:
+    """First position a (window, ring) decode attends for context length ctx."""
+    return _load().oracle_window_start(ctx, block_size, window, ring)
 
 
 def partition_stats(q_row: np.ndarray, layer: np.ndarray, geom: Geom, table_row: np.ndarray,

@@ -135,23 +135,46 @@ int oracle_reshape_and_cache(uint16_t* layer, const oracle_geom* g,
 
 /* ---------------- gather by block table ---------------- */
 
-/* Copy sequence tokens 0..ctx-1 of one kv head into contiguous K[ctx][D],
- * V[ctx][D] (doubles), reading token t from (block_table[t / bs], t % bs).
+/* Copy tokens t in [t0, t1) of one kv head into contiguous K[t1-t0][D],
+ * V[t1-t0][D] (doubles), reading token t from slot t % bs of block
+ * table_row[j] with j = t / bs, or j = (t / bs) % ring when the table row is a
+ * ring of `ring` blocks (sliding window; the "vLLM" block manager of the FAQ
+ * page reuses block_table[logical_idx % block_sliding_window]).
  * Returns ORC_ERR_BLOCK_ID if any needed table entry is out of range. */
-int oracle_gather(const uint16_t* layer, const oracle_geom* g, const int32_t* table_row,
-                  int32_t ctx, int32_t kv_head, double* K, double* V) {
-    for (int32_t t = 0; t < ctx; ++t) {
-        const int32_t block = table_row[t / g->block_size];
+int oracle_gather_range(const uint16_t* layer, const oracle_geom* g, const int32_t* table_row,
+                        int32_t t0, int32_t t1, int32_t ring, int32_t kv_head, double* K, double* V) {
+    for (int32_t t = t0; t < t1; ++t) {
+        const int32_t j = ring > 0 ? (t / g->block_size) % ring : t / g->block_size;
+        const int32_t block = table_row[j];
         if (block < 0 || block >= g->num_blocks) return ORC_ERR_BLOCK_ID;
         const int64_t slot = t % g->block_size;
         for (int32_t d = 0; d < g->head_size; ++d) {
-            K[(int64_t)t * g->head_size + d] =
+            K[(int64_t)(t - t0) * g->head_size + d] =
                 elem_to_double(layer[cache_offset(g, block, kv_head, 0, slot, d)], g->dtype);
-            V[(int64_t)t * g->head_size + d] =
+            V[(int64_t)(t - t0) * g->head_size + d] =
                 elem_to_double(layer[cache_offset(g, block, kv_head, 1, slot, d)], g->dtype);
         }
     }
     return 0;
+}
+
+/* All tokens 0..ctx-1 through a linear table row. */
+int oracle_gather(const uint16_t* layer, const oracle_geom* g, const int32_t* table_row,
+                  int32_t ctx, int32_t kv_head, double* K, double* V) {
+    return oracle_gather_range(layer, g, table_row, 0, ctx, 0, kv_head, K, V);
+}
+
+/* First position attended for context length ctx: the window keeps positions
+ * >= ctx - window (window > 0), and a ring of `ring` blocks only still holds
+ * positions from the start of block (ctx-1)/bs - ring + 1 on. */
+int32_t oracle_window_start(int32_t ctx, int32_t block_size, int32_t window, int32_t ring) {
+    int32_t t = 0;
+    if (window > 0 && ctx - window > t) t = ctx - window;
+    if (ring > 0) {
+        const int32_t held = ((ctx - 1) / block_size - ring + 1) * block_size;
+        if (held > t) t = held;
+    }
+    return t;
 }
 
 /* ---------------- textbook attention on contiguous arrays ---------------- */
@@ -192,11 +215,11 @@ void oracle_contiguous_attention(const double* q, const double* K, const double*
  * an out-of-range block id, gives zeros and sets an error bit.
  * If sel != NULL only the nsel (s, h) pairs listed in sel[2*i], sel[2*i+1] are
  * computed (out is then [nsel][D]).  Returns the OR of error bits. */
-int oracle_decode(double* out, const uint16_t* q, int64_t q_seq_stride, const uint16_t* layer,
-                  const oracle_geom* g, const int32_t* block_tables, int32_t bt_stride,
-                  const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
-                  int32_t max_context_len, double scale, const int32_t* sel, int32_t nsel,
-                  int32_t nthreads) {
+int oracle_decode_window(double* out, const uint16_t* q, int64_t q_seq_stride, const uint16_t* layer,
+                         const oracle_geom* g, const int32_t* block_tables, int32_t bt_stride,
+                         const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t max_context_len, double scale, int32_t window, int32_t ring,
+                         const int32_t* sel, int32_t nsel, int32_t nthreads) {
     const int32_t D = g->head_size;
     const int32_t G = num_q_heads / g->num_kv_heads;
     const int64_t items = sel ? nsel : (int64_t)num_seqs * num_q_heads;
@@ -212,26 +235,38 @@ int oracle_decode(double* out, const uint16_t* q, int64_t q_seq_stride, const ui
         for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
         const int32_t ctx = context_lens[s];
         if (ctx <= 0) continue;
-        if ((int64_t)ctx > (int64_t)bt_stride * g->block_size || ctx > max_context_len) {
+        if ((ring <= 0 && (int64_t)ctx > (int64_t)bt_stride * g->block_size) || ctx > max_context_len) {
             err |= ORC_ERR_CONTEXT;
             continue;
         }
-        double* K = (double*)malloc(sizeof(double) * (size_t)ctx * D);
-        double* V = (double*)malloc(sizeof(double) * (size_t)ctx * D);
+        const int32_t t0 = oracle_window_start(ctx, g->block_size, window, ring);
+        const int32_t n = ctx - t0;
+        double* K = (double*)malloc(sizeof(double) * (size_t)n * D);
+        double* V = (double*)malloc(sizeof(double) * (size_t)n * D);
         double* qd = (double*)malloc(sizeof(double) * (size_t)D);
-        const int e = oracle_gather(layer, g, block_tables + (int64_t)s * bt_stride, ctx, h / G, K, V);
+        const int e = oracle_gather_range(layer, g, block_tables + (int64_t)s * bt_stride, t0, ctx, ring, h / G,
+                                          K, V);
         if (e) {
             err |= e;
         } else {
             for (int32_t d = 0; d < D; ++d)
                 qd[d] = elem_to_double(q[(int64_t)s * q_seq_stride + (int64_t)h * D + d], g->dtype);
-            oracle_contiguous_attention(qd, K, V, ctx, D, scale, o);
+            oracle_contiguous_attention(qd, K, V, n, D, scale, o);
         }
         free(K);
         free(V);
         free(qd);
     }
     return err;
+}
+
+int oracle_decode(double* out, const uint16_t* q, int64_t q_seq_stride, const uint16_t* layer,
+                  const oracle_geom* g, const int32_t* block_tables, int32_t bt_stride,
+                  const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                  int32_t max_context_len, double scale, const int32_t* sel, int32_t nsel,
+                  int32_t nthreads) {
+    return oracle_decode_window(out, q, q_seq_stride, layer, g, block_tables, bt_stride, context_lens,
+                                num_seqs, num_q_heads, max_context_len, scale, 0, 0, sel, nsel, nthreads);
 }
 
 /* ---------------- split-context partitions and log-sum-exp merge ---------------- */

@@ -77,3 +77,40 @@ class Paged:
             o = torch.nn.functional.scaled_dot_product_attention(q, K, V, scale=scale)
             out[s] = o[:, 0, :].numpy()
         return out
+
+
+class RingPaged:
+    """Sequences written token by token into ring block tables (a sliding-window
+    cache): token t goes to slot t % bs of block ring_table[(t / bs) % ring], so
+    later tokens overwrite the ring's oldest block."""
+
+    def __init__(self, rng, S, Hq, Hkv, D, bs, ctx, ring, dtype="bf16", num_blocks=None):
+        self.S, self.Hq, self.Hkv, self.D, self.bs, self.dtype, self.ring = S, Hq, Hkv, D, bs, dtype, ring
+        self.ctx = np.asarray(ctx, dtype=np.int32)
+        self.num_blocks = num_blocks or S * ring + 3
+        self.geom = oracle.Geom(self.num_blocks, bs, Hkv, D, dtype)
+        self.K = [bits_to_f64(to_bits(rng.standard_normal((c, Hkv, D)), dtype), dtype) for c in self.ctx]
+        self.V = [bits_to_f64(to_bits(rng.standard_normal((c, Hkv, D)), dtype), dtype) for c in self.ctx]
+        self.q_bits = to_bits(rng.standard_normal((S, Hq, D)), dtype)
+        self.q = bits_to_f64(self.q_bits, dtype)
+        perm = rng.permutation(self.num_blocks)
+        self.tables = perm[:S * ring].reshape(S, ring).astype(np.int32)
+        self.pool = np.full(self.geom.layer_elems, NAN_BITS[dtype], dtype=np.uint16)
+        for s in range(S):
+            t = np.arange(int(self.ctx[s]))
+            slots = self.tables[s, (t // bs) % ring].astype(np.int64) * bs + t % bs
+            assert oracle.reshape_and_cache(self.pool, self.geom, to_bits(self.K[s], dtype),
+                                            to_bits(self.V[s], dtype), slots) == 0
+
+    def expected_window(self, scale, window):
+        """torch fp64 SDPA over the last `window` logical tokens of each sequence."""
+        G = self.Hq // self.Hkv
+        out = np.zeros((self.S, self.Hq, self.D))
+        for s in range(self.S):
+            c = int(self.ctx[s])
+            lo = max(0, c - window)
+            q = torch.from_numpy(self.q[s]).unsqueeze(1)
+            K = torch.from_numpy(self.K[s][lo:c]).permute(1, 0, 2).repeat_interleave(G, 0)
+            V = torch.from_numpy(self.V[s][lo:c]).permute(1, 0, 2).repeat_interleave(G, 0)
+            out[s] = torch.nn.functional.scaled_dot_product_attention(q, K, V, scale=scale)[:, 0, :].numpy()
+        return out

@@ -335,3 +335,44 @@ def test_paging_wastes_at_most_one_partial_block_per_sequence():
         assert np.all(slots - ctx <= cfg.block_size - 1)       # at most 15 tokens at block 16
         if cfg.name in ("7b", "8b", "70b", "beam"):
             assert (slots - ctx).sum() / slots.sum() < 0.04   # "under 4%" waste
+
+
+# ---------------------------------------------------------------- sliding window over ring tables
+
+def test_window_start_closed_forms():
+    assert oracle.window_start(40, 16, 0, 0) == 0
+    assert oracle.window_start(5, 16, 10, 0) == 0
+    assert oracle.window_start(40, 16, 32, 0) == 8
+    assert oracle.window_start(40, 16, 32, 3) == 8      # ring of 3 blocks holds [0, 48): the window rules
+    assert oracle.window_start(40, 16, 32, 2) == 16     # ring of ceil(32/16) blocks only holds [16, 40)
+    assert oracle.window_start(33, 16, 0, 1) == 32      # a one-block ring holds just the current block
+
+
+def test_window_covering_the_context_equals_plain_decode():
+    rng = np.random.default_rng(20)
+    p = Paged(rng, S=3, Hq=4, Hkv=2, D=64, bs=16, ctx=[5, 40, 77])
+    plain, _ = oracle.decode(p.q_bits, p.pool, p.geom, p.tables, p.ctx, 0.125)
+    wide, err = oracle.decode(p.q_bits, p.pool, p.geom, p.tables, p.ctx, 0.125, window=77)
+    assert err == 0 and np.array_equal(plain, wide)
+
+
+def test_window_of_one_token_returns_the_last_value():
+    rng = np.random.default_rng(21)
+    p = Paged(rng, S=2, Hq=4, Hkv=2, D=64, bs=8, ctx=[9, 30])
+    out, err = oracle.decode(p.q_bits, p.pool, p.geom, p.tables, p.ctx, 0.3, window=1)
+    assert err == 0
+    for s in range(2):
+        for h in range(4):
+            assert np.array_equal(out[s, h], p.V[s][p.ctx[s] - 1, h // 2])
+
+
+@pytest.mark.parametrize("bs,W", [(16, 32), (16, 20), (8, 8), (1, 5), (32, 100)])
+def test_ring_cache_window_equals_sdpa_on_last_tokens(bs, W):
+    from paged_helpers import RingPaged
+    rng = np.random.default_rng(22)
+    ring = -(-(W - 1) // bs) + 1                       # enough blocks for an exact window
+    p = RingPaged(rng, S=4, Hq=8, Hkv=2, D=64, bs=bs, ctx=[3, W, W + 7, 5 * W + 3], ring=ring)
+    out, err = oracle.decode(p.q_bits, p.pool, p.geom, p.tables, p.ctx, 0.125, max_context_len=10 ** 6,
+                             window=W, ring=ring)
+    assert err == 0
+    assert np.allclose(out, p.expected_window(0.125, W), rtol=1e-12, atol=1e-12)

@@ -172,6 +172,35 @@ pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* 
  * (32 MiB on every device that loads the library, held until the process exits). */
 #define PA_STATIC_WORKSPACE_BYTES (32u * 1024u * 1024u)
 
+/* Paged decode over a sliding window, with optional ring block tables.
+ * The vLLM block manager ("推理框架知识点" page, vLLM BlockSpaceManagerV1) keeps a
+ * sliding-window sequence in ceil(window / block_size) blocks and reuses
+ * block_table[logical_block % that count]; such a table row is a ring.
+ *   window       > 0: attend only positions >= ctx - window (0: no window).
+ *   ring_blocks  > 0: logical block j of a sequence is at table entry
+ *                j % ring_blocks (<= block_table_stride); the ring only still
+ *                holds positions from the start of block (ctx-1)/bs - ring + 1,
+ *                so the attended positions are [t, ctx) with
+ *                t = max(0, ctx - window, ((ctx-1)/bs - ring_blocks + 1) * bs).
+ *                The window is exact when ring_blocks >= ceil((window-1)/bs) + 1.
+ *                0: linear rows (then ctx must fit the row, as in pa_decode).
+ * Other arguments as pa_decode; size the workspace with
+ * pa_decode_workspace_bytes(num_seqs, num_q_heads, head_size,
+ * pa_decode_window_span(max_context_len, block_size, window, ring_blocks),
+ * partition_size).  pa_decode is this call with window = ring_blocks = 0. */
+pa_status pa_decode_window(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,
+                           const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
+                           int32_t block_table_stride, const int32_t* context_lens, int32_t num_seqs,
+                           int32_t num_q_heads, int32_t max_context_len, float scale, int32_t window,
+                           int32_t ring_blocks, int32_t partition_size, void* workspace, size_t workspace_bytes,
+                           uint32_t* dev_err, void* stream);
+
+/* Upper bound on the tokens one sequence's windowed decode spans (from the
+ * block holding its first attended position): min(max_context_len,
+ * window + block_size - 1 if window > 0, ring_blocks * block_size if
+ * ring_blocks > 0).  Pass it as max_context_len to pa_decode_workspace_bytes. */
+int32_t pa_decode_window_span(int32_t max_context_len, int32_t block_size, int32_t window, int32_t ring_blocks);
+
 /* pa_decode for callers that cannot allocate device memory.  The pages describe
  * no such entry point; it exists for this library's users.  Some callers cannot
  * call cudaMalloc where they call decode: a plugin inside a framework whose

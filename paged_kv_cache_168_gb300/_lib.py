@@ -25,7 +25,8 @@ DTYPE_CODE = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 
 EXPORTED = [
     "pa_cache_bytes", "pa_cache_element_offset", "pa_reshape_and_cache", "pa_decode_workspace_bytes",
-    "pa_decode_partition_size", "pa_decode", "pa_decode_static_workspace", "pa_copy_blocks", "pa_swap_blocks", "pa_read_device_errors",
+    "pa_decode_partition_size", "pa_decode", "pa_decode_window", "pa_decode_window_span",
+    "pa_decode_static_workspace", "pa_copy_blocks", "pa_swap_blocks", "pa_read_device_errors",
     "pa_status_string", "pa_last_error_message",
 ]
 
@@ -86,6 +87,11 @@ def load():
     lib.pa_decode_partition_size.restype = i32
     lib.pa_decode.argtypes = [P, P, i64, P, D, i32, P, i32, P, i32, i32, i32, ctypes.c_float, i32, P, sz, P, P]
     lib.pa_decode.restype = ctypes.c_int
+    lib.pa_decode_window.argtypes = [P, P, i64, P, D, i32, P, i32, P, i32, i32, i32, ctypes.c_float, i32, i32, i32,
+                                     P, sz, P, P]
+    lib.pa_decode_window.restype = ctypes.c_int
+    lib.pa_decode_window_span.argtypes = [i32, i32, i32, i32]
+    lib.pa_decode_window_span.restype = i32
     lib.pa_decode_static_workspace.argtypes = [P, P, i64, P, D, i32, P, i32, P, i32, i32, i32, ctypes.c_float,
                                                i32, P, P]
     lib.pa_decode_static_workspace.restype = ctypes.c_int
@@ -167,6 +173,24 @@ def decode(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor, desc: Cac
                             _ptr(block_tables), block_tables.stride(0), _ptr(context_lens), S, Hq,
                             max_context_len, scale, partition_size, _ptr(workspace), ws_bytes, _ptr(dev_err),
                             _stream(stream)))
+
+
+def decode_window(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor, desc: CacheDesc,
+                  block_tables: torch.Tensor, context_lens: torch.Tensor, max_context_len: int, scale: float,
+                  window: int, ring_blocks: int = 0, workspace: torch.Tensor | None = None, partition_size: int = 0,
+                  layer: int = 0, dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """pa_decode_window: decode over the last `window` positions; ring_blocks > 0
+    reads table rows as rings (logical block j at entry j % ring_blocks)."""
+    S, Hq = q.shape[0], q.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pa_decode_window(_ptr(out), _ptr(q), q.stride(0), _ptr(kv_cache), ctypes.byref(desc.c()), layer,
+                                   _ptr(block_tables), block_tables.stride(0), _ptr(context_lens), S, Hq,
+                                   max_context_len, scale, window, ring_blocks, partition_size, _ptr(workspace),
+                                   ws_bytes, _ptr(dev_err), _stream(stream)))
+
+
+def decode_window_span(max_context_len: int, block_size: int, window: int, ring_blocks: int = 0) -> int:
+    return load().pa_decode_window_span(max_context_len, block_size, window, ring_blocks)
 
 
 STATIC_WORKSPACE_BYTES = 32 * 1024 * 1024

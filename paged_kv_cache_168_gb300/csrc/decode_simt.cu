@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
   const int bs = p.block_size, P = p.partition_size;
   const int ctx = p.context_lens[s];
 
-  if ((int64_t)ctx > (int64_t)p.bt_stride * bs || ctx > p.max_context_len) {
+  if (!context_ok(p, ctx)) {
     if (part == 0) {
       write_zero_rows<T, D, G>(p, s, kvh);
       if (threadIdx.x == 0) report(p.dev_err, PA_DEVERR_CONTEXT);
@@ -92,10 +92,12 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
     if (part == 0) write_zero_rows<T, D, G>(p, s, kvh);
     return;
   }
-  const int t0 = part * P;
+  const int t_first = window_start(ctx, bs, p.window, p.ring_blocks);   // first attended position
+  const int t_base = (t_first / bs) * bs;                              // partitions start here
+  const int t0 = t_base + part * P;
   if (t0 >= ctx) return;
   const int t1 = min(ctx, t0 + P);
-  const int n_parts = (ctx + P - 1) / P;
+  const int n_parts = (ctx - t_base + P - 1) / P;
   const int j0 = t0 / bs;
   const int nblk = (t1 - t0 + bs - 1) / bs;
   const int64_t chunk_bytes = 2LL * bs * D * 2;
@@ -115,7 +117,7 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
   }
   __syncthreads();
   for (int i = threadIdx.x; i < nblk; i += blockDim.x) {
-    const int b = p.block_tables[(int64_t)s * p.bt_stride + j0 + i];
+    const int b = p.block_tables[(int64_t)s * p.bt_stride + table_index(j0 + i, p.ring_blocks)];
     ids[i] = b;
     if (b < 0 || b >= p.num_blocks) flag_bad = 1;
   }
@@ -211,6 +213,7 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
     }
     const uint8_t* buf = stages + slot * C::kStageBytes;
     const int valid = min(C::kStageTokens, t1 - (t0 + st * C::kStageTokens));
+    const int lo = t_first - (t0 + st * C::kStageTokens);   // positions before the window (first stage only)
 
     float sc[TPG][HPW];
 #pragma unroll
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
       float part_dot[HPW];
 #pragma unroll
       for (int i = 0; i < HPW; ++i) part_dot[i] = 0.f;
-      if (pos < valid) {
+      if (pos >= lo && pos < valid) {
         const int blk = pos / bs, tb = pos % bs, g8 = tb / R, r = tb % R;
         const uint8_t* kb = buf + blk * chunk_bytes + (g8 * 2 * A) * atom_bytes + r * 128 + ((j ^ r) << 4);
 #pragma unroll
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
         v += __shfl_xor_sync(0xffffffffu, v, 1);
         v += __shfl_xor_sync(0xffffffffu, v, 2);
         v += __shfl_xor_sync(0xffffffffu, v, 4);
-        sc[k][i] = pos < valid ? v : -INFINITY;
+        sc[k][i] = (pos >= lo && pos < valid) ? v : -INFINITY;
       }
     }
 #pragma unroll
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
 #pragma unroll
     for (int k = 0; k < TPG; ++k) {
       const int pos = tw * 4 + gi + k * 4 * C::TW;
-      if (pos < valid) {
+      if (pos >= lo && pos < valid) {
         const int blk = pos / bs, tb = pos % bs, g8 = tb / R, r = tb % R;
         const uint8_t* vb = buf + blk * chunk_bytes + ((g8 * 2 + 1) * A) * atom_bytes + r * 128 + ((j ^ r) << 4);
         float w[HPW];
@@ -371,8 +374,9 @@ __global__ void __launch_bounds__(D) merge_partitions_kernel(const __grid_consta
   const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
   const int ctx = p.context_lens[s];
   const int P = p.partition_size;
-  if (ctx <= P || (int64_t)ctx > (int64_t)p.bt_stride * p.block_size || ctx > p.max_context_len) return;
-  const int n = (ctx + P - 1) / P;
+  if (ctx <= 0 || !context_ok(p, ctx)) return;
+  const int n = (ctx - attended_from(p, ctx) + P - 1) / P;
+  if (n <= 1) return;
   const int64_t row0 = ((int64_t)s * p.num_q_heads + h) * p.max_parts;
   __shared__ float sm_w[256];
   float M = -INFINITY;

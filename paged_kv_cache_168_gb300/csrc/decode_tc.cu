@@ -59,8 +59,8 @@ constexpr uint32_t kTmemCols = 128;                // S0 S1 (16 columns each) | 
 constexpr uint32_t kFull = 0xffffffffu;
 
 struct TileMeta {
-  int s, kvh, part, valid;       // sequence (< 0: no more work), kv head, partition, valid tokens
-  int last, qslot, n_parts, pad;
+  int s, kvh, part, valid;       // sequence (< 0: no more work), kv head, partition, rows < valid hold tokens
+  int last, qslot, n_parts, lo;  // last tile of the item, Q buffer, partitions, rows < lo precede the window
 };
 
 template <int NS>
@@ -81,14 +81,12 @@ struct Shared {
   volatile int abort_flag;
 };
 
-__device__ __forceinline__ bool ctx_invalid(const DecodeParams& p, int ctx) {
-  return (int64_t)ctx > (int64_t)p.bt_stride * p.block_size || ctx > p.max_context_len;
-}
+__device__ __forceinline__ bool ctx_invalid(const DecodeParams& p, int ctx) { return !context_ok(p, ctx); }
 
 // Work items of one sequence: its partitions, or one item that only writes zeros.
 __device__ __forceinline__ int items_of(const DecodeParams& p, int ctx) {
   if (ctx <= 0 || ctx_invalid(p, ctx)) return 1;
-  return (ctx + p.partition_size - 1) / p.partition_size;
+  return (ctx - attended_from(p, ctx) + p.partition_size - 1) / p.partition_size;
 }
 
 template <typename T, int G>
@@ -166,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     __syncwarp();
     const int total = carry * Hkv;
     const int P = p.partition_size;
+    const bool windowed = p.window > 0 || p.ring_blocks > 0;
     constexpr int kQChunks = (G * 16 + 31) / 32;
     // The next item's independent loads (context length, its first 32 block ids,
     // the query rows) are issued while the current item streams, so an item's
@@ -186,9 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       }
       r.s = lo;
       r.part = j - pre[lo];
-      const int jb = r.part * (P / bs);
       r.ctx = p.context_lens[r.s];
-      r.id_lane = (lane < P / bs && jb + lane < p.bt_stride) ? p.block_tables[(int64_t)r.s * p.bt_stride + jb + lane] : 0;
+      // first logical block of the partition (a window makes it depend on ctx)
+      const int jb = ((windowed ? attended_from(p, r.ctx) : 0) + r.part * P) / bs;
+      const int ti = table_index(jb + lane, p.ring_blocks);
+      r.id_lane = (lane < P / bs && ti < p.bt_stride && ti >= 0) ? p.block_tables[(int64_t)r.s * p.bt_stride + ti] : 0;
       const T* qsrc = static_cast<const T*>(p.q) + (int64_t)r.s * p.q_seq_stride + (int64_t)r.kvh * G * kD;
 #pragma unroll
       for (int k = 0; k < kQChunks; ++k) {
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       const Item cur = nxt;
       if (it + (int)gridDim.x < total) nxt = fetch(it + gridDim.x);
       const int s = cur.s, kvh = cur.kvh, part = cur.part, ctx = cur.ctx, id_lane = cur.id_lane;
-      const int32_t* row = p.block_tables + (int64_t)s * p.bt_stride + part * (P / bs);
+      const int32_t* row = p.block_tables + (int64_t)s * p.bt_stride;   // entry table_index(j) holds block j
       if (ctx_invalid(p, ctx)) {
         warp_zero_rows<T, G>(p, s, kvh, lane);
         if (lane == 0) report(p.dev_err, PA_DEVERR_CONTEXT);
@@ -216,12 +217,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         warp_zero_rows<T, G>(p, s, kvh, lane);
         continue;
       }
-      const int n_parts = (ctx + P - 1) / P;
-      const int t0 = part * P, t1 = min(ctx, t0 + P);
+      const int t_first = window_start(ctx, bs, p.window, p.ring_blocks);
+      const int t_base = (t_first / bs) * bs;
+      const int n_parts = (ctx - t_base + P - 1) / P;
+      const int t0 = t_base + part * P, t1 = min(ctx, t0 + P);
+      const int jb = t0 / bs;
       const int nblk = (t1 - t0 + bs - 1) / bs;
       bool bad = lane < nblk && (id_lane < 0 || id_lane >= p.num_blocks);
       for (int b = lane + 32; b < nblk; b += 32) {
-        const int id = row[b];
+        const int id = row[table_index(jb + b, p.ring_blocks)];
         bad |= (id < 0 || id >= p.num_blocks);
       }
       if (__any_sync(kFull, bad)) {
@@ -268,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         if (lane == 0) {
           TileMeta m;
           m.s = s; m.kvh = kvh; m.part = part; m.valid = valid;
-          m.last = (k == ntiles - 1); m.qslot = qslot; m.n_parts = n_parts; m.pad = 0;
+          m.last = (k == ntiles - 1); m.qslot = qslot; m.n_parts = n_parts;
+          m.lo = max(0, t_first - (t0 + k * kTile));
           sh.meta[slot] = m;
           mbar_arrive_expect_tx(&sh.full[slot], (uint32_t)(nb * chunk_bytes));
         }
@@ -276,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         const int bi = k * (kTile / bs) + lane;             // block of this lane's copy
         const int id_sh = __shfl_sync(kFull, id_lane, bi & 31);
         if (lane < nb) {
-          const int id = bi < 32 ? id_sh : row[bi];
+          const int id = bi < 32 ? id_sh : row[table_index(jb + bi, p.ring_blocks)];
           bulk_g2s(stages + slot * kTileBytes + lane * chunk_bytes,
                    p.cache + ((int64_t)id * Hkv + kvh) * chunk_bytes, (uint32_t)chunk_bytes, &sh.full[slot]);
         }
@@ -405,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.s_free[sb]);
-      const bool rv = row < mt.valid;
+      const bool rv = row >= mt.lo && row < mt.valid;
       float x[G], corr[G];
 #pragma unroll
       for (int n = 0; n < G; ++n) {

@@ -34,7 +34,36 @@ struct DecodeParams {
   float* ws_o;                // [S, Hq, max_parts, D] unnormalised partition outputs
   float* ws_ml;               // [S, Hq, max_parts, 2] (running max in base-2 units, sum)
   uint32_t* dev_err;
+  int32_t window;             // > 0: attend only positions >= ctx - window
+  int32_t ring_blocks;        // > 0: table rows are rings; logical block j at entry j % ring_blocks
 };
+
+// First position a decode attends for context length ctx: inside the window
+// (>= ctx - window when window > 0) and still held by a ring table (from the
+// start of block (ctx-1)/bs - ring + 1 when ring > 0).
+__host__ __device__ inline int window_start(int ctx, int bs, int window, int ring) {
+  int t = 0;
+  if (window > 0 && ctx - window > t) t = ctx - window;
+  if (ring > 0) {
+    const int held = ((ctx - 1) / bs - ring + 1) * bs;
+    if (held > t) t = held;
+  }
+  return t;
+}
+
+// Table entry holding logical block j.
+__host__ __device__ inline int table_index(int j, int ring) { return ring > 0 ? j % ring : j; }
+
+// Whether a context length can be served: linear rows must hold it; every
+// context must be within max_context_len.
+__host__ __device__ inline bool context_ok(const DecodeParams& p, int ctx) {
+  return (p.ring_blocks > 0 || (int64_t)ctx <= (int64_t)p.bt_stride * p.block_size) && ctx <= p.max_context_len;
+}
+
+// Partitions of a sequence: windows start at the block holding window_start.
+__host__ __device__ inline int attended_from(const DecodeParams& p, int ctx) {
+  return (window_start(ctx, p.block_size, p.window, p.ring_blocks) / p.block_size) * p.block_size;
+}
 
 cudaError_t launch_reshape_and_cache(uint8_t* layer_base, int32_t num_blocks, int32_t block_size,
                                      int32_t num_kv_heads, int32_t head_size, const void* key,

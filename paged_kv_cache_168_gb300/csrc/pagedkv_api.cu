@@ -181,11 +181,19 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
   return (size_t)((int64_t)num_seqs * num_q_heads * parts * (head_size + 2) * 4);
 }
 
-pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,
-                    const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
-                    int32_t block_table_stride, const int32_t* context_lens, int32_t num_seqs,
-                    int32_t num_q_heads, int32_t max_context_len, float scale, int32_t partition_size,
-                    void* workspace, size_t workspace_bytes, uint32_t* dev_err, void* stream) {
+int32_t pa_decode_window_span(int32_t max_context_len, int32_t block_size, int32_t window, int32_t ring_blocks) {
+  int64_t span = max_context_len;
+  if (window > 0 && (int64_t)window + block_size - 1 < span) span = (int64_t)window + block_size - 1;
+  if (ring_blocks > 0 && (int64_t)ring_blocks * block_size < span) span = (int64_t)ring_blocks * block_size;
+  return (int32_t)span;
+}
+
+pa_status pa_decode_window(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,
+                           const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
+                           int32_t block_table_stride, const int32_t* context_lens, int32_t num_seqs,
+                           int32_t num_q_heads, int32_t max_context_len, float scale, int32_t window,
+                           int32_t ring_blocks, int32_t partition_size, void* workspace, size_t workspace_bytes,
+                           uint32_t* dev_err, void* stream) {
   pa_status st = check_desc(desc);
   if (st != PA_OK) return st;
   if (layer < 0 || layer >= desc->num_layers) return fail(PA_ERR_INVALID_ARG, "layer %d", layer);
@@ -210,11 +218,16 @@ pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* 
     return fail(PA_ERR_INVALID_ARG, "q_seq_stride must be >= num_q_heads*head_size and a multiple of 8");
   if (block_table_stride <= 0) return fail(PA_ERR_INVALID_ARG, "block_table_stride %d", block_table_stride);
   if (max_context_len <= 0) return fail(PA_ERR_INVALID_ARG, "max_context_len %d", max_context_len);
-  const int32_t P = pa_decode_partition_size(partition_size, max_context_len);
+  if (window < 0) return fail(PA_ERR_INVALID_ARG, "window %d < 0", window);
+  if (ring_blocks < 0 || ring_blocks > block_table_stride)
+    return fail(PA_ERR_INVALID_ARG, "ring_blocks %d not in [0, block_table_stride %d]", ring_blocks,
+                block_table_stride);
+  const int32_t span = pa_decode_window_span(max_context_len, desc->block_size, window, ring_blocks);
+  const int32_t P = pa_decode_partition_size(partition_size, span);
   if (P % 128 || P < 128 || P > 8192)
     return fail(PA_ERR_INVALID_ARG, "partition_size %d must be a multiple of 128 in [128, 8192]", P);
   if (!(scale > 0.f) || scale != scale) return fail(PA_ERR_INVALID_ARG, "scale must be a positive number");
-  const size_t need = pa_decode_workspace_bytes(num_seqs, num_q_heads, desc->head_size, max_context_len, P);
+  const size_t need = pa_decode_workspace_bytes(num_seqs, num_q_heads, desc->head_size, span, P);
   if (workspace_bytes < need)
     return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", workspace_bytes, need);
   if (need && (!workspace || !aligned16(workspace)))
@@ -235,7 +248,9 @@ pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* 
   p.num_q_heads = num_q_heads;
   p.max_context_len = max_context_len;
   p.partition_size = P;
-  p.max_parts = (max_context_len + P - 1) / P;
+  p.max_parts = (span + P - 1) / P;
+  p.window = window;
+  p.ring_blocks = ring_blocks;
   p.scale_log2 = scale * 1.4426950408889634f;
   const int64_t parts = p.max_parts;
   p.ws_o = need ? static_cast<float*>(workspace) : nullptr;
@@ -252,6 +267,17 @@ pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* 
     e = pkv::launch_decode_simt(p, desc->dtype, desc->head_size, group, static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? PA_OK : cuda_fail(e, "decode launch");
+}
+
+
+pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,
+                    const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
+                    int32_t block_table_stride, const int32_t* context_lens, int32_t num_seqs,
+                    int32_t num_q_heads, int32_t max_context_len, float scale, int32_t partition_size,
+                    void* workspace, size_t workspace_bytes, uint32_t* dev_err, void* stream) {
+  return pa_decode_window(out, q, q_seq_stride, kv_cache, desc, layer, block_tables, block_table_stride,
+                          context_lens, num_seqs, num_q_heads, max_context_len, scale, 0, 0, partition_size,
+                          workspace, workspace_bytes, dev_err, stream);
 }
 
 pa_status pa_copy_blocks(void* kv_cache, const pa_cache_desc* desc, const int64_t* pairs, int32_t num_pairs,

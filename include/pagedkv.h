@@ -26,9 +26,10 @@
  *
  * Conventions
  *   Ownership:  the caller allocates every buffer (cache pools, workspace,
- *               error word).  The library allocates no memory and keeps no
- *               per-call state (pa_decode_static_workspace alone uses a fixed
- *               array the library carries; see its comment).
+ *               error word).  The library allocates no device memory and keeps
+ *               no per-call state (pa_decode_static_workspace alone uses a
+ *               fixed array the library carries; see its comment); the block
+ *               manager keeps host memory for its own bookkeeping.
  *   Streams:    every call except pa_read_device_errors is asynchronous on the
  *               given CUDA stream (a cudaStream_t passed as void*; NULL = the
  *               legacy default stream) and performs no host synchronisation.
@@ -71,7 +72,8 @@ typedef enum pa_status {
     PA_ERR_INVALID_ARG = 1,        /* bad pointer, size, id or pair list */
     PA_ERR_UNSUPPORTED = 2,        /* valid but not implemented (head_size, block_size, group) */
     PA_ERR_CUDA = 3,               /* a CUDA runtime call failed (launch, copy, attribute query) */
-    PA_ERR_WORKSPACE_TOO_SMALL = 4 /* workspace_bytes < pa_decode_workspace_bytes(...) */
+    PA_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes < pa_decode_workspace_bytes(...) */
+    PA_ERR_OUT_OF_BLOCKS = 5        /* block manager: not enough free blocks (nothing changed) */
 } pa_status;
 
 typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
@@ -244,6 +246,68 @@ pa_status pa_copy_blocks(void* kv_cache, const pa_cache_desc* desc, const int64_
 pa_status pa_swap_blocks(void* dst_pool, const pa_cache_desc* dst_desc, const void* src_pool,
                          const pa_cache_desc* src_desc, int32_t direction, const int64_t* pairs,
                          int32_t num_pairs, void* stream);
+
+/* ---------------------------------------------------------------- block manager
+ * Host-side bookkeeping that turns sequences of token ids into the block
+ * tables, slots, copy-on-write pairs and swap pairs the calls above consume --
+ * the vLLM block manager of the "推理框架知识点" page (BlockSpaceManagerV1 with its
+ * uncached and prefix-caching allocators and LRU evictor), with the mlqm.cn
+ * article's copy-on-write example and nano-vLLM's chain-hashed prefix blocks
+ * (section 5.2.1).  It holds only host memory (its own metadata); block ids are
+ * indices into the device pool (and, for swapped sequences, the host pool).
+ * Free blocks are handed out last-freed first, starting from the highest id.
+ * Not thread-safe: one caller at a time per manager. */
+typedef struct pa_block_manager pa_block_manager;
+
+typedef enum pa_alloc_status { PA_ALLOC_OK = 0, PA_ALLOC_LATER = 1, PA_ALLOC_NEVER = 2 } pa_alloc_status;
+
+/* num_cpu_blocks: host (swap) pool size.  watermark: fraction of device blocks
+ * kept free by admission.  sliding_window > 0: logical block i of a sequence
+ * reuses table entry i % ceil(sliding_window / block_size).  With
+ * enable_prefix_caching, full blocks are shared between sequences whose token
+ * ids agree up to and including that block (not combinable with a window). */
+pa_status pa_bm_create(int32_t block_size, int32_t num_gpu_blocks, int32_t num_cpu_blocks, float watermark,
+                       int32_t sliding_window, int32_t enable_prefix_caching, pa_block_manager** out);
+void pa_bm_destroy(pa_block_manager* bm);
+
+/* Admission of a prompt of num_tokens tokens: a pa_alloc_status. */
+int32_t pa_bm_can_allocate(pa_block_manager* bm, int32_t num_tokens);
+
+/* Blocks for a new sequence's prompt (token_ids[0..num_tokens-1]).  Returns
+ * PA_ERR_OUT_OF_BLOCKS (and changes nothing) when the pool runs out. */
+pa_status pa_bm_allocate(pa_block_manager* bm, int64_t seq_id, const int32_t* token_ids, int32_t num_tokens);
+
+/* Room for one more token: *slot receives its cache slot (block * block_size +
+ * offset, for pa_reshape_and_cache); when the last block was shared it is
+ * copied first and (*cow_src, *cow_dst) name the pair for pa_copy_blocks, else
+ * both are -1. */
+pa_status pa_bm_append_slot(pa_block_manager* bm, int64_t seq_id, int32_t token_id, int64_t* slot,
+                            int64_t* cow_src, int64_t* cow_dst);
+
+/* The child shares every block of the parent (parallel sampling, beam search). */
+pa_status pa_bm_fork(pa_block_manager* bm, int64_t parent_id, int64_t child_id);
+
+/* Release a sequence's blocks. */
+pa_status pa_bm_free(pa_block_manager* bm, int64_t seq_id);
+
+/* A sequence's block table (capacity entries at `table`, may be NULL to query
+ * sizes), its number of blocks and of tokens. */
+pa_status pa_bm_block_table(pa_block_manager* bm, int64_t seq_id, int32_t* table, int32_t capacity,
+                            int32_t* num_blocks, int32_t* num_tokens);
+
+/* Move every block of the n sequences to the host pool (swap_out) or back
+ * (swap_in); pairs receives [*num_pairs][2] (src, dst) ids for pa_swap_blocks
+ * (may be NULL to count).  A block shared by several of them moves once. */
+pa_status pa_bm_swap_out(pa_block_manager* bm, const int64_t* seq_ids, int32_t n, int64_t* pairs, int32_t capacity,
+                         int32_t* num_pairs);
+pa_status pa_bm_swap_in(pa_block_manager* bm, const int64_t* seq_ids, int32_t n, int64_t* pairs, int32_t capacity,
+                        int32_t* num_pairs);
+
+/* Free blocks (the evictor's cached blocks included) on the device (0) or host (1) side. */
+int32_t pa_bm_num_free_blocks(pa_block_manager* bm, int32_t on_host);
+
+/* Reference count of a block (-1 for an id out of range). */
+int32_t pa_bm_ref_count(pa_block_manager* bm, int32_t on_host, int32_t block);
 
 /* Synchronise `stream`, copy the device error word into *host_bits, and reset
  * it to 0 when `clear` is non-zero. */

@@ -18,7 +18,8 @@ import torch
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedkv.so")
 _lib = None
 
-PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_WORKSPACE_TOO_SMALL = range(5)
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_WORKSPACE_TOO_SMALL, PA_ERR_OUT_OF_BLOCKS = range(6)
+PA_ALLOC_OK, PA_ALLOC_LATER, PA_ALLOC_NEVER = range(3)
 PA_F16, PA_BF16 = 0, 1
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_CONTEXT, DEVERR_TIMEOUT = 1, 2, 4, 8
 DTYPE_CODE = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
@@ -28,6 +29,9 @@ EXPORTED = [
     "pa_decode_partition_size", "pa_decode", "pa_decode_window", "pa_decode_window_span",
     "pa_decode_static_workspace", "pa_copy_blocks", "pa_swap_blocks", "pa_read_device_errors",
     "pa_status_string", "pa_last_error_message",
+    "pa_bm_create", "pa_bm_destroy", "pa_bm_can_allocate", "pa_bm_allocate", "pa_bm_append_slot", "pa_bm_fork",
+    "pa_bm_free", "pa_bm_block_table", "pa_bm_swap_out", "pa_bm_swap_in", "pa_bm_num_free_blocks",
+    "pa_bm_ref_count",
 ]
 
 
@@ -101,6 +105,32 @@ def load():
     lib.pa_swap_blocks.restype = ctypes.c_int
     lib.pa_read_device_errors.argtypes = [P, P, i32, P]
     lib.pa_read_device_errors.restype = ctypes.c_int
+    B = ctypes.c_void_p
+    PI64, PI32 = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
+    lib.pa_bm_create.argtypes = [i32, i32, i32, ctypes.c_float, i32, i32, ctypes.POINTER(ctypes.c_void_p)]
+    lib.pa_bm_create.restype = ctypes.c_int
+    lib.pa_bm_destroy.argtypes = [B]
+    lib.pa_bm_destroy.restype = None
+    lib.pa_bm_can_allocate.argtypes = [B, i32]
+    lib.pa_bm_can_allocate.restype = i32
+    lib.pa_bm_allocate.argtypes = [B, i64, P, i32]
+    lib.pa_bm_allocate.restype = ctypes.c_int
+    lib.pa_bm_append_slot.argtypes = [B, i64, i32, PI64, PI64, PI64]
+    lib.pa_bm_append_slot.restype = ctypes.c_int
+    lib.pa_bm_fork.argtypes = [B, i64, i64]
+    lib.pa_bm_fork.restype = ctypes.c_int
+    lib.pa_bm_free.argtypes = [B, i64]
+    lib.pa_bm_free.restype = ctypes.c_int
+    lib.pa_bm_block_table.argtypes = [B, i64, P, i32, PI32, PI32]
+    lib.pa_bm_block_table.restype = ctypes.c_int
+    lib.pa_bm_swap_out.argtypes = [B, P, i32, P, i32, PI32]
+    lib.pa_bm_swap_out.restype = ctypes.c_int
+    lib.pa_bm_swap_in.argtypes = [B, P, i32, P, i32, PI32]
+    lib.pa_bm_swap_in.restype = ctypes.c_int
+    lib.pa_bm_num_free_blocks.argtypes = [B, i32]
+    lib.pa_bm_num_free_blocks.restype = i32
+    lib.pa_bm_ref_count.argtypes = [B, i32, i32]
+    lib.pa_bm_ref_count.restype = i32
     lib.pa_status_string.argtypes = [ctypes.c_int]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_last_error_message.argtypes = []
@@ -234,3 +264,78 @@ def read_device_errors(dev_err: torch.Tensor, clear: bool = True, stream=None) -
 
 def status_string(status: int) -> str:
     return load().pa_status_string(status).decode()
+
+
+class BlockManager:
+    """Host-side block manager (pa_bm_*): block tables, slots, copy-on-write and
+    swap pairs for sequences of token ids."""
+
+    def __init__(self, block_size: int, num_gpu_blocks: int, num_cpu_blocks: int = 0, watermark: float = 0.0,
+                 sliding_window: int = 0, prefix_caching: bool = False):
+        self._lib = load()
+        h = ctypes.c_void_p()
+        _check(self._lib.pa_bm_create(block_size, num_gpu_blocks, num_cpu_blocks, watermark, sliding_window,
+                                      int(prefix_caching), ctypes.byref(h)))
+        self._h = h
+        self.block_size = block_size
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.pa_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def can_allocate(self, num_tokens: int) -> int:
+        return self._lib.pa_bm_can_allocate(self._h, num_tokens)
+
+    def allocate(self, seq_id: int, token_ids) -> None:
+        t = np.ascontiguousarray(np.asarray(token_ids, dtype=np.int32))
+        _check(self._lib.pa_bm_allocate(self._h, seq_id, t.ctypes.data_as(ctypes.c_void_p), t.size))
+
+    def append_slot(self, seq_id: int, token_id: int):
+        """Slot of the new token and the copy-on-write pair (src, dst), or None."""
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(self._lib.pa_bm_append_slot(self._h, seq_id, token_id, ctypes.byref(slot), ctypes.byref(src),
+                                           ctypes.byref(dst)))
+        return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def fork(self, parent: int, child: int) -> None:
+        _check(self._lib.pa_bm_fork(self._h, parent, child))
+
+    def free(self, seq_id: int) -> None:
+        _check(self._lib.pa_bm_free(self._h, seq_id))
+
+    def block_table(self, seq_id: int):
+        """(int32 block ids of the sequence, its number of tokens)."""
+        nb, nt = ctypes.c_int32(), ctypes.c_int32()
+        _check(self._lib.pa_bm_block_table(self._h, seq_id, None, 0, ctypes.byref(nb), ctypes.byref(nt)))
+        out = np.zeros(nb.value, dtype=np.int32)
+        _check(self._lib.pa_bm_block_table(self._h, seq_id, out.ctypes.data_as(ctypes.c_void_p), out.size,
+                                           ctypes.byref(nb), ctypes.byref(nt)))
+        return out, nt.value
+
+    def _swap(self, fn, seq_ids):
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        n = ctypes.c_int32()
+        _check(fn(self._h, ids.ctypes.data_as(ctypes.c_void_p), ids.size, None, 0, ctypes.byref(n)))
+        # counting call changes nothing; the second call performs the move
+        pairs = np.zeros((max(n.value, 1), 2), dtype=np.int64)
+        _check(fn(self._h, ids.ctypes.data_as(ctypes.c_void_p), ids.size, pairs.ctypes.data_as(ctypes.c_void_p),
+                  pairs.shape[0], ctypes.byref(n)))
+        return pairs[:n.value]
+
+    def swap_out(self, seq_ids):
+        """Move the sequences' blocks to the host pool; (device, host) pairs."""
+        return self._swap(self._lib.pa_bm_swap_out, seq_ids)
+
+    def swap_in(self, seq_ids):
+        """Move the sequences' blocks back to the device pool; (host, device) pairs."""
+        return self._swap(self._lib.pa_bm_swap_in, seq_ids)
+
+    def num_free(self, on_host: bool = False) -> int:
+        return self._lib.pa_bm_num_free_blocks(self._h, int(on_host))
+
+    def ref_count(self, block: int, on_host: bool = False) -> int:
+        return self._lib.pa_bm_ref_count(self._h, int(on_host), block)

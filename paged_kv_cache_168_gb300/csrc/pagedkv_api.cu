@@ -343,6 +343,7 @@ const char* pa_status_string(pa_status status) {
     case PA_ERR_UNSUPPORTED: return "unsupported shape or type";
     case PA_ERR_CUDA: return "CUDA runtime error";
     case PA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PA_ERR_OUT_OF_BLOCKS: return "out of blocks";
   }
   return "unknown status";
 }

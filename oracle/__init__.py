@@ -114,6 +114,14 @@ def _load():
     lib.oracle_copy_blocks.restype = ctypes.c_int
     lib.oracle_swap_blocks.argtypes = [P, G, P, G, P, i32]
     lib.oracle_swap_blocks.restype = ctypes.c_int
+    lib.oracle_i8_chunk_bytes.argtypes = [G]
+    lib.oracle_i8_chunk_bytes.restype = i64
+    lib.oracle_reshape_and_cache_i8.argtypes = [P, G, P, i64, P, i64, P, i32]
+    lib.oracle_reshape_and_cache_i8.restype = ctypes.c_int
+    lib.oracle_decode_i8.argtypes = [P, P, i64, P, G, P, i32, P, i32, i32, i32, dbl, i32]
+    lib.oracle_decode_i8.restype = ctypes.c_int
+    lib.oracle_copy_blocks_bytes.argtypes = [P, i64, i32, i32, i64, P, i32]
+    lib.oracle_copy_blocks_bytes.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     _lib = lib
@@ -248,3 +256,47 @@ def swap_blocks(dst: np.ndarray, dst_geom: Geom, src: np.ndarray, src_geom: Geom
     pr = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
     return _load().oracle_swap_blocks(_ptr(dst), ctypes.byref(dst_geom.c()), _ptr(src),
                                       ctypes.byref(src_geom.c()), _ptr(pr), pr.shape[0])
+
+
+# ---------------------------------------------------------------- 8-bit KV cache
+# Geom.dtype names the 16-bit type of q / new K,V / output ("f16" or "bf16");
+# the pool holds int8 codes and fp32 scales (uint8 arrays here).
+
+def i8_block_bytes(geom: Geom) -> int:
+    """Bytes of one block (all kv heads) of an 8-bit cache."""
+    return geom.num_kv_heads * _load().oracle_i8_chunk_bytes(ctypes.byref(geom.c()))
+
+
+def reshape_and_cache_i8(layer: np.ndarray, geom: Geom, key: np.ndarray, value: np.ndarray,
+                         slot_mapping: np.ndarray) -> int:
+    """Quantise and write new tokens' K/V (uint16 [N, Hkv, D]) into an 8-bit layer (uint8)."""
+    assert layer.dtype == np.uint8
+    key, value = _u16(key), _u16(value)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    row = geom.num_kv_heads * geom.head_size
+    return _load().oracle_reshape_and_cache_i8(_ptr(layer), ctypes.byref(geom.c()), _ptr(key), row, _ptr(value),
+                                               row, _ptr(sm), sm.shape[0])
+
+
+def decode_i8(q: np.ndarray, layer: np.ndarray, geom: Geom, block_tables: np.ndarray, context_lens: np.ndarray,
+              scale: float, max_context_len: int | None = None, nthreads: int = 0):
+    """Paged decode over an 8-bit cache (values = code * scale), in fp64."""
+    assert layer.dtype == np.uint8
+    q = _u16(q)
+    S, Hq, D = q.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    if max_context_len is None:
+        max_context_len = int(cl.max()) if cl.size else 0
+    out = np.zeros((S, Hq, D))
+    err = _load().oracle_decode_i8(_ptr(out), _ptr(q), Hq * D, _ptr(layer), ctypes.byref(geom.c()), _ptr(bt),
+                                   bt.shape[1], _ptr(cl), S, Hq, max_context_len, scale, nthreads)
+    return out, err
+
+
+def copy_blocks_bytes(pool: np.ndarray, block_bytes: int, num_blocks: int, pairs: np.ndarray, num_layers: int = 1,
+                      layer_stride: int = 0) -> int:
+    """Whole-block copies for any block encoding (pool as uint8)."""
+    pr = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+    return _load().oracle_copy_blocks_bytes(_ptr(pool), block_bytes, num_blocks, num_layers,
+                                            layer_stride or block_bytes * num_blocks, _ptr(pr), pr.shape[0])

@@ -269,6 +269,139 @@ int oracle_decode(double* out, const uint16_t* q, int64_t q_seq_stride, const ui
                                 num_seqs, num_q_heads, max_context_len, scale, 0, 0, sel, nsel, nthreads);
 }
 
+/* ---------------- 8-bit KV cache ---------------- */
+
+/* An 8-bit cache ("8bit KV Cache" quantisation, the TurboMind section of the
+ * inference-framework FAQ page) stores each token's K and V vector of one kv
+ * head as signed 8-bit codes with one scale: scale = max|x| / 127 and
+ * code = round-half-even(x * (127 / max|x|)) clipped to [-127, 127], the
+ * decision taken in IEEE binary32 (as the writer on the device does); the
+ * value a code stands for is code * scale.
+ * Chunk (block, kv head) of head_size 128: K codes [bs][128], V codes
+ * [bs][128], K scales [bs] (fp32, padded to 16 bytes), V scales [bs] (same). */
+static int64_t i8_scale_bytes(int64_t bs) { return ((bs * 4 + 15) / 16) * 16; }
+static int64_t i8_chunk_bytes(const oracle_geom* g) {
+    return 2 * (int64_t)g->block_size * g->head_size + 2 * i8_scale_bytes(g->block_size);
+}
+int64_t oracle_i8_chunk_bytes(const oracle_geom* g) { return i8_chunk_bytes(g); }
+
+static double i8_value(const uint8_t* layer, const oracle_geom* g, int64_t block, int64_t head, int part,
+                       int64_t t, int64_t d) {
+    const uint8_t* chunk = layer + (block * g->num_kv_heads + head) * i8_chunk_bytes(g);
+    const int8_t code = (int8_t)chunk[(part * g->block_size + t) * g->head_size + d];
+    float scale;
+    memcpy(&scale, chunk + 2 * g->block_size * g->head_size + part * i8_scale_bytes(g->block_size) + t * 4, 4);
+    return (double)code * (double)scale;
+}
+
+/* Quantise one vector of n 16-bit elements; codes to out[0..n-1], returns the scale. */
+static float i8_quantise(const uint16_t* x, int dtype, int64_t n, int8_t* out) {
+    float amax = 0.0f;
+    for (int64_t d = 0; d < n; ++d) {
+        const float v = (float)fabs(elem_to_double(x[d], dtype));
+        if (v > amax) amax = v;
+    }
+    if (!(amax > 0.0f)) {
+        for (int64_t d = 0; d < n; ++d) out[d] = 0;
+        return 0.0f;
+    }
+    const float inv = 127.0f / amax;
+    for (int64_t d = 0; d < n; ++d) {
+        float y = (float)elem_to_double(x[d], dtype) * inv;
+        long c = lrintf(y);
+        if (c > 127) c = 127;
+        if (c < -127) c = -127;
+        out[d] = (int8_t)c;
+    }
+    return amax / 127.0f;
+}
+
+int oracle_reshape_and_cache_i8(uint8_t* layer, const oracle_geom* g, const uint16_t* key, int64_t key_stride,
+                                const uint16_t* value, int64_t value_stride, const int64_t* slot_mapping,
+                                int32_t n) {
+    int err = 0;
+    const int64_t nslots = (int64_t)g->num_blocks * g->block_size;
+    const int64_t D = g->head_size;
+    for (int32_t i = 0; i < n; ++i) {
+        const int64_t slot = slot_mapping[i];
+        if (slot == -1) continue;
+        if (slot < 0 || slot >= nslots) { err |= ORC_ERR_SLOT; continue; }
+        const int64_t block = slot / g->block_size, t = slot % g->block_size;
+        for (int64_t h = 0; h < g->num_kv_heads; ++h)
+            for (int part = 0; part < 2; ++part) {
+                const uint16_t* src = (part ? value + i * value_stride : key + i * key_stride) + h * D;
+                uint8_t* chunk = layer + (block * g->num_kv_heads + h) * i8_chunk_bytes(g);
+                const float scale = i8_quantise(src, g->dtype, D, (int8_t*)(chunk + (part * g->block_size + t) * D));
+                memcpy(chunk + 2 * g->block_size * D + part * i8_scale_bytes(g->block_size) + t * 4, &scale, 4);
+            }
+    }
+    return err;
+}
+
+int oracle_decode_i8(double* out, const uint16_t* q, int64_t q_seq_stride, const uint8_t* layer,
+                     const oracle_geom* g, const int32_t* block_tables, int32_t bt_stride,
+                     const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                     double scale, int32_t nthreads) {
+    const int32_t D = g->head_size;
+    const int32_t G = num_q_heads / g->num_kv_heads;
+    int err = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+#endif
+    for (int64_t it = 0; it < (int64_t)num_seqs * num_q_heads; ++it) {
+        const int32_t s = (int32_t)(it / num_q_heads), h = (int32_t)(it % num_q_heads);
+        double* o = out + it * D;
+        for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+        const int32_t ctx = context_lens[s];
+        if (ctx <= 0) continue;
+        if ((int64_t)ctx > (int64_t)bt_stride * g->block_size || ctx > max_context_len) {
+            err |= ORC_ERR_CONTEXT;
+            continue;
+        }
+        double* K = (double*)malloc(sizeof(double) * (size_t)ctx * D);
+        double* V = (double*)malloc(sizeof(double) * (size_t)ctx * D);
+        double* qd = (double*)malloc(sizeof(double) * (size_t)D);
+        int bad = 0;
+        for (int32_t t = 0; t < ctx && !bad; ++t) {
+            const int32_t block = block_tables[(int64_t)s * bt_stride + t / g->block_size];
+            if (block < 0 || block >= g->num_blocks) { bad = 1; break; }
+            for (int32_t d = 0; d < D; ++d) {
+                K[(int64_t)t * D + d] = i8_value(layer, g, block, h / G, 0, t % g->block_size, d);
+                V[(int64_t)t * D + d] = i8_value(layer, g, block, h / G, 1, t % g->block_size, d);
+            }
+        }
+        if (bad) {
+            err |= ORC_ERR_BLOCK_ID;
+        } else {
+            for (int32_t d = 0; d < D; ++d)
+                qd[d] = elem_to_double(q[(int64_t)s * q_seq_stride + (int64_t)h * D + d], g->dtype);
+            oracle_contiguous_attention(qd, K, V, ctx, D, scale, o);
+        }
+        free(K);
+        free(V);
+        free(qd);
+    }
+    return err;
+}
+
+int oracle_copy_blocks_bytes(uint8_t* pool, int64_t block_bytes, int32_t num_blocks, int32_t num_layers,
+                             int64_t layer_stride, const int64_t* pairs, int32_t n) {
+    for (int32_t i = 0; i < n; ++i)
+        for (int k = 0; k < 2; ++k)
+            if (pairs[2 * i + k] < 0 || pairs[2 * i + k] >= num_blocks) return ORC_ERR_BLOCK_ID;
+    uint8_t* tmp = (uint8_t*)malloc((size_t)(block_bytes * (n > 0 ? n : 1)));
+    for (int32_t l = 0; l < num_layers; ++l) {
+        uint8_t* layer = pool + (int64_t)l * layer_stride;
+        for (int32_t i = 0; i < n; ++i)
+            memcpy(tmp + (int64_t)i * block_bytes, layer + pairs[2 * i] * block_bytes, (size_t)block_bytes);
+        for (int32_t i = 0; i < n; ++i)
+            memcpy(layer + pairs[2 * i + 1] * block_bytes, tmp + (int64_t)i * block_bytes, (size_t)block_bytes);
+    }
+    free(tmp);
+    return 0;
+}
+
 /* ---------------- split-context partitions and log-sum-exp merge ---------------- */
 
 /* For one (s, h): split tokens into consecutive partitions of P tokens.  For

@@ -376,3 +376,84 @@ def test_ring_cache_window_equals_sdpa_on_last_tokens(bs, W):
                              window=W, ring=ring)
     assert err == 0
     assert np.allclose(out, p.expected_window(0.125, W), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- 8-bit KV cache
+
+def _i8_pool(geom, num_blocks):
+    return np.zeros(oracle.i8_block_bytes(geom) * num_blocks, dtype=np.uint8)
+
+
+def _read_i8(pool, geom, block, head, part, t):
+    """(codes, scale) of one stored vector, read by the chunk description
+    [K codes | V codes | K scales | V scales] (each scale area padded to 16 bytes)."""
+    bs, D = geom.block_size, geom.head_size
+    chunk = oracle.i8_block_bytes(geom) // geom.num_kv_heads
+    base = (block * geom.num_kv_heads + head) * chunk
+    codes = pool[base + (part * bs + t) * D: base + (part * bs + t + 1) * D].view(np.int8)
+    sbytes = -(-bs * 4 // 16) * 16
+    off = base + 2 * bs * D + part * sbytes + t * 4
+    return codes, float(pool[off:off + 4].view(np.float32)[0])
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_i8_quantisation_properties(dtype):
+    rng = np.random.default_rng(30)
+    g = oracle.Geom(4, 16, 2, 128, dtype)
+    pool = _i8_pool(g, 4)
+    x = rng.standard_normal((20, 2, 128)) * rng.uniform(0.01, 100, (20, 2, 1))
+    x[3, 1] = 0.0                                       # an all-zero vector
+    k = to_bits(x, dtype)
+    v = to_bits(-x, dtype)
+    slots = rng.choice(64, 20, replace=False)
+    assert oracle.reshape_and_cache_i8(pool, g, k, v, slots) == 0
+    kd, vd = bits_to_f64(k, dtype), bits_to_f64(v, dtype)
+    for i, slot in enumerate(slots):
+        for h in range(2):
+            for part, src in ((0, kd), (1, vd)):
+                codes, scale = _read_i8(pool, g, slot // 16, h, part, slot % 16)
+                vec = src[i, h]
+                amax = np.abs(vec).max()
+                if amax == 0:
+                    assert scale == 0 and np.all(codes == 0)
+                    continue
+                assert np.isclose(scale, amax / 127, rtol=1e-6)
+                assert np.abs(codes).max() == 127 and codes[np.argmax(np.abs(vec))] == np.sign(vec[np.argmax(np.abs(vec))]) * 127
+                assert np.all(np.abs(vec - codes * scale) <= scale * 0.5 * (1 + 1e-5))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_i8_decode_on_grid_values_equals_16bit_decode(dtype):
+    # values code * 2^-6 with one code of +-127 per vector are stored exactly by
+    # the 8-bit cache (scale = 2^-6), so its decode equals the 16-bit decode
+    rng = np.random.default_rng(31)
+    S, Hq, Hkv, D, bs = 4, 8, 2, 128, 16
+    ctx = [1, 17, 40, 90]
+    p = Paged(rng, S=S, Hq=Hq, Hkv=Hkv, D=D, bs=bs, ctx=ctx, dtype=dtype)
+    g = oracle.Geom(p.num_blocks, bs, Hkv, D, dtype)
+    pool = _i8_pool(g, p.num_blocks)
+    for s in range(S):
+        c = ctx[s]
+        codes = rng.integers(-127, 128, (2, c, Hkv, D))
+        codes[:, :, :, 0] = 127
+        vals = codes * 2.0 ** -6
+        p.K[s], p.V[s] = vals[0], vals[1]
+        t = np.arange(c)
+        slots = p.tables[s, t // bs].astype(np.int64) * bs + t % bs
+        assert oracle.reshape_and_cache_i8(pool, g, to_bits(vals[0], dtype), to_bits(vals[1], dtype), slots) == 0
+    p.write_all()
+    scale = 1 / math.sqrt(D)
+    ref, _ = oracle.decode(p.q_bits, p.pool, p.geom, p.tables, p.ctx, scale)
+    got, err = oracle.decode_i8(p.q_bits, pool, g, p.tables, p.ctx, scale)
+    assert err == 0
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(got, p.expected_contiguous(scale), rtol=1e-12, atol=1e-12)
+
+
+def test_byte_block_copy_matches_numpy():
+    rng = np.random.default_rng(32)
+    pool = rng.integers(0, 256, 7 * 300, dtype=np.uint8)
+    ref = pool.reshape(7, 300).copy()
+    ref[[5, 2]] = ref[[0, 1]]
+    assert oracle.copy_blocks_bytes(pool, 300, 7, np.array([[0, 5], [1, 2]])) == 0
+    assert np.array_equal(pool.reshape(7, 300), ref)

@@ -270,7 +270,7 @@ def i8_block_bytes(geom: Geom) -> int:
 def reshape_and_cache_i8(layer: np.ndarray, geom: Geom, key: np.ndarray, value: np.ndarray,
                          slot_mapping: np.ndarray) -> int:
     """Quantise and write new tokens' K/V (uint16 [N, Hkv, D]) into an 8-bit layer (uint8)."""
-    assert layer.dtype == np.uint8
+    assert layer.dtype == np.uint8 and geom.head_size == 128
     key, value = _u16(key), _u16(value)
     sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     row = geom.num_kv_heads * geom.head_size
@@ -281,7 +281,7 @@ def reshape_and_cache_i8(layer: np.ndarray, geom: Geom, key: np.ndarray, value: 
 def decode_i8(q: np.ndarray, layer: np.ndarray, geom: Geom, block_tables: np.ndarray, context_lens: np.ndarray,
               scale: float, max_context_len: int | None = None, nthreads: int = 0):
     """Paged decode over an 8-bit cache (values = code * scale), in fp64."""
-    assert layer.dtype == np.uint8
+    assert layer.dtype == np.uint8 and geom.head_size == 128
     q = _u16(q)
     S, Hq, D = q.shape
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)

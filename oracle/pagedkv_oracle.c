@@ -278,17 +278,22 @@ int oracle_decode(double* out, const uint16_t* q, int64_t q_seq_stride, const ui
  * decision taken in IEEE binary32 (as the writer on the device does); the
  * value a code stands for is code * scale.
  * Chunk (block, kv head) of head_size 128: K codes [bs][128], V codes
- * [bs][128], K scales [bs] (fp32, padded to 16 bytes), V scales [bs] (same). */
+ * [bs][128], K scales [bs] (fp32, padded to 16 bytes), V scales [bs] (same).
+ * Inside a 128-byte code row of slot t, the 16 codes of dims 16c..16c+15 sit at
+ * piece position c XOR (t mod 8), like the rows of the 16-bit cache. */
 static int64_t i8_scale_bytes(int64_t bs) { return ((bs * 4 + 15) / 16) * 16; }
 static int64_t i8_chunk_bytes(const oracle_geom* g) {
     return 2 * (int64_t)g->block_size * g->head_size + 2 * i8_scale_bytes(g->block_size);
 }
 int64_t oracle_i8_chunk_bytes(const oracle_geom* g) { return i8_chunk_bytes(g); }
 
+/* Byte position of dim d inside the code row of slot t. */
+static int64_t i8_pos(int64_t t, int64_t d) { return ((((d >> 4) ^ (t & 7)) << 4) | (d & 15)); }
+
 static double i8_value(const uint8_t* layer, const oracle_geom* g, int64_t block, int64_t head, int part,
                        int64_t t, int64_t d) {
     const uint8_t* chunk = layer + (block * g->num_kv_heads + head) * i8_chunk_bytes(g);
-    const int8_t code = (int8_t)chunk[(part * g->block_size + t) * g->head_size + d];
+    const int8_t code = (int8_t)chunk[(part * g->block_size + t) * g->head_size + i8_pos(t, d)];
     float scale;
     memcpy(&scale, chunk + 2 * g->block_size * g->head_size + part * i8_scale_bytes(g->block_size) + t * 4, 4);
     return (double)code * (double)scale;
@@ -331,7 +336,9 @@ int oracle_reshape_and_cache_i8(uint8_t* layer, const oracle_geom* g, const uint
             for (int part = 0; part < 2; ++part) {
                 const uint16_t* src = (part ? value + i * value_stride : key + i * key_stride) + h * D;
                 uint8_t* chunk = layer + (block * g->num_kv_heads + h) * i8_chunk_bytes(g);
-                const float scale = i8_quantise(src, g->dtype, D, (int8_t*)(chunk + (part * g->block_size + t) * D));
+                int8_t codes[128];
+                const float scale = i8_quantise(src, g->dtype, D, codes);
+                for (int64_t d = 0; d < D; ++d) chunk[(part * g->block_size + t) * D + i8_pos(t, d)] = (uint8_t)codes[d];
                 memcpy(chunk + 2 * g->block_size * D + part * i8_scale_bytes(g->block_size) + t * 4, &scale, 4);
             }
     }

@@ -386,11 +386,14 @@ def _i8_pool(geom, num_blocks):
 
 def _read_i8(pool, geom, block, head, part, t):
     """(codes, scale) of one stored vector, read by the chunk description
-    [K codes | V codes | K scales | V scales] (each scale area padded to 16 bytes)."""
+    [K codes | V codes | K scales | V scales] (each scale area padded to 16 bytes;
+    16-byte pieces of a code row swizzled by the slot's row index mod 8)."""
     bs, D = geom.block_size, geom.head_size
     chunk = oracle.i8_block_bytes(geom) // geom.num_kv_heads
     base = (block * geom.num_kv_heads + head) * chunk
-    codes = pool[base + (part * bs + t) * D: base + (part * bs + t + 1) * D].view(np.int8)
+    row = pool[base + (part * bs + t) * D: base + (part * bs + t + 1) * D].view(np.int8)
+    pos = (((np.arange(D) >> 4) ^ (t & 7)) << 4) | (np.arange(D) & 15)   # piece c of the row at c ^ (t % 8)
+    codes = row[pos]
     sbytes = -(-bs * 4 // 16) * 16
     off = base + 2 * bs * D + part * sbytes + t * 4
     return codes, float(pool[off:off + 4].view(np.float32)[0])

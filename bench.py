@@ -50,6 +50,11 @@ DESCRIPTIONS = {
             "bf16, 2048-token shared prompt, tails ~U[0,256], CoW copy_blocks + 10% swap_blocks",
     "7b_bs1": "Llama-2-7B-shaped decode layer with token-granular paging (block_size 1): 64 seqs, 32/32 heads, "
               "head_size 128, fp16, context_lens ~U[512,4096]",
+    "7b_int8": "Llama-2-7B-shaped decode layer over an 8-bit KV cache (int8 codes + fp32 scale per token and "
+               "kv head): 64 seqs, 32/32 heads, head_size 128, block_size 16, fp16 q/out, history K/V ~N(0,1) "
+               "quantised by the library's writer, context_lens ~U[512,4096]",
+    "8b_int8": "Llama-3-8B-shaped GQA decode over an 8-bit KV cache: 256 seqs, 32 q/8 kv heads, head_size 128, "
+               "block_size 16, bf16 q/out, context_lens lognormal(median 1024, sigma 0.8) capped at 8192",
 }
 
 
@@ -173,15 +178,41 @@ _ORACLE_INPUTS = {}
 
 
 def oracle_inputs(w):
-    """Host copies (raw 16-bit bits) of the workload for the oracle, made once."""
+    """Host copies (raw 16-bit bits) of the workload for the oracle, made once.
+    An 8-bit cache starts as an empty oracle pool that oracle_build_blocks fills."""
     import oracle
     from paged_kv_cache_168_gb300.workloads import as_u16
     key = id(w)
     if key not in _ORACLE_INPUTS:
         cfg = w.cfg
         g = oracle.Geom(w.num_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_size, cfg.dtype)
-        _ORACLE_INPUTS[key] = (g, as_u16(w.kv_cache).reshape(-1), as_u16(w.q))
+        if cfg.kv_int8:
+            pool = np.zeros(w.num_blocks * oracle.i8_block_bytes(g), np.uint8)
+            built = np.zeros(w.num_blocks, dtype=bool)
+            _ORACLE_INPUTS[key] = (g, pool, as_u16(w.q), built)
+        else:
+            _ORACLE_INPUTS[key] = (g, as_u16(w.kv_cache).reshape(-1), as_u16(w.q), None)
     return _ORACLE_INPUTS[key]
+
+
+def oracle_build_blocks(w, s):
+    """8-bit cache: the oracle quantises sequence s's blocks from the workload's
+    logical history (blocks it has not built yet)."""
+    import oracle
+    from paged_kv_cache_168_gb300.workloads import as_u16
+    g, pool, _, built = oracle_inputs(w)
+    bs = w.cfg.block_size
+    blocks = w.block_tables_np[s, :-(-int(w.context_lens_np[s]) // bs)]
+    blocks = np.unique(blocks[~built[blocks]])
+    if blocks.size == 0:
+        return
+    part = w.kv_logical[torch.from_numpy(blocks).to(w.kv_logical.device)]        # [n, Hkv, 2, bs, D]
+    n, hkv, _, _, d = part.shape
+    key = as_u16(part[:, :, 0].permute(0, 2, 1, 3).reshape(n * bs, hkv, d))
+    value = as_u16(part[:, :, 1].permute(0, 2, 1, 3).reshape(n * bs, hkv, d))
+    slots = (blocks[:, None].astype(np.int64) * bs + np.arange(bs)).reshape(-1)
+    assert oracle.reshape_and_cache_i8(pool, g, key, value, slots) == 0
+    built[blocks] = True
 
 
 def oracle_sample(w, budget_s: float, max_items: int | None = None, start: int = 0):
@@ -190,15 +221,21 @@ def oracle_sample(w, budget_s: float, max_items: int | None = None, start: int =
     (GB/s of algorithmic KV bytes, seq-steps/s, description, cores, seconds)."""
     import oracle
     cfg = w.cfg
-    g, pool, q = oracle_inputs(w)
-    kv_tok = 2 * cfg.num_kv_heads * cfg.head_size * 2
+    g, pool, q, _ = oracle_inputs(w)
+    kv_tok = cfg.num_kv_heads * (2 * cfg.head_size + 8) if cfg.kv_int8 else 2 * cfg.num_kv_heads * cfg.head_size * 2
     done_bytes, done_seqs, t_total = 0, 0, 0.0
     order = np.random.default_rng(start).permutation(cfg.num_seqs)
     for s in order:
-        sel = np.array([[s, h] for h in range(cfg.num_q_heads)], dtype=np.int32)
-        t0 = time.perf_counter()
-        oracle.decode(q, pool, g, w.block_tables_np, w.context_lens_np, w.scale,
-                      max_context_len=w.max_context_len, sel=sel)
+        if cfg.kv_int8:
+            oracle_build_blocks(w, s)           # cache construction, not timed
+            t0 = time.perf_counter()
+            oracle.decode_i8(q[s:s + 1], pool, g, w.block_tables_np[s:s + 1], w.context_lens_np[s:s + 1],
+                             w.scale, max_context_len=w.max_context_len)
+        else:
+            sel = np.array([[s, h] for h in range(cfg.num_q_heads)], dtype=np.int32)
+            t0 = time.perf_counter()
+            oracle.decode(q, pool, g, w.block_tables_np, w.context_lens_np, w.scale,
+                          max_context_len=w.max_context_len, sel=sel)
         t_total += time.perf_counter() - t0
         done_bytes += int(w.context_lens_np[s]) * kv_tok
         done_seqs += 1
@@ -347,13 +384,14 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": w.cfg.dtype, "data": "synthetic",
+            "vs_baseline": None, "dtype": w.cfg.dtype + ("+int8 cache" if w.cfg.kv_int8 else ""),
+            "data": "synthetic",
             "config": {"workload": DESCRIPTIONS[args.workload] + (f" (first {args.seqs} sequences)" if args.seqs else ""),
                        "global_batch": w.cfg.num_seqs * world,
                        "max_context_len": w.max_context_len, "tokens_in_context": int(w.context_lens_np.sum()),
                        "partition_size": _lib.decode_partition_size(args.partition_size, w.max_context_len),
                        "parallelism": f"replicas{world}",
-                       "l2": f"inputs larger than L2: {w.kv_cache.numel() * 2 / 1e9:.2f} GB pool, "
+                       "l2": f"inputs larger than L2: {step.kv_cache.numel() * step.kv_cache.element_size() / 1e9:.2f} GB pool, "
                              f"{nbytes['decode_kv'] / 1e9:.2f} GB of KV read per step"},
             "seq_steps_per_s": round(world * w.cfg.num_seqs / (ms * 1e-3), 1),
             "decode_kv_gbs": round(nbytes["decode_kv"] / (dec_ms * 1e-3) / 1e9, 2),

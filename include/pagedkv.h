@@ -41,8 +41,10 @@
  *               block table) set bits in the optional device error word
  *               `dev_err`; the affected item is skipped (its output zeroed).
  *               Kernels never trap.
- *   Types:      cache, query, key, value and output elements are fp16 or bf16
- *               (one dtype per call); arithmetic is fp32.
+ *   Types:      query, key, value and output elements are fp16 or bf16 (one
+ *               dtype per call); the cache holds the same 16-bit type, or 8-bit
+ *               codes with fp32 scales (PA_INT8_F16 / PA_INT8_BF16, below);
+ *               arithmetic is fp32.
  *
  * Cache layout (one layer; a pool may hold several layers `layer_stride_bytes`
  * apart).  The pool is num_blocks blocks; block b holds, for each kv head h,
@@ -56,6 +58,19 @@
  * so one bulk copy per chunk stages a block ready for both CUDA-core and
  * tensor-core consumers.  pa_cache_element_offset() computes the position of
  * any element.
+ *
+ * 8-bit cache (dtype PA_INT8_F16 / PA_INT8_BF16; head_size 128).  The TurboMind
+ * section of the inference-framework notes lists an "8bit KV Cache"; the scheme
+ * here is per token and per kv head symmetric quantisation: each stored K or V
+ * vector x gets scale = max|x| / 127 and codes round-half-even(x * (127 /
+ * max|x|)) clipped to [-127, 127], both decided in IEEE fp32 (an all-zero
+ * vector stores scale 0 and zero codes); the value a code stands for is
+ * code * scale.  Chunk (block, kv head) holds, in bytes: K codes [block_size]
+ * [128] row-major, V codes [block_size][128], K scales (fp32 [block_size]
+ * padded to a multiple of 16 bytes), V scales (same).  Chunk bytes =
+ * 2 * block_size * 128 + 2 * roundup16(4 * block_size); chunks are ordered by
+ * (block, kv head) as above.  pa_cache_element_offset() gives code byte
+ * offsets and pa_cache_scale_offset() scale byte offsets.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -76,7 +91,10 @@ typedef enum pa_status {
     PA_ERR_OUT_OF_BLOCKS = 5        /* block manager: not enough free blocks (nothing changed) */
 } pa_status;
 
-typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+/* Element types.  PA_F16 / PA_BF16: cache, query, key, value and output all of
+ * that type.  PA_INT8_F16 / PA_INT8_BF16: 8-bit cache (layout above) with
+ * query, key, value and output in fp16 / bf16. */
+typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1, PA_INT8_F16 = 2, PA_INT8_BF16 = 3 } pa_dtype;
 
 /* Bits of the device error word. */
 #define PA_DEVERR_BLOCK_ID 0x1u  /* a block-table entry that must be read is < 0 or >= num_blocks */
@@ -100,20 +118,30 @@ typedef struct pa_cache_desc {
 
 /* Bytes of one layer of the pool: num_blocks * num_kv_heads * 2 * block_size *
  * head_size * 2 (the KV-size formula of the mlqm.cn article, section 二.2.1,
- * rounded up to whole blocks).  Returns 0 for an invalid descriptor. */
+ * rounded up to whole blocks); for an 8-bit cache num_blocks * num_kv_heads *
+ * the chunk bytes given above.  Returns 0 for an invalid descriptor. */
 size_t pa_cache_bytes(const pa_cache_desc* desc);
 
-/* Element offset (in 16-bit elements from the start of a layer) of dim `dim` of
- * the K (part = 0) or V (part = 1) vector stored in slot `slot` of block `block`
- * for kv head `kv_head`.  Returns -1 for out-of-range arguments.  Host only. */
+/* Element offset (from the start of a layer, in cache elements: 16-bit elements,
+ * or bytes for an 8-bit cache) of dim `dim` of the K (part = 0) or V (part = 1)
+ * vector stored in slot `slot` of block `block` for kv head `kv_head`.  Returns
+ * -1 for out-of-range arguments.  Host only. */
 int64_t pa_cache_element_offset(const pa_cache_desc* desc, int64_t block, int32_t kv_head,
                                 int32_t part, int32_t slot, int32_t dim);
+
+/* Byte offset (from the start of a layer) of the fp32 scale of the K (part = 0)
+ * or V (part = 1) vector in slot `slot` of block `block`, kv head `kv_head`, of
+ * an 8-bit cache.  Returns -1 for a 16-bit cache or out-of-range arguments.
+ * Host only; this library's own addition (the notes name no layout). */
+int64_t pa_cache_scale_offset(const pa_cache_desc* desc, int64_t block, int32_t kv_head,
+                              int32_t part, int32_t slot);
 
 /* Write each new token's K and V into the cache.
  * Follows store_kvcache (nano-vLLM article, section 5.2.3): for token i with
  * slot = slot_mapping[i] != -1, block = slot / block_size and offset =
  * slot % block_size, the num_kv_heads x head_size K and V elements are copied
- * bit for bit into that slot of layer `layer`.
+ * bit for bit into that slot of layer `layer` (an 8-bit cache stores each head
+ * vector's codes and scale instead, quantised as described above).
  *   kv_cache     device pool (see layout above), 16-byte aligned.
  *   key, value   device [num_tokens, num_kv_heads, head_size], heads and dims
  *                contiguous; token strides key_token_stride / value_token_stride
@@ -162,7 +190,10 @@ int32_t pa_decode_partition_size(int32_t partition_size, int32_t max_context_len
  *   dev_err       optional device uint32 error word (PA_DEVERR_* bits).
  * Supported: head_size 64 or 128, block_size 1/2/4/8/16/32, num_q_heads a
  * multiple of num_kv_heads with group size 1, 2, 4 or 8, and 16 at head_size 128
- * with block_size >= 8 (PA_ERR_UNSUPPORTED otherwise). */
+ * with block_size >= 8 (PA_ERR_UNSUPPORTED otherwise).  An 8-bit cache
+ * (PA_INT8_F16 / PA_INT8_BF16) attends over code * scale: head_size 128, group
+ * size 1, 2, 4 or 8, any supported block_size; q and out are the dtype's 16-bit
+ * type; pa_decode_window with window or ring_blocks > 0 is PA_ERR_UNSUPPORTED. */
 pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,
                     const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
                     int32_t block_table_stride, const int32_t* context_lens, int32_t num_seqs,

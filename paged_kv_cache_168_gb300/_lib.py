@@ -20,12 +20,12 @@ _lib = None
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_WORKSPACE_TOO_SMALL, PA_ERR_OUT_OF_BLOCKS = range(6)
 PA_ALLOC_OK, PA_ALLOC_LATER, PA_ALLOC_NEVER = range(3)
-PA_F16, PA_BF16 = 0, 1
+PA_F16, PA_BF16, PA_INT8_F16, PA_INT8_BF16 = 0, 1, 2, 3
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_CONTEXT, DEVERR_TIMEOUT = 1, 2, 4, 8
 DTYPE_CODE = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 
 EXPORTED = [
-    "pa_cache_bytes", "pa_cache_element_offset", "pa_reshape_and_cache", "pa_decode_workspace_bytes",
+    "pa_cache_bytes", "pa_cache_element_offset", "pa_cache_scale_offset", "pa_reshape_and_cache", "pa_decode_workspace_bytes",
     "pa_decode_partition_size", "pa_decode", "pa_decode_window", "pa_decode_window_span",
     "pa_decode_static_workspace", "pa_copy_blocks", "pa_swap_blocks", "pa_read_device_errors",
     "pa_status_string", "pa_last_error_message",
@@ -55,7 +55,8 @@ class _Desc(ctypes.Structure):
 
 @dataclass
 class CacheDesc:
-    """Geometry of a cache pool (mirrors pa_cache_desc)."""
+    """Geometry of a cache pool (mirrors pa_cache_desc).  dtype is the 16-bit type
+    of q / K / V / out; kv_int8 stores the cache as 8-bit codes with fp32 scales."""
     num_blocks: int
     block_size: int
     num_kv_heads: int
@@ -63,10 +64,12 @@ class CacheDesc:
     dtype: torch.dtype = torch.float16
     num_layers: int = 1
     layer_stride_bytes: int = 0
+    kv_int8: bool = False
 
     def c(self) -> _Desc:
         return _Desc(self.num_blocks, self.block_size, self.num_kv_heads, self.head_size,
-                     DTYPE_CODE[self.dtype], self.num_layers, self.layer_stride_bytes)
+                     DTYPE_CODE[self.dtype] + (2 if self.kv_int8 else 0), self.num_layers,
+                     self.layer_stride_bytes)
 
 
 def load():
@@ -83,6 +86,8 @@ def load():
     lib.pa_cache_bytes.restype = sz
     lib.pa_cache_element_offset.argtypes = [D, i64, i32, i32, i32, i32]
     lib.pa_cache_element_offset.restype = i64
+    lib.pa_cache_scale_offset.argtypes = [D, i64, i32, i32, i32]
+    lib.pa_cache_scale_offset.restype = i64
     lib.pa_reshape_and_cache.argtypes = [P, D, i32, P, i64, P, i64, P, i32, P, P]
     lib.pa_reshape_and_cache.restype = ctypes.c_int
     lib.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
@@ -171,6 +176,10 @@ def cache_bytes(desc: CacheDesc) -> int:
 
 def cache_element_offset(desc: CacheDesc, block: int, kv_head: int, part: int, slot: int, dim: int) -> int:
     return load().pa_cache_element_offset(ctypes.byref(desc.c()), block, kv_head, part, slot, dim)
+
+
+def cache_scale_offset(desc: CacheDesc, block: int, kv_head: int, part: int, slot: int) -> int:
+    return load().pa_cache_scale_offset(ctypes.byref(desc.c()), block, kv_head, part, slot)
 
 
 def reshape_and_cache(kv_cache: torch.Tensor, desc: CacheDesc, key: torch.Tensor, value: torch.Tensor,

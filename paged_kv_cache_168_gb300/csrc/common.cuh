@@ -34,6 +34,23 @@ struct Layout {
   }
 };
 
+// 8-bit cache (head_size 128): chunk = K codes [bs][128] | V codes [bs][128] |
+// K scales fp32 [bs] | V scales fp32 [bs], each scale area padded to 16 bytes;
+// the 16-byte piece c of the code row of slot t sits at piece (c ^ (t & 7)).
+struct I8Layout {
+  int bs, Hkv;
+  static constexpr int D = 128;
+  __host__ __device__ int64_t scale_bytes() const { return ((int64_t)bs * 4 + 15) / 16 * 16; }
+  __host__ __device__ int64_t chunk_bytes() const { return 2LL * bs * D + 2 * scale_bytes(); }
+  __host__ __device__ int64_t chunk(int64_t block, int head) const { return (block * Hkv + head) * chunk_bytes(); }
+  __host__ __device__ int64_t code(int64_t block, int head, int part, int t, int d) const {
+    return chunk(block, head) + (int64_t)(part * bs + t) * D + ((((d >> 4) ^ (t & 7)) << 4) | (d & 15));
+  }
+  __host__ __device__ int64_t scale(int64_t block, int head, int part, int t) const {
+    return chunk(block, head) + 2LL * bs * D + part * scale_bytes() + 4LL * t;
+  }
+};
+
 // ------------------------------------------------------------------ element types
 template <typename T> struct Elem;
 template <> struct Elem<__half> {

@@ -71,6 +71,12 @@ cudaError_t launch_reshape_and_cache(uint8_t* layer_base, int32_t num_blocks, in
                                      const int64_t* slot_mapping, int32_t n, uint32_t* dev_err,
                                      cudaStream_t stream);
 
+// 8-bit cache (head_size 128); key / value in act_dtype (PA_F16 or PA_BF16).
+cudaError_t launch_reshape_and_cache_i8(uint8_t* layer_base, int32_t num_blocks, int32_t block_size,
+                                        int32_t num_kv_heads, int act_dtype, const void* key, int64_t key_stride,
+                                        const void* value, int64_t value_stride, const int64_t* slot_mapping,
+                                        int32_t n, uint32_t* dev_err, cudaStream_t stream);
+
 // Copies `pairs.n` whole blocks of `block_bytes` for each of `layers` layers.
 cudaError_t launch_block_copy(uint8_t* dst, int64_t dst_layer_stride, const uint8_t* src,
                               int64_t src_layer_stride, int64_t block_bytes, int32_t layers,
@@ -89,5 +95,9 @@ cudaError_t launch_merge(const DecodeParams& p, int dtype, int head_size, cudaSt
 // at most kTcMaxSeqs sequences.  Launches the decode kernel and the merge.
 constexpr int kTcMaxSeqs = 8192;
 cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, int group, int num_sms, cudaStream_t stream);
+
+// Paged decode over an 8-bit cache on CUDA cores: head_size 128, group 1/2/4/8;
+// q / out in act_dtype.  Launches the decode kernel and the merge.
+cudaError_t launch_decode_i8(const DecodeParams& p, int act_dtype, int group, cudaStream_t stream);
 
 }  // namespace pkv

@@ -46,7 +46,13 @@ bool use_tensor_cores(int head_size, int block_size, int group, int num_seqs) {
   return !(env && strcmp(env, "simt") == 0);
 }
 
+bool is_i8(const pa_cache_desc* d) { return d->dtype == PA_INT8_F16 || d->dtype == PA_INT8_BF16; }
+
+// 16-bit type of q, key, value and out (and of a 16-bit cache).
+int act_dtype(const pa_cache_desc* d) { return d->dtype == PA_INT8_BF16 || d->dtype == PA_BF16 ? PA_BF16 : PA_F16; }
+
 int64_t block_bytes(const pa_cache_desc* d) {
+  if (is_i8(d)) return (int64_t)d->num_kv_heads * pkv::I8Layout{d->block_size, d->num_kv_heads}.chunk_bytes();
   return (int64_t)d->num_kv_heads * 2 * d->block_size * d->head_size * 2;
 }
 
@@ -54,9 +60,11 @@ pa_status check_desc(const pa_cache_desc* d) {
   if (!d) return fail(PA_ERR_INVALID_ARG, "desc is NULL");
   if (d->num_blocks <= 0 || d->num_kv_heads <= 0 || d->num_layers <= 0)
     return fail(PA_ERR_INVALID_ARG, "num_blocks, num_kv_heads and num_layers must be > 0");
-  if (d->dtype != PA_F16 && d->dtype != PA_BF16) return fail(PA_ERR_INVALID_ARG, "dtype %d", d->dtype);
+  if (d->dtype < PA_F16 || d->dtype > PA_INT8_BF16) return fail(PA_ERR_INVALID_ARG, "dtype %d", d->dtype);
   if (d->head_size != 64 && d->head_size != 128)
     return fail(PA_ERR_UNSUPPORTED, "head_size %d (supported: 64, 128)", d->head_size);
+  if (is_i8(d) && d->head_size != 128)
+    return fail(PA_ERR_UNSUPPORTED, "8-bit cache with head_size %d (supported: 128)", d->head_size);
   if (d->block_size != 1 && d->block_size != 2 && d->block_size != 4 && d->block_size != 8 &&
       d->block_size != 16 && d->block_size != 32)
     return fail(PA_ERR_UNSUPPORTED, "block_size %d (supported: 1, 2, 4, 8, 16, 32)", d->block_size);
@@ -135,8 +143,18 @@ int64_t pa_cache_element_offset(const pa_cache_desc* desc, int64_t block, int32_
   if (block < 0 || block >= desc->num_blocks || kv_head < 0 || kv_head >= desc->num_kv_heads || part < 0 ||
       part > 1 || slot < 0 || slot >= desc->block_size || dim < 0 || dim >= desc->head_size)
     return -1;
+  if (is_i8(desc)) return pkv::I8Layout{desc->block_size, desc->num_kv_heads}.code(block, kv_head, part, slot, dim);
   pkv::Layout L{desc->block_size, desc->head_size, desc->num_kv_heads};
   return L.offset(block, kv_head, part, slot, dim);
+}
+
+int64_t pa_cache_scale_offset(const pa_cache_desc* desc, int64_t block, int32_t kv_head, int32_t part,
+                              int32_t slot) {
+  if (check_desc(desc) != PA_OK || !is_i8(desc)) return -1;
+  if (block < 0 || block >= desc->num_blocks || kv_head < 0 || kv_head >= desc->num_kv_heads || part < 0 ||
+      part > 1 || slot < 0 || slot >= desc->block_size)
+    return -1;
+  return pkv::I8Layout{desc->block_size, desc->num_kv_heads}.scale(block, kv_head, part, slot);
 }
 
 pa_status pa_reshape_and_cache(void* kv_cache, const pa_cache_desc* desc, int32_t layer, const void* key,
@@ -158,6 +176,13 @@ pa_status pa_reshape_and_cache(void* kv_cache, const pa_cache_desc* desc, int32_
   if (key_token_stride < row || value_token_stride < row || key_token_stride % 8 || value_token_stride % 8)
     return fail(PA_ERR_INVALID_ARG, "token strides must be >= num_kv_heads*head_size and multiples of 8");
   uint8_t* base = static_cast<uint8_t*>(kv_cache) + layer * layer_stride(desc);
+  if (is_i8(desc)) {
+    cudaError_t e = pkv::launch_reshape_and_cache_i8(base, desc->num_blocks, desc->block_size, desc->num_kv_heads,
+                                                     act_dtype(desc), key, key_token_stride, value,
+                                                     value_token_stride, slot_mapping, num_tokens, dev_err,
+                                                     static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "reshape_and_cache launch");
+  }
   cudaError_t e = pkv::launch_reshape_and_cache(base, desc->num_blocks, desc->block_size, desc->num_kv_heads,
                                                 desc->head_size, key, key_token_stride, value,
                                                 value_token_stride, slot_mapping, num_tokens, dev_err,
@@ -208,6 +233,10 @@ pa_status pa_decode_window(void* out, const void* q, int64_t q_seq_stride, const
     return fail(PA_ERR_UNSUPPORTED,
                 "query heads per kv head %d (supported: 1, 2, 4, 8; 16 at head_size 128 with block_size >= 8)", group);
   if (desc->num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads > 65535");
+  if (is_i8(desc) && group > 8)
+    return fail(PA_ERR_UNSUPPORTED, "8-bit cache with %d query heads per kv head (supported: 1, 2, 4, 8)", group);
+  if (is_i8(desc) && (window > 0 || ring_blocks > 0))
+    return fail(PA_ERR_UNSUPPORTED, "8-bit cache with a window or ring tables");
   if (!out || !q || !kv_cache || !block_tables || !context_lens)
     return fail(PA_ERR_INVALID_ARG, "out, q, kv_cache, block_tables and context_lens must be non-NULL");
   if (!aligned16(out) || !aligned16(q) || !aligned16(kv_cache))
@@ -258,7 +287,9 @@ pa_status pa_decode_window(void* out, const void* q, int64_t q_seq_stride, const
                  : nullptr;
   p.dev_err = dev_err;
   cudaError_t e;
-  if (use_tensor_cores(desc->head_size, desc->block_size, group, num_seqs)) {
+  if (is_i8(desc)) {
+    e = pkv::launch_decode_i8(p, act_dtype(desc), group, static_cast<cudaStream_t>(stream));
+  } else if (use_tensor_cores(desc->head_size, desc->block_size, group, num_seqs)) {
     int dev = 0, sms = 0;
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -15,12 +15,23 @@ from .workloads import Workload
 
 
 class DecodeStep:
+    """One decode step over a workload.  For an 8-bit cache the pool is built
+    here (outside any timed step) by writing the workload's logical history into
+    every slot of every block with pa_reshape_and_cache, which quantises it."""
+
     def __init__(self, w: Workload, partition_size: int = 0, stream: torch.cuda.Stream | None = None):
         cfg = w.cfg
         dev = w.q.device
         self.w = w
         self.stream = stream or torch.cuda.current_stream(dev)
-        self.desc = _lib.CacheDesc(w.num_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_size, w.dtype)
+        self.desc = _lib.CacheDesc(w.num_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_size, w.dtype,
+                                   kv_int8=cfg.kv_int8)
+        self.block_bytes = _lib.cache_bytes(self.desc) // w.num_blocks
+        if cfg.kv_int8:
+            self.kv_cache = torch.zeros(_lib.cache_bytes(self.desc), dtype=torch.uint8, device=dev)
+            self.fill_from_logical(w.kv_logical)
+        else:
+            self.kv_cache = w.kv_cache
         self.partition_size = partition_size
         self.out = torch.empty_like(w.q)
         nbytes = _lib.decode_workspace_bytes(cfg.num_seqs, cfg.num_q_heads, cfg.head_size, w.max_context_len,
@@ -30,22 +41,33 @@ class DecodeStep:
         self.host_pool = None
         if w.host_blocks:
             self.host_desc = _lib.CacheDesc(w.host_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_size,
-                                            w.dtype)
-            self.host_pool = torch.empty(w.host_blocks * w.kv_cache[0].numel(), dtype=w.dtype).pin_memory()
+                                            w.dtype, kv_int8=cfg.kv_int8)
+            self.host_pool = torch.empty(w.host_blocks * self.block_bytes, dtype=torch.uint8).pin_memory()
+
+    def fill_from_logical(self, logical: torch.Tensor, chunk_blocks: int = 4096):
+        """Write logical K/V [NB, Hkv, 2, bs, D] into slot b * bs + t of every block b."""
+        NB, Hkv, _, bs, D = logical.shape
+        for b0 in range(0, NB, chunk_blocks):
+            part = logical[b0:b0 + chunk_blocks]
+            n = part.shape[0] * bs
+            key = part[:, :, 0].permute(0, 2, 1, 3).reshape(n, Hkv, D).contiguous()
+            value = part[:, :, 1].permute(0, 2, 1, 3).reshape(n, Hkv, D).contiguous()
+            slots = torch.arange(b0 * bs, b0 * bs + n, dtype=torch.int64, device=logical.device)
+            _lib.reshape_and_cache(self.kv_cache, self.desc, key, value, slots, stream=self.stream)
 
     def cache_ops(self):
         w, s = self.w, self.stream
         if self.host_pool is not None:
-            _lib.swap_blocks(self.host_pool, self.host_desc, w.kv_cache, self.desc, 0, w.swap_out_pairs, stream=s)
-            _lib.swap_blocks(w.kv_cache, self.desc, self.host_pool, self.host_desc, 1, w.swap_in_pairs, stream=s)
+            _lib.swap_blocks(self.host_pool, self.host_desc, self.kv_cache, self.desc, 0, w.swap_out_pairs, stream=s)
+            _lib.swap_blocks(self.kv_cache, self.desc, self.host_pool, self.host_desc, 1, w.swap_in_pairs, stream=s)
         if w.copy_pairs.shape[0]:
-            _lib.copy_blocks(w.kv_cache, self.desc, w.copy_pairs, stream=s)
-        _lib.reshape_and_cache(w.kv_cache, self.desc, w.key, w.value, w.slot_mapping, dev_err=self.dev_err,
+            _lib.copy_blocks(self.kv_cache, self.desc, w.copy_pairs, stream=s)
+        _lib.reshape_and_cache(self.kv_cache, self.desc, w.key, w.value, w.slot_mapping, dev_err=self.dev_err,
                                stream=s)
 
     def attention(self, q=None, out=None):
         w = self.w
-        _lib.decode(self.out if out is None else out, w.q if q is None else q, w.kv_cache, self.desc,
+        _lib.decode(self.out if out is None else out, w.q if q is None else q, self.kv_cache, self.desc,
                     w.block_tables, w.context_lens, w.max_context_len, w.scale, self.workspace,
                     self.partition_size, dev_err=self.dev_err, stream=self.stream)
 
@@ -71,13 +93,15 @@ class DecodeStep:
         """Bytes the method must move per step (what each kernel reads + writes)."""
         w, cfg = self.w, self.w.cfg
         esz = 2
-        kv_tok = 2 * cfg.num_kv_heads * cfg.head_size * esz
+        in_tok = 2 * cfg.num_kv_heads * cfg.head_size * esz        # one token's K and V, 16-bit
+        # one token's K and V as stored: 16-bit, or 8-bit codes + two fp32 scales per kv head
+        kv_tok = cfg.num_kv_heads * (2 * cfg.head_size + 8) if cfg.kv_int8 else in_tok
         ctx = w.context_lens_np.astype("int64")
         nblk = -(-ctx // cfg.block_size)
         decode = int(ctx.sum()) * kv_tok + 2 * cfg.num_seqs * cfg.num_q_heads * cfg.head_size * esz \
             + 4 * int(nblk.sum()) + 4 * cfg.num_seqs
-        reshape = 2 * cfg.num_seqs * kv_tok + 8 * cfg.num_seqs
-        block_bytes = w.kv_cache[0].numel() * esz
+        reshape = cfg.num_seqs * (in_tok + kv_tok) + 8 * cfg.num_seqs
+        block_bytes = self.block_bytes
         copy = 2 * w.copy_pairs.shape[0] * block_bytes
         swap = (w.swap_out_pairs.shape[0] + w.swap_in_pairs.shape[0]) * block_bytes * 2
         return {"decode": decode, "decode_kv": int(ctx.sum()) * kv_tok, "reshape": reshape, "copy": copy,

@@ -44,6 +44,7 @@ class Config:
     pool_blocks: int = 0    # fixed pool size; 0 -> 1.2 x the blocks the tables need
     beams: int = 1          # beams per prompt group (beam workload)
     swap_fraction: float = 0.0
+    kv_int8: bool = False   # cache stored as 8-bit codes + scales (q/out/K/V stay `dtype`)
 
     @property
     def seed(self) -> int:
@@ -69,6 +70,9 @@ CONFIGS = {
                swap_fraction=0.10),
         # token-granular paging (block_size 1) on the Llama-2-7B-shaped layer
         Config("7b_bs1", 5, 64, 32, 32, 128, 1, "f16", "normal", ("uniform", 512, 4096)),
+        # 8-bit KV cache on the 7B- and 8B-shaped layers
+        Config("7b_int8", 6, 64, 32, 32, 128, 16, "f16", "normal", ("uniform", 512, 4096), kv_int8=True),
+        Config("8b_int8", 7, 256, 32, 8, 128, 16, "bf16", "normal", ("lognormal", 1024, 0.8, 8192), kv_int8=True),
     ]
 }
 
@@ -80,7 +84,7 @@ class Workload:
     q: torch.Tensor                  # [S, Hq, D]
     key: torch.Tensor                # [S, Hkv, D]  new token's K
     value: torch.Tensor              # [S, Hkv, D]  new token's V
-    kv_cache: torch.Tensor           # [NB, Hkv, 2 * bs * D] opaque chunks
+    kv_cache: torch.Tensor           # [NB, Hkv, 2 * bs * D] opaque chunks (16-bit caches; None for 8-bit)
     block_tables: torch.Tensor       # int32 [S, max_blocks_per_seq], unused entries = -1
     context_lens: torch.Tensor       # int32 [S], includes the new token
     slot_mapping: torch.Tensor       # int64 [S]
@@ -97,6 +101,10 @@ class Workload:
     swap_out_pairs: np.ndarray = field(default_factory=lambda: np.zeros((0, 2), np.int64))
     swap_in_pairs: np.ndarray = field(default_factory=lambda: np.zeros((0, 2), np.int64))
     host_blocks: int = 0
+    # 8-bit caches: the history as logical 16-bit values [NB, Hkv, 2 (K, V), bs, D];
+    # every slot of every block holds a drawn vector, quantised by whichever side
+    # builds the cache from it
+    kv_logical: torch.Tensor = None
 
     @property
     def dtype(self) -> torch.dtype:
@@ -213,6 +221,10 @@ def make_workload(name_or_cfg, device="cpu", seed: int | None = None, nan_unused
     pool = torch.empty((NB, Hkv, 2 * bs * D), dtype=dt, device=dev)
     for t in (q, key, value, pool):
         fill_values(t, cfg.values, gen)
+    logical = None
+    if cfg.kv_int8:
+        logical, pool = pool.view(NB, Hkv, 2, bs, D), None
+        nan_unused = False      # an 8-bit cache has no NaN codes to plant
     if nan_unused:
         keep = np.zeros(NB, dtype=bool)
         keep[used] = True
@@ -230,7 +242,7 @@ def make_workload(name_or_cfg, device="cpu", seed: int | None = None, nan_unused
         max_context_len=int(cap), scale=1.0 / math.sqrt(D),
         block_tables_np=tables, context_lens_np=ctx, slot_mapping_np=slots, used_blocks=used,
         block_tables_before_cow_np=before, copy_pairs=copy_pairs,
-        swap_out_pairs=swap_out, swap_in_pairs=swap_in, host_blocks=host_blocks,
+        swap_out_pairs=swap_out, swap_in_pairs=swap_in, host_blocks=host_blocks, kv_logical=logical,
     )
 
 

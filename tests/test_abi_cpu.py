@@ -12,6 +12,7 @@ import torch
 import oracle
 from paged_kv_cache_168_gb300 import _lib, build as build_mod
 from paged_kv_cache_168_gb300._lib import CacheDesc
+from paged_helpers import to_bits
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -146,3 +147,57 @@ def test_swap_rejects_mismatched_pools(lib):
 
 def test_read_device_errors_rejects_null(lib):
     assert lib.pa_read_device_errors(None, None, 0, None) == _lib.PA_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- 8-bit cache (host side)
+
+def test_int8_cache_bytes(lib):
+    # per block and kv head: K and V codes (2 x bs x 128 bytes) + two fp32 scale areas padded to 16 bytes
+    assert _lib.cache_bytes(CacheDesc(10, 16, 2, 128, kv_int8=True)) == 10 * 2 * (2 * 16 * 128 + 2 * 64)
+    assert _lib.cache_bytes(CacheDesc(10, 1, 2, 128, kv_int8=True)) == 10 * 2 * (2 * 128 + 2 * 16)
+    assert _lib.cache_bytes(CacheDesc(10, 2, 3, 128, kv_int8=True)) == 10 * 3 * (2 * 2 * 128 + 2 * 16)
+    assert _lib.cache_bytes(CacheDesc(10, 16, 2, 64, kv_int8=True)) == 0     # 8-bit needs head_size 128
+    for bs in (1, 2, 4, 8, 16, 32):
+        g = oracle.Geom(5, bs, 3, 128, "bf16")
+        assert _lib.cache_bytes(CacheDesc(5, bs, 3, 128, torch.bfloat16, kv_int8=True)) == 5 * oracle.i8_block_bytes(g)
+
+
+@pytest.mark.parametrize("bs", [1, 2, 8, 16, 32])
+def test_int8_offsets_point_at_what_the_oracle_writes(lib, bs):
+    # A vector with one non-zero element d quantises to code 127 at d, zeros
+    # elsewhere, and scale |x_d| / 127: the library's offsets must find them.
+    rng = np.random.default_rng(bs)
+    nb, hkv = 3, 2
+    g = oracle.Geom(nb, bs, hkv, 128, "f16")
+    d = CacheDesc(nb, bs, hkv, 128, torch.float16, kv_int8=True)
+    for _ in range(12):
+        slot, h, part, dim = int(rng.integers(nb * bs)), int(rng.integers(hkv)), int(rng.integers(2)), \
+            int(rng.integers(128))
+        pool = np.zeros(nb * oracle.i8_block_bytes(g), np.uint8)
+        kv = np.zeros((2, 1, hkv, 128))
+        kv[part, 0, h, dim] = 2.5
+        assert oracle.reshape_and_cache_i8(pool, g, to_bits(kv[0], "f16"), to_bits(kv[1], "f16"),
+                                           np.array([slot])) == 0
+        b, t = slot // bs, slot % bs
+        off = _lib.cache_element_offset(d, b, h, part, t, dim)
+        assert pool.view(np.int8)[off] == 127
+        assert int(np.count_nonzero(pool.view(np.int8) == 127)) == 1
+        so = _lib.cache_scale_offset(d, b, h, part, t)
+        assert so % 4 == 0 and pool[so:so + 4].view(np.float32)[0] == np.float32(2.5) / np.float32(127)
+    assert _lib.cache_scale_offset(CacheDesc(nb, bs, hkv, 128), 0, 0, 0, 0) == -1    # 16-bit cache
+    assert _lib.cache_scale_offset(d, nb, 0, 0, 0) == -1
+
+
+def test_int8_decode_limits(lib):
+    d8 = _desc(dtype=torch.bfloat16, kv_int8=True)
+    assert _decode(lib, desc=d8, Hq=32) == _lib.PA_ERR_UNSUPPORTED        # group 16
+    assert _decode(lib, desc=_desc(kv_int8=True, head_size=64)) == _lib.PA_ERR_UNSUPPORTED
+    st = lib.pa_decode_window(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 4 * 128, ctypes.c_void_p(FAKE),
+                              ctypes.byref(d8), 0, ctypes.c_void_p(FAKE), 8, ctypes.c_void_p(FAKE), 2, 4, 100,
+                              0.1, 64, 0, 0, None, 0, None, None)
+    assert st == _lib.PA_ERR_UNSUPPORTED                                    # no window over 8-bit caches
+    # an 8-bit pool and a 16-bit pool are different geometries for swapping
+    arr = np.array([[0, 1]], np.int64)
+    st = lib.pa_swap_blocks(ctypes.c_void_p(FAKE), ctypes.byref(_desc()), ctypes.c_void_p(FAKE),
+                            ctypes.byref(_desc(kv_int8=True)), 0, arr.ctypes.data_as(ctypes.c_void_p), 1, None)
+    assert st == _lib.PA_ERR_INVALID_ARG

@@ -122,6 +122,8 @@ def _load():
     lib.oracle_decode_i8.restype = ctypes.c_int
     lib.oracle_copy_blocks_bytes.argtypes = [P, i64, i32, i32, i64, P, i32]
     lib.oracle_copy_blocks_bytes.restype = ctypes.c_int
+    lib.oracle_prefill.argtypes = [P, P, i64, P, G, P, i32, P, P, i32, i32, dbl, i32]
+    lib.oracle_prefill.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     _lib = lib
@@ -261,6 +263,22 @@ def swap_blocks(dst: np.ndarray, dst_geom: Geom, src: np.ndarray, src_geom: Geom
 # ---------------------------------------------------------------- 8-bit KV cache
 # Geom.dtype names the 16-bit type of q / new K,V / output ("f16" or "bf16");
 # the pool holds int8 codes and fp32 scales (uint8 arrays here).
+
+def prefill(q: np.ndarray, layer: np.ndarray, geom: Geom, block_tables: np.ndarray, context_lens: np.ndarray,
+            query_start_loc: np.ndarray, scale: float, nthreads: int = 0):
+    """Causal prefill / extend over the paged cache: q uint16 [T, Hq, D] packed by
+    query_start_loc (int32 [S + 1]); returns (out [T, Hq, D] fp64, error bits)."""
+    q, layer = _u16(q), _u16(layer)
+    T, Hq, D = q.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    assert qsl.shape[0] == cl.shape[0] + 1
+    out = np.zeros((T, Hq, D))
+    err = _load().oracle_prefill(_ptr(out), _ptr(q), Hq * D, _ptr(layer), ctypes.byref(geom.c()), _ptr(bt),
+                                 bt.shape[1], _ptr(cl), _ptr(qsl), cl.shape[0], Hq, scale, nthreads)
+    return out, err
+
 
 def i8_block_bytes(geom: Geom) -> int:
     """Bytes of one block (all kv heads) of an 8-bit cache."""

@@ -269,6 +269,63 @@ int oracle_decode(double* out, const uint16_t* q, int64_t q_seq_stride, const ui
                                 num_seqs, num_q_heads, max_context_len, scale, 0, 0, sel, nsel, nthreads);
 }
 
+/* ---------------- prefill / extend over the paged cache ---------------- */
+
+/* Several new tokens per sequence (a whole prompt, or one chunk of it under
+ * chunked prefill: the FAQ's vLLM scheduler notes and the "vLLM" page's
+ * prefill/decoding description).  Sequence s owns query tokens
+ * query_start_loc[s] .. query_start_loc[s+1]-1 (q_len of them); they are the
+ * newest q_len positions of its context, already written to the cache, so
+ * query j sits at position ctx - q_len + j and attends (causally) positions
+ * 0 .. ctx - q_len + j through the block table.  For each (token, query head):
+ * gather, then contiguous attention over those positions.  out is
+ * [total tokens][num_q_heads][D] doubles.  q_len <= 0 writes nothing; a
+ * sequence with q_len > ctx or ctx beyond its table row gives zeros and
+ * ORC_ERR_CONTEXT; a bad block id gives zeros and ORC_ERR_BLOCK_ID. */
+int oracle_prefill(double* out, const uint16_t* q, int64_t q_token_stride, const uint16_t* layer,
+                   const oracle_geom* g, const int32_t* block_tables, int32_t bt_stride,
+                   const int32_t* context_lens, const int32_t* query_start_loc, int32_t num_seqs,
+                   int32_t num_q_heads, double scale, int32_t nthreads) {
+    const int32_t D = g->head_size;
+    const int32_t G = num_q_heads / g->num_kv_heads;
+    int err = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+#endif
+    for (int64_t it = 0; it < (int64_t)num_seqs * num_q_heads; ++it) {
+        const int32_t s = (int32_t)(it / num_q_heads), h = (int32_t)(it % num_q_heads);
+        const int32_t first = query_start_loc[s], q_len = query_start_loc[s + 1] - first;
+        const int32_t ctx = context_lens[s];
+        if (q_len <= 0) continue;
+        for (int32_t j = 0; j < q_len; ++j)
+            for (int32_t d = 0; d < D; ++d) out[((int64_t)(first + j) * num_q_heads + h) * D + d] = 0.0;
+        if (q_len > ctx || (int64_t)ctx > (int64_t)bt_stride * g->block_size) {
+            err |= ORC_ERR_CONTEXT;
+            continue;
+        }
+        double* K = (double*)malloc(sizeof(double) * (size_t)ctx * D);
+        double* V = (double*)malloc(sizeof(double) * (size_t)ctx * D);
+        double* qd = (double*)malloc(sizeof(double) * (size_t)D);
+        const int e = oracle_gather(layer, g, block_tables + (int64_t)s * bt_stride, ctx, h / G, K, V);
+        if (e) {
+            err |= e;
+        } else {
+            for (int32_t j = 0; j < q_len; ++j) {
+                const int64_t tok = first + j;
+                for (int32_t d = 0; d < D; ++d)
+                    qd[d] = elem_to_double(q[tok * q_token_stride + (int64_t)h * D + d], g->dtype);
+                oracle_contiguous_attention(qd, K, V, ctx - q_len + j + 1, D, scale,
+                                            out + (tok * num_q_heads + h) * D);
+            }
+        }
+        free(K);
+        free(V);
+        free(qd);
+    }
+    return err;
+}
+
 /* ---------------- 8-bit KV cache ---------------- */
 
 /* An 8-bit cache ("8bit KV Cache" quantisation, the TurboMind section of the

@@ -460,3 +460,88 @@ def test_byte_block_copy_matches_numpy():
     ref[[5, 2]] = ref[[0, 1]]
     assert oracle.copy_blocks_bytes(pool, 300, 7, np.array([[0, 5], [1, 2]])) == 0
     assert np.array_equal(pool.reshape(7, 300), ref)
+
+
+# ---------------------------------------------------------------- prefill / extend
+
+def _prefill_case(rng, q_lens, ctx, Hq=4, Hkv=2, D=64, bs=16, dtype="f16"):
+    """Paged history for each sequence, plus its last q_len tokens as packed queries."""
+    p = Paged(rng, S=len(ctx), Hq=Hq, Hkv=Hkv, D=D, bs=bs, ctx=ctx, dtype=dtype)
+    qsl = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    q_bits = to_bits(rng.standard_normal((int(qsl[-1]), Hq, D)), dtype)
+    return p, qsl, q_bits
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_prefill_of_whole_prompts_equals_causal_sdpa(dtype):
+    rng = np.random.default_rng(40)
+    ctx = [1, 17, 40, 33]
+    p, qsl, qb = _prefill_case(rng, ctx, ctx, dtype=dtype)      # q_len == ctx: a prompt from scratch
+    got, err = oracle.prefill(qb, p.pool, p.geom, p.tables, p.ctx, qsl, 0.125)
+    assert err == 0
+    q = bits_to_f64(qb, dtype)
+    for s, c in enumerate(ctx):
+        qs = torch.from_numpy(q[qsl[s]:qsl[s + 1]]).permute(1, 0, 2)                        # [Hq, c, D]
+        K = torch.from_numpy(p.K[s]).permute(1, 0, 2).repeat_interleave(2, 0)
+        V = torch.from_numpy(p.V[s]).permute(1, 0, 2).repeat_interleave(2, 0)
+        ref = torch.nn.functional.scaled_dot_product_attention(qs, K, V, is_causal=True, scale=0.125)
+        assert np.allclose(got[qsl[s]:qsl[s + 1]], ref.permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_extend_rows_equal_decodes_at_their_positions():
+    rng = np.random.default_rng(41)
+    ctx, q_lens = [50, 20, 130, 9], [7, 20, 1, 3]
+    p, qsl, qb = _prefill_case(rng, q_lens, ctx, Hq=8, Hkv=2, D=128, bs=8, dtype="bf16")
+    got, err = oracle.prefill(qb, p.pool, p.geom, p.tables, p.ctx, qsl, 0.09)
+    assert err == 0
+    for s in range(len(ctx)):
+        for j in range(q_lens[s]):
+            pos = ctx[s] - q_lens[s] + j
+            tok = qsl[s] + j
+            ref, e = oracle.decode(qb[tok:tok + 1], p.pool, p.geom, p.tables[s:s + 1],
+                                   np.array([pos + 1], np.int32), 0.09)
+            assert e == 0 and np.allclose(got[tok], ref[0], rtol=1e-13, atol=1e-13)
+
+
+def test_chunked_prefill_equals_one_shot_prefill():
+    rng = np.random.default_rng(42)
+    total = 45
+    p, qsl, qb = _prefill_case(rng, [total], [total], Hq=2, Hkv=1)
+    whole, e = oracle.prefill(qb, p.pool, p.geom, p.tables, p.ctx, qsl, 0.2)
+    assert e == 0
+    done = 0
+    for chunk in (16, 16, 13):          # the same prompt in three chunks over a growing context
+        part, e = oracle.prefill(qb[done:done + chunk], p.pool, p.geom, p.tables, np.array([done + chunk], np.int32),
+                                 np.array([0, chunk], np.int32), 0.2)
+        assert e == 0 and np.allclose(part, whole[done:done + chunk], rtol=1e-13, atol=1e-13)
+        done += chunk
+
+
+def test_prefill_with_identical_keys_averages_the_causal_prefix():
+    # every key equal -> uniform weights over the attended positions: query j of a
+    # chunk at position ctx - q_len + j gets the mean of V[0 .. that position]
+    rng = np.random.default_rng(43)
+    ctx, q_len = 30, 6
+    p = Paged(rng, S=1, Hq=1, Hkv=1, D=64, bs=16, ctx=[ctx], dtype="f16")
+    p.K[0][:] = p.K[0][0]
+    p.write_all()
+    qb = to_bits(rng.standard_normal((q_len, 1, 64)), "f16")
+    got, e = oracle.prefill(qb, p.pool, p.geom, p.tables, p.ctx, np.array([0, q_len], np.int32), 0.3)
+    assert e == 0
+    for j in range(q_len):
+        pos = ctx - q_len + j
+        assert np.allclose(got[j, 0], p.V[0][:pos + 1, 0].mean(axis=0), rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_error_cases():
+    rng = np.random.default_rng(44)
+    p, qsl, qb = _prefill_case(rng, [5, 3, 2], [20, 2, 40])       # second sequence: q_len 3 > ctx 2
+    got, err = oracle.prefill(qb, p.pool, p.geom, p.tables, p.ctx, qsl, 0.1)
+    assert err == oracle.ERR_CONTEXT and np.all(got[5:8] == 0) and np.any(got[:5] != 0)
+    tables = p.tables.copy()
+    tables[2, 1] = p.num_blocks + 1
+    got, err = oracle.prefill(qb, p.pool, p.geom, tables, p.ctx, qsl, 0.1)
+    assert err & oracle.ERR_BLOCK_ID and np.all(got[8:] == 0) and np.any(got[:5] != 0)
+    # a sequence with no new tokens contributes no rows
+    got, err = oracle.prefill(qb[:5], p.pool, p.geom, p.tables[:2], p.ctx[:2], np.array([0, 5, 5], np.int32), 0.1)
+    assert err == 0 and got.shape == (5, 4, 64)

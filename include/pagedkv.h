@@ -19,6 +19,10 @@
  *   pa_copy_blocks        copy-on-write block copies ("vLLM" page, section
  *                         "CacheEngine": copy / copy_blocks; mlqm.cn article,
  *                         Copy-on-Write example).
+ *   pa_prefill            several new query tokens per sequence (a prompt or
+ *                         a chunk of one) attend causally over the paged cache
+ *                         ("vLLM" page, prefill vs decoding; FAQ, chunked
+ *                         prefill).
  *   pa_swap_blocks        whole-block moves between the GPU cache and a pinned
  *                         CPU cache ("vLLM" page, section "CacheEngine":
  *                         swap_in = CPU->GPU, swap_out = GPU->CPU; section
@@ -200,6 +204,34 @@ pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* 
                     int32_t num_q_heads, int32_t max_context_len, float scale,
                     int32_t partition_size, void* workspace, size_t workspace_bytes,
                     uint32_t* dev_err, void* stream);
+
+/* Causal prefill / extend attention over the paged cache (several new tokens per
+ * sequence: a whole prompt, or one chunk of it under chunked prefill -- the
+ * "vLLM" page's prefill/decoding description and the FAQ's vLLM scheduler notes
+ * on chunked prefill).  Sequence s owns the packed query tokens
+ * query_start_loc[s] .. query_start_loc[s+1]-1 (q_len of them, possibly 0);
+ * they are its newest q_len positions, already written into the cache by
+ * pa_reshape_and_cache, so with ctx = context_lens[s] query j attends
+ *   positions 0 .. ctx - q_len + j   (causal), found through the block table;
+ *   out[token, h, :] = sum_t softmax(scale * q[token, h, :] . K_t) V_t
+ * with fp32 accumulation, rounded to the dtype (round-to-nearest-even).
+ *   out            device [total tokens, num_q_heads, head_size], contiguous.
+ *   q              device [total tokens, num_q_heads, head_size]; token stride
+ *                  q_token_stride elements (multiple of 8); 16-byte aligned.
+ *   query_start_loc device int32 [num_seqs + 1], non-decreasing, starting at 0.
+ *   context_lens   device int32 [num_seqs], counting the new tokens.
+ *   max_query_len  an upper bound of every q_len (sizes the launch); a longer
+ *                  sequence gets zero rows and PA_DEVERR_CONTEXT.
+ *   dev_err        optional; PA_DEVERR_CONTEXT for q_len > ctx or ctx beyond the
+ *                  table row, PA_DEVERR_BLOCK_ID for a bad block id (that query
+ *                  tile's rows are zeroed).
+ * Supported: a 16-bit cache, head_size 64 or 128, block_size 8, 16 or 32, group
+ * size 1, 2, 4, 8 or 16 (PA_ERR_UNSUPPORTED otherwise).  No workspace. */
+pa_status pa_prefill(void* out, const void* q, int64_t q_token_stride, const void* kv_cache,
+                     const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
+                     int32_t block_table_stride, const int32_t* context_lens,
+                     const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads,
+                     int32_t max_query_len, float scale, uint32_t* dev_err, void* stream);
 
 /* Size of the workspace the library carries for pa_decode_static_workspace
  * (32 MiB on every device that loads the library, held until the process exits). */

@@ -26,7 +26,7 @@ DTYPE_CODE = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 
 EXPORTED = [
     "pa_cache_bytes", "pa_cache_element_offset", "pa_cache_scale_offset", "pa_reshape_and_cache", "pa_decode_workspace_bytes",
-    "pa_decode_partition_size", "pa_decode", "pa_decode_window", "pa_decode_window_span",
+    "pa_decode_partition_size", "pa_decode", "pa_decode_window", "pa_decode_window_span", "pa_prefill",
     "pa_decode_static_workspace", "pa_copy_blocks", "pa_swap_blocks", "pa_read_device_errors",
     "pa_status_string", "pa_last_error_message",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_can_allocate", "pa_bm_allocate", "pa_bm_append_slot", "pa_bm_fork",
@@ -99,6 +99,8 @@ def load():
     lib.pa_decode_window.argtypes = [P, P, i64, P, D, i32, P, i32, P, i32, i32, i32, ctypes.c_float, i32, i32, i32,
                                      P, sz, P, P]
     lib.pa_decode_window.restype = ctypes.c_int
+    lib.pa_prefill.argtypes = [P, P, i64, P, D, i32, P, i32, P, P, i32, i32, i32, ctypes.c_float, P, P]
+    lib.pa_prefill.restype = ctypes.c_int
     lib.pa_decode_window_span.argtypes = [i32, i32, i32, i32]
     lib.pa_decode_window_span.restype = i32
     lib.pa_decode_static_workspace.argtypes = [P, P, i64, P, D, i32, P, i32, P, i32, i32, i32, ctypes.c_float,
@@ -226,6 +228,18 @@ def decode_window(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor, de
                                    _ptr(block_tables), block_tables.stride(0), _ptr(context_lens), S, Hq,
                                    max_context_len, scale, window, ring_blocks, partition_size, _ptr(workspace),
                                    ws_bytes, _ptr(dev_err), _stream(stream)))
+
+
+def prefill(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor, desc: CacheDesc,
+            block_tables: torch.Tensor, context_lens: torch.Tensor, query_start_loc: torch.Tensor,
+            max_query_len: int, scale: float, layer: int = 0, dev_err: torch.Tensor | None = None,
+            stream=None) -> None:
+    """pa_prefill: out/q [T, Hq, D] packed by query_start_loc (int32 [S + 1]); causal
+    over each sequence's cache (its last q_len positions are the queries)."""
+    S, Hq = context_lens.shape[0], q.shape[1]
+    _check(load().pa_prefill(_ptr(out), _ptr(q), q.stride(0), _ptr(kv_cache), ctypes.byref(desc.c()), layer,
+                             _ptr(block_tables), block_tables.stride(0), _ptr(context_lens), _ptr(query_start_loc),
+                             S, Hq, max_query_len, scale, _ptr(dev_err), _stream(stream)))
 
 
 def decode_window_span(max_context_len: int, block_size: int, window: int, ring_blocks: int = 0) -> int:

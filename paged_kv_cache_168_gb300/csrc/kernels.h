@@ -96,6 +96,28 @@ cudaError_t launch_merge(const DecodeParams& p, int dtype, int head_size, cudaSt
 constexpr int kTcMaxSeqs = 8192;
 cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, int group, int num_sms, cudaStream_t stream);
 
+// Causal prefill / extend over a 16-bit cache (tcgen05): head_size 64 or 128,
+// block_size >= 8, group 1, 2, 4, 8 or 16.
+struct PrefillParams {
+  void* out;                      // [tokens, Hq, D] q dtype, contiguous
+  const void* q;                  // [tokens, Hq, D], token stride q_token_stride elements
+  int64_t q_token_stride;
+  const uint8_t* cache;           // this layer's pool
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  const int32_t* block_tables;
+  int32_t bt_stride;
+  const int32_t* context_lens;    // [S], counts the new tokens
+  const int32_t* query_start_loc; // [S + 1]
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t max_query_len;
+  float scale_log2;
+  uint32_t* dev_err;
+};
+cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, int head_size, int group, cudaStream_t stream);
+
 // Paged decode over an 8-bit cache on CUDA cores: head_size 128, group 1/2/4/8;
 // q / out in act_dtype.  Launches the decode kernel and the merge.
 cudaError_t launch_decode_i8(const DecodeParams& p, int act_dtype, int group, cudaStream_t stream);

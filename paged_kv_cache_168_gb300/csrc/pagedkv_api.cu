@@ -311,6 +311,64 @@ pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* 
                           workspace, workspace_bytes, dev_err, stream);
 }
 
+pa_status pa_prefill(void* out, const void* q, int64_t q_token_stride, const void* kv_cache,
+                     const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
+                     int32_t block_table_stride, const int32_t* context_lens, const int32_t* query_start_loc,
+                     int32_t num_seqs, int32_t num_q_heads, int32_t max_query_len, float scale, uint32_t* dev_err,
+                     void* stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (is_i8(desc)) return fail(PA_ERR_UNSUPPORTED, "prefill over an 8-bit cache");
+  if (desc->block_size < 8)
+    return fail(PA_ERR_UNSUPPORTED, "prefill with block_size %d (supported: 8, 16, 32)", desc->block_size);
+  if (layer < 0 || layer >= desc->num_layers) return fail(PA_ERR_INVALID_ARG, "layer %d", layer);
+  if (num_seqs < 0 || num_seqs > 65535) return fail(PA_ERR_INVALID_ARG, "num_seqs %d not in [0, 65535]", num_seqs);
+  if (num_seqs == 0 || max_query_len == 0) return PA_OK;
+  if (max_query_len < 0) return fail(PA_ERR_INVALID_ARG, "max_query_len %d < 0", max_query_len);
+  if (num_q_heads <= 0 || num_q_heads % desc->num_kv_heads)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
+                num_q_heads, desc->num_kv_heads);
+  const int group = num_q_heads / desc->num_kv_heads;
+  if (group != 1 && group != 2 && group != 4 && group != 8 && group != 16)
+    return fail(PA_ERR_UNSUPPORTED, "query heads per kv head %d (supported: 1, 2, 4, 8, 16)", group);
+  if (desc->num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads > 65535");
+  if (!out || !q || !kv_cache || !block_tables || !context_lens || !query_start_loc)
+    return fail(PA_ERR_INVALID_ARG,
+                "out, q, kv_cache, block_tables, context_lens and query_start_loc must be non-NULL");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(kv_cache))
+    return fail(PA_ERR_INVALID_ARG, "out, q and kv_cache must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3) || (reinterpret_cast<uintptr_t>(context_lens) & 3) ||
+      (reinterpret_cast<uintptr_t>(query_start_loc) & 3))
+    return fail(PA_ERR_INVALID_ARG, "block_tables, context_lens and query_start_loc must be 4-byte aligned");
+  if (q_token_stride < (int64_t)num_q_heads * desc->head_size || q_token_stride % 8)
+    return fail(PA_ERR_INVALID_ARG, "q_token_stride must be >= num_q_heads*head_size and a multiple of 8");
+  if (block_table_stride <= 0) return fail(PA_ERR_INVALID_ARG, "block_table_stride %d", block_table_stride);
+  if (!(scale > 0.f) || scale != scale) return fail(PA_ERR_INVALID_ARG, "scale must be a positive number");
+  const int rows_per_tile = 128 / group;
+  if ((int64_t)(max_query_len + rows_per_tile - 1) / rows_per_tile > 0x7fffffff)
+    return fail(PA_ERR_INVALID_ARG, "max_query_len too large");
+
+  pkv::PrefillParams p{};
+  p.out = out;
+  p.q = q;
+  p.q_token_stride = q_token_stride;
+  p.cache = static_cast<const uint8_t*>(kv_cache) + layer * layer_stride(desc);
+  p.num_blocks = desc->num_blocks;
+  p.block_size = desc->block_size;
+  p.num_kv_heads = desc->num_kv_heads;
+  p.block_tables = block_tables;
+  p.bt_stride = block_table_stride;
+  p.context_lens = context_lens;
+  p.query_start_loc = query_start_loc;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.max_query_len = max_query_len;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.dev_err = dev_err;
+  cudaError_t e = pkv::launch_prefill_tc(p, desc->dtype, desc->head_size, group, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e, "prefill launch");
+}
+
 pa_status pa_copy_blocks(void* kv_cache, const pa_cache_desc* desc, const int64_t* pairs, int32_t num_pairs,
                          void* stream) {
   pa_status st = check_desc(desc);

@@ -1,0 +1,436 @@
+// prefill_tc.cu -- causal prefill / extend attention over the paged cache on the
+// tensor cores (tcgen05 + TMEM).
+//
+// What is computed: the prefill of the "vLLM" page (the whole prompt, or under
+// chunked prefill one chunk of it, attends over the KV cache with a causal
+// mask; the chunk's own K/V were written by reshape_and_cache first).  Sequence
+// s owns the packed query tokens query_start_loc[s] .. [s+1]; query j of its
+// q_len sits at position ctx - q_len + j and attends positions 0 .. that
+// position, found through the block table as in decode.
+//
+// One CTA per (query tile, kv head, sequence).  A tile is M = 128 rows: 128/G
+// consecutive query positions x the G query heads of the kv head (row =
+// position * G + head), so one pass over the KV serves all G heads.  Per
+// 128-token KV tile t:
+//     S_t = Q K_t^T        (M = 128 rows, N = 128 tokens, K = D)  -> TMEM (fp32)
+//     O  += P_t V_t        (M = 128 rows, N = D, K = 128 tokens)  -> TMEM (fp32)
+// Q (written once, 128B-swizzled K-major) and P (written by the softmax
+// threads, same form, as p_hi and p_lo = p - p_hi so bf16 weights keep ~16
+// bits) are A operands; the cache's 8-token groups staged by bulk copies are
+// directly the K-major B operand (K) and the MN-major B operand (V).
+// Roles:
+//   warp 0      bulk copies of each KV tile's (block, kv head) chunks into a
+//               2-stage ring (mbarrier transaction counts).
+//   warp 1      one lane issues S_{t+1} ahead of O += P_t V_t.
+//   warps 2-5   thread = TMEM lane = query row: causal mask, online softmax in
+//               base 2.  The running max is raised only when a tile's max
+//               exceeds it by more than 8 (a factor 256), and only then is the
+//               row of O rescaled in TMEM; otherwise the stale max is kept for
+//               both p and the sum, which is the same arithmetic.  They also
+//               zero V rows past the tile's last token (0 * NaN = NaN) and
+//               write the output rows at the end.
+// Every wait is bounded; a timeout sets PA_DEVERR_TIMEOUT and the CTA drains
+// its own copies and MMAs before releasing TMEM.
+#include <math.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kRows = 128;                // MMA M: (position, head) rows of one query tile
+constexpr int kKv = 128;                  // tokens per KV tile
+constexpr int kThreads = 192;             // producer, MMA, 4 softmax warps
+constexpr uint32_t kTmemCols = 512;       // S0 [0,128) S1 [128,256) O [256, 256 + D)
+constexpr uint32_t kOCol = 256;
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr float kRescaleThreshold = 8.f;  // base-2 units
+
+template <int D>
+struct Cfg {
+  static constexpr int kAtoms = D / 64;                      // 128-byte rows per K (or V) vector
+  static constexpr int kGroupBytes = 8 * 2 * D * 2;          // one 8-token group: K atoms, then V atoms
+  static constexpr int kStageBytes = kKv * 2 * D * 2;        // K + V of one KV tile
+  static constexpr int kQAtomBytes = kRows * 128;            // one 64-dim column block of Q (or P)
+  static constexpr int kQBytes = kRows * D * 2;
+  static constexpr int kPBytes = kRows * kKv * 2;            // one P operand (hi or lo)
+  static constexpr int kStages = 2;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kQBytes + 2 * (size_t)kPBytes;
+};
+
+struct Shared {
+  uint64_t full[2], empty[2], s_full[2], s_free[2], p_full, pv_done;
+  uint32_t tmem_base;
+  int bad;
+  volatile int abort_flag;
+};
+
+// Offset of the 16-byte piece `piece` (8 elements) of row r in a 128B-swizzled
+// K-major operand of 128 rows whose 64-element column blocks are kQAtomBytes apart.
+__device__ __forceinline__ uint32_t op_offset(int r, int piece) {
+  return (uint32_t)((piece >> 3) * (kRows * 128) + (r >> 3) * 1024 + (r & 7) * 128 + (((piece & 7) ^ (r & 7)) << 4));
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
+  using C = Cfg<D>;
+  constexpr int PT = kRows / G;                      // query positions per tile
+  constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+  __shared__ Shared sh;
+  extern __shared__ __align__(1024) uint8_t dyn_raw[];
+  const uint32_t raw_s = smem_u32(dyn_raw);
+  uint8_t* dyn = dyn_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
+  uint8_t* stages = dyn;
+  uint8_t* qbuf = stages + C::kStages * C::kStageBytes;
+  uint8_t* phi = qbuf + C::kQBytes;
+  uint8_t* plo = phi + C::kPBytes;
+
+  const int tile = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int first = p.query_start_loc[s];
+  const int q_len = p.query_start_loc[s + 1] - first;
+  const int ctx = p.context_lens[s];
+  const int bs = p.block_size;
+  T* out = static_cast<T*>(p.out);
+  auto zero_rows = [&](int q0, int npos) {
+    const int n = npos * G * (D / 8);
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const int r = i / (D / 8), c = i % (D / 8);
+      const int64_t tok = first + q0 + r / G;
+      *reinterpret_cast<uint4*>(out + (tok * p.num_q_heads + kvh * G + r % G) * D + c * 8) = make_uint4(0, 0, 0, 0);
+    }
+  };
+  if (q_len > p.max_query_len) {
+    // the grid does not cover this sequence: tile 0 clears all its rows
+    if (tile == 0) {
+      for (int q0 = 0; q0 < q_len; q0 += PT) zero_rows(q0, min(PT, q_len - q0));
+      if (threadIdx.x == 0) report(p.dev_err, PA_DEVERR_CONTEXT);
+    }
+    return;
+  }
+  const int q0 = tile * PT;
+  if (q0 >= q_len) return;
+  const int npos = min(PT, q_len - q0);
+  if (q_len > ctx || (int64_t)ctx > (int64_t)p.bt_stride * bs) {
+    zero_rows(q0, npos);
+    if (threadIdx.x == 0) report(p.dev_err, PA_DEVERR_CONTEXT);
+    return;
+  }
+  const int pos0 = ctx - q_len + q0;        // position of the tile's first query
+  const int kv_len = pos0 + npos;           // the tile attends positions [0, kv_len)
+  const int nblk = (kv_len + bs - 1) / bs;
+  const int32_t* row_ids = p.block_tables + (int64_t)s * p.bt_stride;
+  if (threadIdx.x == 0) sh.bad = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < nblk; i += blockDim.x) {
+    const int b = row_ids[i];
+    if (b < 0 || b >= p.num_blocks) sh.bad = 1;
+  }
+  __syncthreads();
+  if (sh.bad) {
+    zero_rows(q0, npos);
+    if (threadIdx.x == 0) report(p.dev_err, PA_DEVERR_BLOCK_ID);
+    return;
+  }
+
+  // ---- set-up: barriers, Q tile (rows past the tile's queries are zero), TMEM
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.full[i], 1);
+      mbar_init(&sh.empty[i], 1);
+      mbar_init(&sh.s_full[i], 1);
+      mbar_init(&sh.s_free[i], 4);
+    }
+    mbar_init(&sh.p_full, 4);
+    mbar_init(&sh.pv_done, 1);
+    sh.abort_flag = 0;
+    fence_mbar_init();
+  }
+  {
+    const T* qsrc = static_cast<const T*>(p.q);
+    for (int i = threadIdx.x; i < kRows * (D / 8); i += kThreads) {
+      const int r = i / (D / 8), c = i % (D / 8);
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < npos * G)
+        v = *reinterpret_cast<const uint4*>(qsrc + (int64_t)(first + q0 + r / G) * p.q_token_stride +
+                                            (int64_t)(kvh * G + r % G) * D + c * 8);
+      *reinterpret_cast<uint4*>(qbuf + op_offset(r, c)) = v;
+    }
+    tc::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&sh.tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = sh.tmem_base;
+  const int n_kv = (kv_len + kKv - 1) / kKv;
+  const int64_t chunk_bytes = (int64_t)bs * 2 * D * 2;
+
+  if (warp == 0) {
+    // =================================================================== producer
+    int issued = 0;
+    bool aborted = false;
+    for (int j = 0; j < n_kv; ++j) {
+      const int slot = j & 1;
+      if (j >= 2 && !mbar_wait(&sh.empty[slot], ((j >> 1) - 1) & 1)) {
+        aborted = true;
+        break;
+      }
+      if (sh.abort_flag) {
+        aborted = true;
+        break;
+      }
+      const int valid = min(kKv, kv_len - j * kKv);
+      const int nb = (valid + bs - 1) / bs;
+      if (lane == 0) mbar_arrive_expect_tx(&sh.full[slot], (uint32_t)(nb * chunk_bytes));
+      __syncwarp();
+      for (int b = lane; b < nb; b += 32) {
+        const int id = row_ids[j * (kKv / bs) + b];
+        bulk_g2s(stages + slot * C::kStageBytes + b * chunk_bytes, p.cache + ((int64_t)id * p.num_kv_heads + kvh) * chunk_bytes,
+                 (uint32_t)chunk_bytes, &sh.full[slot]);
+      }
+      issued = j + 1;
+    }
+    if (lane == 0) {
+      if (aborted) {
+        report(p.dev_err, PA_DEVERR_TIMEOUT);
+        sh.abort_flag = 1;
+        for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(&sh.full[j & 1], (j >> 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // =================================================================== MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = tc::idesc_f16(kRows, kKv, kBF16, false, false);
+      const uint32_t id_pv = tc::idesc_f16(kRows, D, kBF16, false, true);
+      const uint32_t qa = smem_u32(qbuf), pha = smem_u32(phi), pla = smem_u32(plo);
+      auto issue_qk = [&](int j) -> bool {
+        const int slot = j & 1;
+        if (!mbar_wait(&sh.full[slot], (j >> 1) & 1)) return false;
+        if (j >= 2 && !mbar_wait(&sh.s_free[slot], ((j >> 1) - 1) & 1)) return false;
+        tc::fence_after_sync();
+        const uint32_t st = smem_u32(stages + slot * C::kStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma_f16(tmem + slot * kKv,
+                      tc::smem_desc(qa + (kk >> 2) * C::kQAtomBytes + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B),
+                      tc::smem_desc(st + (kk >> 2) * 1024 + (kk & 3) * 32, 16, C::kGroupBytes, tc::kSwizzle128B),
+                      id_qk, kk > 0);
+        tc::commit(&sh.s_full[slot]);
+        return true;
+      };
+      bool ok = !sh.abort_flag && issue_qk(0);
+      for (int j = 0; j < n_kv && ok; ++j) {
+        if (j + 1 < n_kv && !issue_qk(j + 1)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(&sh.p_full, j & 1) || sh.abort_flag) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const int slot = j & 1;
+        const uint32_t st = smem_u32(stages + slot * C::kStageBytes);
+        const int valid = min(kKv, kv_len - j * kKv);
+        const int nsteps = (valid + 15) >> 4;
+        for (int kk = 0; kk < nsteps; ++kk) {
+          const uint64_t vdesc =
+              tc::smem_desc(st + kk * 2 * C::kGroupBytes + C::kAtoms * 1024, 1024, C::kGroupBytes, tc::kSwizzle128B);
+          const uint32_t aoff = (kk >> 2) * C::kQAtomBytes + (kk & 3) * 32;
+          tc::mma_f16(tmem + kOCol, tc::smem_desc(pha + aoff, 16, 1024, tc::kSwizzle128B), vdesc, id_pv,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_f16(tmem + kOCol, tc::smem_desc(pla + aoff, 16, 1024, tc::kSwizzle128B), vdesc, id_pv, 1u);
+        }
+        tc::commit(&sh.pv_done);
+        tc::commit(&sh.empty[slot]);
+      }
+      if (!ok) {
+        report(p.dev_err, PA_DEVERR_TIMEOUT);
+        sh.abort_flag = 1;
+      }
+    }
+    __syncwarp();
+  } else {
+    // =================================================================== softmax warps (2-5)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;               // TMEM lane = query row = (position, head)
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int ipos = row / G;
+    const bool row_ok = ipos < npos;
+    const int pos = pos0 + ipos;                       // attends tokens t <= pos
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int sb = j & 1;
+      // wait results are made warp-uniform: the TMEM loads and stores below are
+      // warp-collective (.sync.aligned) and must never run in a diverged warp
+      if (!__all_sync(kFull, mbar_wait(&sh.s_full[sb], (j >> 1) & 1) && !sh.abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      float x[kKv / 16][16];
+#pragma unroll
+      for (int c = 0; c < kKv / 16; ++c) tc::tmem_ld16(lane_addr + sb * kKv + c * 16, x[c]);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.s_free[sb]);
+      const int lim = row_ok ? min(kKv, pos + 1 - j * kKv) : 0;   // tokens of this tile the row attends
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kKv / 16; ++c)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          x[c][e] = (c * 16 + e < lim) ? x[c][e] * p.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, x[c][e]);
+        }
+      // P and O are free once the previous tile's PV has completed
+      if (j > 0) {
+        if (!__all_sync(kFull, mbar_wait(&sh.pv_done, (j - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+      }
+      const float m_new = fmaxf(m, mt);
+      const bool need = m != -INFINITY && m_new > m + kRescaleThreshold;
+      if (m == -INFINITY) m = m_new;
+      bool stored = false;
+      if (__any_sync(kFull, need)) {
+        // the whole warp takes the O round trip; rows that keep their max scale by 1
+        const float alpha = need ? exp2f(m - m_new) : 1.f;
+        if (need) {
+          l *= alpha;
+          m = m_new;
+        }
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          float o[16];
+          tc::tmem_ld16(lane_addr + kOCol + c * 16, o);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] *= alpha;
+          tc::tmem_st16(lane_addr + kOCol + c * 16, o);
+        }
+        stored = true;
+      }
+      // p = 2^(x - m) in fp32; P operand gets round(p) and round(p - round(p))
+#pragma unroll
+      for (int c = 0; c < kKv / 8; ++c) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const float a = (m == -INFINITY) ? 0.f : exp2f(x[c >> 1][(c & 1) * 8 + e] - m);
+          const float b = (m == -INFINITY) ? 0.f : exp2f(x[c >> 1][(c & 1) * 8 + e + 1] - m);
+          l += a + b;
+          hi[e >> 1] = Elem<T>::pack2(a, b);
+          const float2 h = Elem<T>::to_float2(hi[e >> 1]);
+          lo[e >> 1] = Elem<T>::pack2(a - h.x, b - h.y);
+        }
+        const uint32_t off = op_offset(row, c);
+        *reinterpret_cast<uint4*>(phi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(plo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      // V rows of tokens past the tile's last token: zero (thread = token row
+      // here), after the stage's bulk copy is known complete
+      const int valid = min(kKv, kv_len - j * kKv);
+      if (valid & 15) {
+        if (!__all_sync(kFull, mbar_wait(&sh.full[sb], (j >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+      }
+      if (row >= valid && row < ((valid + 15) & ~15)) {
+        uint8_t* vrow = stages + sb * C::kStageBytes + (row >> 3) * C::kGroupBytes + C::kAtoms * 1024 + (row & 7) * 128;
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + a * 1024 + c * 16) = make_uint4(0, 0, 0, 0);
+      }
+      if (stored) tc::tmem_wait_st();
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.p_full);
+    }
+    if (ok && n_kv > 0) ok = __all_sync(kFull, mbar_wait(&sh.pv_done, (n_kv - 1) & 1));
+    if (ok) {
+      tc::fence_after_sync();
+      const float inv = row_ok && l > 0.f ? 1.f / l : 0.f;
+      T* orow = out + ((int64_t)(first + q0 + ipos) * p.num_q_heads + kvh * G + row % G) * D;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        float o[16];
+        tc::tmem_ld16(lane_addr + kOCol + c * 16, o);
+        if (row_ok) {
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) w[e] = Elem<T>::pack2(o[2 * e] * inv, o[2 * e + 1] * inv);
+          *reinterpret_cast<uint4*>(orow + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(orow + c * 16 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      }
+    } else {
+      if (lane == 0) {
+        report(p.dev_err, PA_DEVERR_TIMEOUT);
+        sh.abort_flag = 1;
+      }
+      if (row_ok) {
+        T* orow = out + ((int64_t)(first + q0 + ipos) * p.num_q_heads + kvh * G + row % G) * D;
+        for (int c = 0; c < D / 8; ++c) *reinterpret_cast<uint4*>(orow + c * 8) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+
+  // ---- tear-down: every MMA this CTA issued has completed (pv_done / s_full
+  // waited above, or abandoned after a timeout), then TMEM is released
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_typed(const PrefillParams& p, cudaStream_t stream) {
+  using C = Cfg<D>;
+  cudaError_t e = set_smem_attribute_once<prefill_tc_kernel<T, D, G>>(C::kSmem);
+  if (e != cudaSuccess) return e;
+  constexpr int PT = kRows / G;
+  const dim3 grid((unsigned)((p.max_query_len + PT - 1) / PT), (unsigned)p.num_kv_heads, (unsigned)p.num_seqs);
+  prefill_tc_kernel<T, D, G><<<grid, kThreads, C::kSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_group(const PrefillParams& p, int group, cudaStream_t stream) {
+  switch (group) {
+    case 1: return launch_typed<T, D, 1>(p, stream);
+    case 2: return launch_typed<T, D, 2>(p, stream);
+    case 4: return launch_typed<T, D, 4>(p, stream);
+    case 8: return launch_typed<T, D, 8>(p, stream);
+    case 16: return launch_typed<T, D, 16>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, int head_size, int group, cudaStream_t stream) {
+  if (dtype == PA_F16 && head_size == 128) return launch_group<__half, 128>(p, group, stream);
+  if (dtype == PA_F16 && head_size == 64) return launch_group<__half, 64>(p, group, stream);
+  if (dtype == PA_BF16 && head_size == 128) return launch_group<__nv_bfloat16, 128>(p, group, stream);
+  if (dtype == PA_BF16 && head_size == 64) return launch_group<__nv_bfloat16, 64>(p, group, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

@@ -201,3 +201,21 @@ def test_int8_decode_limits(lib):
     st = lib.pa_swap_blocks(ctypes.c_void_p(FAKE), ctypes.byref(_desc()), ctypes.c_void_p(FAKE),
                             ctypes.byref(_desc(kv_int8=True)), 0, arr.ctypes.data_as(ctypes.c_void_p), 1, None)
     assert st == _lib.PA_ERR_INVALID_ARG
+
+
+def _prefill(lib, desc=None, S=2, Hq=4, max_q=100, q=FAKE, scale=0.1, q_stride=4 * 128):
+    return lib.pa_prefill(ctypes.c_void_p(FAKE), ctypes.c_void_p(q), q_stride, ctypes.c_void_p(FAKE),
+                          ctypes.byref(desc or _desc()), 0, ctypes.c_void_p(FAKE), 8, ctypes.c_void_p(FAKE),
+                          ctypes.c_void_p(FAKE), S, Hq, max_q, scale, None, None)
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    assert _prefill(lib, Hq=3) == _lib.PA_ERR_INVALID_ARG                 # not a multiple of Hkv
+    assert _prefill(lib, Hq=64) == _lib.PA_ERR_UNSUPPORTED                # group 32
+    assert _prefill(lib, desc=_desc(block_size=4)) == _lib.PA_ERR_UNSUPPORTED
+    assert _prefill(lib, desc=_desc(kv_int8=True)) == _lib.PA_ERR_UNSUPPORTED
+    assert _prefill(lib, q=FAKE + 8) == _lib.PA_ERR_INVALID_ARG
+    assert _prefill(lib, q_stride=4 * 128 - 8) == _lib.PA_ERR_INVALID_ARG
+    assert _prefill(lib, scale=-1.0) == _lib.PA_ERR_INVALID_ARG
+    assert _prefill(lib, max_q=-1) == _lib.PA_ERR_INVALID_ARG
+    assert _prefill(lib, S=0) == _lib.PA_OK and _prefill(lib, max_q=0) == _lib.PA_OK    # nothing to do

@@ -58,6 +58,19 @@ DESCRIPTIONS = {
 }
 
 
+PREFILL_METRIC = "paged prefill/extend attention TFLOP/s (causal FLOPs, frac of bf16 tensor peak)"
+FALLBACK_BF16_TFLOPS = 1900.0
+PREFILL_DESCRIPTIONS = {
+    "prefill_8b": "Llama-3-8B-shaped prefill: 16 prompts x 2048 tokens from scratch, 32 q/8 kv heads, head_size 128, "
+                  "block_size 16, bf16 ~N(0,1), random block placement; reshape_and_cache of every prompt token + "
+                  "causal paged attention",
+    "extend_8b": "Llama-3-8B-shaped chunked prefill: 32 sequences, a 512-token chunk each over cached prefixes "
+                 "~U[512,3584], 32 q/8 kv heads, head_size 128, block_size 16, bf16",
+    "prefill_7b": "Llama-2-7B-shaped prefill: 8 prompts x 2048 tokens, 32/32 heads, head_size 128, block_size 16, fp16",
+    "prefill_tiny": "tiny prefill: 3 sequences, 100-token chunks over prefixes ~U[0,300], 8 q/2 kv heads, bf16",
+}
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -65,6 +78,15 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """bf16 dense TFLOP/s: burst figure (a kernel timed alone)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (burst)"
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def source_digest() -> str:
@@ -417,12 +439,164 @@ def run_gpu(args):
     return 0
 
 
+# ------------------------------------------------------------------ prefill / extend
+
+def prefill_oracle_sample(w, budget_s: float, start: int = 0):
+    """Time the fp64 oracle's prefill on 64-query-token windows of the workload
+    (all heads; a window at a random offset of a random sequence, attending
+    everything before it) until ~budget_s seconds: (TFLOP/s of causal FLOPs,
+    description, cores)."""
+    import oracle
+    from paged_kv_cache_168_gb300.workloads import as_u16
+    cfg = w.cfg
+    g = oracle.Geom(w.num_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_size, cfg.dtype)
+    pool = as_u16(w.kv_cache).reshape(-1)
+    q = as_u16(w.q)
+    qsl, ctx = w.query_start_loc_np, w.context_lens_np
+    rng = np.random.default_rng(start)
+    flops, t_total, windows = 0, 0.0, 0
+    while t_total < budget_s and windows < 10000:
+        s = int(rng.integers(cfg.num_seqs))
+        q_len = int(qsl[s + 1] - qsl[s])
+        n = min(q_len, 64)
+        j0 = int(rng.integers(0, q_len - n + 1))
+        c = int(ctx[s]) - q_len + j0 + n                     # the context the window's last token sees
+        t0 = time.perf_counter()
+        oracle.prefill(q[qsl[s] + j0:qsl[s] + j0 + n], pool, g, w.block_tables_np[s:s + 1],
+                       np.array([c], np.int32), np.array([0, n], np.int32), w.scale)
+        t_total += time.perf_counter() - t0
+        flops += 4 * cfg.head_size * cfg.num_q_heads * (n * (c - n) + n * (n + 1) // 2)
+        windows += 1
+    cores = oracle.max_threads()
+    desc = (f"{windows} windows of 64 query tokens (all {cfg.num_q_heads} heads, random sequence and offset) "
+            f"of the {cfg.name} workload, fp64 oracle, {cores} OpenMP threads")
+    return flops / t_total / 1e12, desc, cores
+
+
+def run_gpu_prefill(args):
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": PREFILL_METRIC, "error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    from paged_kv_cache_168_gb300 import _lib
+    from paged_kv_cache_168_gb300.build import build
+    from paged_kv_cache_168_gb300.step import PrefillStep
+    from paged_kv_cache_168_gb300.workloads import PREFILL_CONFIGS, make_prefill_workload
+    build()
+    _lib.load()
+    cfg = PREFILL_CONFIGS[args.workload]
+    w = make_prefill_workload(args.workload, device=device, seed=cfg.seed + 1000 * rank)
+    stream = torch.cuda.Stream(device)
+    step = PrefillStep(w, stream=stream)
+    flops = step.flops()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    assert _lib.read_device_errors(step.dev_err, stream=stream) == 0, "device error during warm-up"
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        clocks.mark_start()
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                ev[i][0].record(stream)
+                step.cache_ops()
+                ev[i][1].record(stream)
+                step.attention()
+                ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        clocks.mark_end()
+        barrier(world)
+    total_ms = reduce_max(ev[0][0].elapsed_time(ev[K - 1][2]), world, device)
+    attn_ms = float(np.mean([ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]))
+    assert _lib.read_device_errors(step.dev_err, stream=stream) == 0, "device error during timed steps"
+
+    # end to end with host buffers: inputs in, output back, every step
+    names = ("q", "key", "value", "block_tables", "context_lens", "query_start_loc", "slot_mapping")
+    host_in = {k: getattr(w, k).cpu().pin_memory() for k in names}
+    dev_in = {k: torch.empty_like(getattr(w, k)) for k in names}
+    host_out = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    saved = {k: getattr(w, k) for k in names}
+    for k in names:
+        setattr(w, k, dev_in[k])
+
+    def e2e_step():
+        for k in names:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        step()
+        host_out.copy_(step.out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world, device)
+    for k, v in saved.items():
+        setattr(w, k, v)
+
+    ms = total_ms / K
+    peak, peak_kind = measured_tensor_peak()
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+    if rank == 0:
+        cpu = None
+        if args.cpu_baseline_seconds > 0:
+            v, desc, cores = prefill_oracle_sample(w, args.cpu_baseline_seconds)
+            cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+        line = {
+            "metric": PREFILL_METRIC, "value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+            "data": "synthetic",
+            "config": {"workload": PREFILL_DESCRIPTIONS[args.workload], "global_batch": cfg.num_seqs * world,
+                       "query_tokens": int(w.query_start_loc_np[-1]),
+                       "tokens_in_context": int(w.context_lens_np.sum()), "parallelism": f"replicas{world}",
+                       "l2": f"inputs larger than L2: q {w.q.numel() * 2 / 1e9:.2f} GB + pool "
+                             f"{w.kv_cache.numel() * 2 / 1e9:.2f} GB per step"},
+            "flops_per_step": flops,
+            "tokens_per_s": round(world * int(w.query_start_loc_np[-1]) / (ms * 1e-3), 1),
+            "roofline": {"bound": "tensor", "kernel": "pa_prefill (prefill_tc_kernel)", "achieved": round(achieved, 2),
+                         "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                         "traffic": None, "attention_ms": round(attn_ms, 4),
+                         "note": "algorithmic causal FLOPs; the kernel also issues the p_lo half of PV and "
+                                 "full 128x128 diagonal tiles"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(world * flops / (e2e_ms / K * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K, 4)},
+            "gpu_launches": K * step.kernel_launches() * world,
+            "clocks": clocks.summary(),
+            "source_digest": source_digest(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="7b", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--workload", default="7b", choices=sorted(DESCRIPTIONS) + sorted(PREFILL_DESCRIPTIONS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--seqs", type=int, default=None, help="use only the first N sequences (small profiling runs)")
@@ -433,6 +607,8 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload in PREFILL_DESCRIPTIONS:
+        return run_gpu_prefill(args)
     return run_gpu(args)
 
 

@@ -8,6 +8,7 @@ step; the step itself only launches kernels on one stream.
 """
 from __future__ import annotations
 
+import numpy as np
 import torch
 
 from . import _lib
@@ -106,3 +107,54 @@ class DecodeStep:
         swap = (w.swap_out_pairs.shape[0] + w.swap_in_pairs.shape[0]) * block_bytes * 2
         return {"decode": decode, "decode_kv": int(ctx.sum()) * kv_tok, "reshape": reshape, "copy": copy,
                 "swap": swap, "total": decode + reshape + copy + swap}
+
+
+class PrefillStep:
+    """One prefill / extend step of one layer: reshape_and_cache of every new
+    token, then causal attention of the new tokens over the paged cache."""
+
+    def __init__(self, w, stream: torch.cuda.Stream | None = None):
+        cfg = w.cfg
+        self.w = w
+        self.stream = stream or torch.cuda.current_stream(w.q.device)
+        self.desc = _lib.CacheDesc(w.num_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_size, w.dtype)
+        self.kv_cache = w.kv_cache
+        self.out = torch.empty_like(w.q)
+        self.dev_err = torch.zeros(1, dtype=torch.int32, device=w.q.device)
+
+    def cache_ops(self):
+        w = self.w
+        _lib.reshape_and_cache(self.kv_cache, self.desc, w.key, w.value, w.slot_mapping, dev_err=self.dev_err,
+                               stream=self.stream)
+
+    def attention(self, q=None, out=None):
+        w = self.w
+        _lib.prefill(self.out if out is None else out, w.q if q is None else q, self.kv_cache, self.desc,
+                     w.block_tables, w.context_lens, w.query_start_loc, w.max_query_len, w.scale,
+                     dev_err=self.dev_err, stream=self.stream)
+
+    def __call__(self):
+        self.cache_ops()
+        self.attention()
+        return self.out
+
+    def kernel_launches(self) -> int:
+        return 2
+
+    def flops(self) -> int:
+        """Causal attention FLOPs: 4 * D per (query row, attended position)."""
+        cfg = self.w.cfg
+        ctx = self.w.context_lens_np.astype(np.int64)
+        q_len = np.diff(self.w.query_start_loc_np).astype(np.int64)
+        # sum over j < q_len of (ctx - q_len + j + 1)
+        attended = q_len * (ctx - q_len) + q_len * (q_len + 1) // 2
+        return int(4 * cfg.head_size * cfg.num_q_heads * attended.sum())
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes the step must move at least: new K/V read + written, q read, out written,
+        and each sequence's KV once per kv head."""
+        w, cfg = self.w, self.w.cfg
+        T = int(self.w.query_start_loc_np[-1])
+        kv_tok = 2 * cfg.num_kv_heads * cfg.head_size * 2
+        return int(2 * T * kv_tok + 2 * T * cfg.num_q_heads * cfg.head_size * 2
+                   + int(w.context_lens_np.astype(np.int64).sum()) * kv_tok)

@@ -249,3 +249,104 @@ def make_workload(name_or_cfg, device="cpu", seed: int | None = None, nan_unused
 def as_u16(t: torch.Tensor) -> np.ndarray:
     """Raw 16-bit pattern of a CPU/GPU fp16/bf16 tensor as a numpy uint16 array."""
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+# ------------------------------------------------------------------ prefill / extend
+
+@dataclass(frozen=True)
+class PrefillConfig:
+    name: str
+    index: int              # seed = 2000 + index
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_size: int
+    block_size: int
+    dtype: str
+    q_len: int              # new tokens per sequence (a prompt, or a chunk of one)
+    prefix: tuple           # cached tokens before them: ("fixed", n) | ("uniform", lo, hi)
+
+    @property
+    def seed(self) -> int:
+        return 2000 + self.index
+
+
+PREFILL_CONFIGS = {
+    c.name: c for c in [
+        # whole prompts: 16 x 2048 tokens on a Llama-3-8B-shaped layer
+        PrefillConfig("prefill_8b", 0, 16, 32, 8, 128, 16, "bf16", 2048, ("fixed", 0)),
+        # chunked prefill: 512-token chunks over cached prefixes of 512..3584 tokens
+        PrefillConfig("extend_8b", 1, 32, 32, 8, 128, 16, "bf16", 512, ("uniform", 512, 3584)),
+        # whole prompts on a Llama-2-7B-shaped (MHA) layer
+        PrefillConfig("prefill_7b", 2, 8, 32, 32, 128, 16, "f16", 2048, ("fixed", 0)),
+        # small case for parity tests
+        PrefillConfig("prefill_tiny", 3, 3, 8, 2, 128, 16, "bf16", 100, ("uniform", 0, 300)),
+    ]
+}
+
+
+@dataclass
+class PrefillWorkload:
+    cfg: PrefillConfig
+    num_blocks: int
+    q: torch.Tensor                  # [T, Hq, D] packed new tokens
+    key: torch.Tensor                # [T, Hkv, D] their K
+    value: torch.Tensor              # [T, Hkv, D] their V
+    kv_cache: torch.Tensor           # [NB, Hkv, 2 * bs * D] opaque chunks (history)
+    block_tables: torch.Tensor       # int32 [S, W]
+    context_lens: torch.Tensor       # int32 [S] = prefix + q_len
+    query_start_loc: torch.Tensor    # int32 [S + 1]
+    slot_mapping: torch.Tensor       # int64 [T] slots of the new tokens
+    max_query_len: int
+    scale: float
+    block_tables_np: np.ndarray = None
+    context_lens_np: np.ndarray = None
+    query_start_loc_np: np.ndarray = None
+    slot_mapping_np: np.ndarray = None
+
+    @property
+    def dtype(self) -> torch.dtype:
+        return DTYPES[self.cfg.dtype]
+
+
+def make_prefill_workload(name_or_cfg, device="cpu", seed: int | None = None) -> PrefillWorkload:
+    cfg = PREFILL_CONFIGS[name_or_cfg] if isinstance(name_or_cfg, str) else name_or_cfg
+    seed = cfg.seed if seed is None else seed
+    rng = np.random.Generator(np.random.PCG64(seed))
+    S, Hq, Hkv, D, bs = cfg.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_size, cfg.block_size
+    if cfg.prefix[0] == "fixed":
+        prefix = np.full(S, cfg.prefix[1], dtype=np.int64)
+    else:
+        prefix = rng.integers(cfg.prefix[1], cfg.prefix[2] + 1, size=S)
+    ctx = (prefix + cfg.q_len).astype(np.int32)
+    nblk = (ctx + bs - 1) // bs
+    width = int(nblk.max())
+    NB = int(math.ceil(1.2 * int(nblk.sum())))
+    perm = rng.permutation(NB).astype(np.int64)
+    tables = np.full((S, width), -1, dtype=np.int32)
+    nxt = 0
+    for s in range(S):
+        tables[s, :nblk[s]] = perm[nxt:nxt + nblk[s]]
+        nxt += nblk[s]
+    qsl = np.concatenate([[0], np.cumsum(np.full(S, cfg.q_len))]).astype(np.int32)
+    pos = np.concatenate([np.arange(prefix[s], ctx[s]) for s in range(S)]).astype(np.int64)
+    seq = np.repeat(np.arange(S), cfg.q_len)
+    slots = tables[seq, pos // bs].astype(np.int64) * bs + pos % bs
+    T = int(qsl[-1])
+    dt = DTYPES[cfg.dtype]
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    q = torch.empty((T, Hq, D), dtype=dt, device=dev)
+    key = torch.empty((T, Hkv, D), dtype=dt, device=dev)
+    value = torch.empty((T, Hkv, D), dtype=dt, device=dev)
+    pool = torch.empty((NB, Hkv, 2 * bs * D), dtype=dt, device=dev)
+    for t in (q, key, value, pool):
+        fill_values(t, "normal", gen)
+    return PrefillWorkload(
+        cfg=cfg, num_blocks=NB, q=q, key=key, value=value, kv_cache=pool,
+        block_tables=torch.from_numpy(tables).to(dev), context_lens=torch.from_numpy(ctx).to(dev),
+        query_start_loc=torch.from_numpy(qsl).to(dev), slot_mapping=torch.from_numpy(slots).to(dev),
+        max_query_len=cfg.q_len, scale=1.0 / math.sqrt(D),
+        block_tables_np=tables, context_lens_np=ctx, query_start_loc_np=qsl, slot_mapping_np=slots,
+    )

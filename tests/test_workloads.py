@@ -47,3 +47,20 @@ def test_nan_unused_blocks():
     used = set(w.used_blocks.tolist())
     for b in range(w.num_blocks):
         assert bool(torch.isnan(w.kv_cache[b]).all()) == (b not in used)
+
+
+def test_prefill_workloads_are_seeded_and_consistent():
+    from paged_kv_cache_168_gb300.workloads import PREFILL_CONFIGS, make_prefill_workload
+    for name in PREFILL_CONFIGS:
+        a, b = make_prefill_workload(name), make_prefill_workload(name)
+        assert torch.equal(a.q, b.q) and np.array_equal(a.slot_mapping_np, b.slot_mapping_np)
+        cfg = a.cfg
+        qsl, ctx, bs = a.query_start_loc_np, a.context_lens_np, cfg.block_size
+        assert qsl[0] == 0 and np.all(np.diff(qsl) == cfg.q_len) and a.q.shape[0] == qsl[-1]
+        # the new tokens are each sequence's last q_len positions, in its own blocks
+        for s in range(cfg.num_seqs):
+            pos = np.arange(ctx[s] - cfg.q_len, ctx[s])
+            want = a.block_tables_np[s, pos // bs].astype(np.int64) * bs + pos % bs
+            assert np.array_equal(a.slot_mapping_np[qsl[s]:qsl[s + 1]], want)
+        used = a.block_tables_np[a.block_tables_np >= 0]
+        assert np.unique(used).size == used.size and used.max() < a.num_blocks

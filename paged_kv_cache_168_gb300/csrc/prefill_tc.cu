@@ -15,20 +15,25 @@
 //     S_t = Q K_t^T        (M = 128 rows, N = 128 tokens, K = D)  -> TMEM (fp32)
 //     O  += P_t V_t        (M = 128 rows, N = D, K = 128 tokens)  -> TMEM (fp32)
 // Q (written once, 128B-swizzled K-major) and P (written by the softmax
-// threads, same form, as p_hi and p_lo = p - p_hi so bf16 weights keep ~16
-// bits) are A operands; the cache's 8-token groups staged by bulk copies are
-// directly the K-major B operand (K) and the MN-major B operand (V).
+// threads, same form) are A operands; the cache's 8-token groups staged by
+// bulk copies are directly the K-major B operand (K) and the MN-major B
+// operand (V).  For bf16, P goes to the tensor core as p_hi = round(p) and
+// p_lo = round(p - p_hi) (two products, ~16 significant bits); at head_size
+// 128 p_lo is written over the K atoms of the tile's own stage, dead once S_t
+// is computed.  fp16 weights (11 bits) need no p_lo.
 // Roles:
 //   warp 0      bulk copies of each KV tile's (block, kv head) chunks into a
 //               2-stage ring (mbarrier transaction counts).
 //   warp 1      one lane issues S_{t+1} ahead of O += P_t V_t.
-//   warps 2-5   thread = TMEM lane = query row: causal mask, online softmax in
-//               base 2.  The running max is raised only when a tile's max
-//               exceeds it by more than 8 (a factor 256), and only then is the
-//               row of O rescaled in TMEM; otherwise the stale max is kept for
-//               both p and the sum, which is the same arithmetic.  They also
-//               zero V rows past the tile's last token (0 * NaN = NaN) and
-//               write the output rows at the end.
+//   warps 2-9   thread = TMEM lane = query row, in two warpgroups that own
+//               half of the tile's 128 columns (and half of O's columns)
+//               each: causal mask, online softmax in base 2 with the row
+//               maxima exchanged through shared memory.  The running max is
+//               raised only when a tile's max exceeds it by more than 8 (a
+//               factor 256), and only then is the row of O rescaled in TMEM;
+//               otherwise the stale max is kept for both p and the sum, which
+//               is the same arithmetic.  They also zero V rows past the tile's
+//               last token (0 * NaN = NaN) and write the output rows.
 // Every wait is bounded; a timeout sets PA_DEVERR_TIMEOUT and the CTA drains
 // its own copies and MMAs before releasing TMEM.
 #include <math.h>
@@ -44,7 +49,8 @@ namespace {
 
 constexpr int kRows = 128;                // MMA M: (position, head) rows of one query tile
 constexpr int kKv = 128;                  // tokens per KV tile
-constexpr int kThreads = 192;             // producer, MMA, 4 softmax warps
+constexpr int kThreads = 320;             // producer, MMA, 8 softmax warps (two column halves)
+constexpr int kSoftmaxWarps = 8;
 constexpr uint32_t kTmemCols = 512;       // S0 [0,128) S1 [128,256) O [256, 256 + D)
 constexpr uint32_t kOCol = 256;
 constexpr uint32_t kFull = 0xffffffffu;
@@ -59,11 +65,18 @@ struct Cfg {
   static constexpr int kQBytes = kRows * D * 2;
   static constexpr int kPBytes = kRows * kKv * 2;            // one P operand (hi or lo)
   static constexpr int kStages = 2;
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kQBytes + 2 * (size_t)kPBytes;
+  // p_lo lives in the K half of its tile's stage when that half is a whole
+  // 128 x 128 operand (D = 128: 16 groups x 2 KiB, 4 KiB apart); S of the tile
+  // has been computed by the time it is written
+  static constexpr bool kLoInStage = D == 128;
+  static constexpr size_t kSmem =
+      1024 + (size_t)kStages * kStageBytes + kQBytes + (size_t)kPBytes * (kLoInStage ? 1 : 2);
 };
 
 struct Shared {
   uint64_t full[2], empty[2], s_full[2], s_free[2], p_full, pv_done;
+  uint64_t xbar;                  // the two softmax warpgroups' per-row exchanges
+  float red[2][2][kRows];         // [exchange parity][warpgroup][row]
   uint32_t tmem_base;
   int bad;
   volatile int abort_flag;
@@ -73,6 +86,14 @@ struct Shared {
 // K-major operand of 128 rows whose 64-element column blocks are kQAtomBytes apart.
 __device__ __forceinline__ uint32_t op_offset(int r, int piece) {
   return (uint32_t)((piece >> 3) * (kRows * 128) + (r >> 3) * 1024 + (r & 7) * 128 + (((piece & 7) ^ (r & 7)) << 4));
+}
+
+// The same operand laid over the K atoms of a staged tile: row group r / 8 in
+// the tile's 8-token group r / 8, 64-column block a in K atom a.
+template <int D>
+__device__ __forceinline__ uint32_t stage_op_offset(int r, int piece) {
+  return (uint32_t)((r >> 3) * Cfg<D>::kGroupBytes + (piece >> 3) * 1024 + (r & 7) * 128 +
+                    (((piece & 7) ^ (r & 7)) << 4));
 }
 
 template <typename T, int D, int G>
@@ -87,7 +108,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   uint8_t* stages = dyn;
   uint8_t* qbuf = stages + C::kStages * C::kStageBytes;
   uint8_t* phi = qbuf + C::kQBytes;
-  uint8_t* plo = phi + C::kPBytes;
+  uint8_t* plo = phi + C::kPBytes;                   // unused when p_lo lives in the stage
+  constexpr bool kLo = kBF16;                        // fp16 weights keep 11 bits: no p_lo
 
   const int tile = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -143,10 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       mbar_init(&sh.full[i], 1);
       mbar_init(&sh.empty[i], 1);
       mbar_init(&sh.s_full[i], 1);
-      mbar_init(&sh.s_free[i], 4);
+      mbar_init(&sh.s_free[i], kSoftmaxWarps);
     }
-    mbar_init(&sh.p_full, 4);
+    mbar_init(&sh.p_full, kSoftmaxWarps);
     mbar_init(&sh.pv_done, 1);
+    mbar_init(&sh.xbar, kSoftmaxWarps);
     sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -248,7 +271,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           const uint32_t aoff = (kk >> 2) * C::kQAtomBytes + (kk & 3) * 32;
           tc::mma_f16(tmem + kOCol, tc::smem_desc(pha + aoff, 16, 1024, tc::kSwizzle128B), vdesc, id_pv,
                       (j > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_f16(tmem + kOCol, tc::smem_desc(pla + aoff, 16, 1024, tc::kSwizzle128B), vdesc, id_pv, 1u);
+          if (kLo) {
+            const uint64_t lo = C::kLoInStage
+                ? tc::smem_desc(st + (kk >> 2) * 1024 + (kk & 3) * 32, 16, C::kGroupBytes, tc::kSwizzle128B)
+                : tc::smem_desc(pla + aoff, 16, 1024, tc::kSwizzle128B);
+            tc::mma_f16(tmem + kOCol, lo, vdesc, id_pv, 1u);
+          }
         }
         tc::commit(&sh.pv_done);
         tc::commit(&sh.empty[slot]);
@@ -260,15 +288,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
     __syncwarp();
   } else {
-    // =================================================================== softmax warps (2-5)
+    // =================================================================== softmax warps (2-9)
+    // Warpgroup wg = 0 / 1 owns S columns [64 wg, 64 wg + 64) (tokens) and O
+    // columns [D/2 wg, D/2 wg + D/2) of the same 128 rows; per tile the two
+    // exchange their row maxima (and at the end their row sums) through shared
+    // memory under a bounded mbarrier.
+    constexpr int kCols = kKv / 2;
+    constexpr int kOC = D / 2;
+    const int wg = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;               // TMEM lane = query row = (position, head)
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     const int ipos = row / G;
     const bool row_ok = ipos < npos;
     const int pos = pos0 + ipos;                       // attends tokens t <= pos
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;                      // l: this half's share of the row sum
     bool ok = true;
+    auto exchange = [&](int k, float v) -> float {     // k-th exchange: returns the other half's v
+      sh.red[k & 1][wg][row] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.xbar);
+      if (!__all_sync(kFull, mbar_wait(&sh.xbar, k & 1))) {
+        ok = false;
+        return 0.f;
+      }
+      return sh.red[k & 1][wg ^ 1][row];
+    };
     for (int j = 0; j < n_kv; ++j) {
       const int sb = j & 1;
       // wait results are made warp-uniform: the TMEM loads and stores below are
@@ -278,21 +323,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         break;
       }
       tc::fence_after_sync();
-      float x[kKv / 16][16];
+      float x[kCols / 16][16];
 #pragma unroll
-      for (int c = 0; c < kKv / 16; ++c) tc::tmem_ld16(lane_addr + sb * kKv + c * 16, x[c]);
+      for (int c = 0; c < kCols / 16; ++c) tc::tmem_ld16(lane_addr + sb * kKv + wg * kCols + c * 16, x[c]);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.s_free[sb]);
-      const int lim = row_ok ? min(kKv, pos + 1 - j * kKv) : 0;   // tokens of this tile the row attends
+      const int lim = (row_ok ? min(kKv, pos + 1 - j * kKv) : 0) - wg * kCols;   // columns of this half attended
       float mt = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kKv / 16; ++c)
+      for (int c = 0; c < kCols / 16; ++c)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           x[c][e] = (c * 16 + e < lim) ? x[c][e] * p.scale_log2 : -INFINITY;
           mt = fmaxf(mt, x[c][e]);
         }
+      mt = fmaxf(mt, exchange(j, mt));
+      if (!ok) break;
       // P and O are free once the previous tile's PV has completed
       if (j > 0) {
         if (!__all_sync(kFull, mbar_wait(&sh.pv_done, (j - 1) & 1))) {
@@ -301,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
         tc::fence_after_sync();
       }
+      // both halves see the same m and mt, so they take the same decisions
       const float m_new = fmaxf(m, mt);
       const bool need = m != -INFINITY && m_new > m + kRescaleThreshold;
       if (m == -INFINITY) m = m_new;
@@ -313,18 +361,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           m = m_new;
         }
 #pragma unroll
-        for (int c = 0; c < D / 16; ++c) {
+        for (int c = 0; c < kOC / 16; ++c) {
           float o[16];
-          tc::tmem_ld16(lane_addr + kOCol + c * 16, o);
+          tc::tmem_ld16(lane_addr + kOCol + wg * kOC + c * 16, o);
 #pragma unroll
           for (int e = 0; e < 16; ++e) o[e] *= alpha;
-          tc::tmem_st16(lane_addr + kOCol + c * 16, o);
+          tc::tmem_st16(lane_addr + kOCol + wg * kOC + c * 16, o);
         }
         stored = true;
       }
-      // p = 2^(x - m) in fp32; P operand gets round(p) and round(p - round(p))
+      // the stage's bulk copy is complete before this thread writes into it
+      // (p_lo over its K atoms, zeros over V rows past the tile's end)
+      const int valid = min(kKv, kv_len - j * kKv);
+      if ((kLo && C::kLoInStage) || (valid & 15)) {
+        if (!__all_sync(kFull, mbar_wait(&sh.full[sb], (j >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+      }
+      uint8_t* stage = stages + sb * C::kStageBytes;
+      // p = 2^(x - m) in fp32; the P operand gets round(p) (and round(p - round(p)))
 #pragma unroll
-      for (int c = 0; c < kKv / 8; ++c) {
+      for (int c = 0; c < kCols / 8; ++c) {
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
@@ -332,28 +390,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           const float b = (m == -INFINITY) ? 0.f : exp2f(x[c >> 1][(c & 1) * 8 + e + 1] - m);
           l += a + b;
           hi[e >> 1] = Elem<T>::pack2(a, b);
-          const float2 h = Elem<T>::to_float2(hi[e >> 1]);
-          lo[e >> 1] = Elem<T>::pack2(a - h.x, b - h.y);
+          if (kLo) {
+            const float2 h = Elem<T>::to_float2(hi[e >> 1]);
+            lo[e >> 1] = Elem<T>::pack2(a - h.x, b - h.y);
+          }
         }
-        const uint32_t off = op_offset(row, c);
-        *reinterpret_cast<uint4*>(phi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(plo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-      // V rows of tokens past the tile's last token: zero (thread = token row
-      // here), after the stage's bulk copy is known complete
-      const int valid = min(kKv, kv_len - j * kKv);
-      if (valid & 15) {
-        if (!__all_sync(kFull, mbar_wait(&sh.full[sb], (j >> 1) & 1))) {
-          ok = false;
-          break;
+        const int piece = wg * (kCols / 8) + c;
+        *reinterpret_cast<uint4*>(phi + op_offset(row, piece)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        if (kLo) {
+          uint8_t* dst = C::kLoInStage ? stage + stage_op_offset<D>(row, piece) : plo + op_offset(row, piece);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
+      // V rows of tokens past the tile's last token (thread = token row here):
+      // zero, half of the 64-dim atoms per warpgroup
       if (row >= valid && row < ((valid + 15) & ~15)) {
-        uint8_t* vrow = stages + sb * C::kStageBytes + (row >> 3) * C::kGroupBytes + C::kAtoms * 1024 + (row & 7) * 128;
+        uint8_t* vrow = stage + (row >> 3) * C::kGroupBytes + C::kAtoms * 1024 + (row & 7) * 128;
 #pragma unroll
         for (int a = 0; a < C::kAtoms; ++a)
+          if ((a & 1) == wg)
 #pragma unroll
-          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + a * 1024 + c * 16) = make_uint4(0, 0, 0, 0);
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + a * 1024 + c * 16) = make_uint4(0, 0, 0, 0);
       }
       if (stored) tc::tmem_wait_st();
       tc::fence_proxy_async_smem();
@@ -362,14 +419,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (lane == 0) mbar_arrive(&sh.p_full);
     }
     if (ok && n_kv > 0) ok = __all_sync(kFull, mbar_wait(&sh.pv_done, (n_kv - 1) & 1));
+    float l_tot = 0.f;
+    if (ok) l_tot = l + exchange(n_kv, l);
     if (ok) {
       tc::fence_after_sync();
-      const float inv = row_ok && l > 0.f ? 1.f / l : 0.f;
-      T* orow = out + ((int64_t)(first + q0 + ipos) * p.num_q_heads + kvh * G + row % G) * D;
+      const float inv = row_ok && l_tot > 0.f ? 1.f / l_tot : 0.f;
+      T* orow = out + ((int64_t)(first + q0 + ipos) * p.num_q_heads + kvh * G + row % G) * D + wg * kOC;
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
+      for (int c = 0; c < kOC / 16; ++c) {
         float o[16];
-        tc::tmem_ld16(lane_addr + kOCol + c * 16, o);
+        tc::tmem_ld16(lane_addr + kOCol + wg * kOC + c * 16, o);
         if (row_ok) {
           uint32_t w[8];
 #pragma unroll
@@ -384,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         sh.abort_flag = 1;
       }
       if (row_ok) {
-        T* orow = out + ((int64_t)(first + q0 + ipos) * p.num_q_heads + kvh * G + row % G) * D;
-        for (int c = 0; c < D / 8; ++c) *reinterpret_cast<uint4*>(orow + c * 8) = make_uint4(0, 0, 0, 0);
+        T* orow = out + ((int64_t)(first + q0 + ipos) * p.num_q_heads + kvh * G + row % G) * D + wg * kOC;
+        for (int c = 0; c < kOC / 8; ++c) *reinterpret_cast<uint4*>(orow + c * 8) = make_uint4(0, 0, 0, 0);
       }
     }
   }

@@ -14,17 +14,24 @@
 // 128-token KV tile t:
 //     S_t = Q K_t^T        (M = 128 rows, N = 128 tokens, K = D)  -> TMEM (fp32)
 //     O  += P_t V_t        (M = 128 rows, N = D, K = 128 tokens)  -> TMEM (fp32)
-// Q (written once, 128B-swizzled K-major) and P (written by the softmax
-// threads, same form) are A operands; the cache's 8-token groups staged by
-// bulk copies are directly the K-major B operand (K) and the MN-major B
-// operand (V).  For bf16, P goes to the tensor core as p_hi = round(p) and
-// p_lo = round(p - p_hi) (two products, ~16 significant bits); at head_size
-// 128 p_lo is written over the K atoms of the tile's own stage, dead once S_t
-// is computed.  fp16 weights (11 bits) need no p_lo.
+// Q (written once, 128B-swizzled K-major, shared memory) is the A operand of
+// S; the cache's 8-token groups staged by bulk copies are directly the K-major
+// B operand (K) and the MN-major B operand (V).  P is written by the softmax
+// threads into TMEM over the S columns they have just read and is the A
+// operand of PV straight from TMEM, so P double-buffers with S: the softmax
+// of tile t+1 runs while PV of tile t executes.  (This relies on the tcgen05
+// operations of the issuing thread executing in issue order: S_{t+2} is
+// issued after PV_t has been, and overwrites P_t only after PV_t read it.)
+// For bf16, P goes to the tensor core as p_hi = round(p) and p_lo =
+// round(p - p_hi) (two products, ~16 significant bits); fp16 weights (11
+// bits) need no p_lo.
 // Roles:
 //   warp 0      bulk copies of each KV tile's (block, kv head) chunks into a
 //               2-stage ring (mbarrier transaction counts).
 //   warp 1      one lane issues S_{t+1} ahead of O += P_t V_t.
+// TMEM columns: S/P buffer 0 [0, 128), S/P buffer 1 [128, 256), O [256, 256 + D);
+// within a buffer P occupies p_hi [0, 64) and p_lo [64, 128) (tokens packed
+// two per column).
 //   warps 2-9   thread = TMEM lane = query row, in two warpgroups that own
 //               half of the tile's 128 columns (and half of O's columns)
 //               each: causal mask, online softmax in base 2 with the row
@@ -63,14 +70,8 @@ struct Cfg {
   static constexpr int kStageBytes = kKv * 2 * D * 2;        // K + V of one KV tile
   static constexpr int kQAtomBytes = kRows * 128;            // one 64-dim column block of Q (or P)
   static constexpr int kQBytes = kRows * D * 2;
-  static constexpr int kPBytes = kRows * kKv * 2;            // one P operand (hi or lo)
   static constexpr int kStages = 2;
-  // p_lo lives in the K half of its tile's stage when that half is a whole
-  // 128 x 128 operand (D = 128: 16 groups x 2 KiB, 4 KiB apart); S of the tile
-  // has been computed by the time it is written
-  static constexpr bool kLoInStage = D == 128;
-  static constexpr size_t kSmem =
-      1024 + (size_t)kStages * kStageBytes + kQBytes + (size_t)kPBytes * (kLoInStage ? 1 : 2);
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kQBytes;
 };
 
 struct Shared {
@@ -88,14 +89,6 @@ __device__ __forceinline__ uint32_t op_offset(int r, int piece) {
   return (uint32_t)((piece >> 3) * (kRows * 128) + (r >> 3) * 1024 + (r & 7) * 128 + (((piece & 7) ^ (r & 7)) << 4));
 }
 
-// The same operand laid over the K atoms of a staged tile: row group r / 8 in
-// the tile's 8-token group r / 8, 64-column block a in K atom a.
-template <int D>
-__device__ __forceinline__ uint32_t stage_op_offset(int r, int piece) {
-  return (uint32_t)((r >> 3) * Cfg<D>::kGroupBytes + (piece >> 3) * 1024 + (r & 7) * 128 +
-                    (((piece & 7) ^ (r & 7)) << 4));
-}
-
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
   using C = Cfg<D>;
@@ -107,8 +100,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   uint8_t* dyn = dyn_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   uint8_t* stages = dyn;
   uint8_t* qbuf = stages + C::kStages * C::kStageBytes;
-  uint8_t* phi = qbuf + C::kQBytes;
-  uint8_t* plo = phi + C::kPBytes;                   // unused when p_lo lives in the stage
   constexpr bool kLo = kBF16;                        // fp16 weights keep 11 bits: no p_lo
 
   const int tile = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
@@ -234,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     if (lane == 0) {
       const uint32_t id_qk = tc::idesc_f16(kRows, kKv, kBF16, false, false);
       const uint32_t id_pv = tc::idesc_f16(kRows, D, kBF16, false, true);
-      const uint32_t qa = smem_u32(qbuf), pha = smem_u32(phi), pla = smem_u32(plo);
+      const uint32_t qa = smem_u32(qbuf);
       auto issue_qk = [&](int j) -> bool {
         const int slot = j & 1;
         if (!mbar_wait(&sh.full[slot], (j >> 1) & 1)) return false;
@@ -268,15 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         for (int kk = 0; kk < nsteps; ++kk) {
           const uint64_t vdesc =
               tc::smem_desc(st + kk * 2 * C::kGroupBytes + C::kAtoms * 1024, 1024, C::kGroupBytes, tc::kSwizzle128B);
-          const uint32_t aoff = (kk >> 2) * C::kQAtomBytes + (kk & 3) * 32;
-          tc::mma_f16(tmem + kOCol, tc::smem_desc(pha + aoff, 16, 1024, tc::kSwizzle128B), vdesc, id_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-          if (kLo) {
-            const uint64_t lo = C::kLoInStage
-                ? tc::smem_desc(st + (kk >> 2) * 1024 + (kk & 3) * 32, 16, C::kGroupBytes, tc::kSwizzle128B)
-                : tc::smem_desc(pla + aoff, 16, 1024, tc::kSwizzle128B);
-            tc::mma_f16(tmem + kOCol, lo, vdesc, id_pv, 1u);
-          }
+          const uint32_t pa = tmem + slot * kKv + kk * 8;      // 16 tokens = 8 packed columns
+          tc::mma_f16_ta(tmem + kOCol, pa, vdesc, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          if (kLo) tc::mma_f16_ta(tmem + kOCol, pa + kKv / 2, vdesc, id_pv, 1u);
         }
         tc::commit(&sh.pv_done);
         tc::commit(&sh.empty[slot]);
@@ -338,23 +323,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           x[c][e] = (c * 16 + e < lim) ? x[c][e] * p.scale_log2 : -INFINITY;
           mt = fmaxf(mt, x[c][e]);
         }
+      // after the exchange both halves have read their S columns, so P may be
+      // written over them
       mt = fmaxf(mt, exchange(j, mt));
       if (!ok) break;
-      // P and O are free once the previous tile's PV has completed
-      if (j > 0) {
+      // both halves see the same m and mt, so they take the same decisions
+      const float m_new = fmaxf(m, mt);
+      const bool need = m != -INFINITY && m_new > m + kRescaleThreshold;
+      if (m == -INFINITY) m = m_new;
+      if (__any_sync(kFull, need)) {
+        // O holds exactly tiles < j once PV_{j-1} has completed (PV_j waits for
+        // this warp's P).  The whole warp takes the O round trip; rows that keep
+        // their max scale by 1.
         if (!__all_sync(kFull, mbar_wait(&sh.pv_done, (j - 1) & 1))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-      }
-      // both halves see the same m and mt, so they take the same decisions
-      const float m_new = fmaxf(m, mt);
-      const bool need = m != -INFINITY && m_new > m + kRescaleThreshold;
-      if (m == -INFINITY) m = m_new;
-      bool stored = false;
-      if (__any_sync(kFull, need)) {
-        // the whole warp takes the O round trip; rows that keep their max scale by 1
         const float alpha = need ? exp2f(m - m_new) : 1.f;
         if (need) {
           l *= alpha;
@@ -368,40 +353,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           for (int e = 0; e < 16; ++e) o[e] *= alpha;
           tc::tmem_st16(lane_addr + kOCol + wg * kOC + c * 16, o);
         }
-        stored = true;
       }
-      // the stage's bulk copy is complete before this thread writes into it
-      // (p_lo over its K atoms, zeros over V rows past the tile's end)
+      // p = 2^(x - m) in fp32; P (in TMEM, two tokens per column) gets round(p)
+      // and, for bf16, round(p - round(p))
+#pragma unroll
+      for (int h = 0; h < kCols / 32; ++h) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c = h * 32 + 2 * e;
+          const float a = (m == -INFINITY) ? 0.f : exp2f(x[c >> 4][c & 15] - m);
+          const float b = (m == -INFINITY) ? 0.f : exp2f(x[c >> 4][(c & 15) + 1] - m);
+          l += a + b;
+          hi[e] = Elem<T>::pack2(a, b);
+          if (kLo) {
+            const float2 r = Elem<T>::to_float2(hi[e]);
+            lo[e] = Elem<T>::pack2(a - r.x, b - r.y);
+          }
+        }
+        const uint32_t col = lane_addr + sb * kKv + wg * (kCols / 2) + h * 16;
+        tc::tmem_st16u(col, hi);
+        if (kLo) tc::tmem_st16u(col + kKv / 2, lo);
+      }
+      // V rows of tokens past the tile's last token must not hold NaN/Inf
+      // (0 * NaN = NaN): zero them, after the stage's bulk copy is complete
       const int valid = min(kKv, kv_len - j * kKv);
-      if ((kLo && C::kLoInStage) || (valid & 15)) {
+      if (valid & 15) {
         if (!__all_sync(kFull, mbar_wait(&sh.full[sb], (j >> 1) & 1))) {
           ok = false;
           break;
         }
       }
       uint8_t* stage = stages + sb * C::kStageBytes;
-      // p = 2^(x - m) in fp32; the P operand gets round(p) (and round(p - round(p)))
-#pragma unroll
-      for (int c = 0; c < kCols / 8; ++c) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const float a = (m == -INFINITY) ? 0.f : exp2f(x[c >> 1][(c & 1) * 8 + e] - m);
-          const float b = (m == -INFINITY) ? 0.f : exp2f(x[c >> 1][(c & 1) * 8 + e + 1] - m);
-          l += a + b;
-          hi[e >> 1] = Elem<T>::pack2(a, b);
-          if (kLo) {
-            const float2 h = Elem<T>::to_float2(hi[e >> 1]);
-            lo[e >> 1] = Elem<T>::pack2(a - h.x, b - h.y);
-          }
-        }
-        const int piece = wg * (kCols / 8) + c;
-        *reinterpret_cast<uint4*>(phi + op_offset(row, piece)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        if (kLo) {
-          uint8_t* dst = C::kLoInStage ? stage + stage_op_offset<D>(row, piece) : plo + op_offset(row, piece);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-      }
       // V rows of tokens past the tile's last token (thread = token row here):
       // zero, half of the 64-dim atoms per warpgroup
       if (row >= valid && row < ((valid + 15) & ~15)) {
@@ -412,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
             for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + a * 1024 + c * 16) = make_uint4(0, 0, 0, 0);
       }
-      if (stored) tc::tmem_wait_st();
+      tc::tmem_wait_st();
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();

@@ -55,15 +55,21 @@ constexpr int kN = 16;                             // MMA N: query heads, zero-p
 constexpr int kQBytes = kN * kD * 2;               // 4 KiB
 constexpr int kPBytes = kTile * 32 * 2;            // P^T operand: 128 tokens x up to 32 columns (8 KiB)
 constexpr int kThreads = 320;                      // producer, MMA, 4 softmax warps, 4 output warps
+// 8-bit caches add converter warps: 8 when the registers allow it (group <= 4), else 4
+__host__ __device__ constexpr int converter_warps(int G) { return G <= 4 ? 8 : 4; }
+__host__ __device__ constexpr int threads_of(bool i8, int G) { return kThreads + (i8 ? 32 * converter_warps(G) : 0); }
+constexpr int kRawBytes = 64 * (2 * kD + 32);      // one 64-token half tile of 8-bit chunks (bs 1: 288 B/token)
+constexpr int kRaw = 3;                            // raw half tiles in flight
 constexpr uint32_t kTmemCols = 128;                // S0 S1 (16 columns each) | O0 O1 (32 columns each)
 constexpr uint32_t kFull = 0xffffffffu;
 
 struct TileMeta {
   int s, kvh, part, valid;       // sequence (< 0: no more work), kv head, partition, rows < valid hold tokens
   int last, qslot, n_parts, lo;  // last tile of the item, Q buffer, partitions, rows < lo precede the window
+  float qinv;                    // 8-bit caches with bf16 q: 2^-e undoing the exact prescale of Q to fp16
 };
 
-template <int NS>
+template <int NS, bool I8>
 struct Shared {
   uint64_t full[NS], empty[NS];
   uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2], q_free[2];
@@ -79,7 +85,41 @@ struct Shared {
   float red_sum[4][kN];
   uint32_t tmem_base;
   volatile int abort_flag;
+  // 8-bit caches: producer -> converter ring of raw half tiles, and the token
+  // scales of each converted stage
+  uint64_t raw_full[I8 ? kRaw : 1], raw_empty[I8 ? kRaw : 1];
+  TileMeta raw_meta[I8 ? kRaw : 1];
+  float sk[I8 ? NS : 1][I8 ? kTile : 1];
+  float sv[I8 ? NS : 1][I8 ? kTile : 1];
 };
+
+// 16 8-bit codes -> 16 exact 16-bit values (8 words, two per word, in order).
+// fp16: the byte goes into the mantissa of 1024 (0x64XX = 1024 + byte), then
+// 1152 is taken off; bf16: the byte goes into the mantissa of 2^23 in fp32,
+// 2^23 + 128 is taken off, and the (exact) high halves are packed.
+template <typename T>
+__device__ __forceinline__ void codes_to_16bit(const uint4 w4, uint32_t (&o)[8]) {
+  const uint32_t w[4] = {w4.x ^ 0x80808080u, w4.y ^ 0x80808080u, w4.z ^ 0x80808080u, w4.w ^ 0x80808080u};
+  if constexpr (std::is_same<T, __half>::value) {
+    const __half2 off = __half2half2(__ushort_as_half((unsigned short)0x6480));   // 1152
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t a = __byte_perm(w[k], 0x64646464u, 0x4140), b = __byte_perm(w[k], 0x64646464u, 0x4342);
+      __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), off), hb = __hsub2(*reinterpret_cast<__half2*>(&b), off);
+      o[2 * k] = *reinterpret_cast<uint32_t*>(&ha);
+      o[2 * k + 1] = *reinterpret_cast<uint32_t*>(&hb);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int b = 0; b < 4; b += 2) {
+        const float f0 = __uint_as_float(__byte_perm(w[k], 0x4B000000u, 0x7540 + b)) - 8388736.0f;
+        const float f1 = __uint_as_float(__byte_perm(w[k], 0x4B000000u, 0x7540 + b + 1)) - 8388736.0f;
+        o[2 * k + (b >> 1)] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+      }
+  }
+}
 
 __device__ __forceinline__ bool ctx_invalid(const DecodeParams& p, int ctx) { return !context_ok(p, ctx); }
 
@@ -95,31 +135,44 @@ __device__ void warp_zero_rows(const DecodeParams& p, int s, int kvh, int lane) 
   for (int i = lane * 8; i < G * kD; i += 32 * 8) *reinterpret_cast<uint4*>(out + i) = make_uint4(0, 0, 0, 0);
 }
 
-template <typename T, int G, int NS>
-__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
+template <typename T, int G, int NS, bool I8>
+__global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
   // P^T holds p_hi for the G heads in columns [0, HG) and p_lo in [HG, 2 HG):
   // one PV product (N = 2 HG) yields both halves of O^T.
   constexpr int HG = G < 8 ? 8 : G;
   constexpr int NPV = 2 * HG;
-  __shared__ Shared<NS> sh;
+  __shared__ Shared<NS, I8> sh;
   extern __shared__ __align__(1024) uint8_t dyn_raw[];
   const uint32_t raw_s = smem_u32(dyn_raw);
   uint8_t* dyn = dyn_raw + (((raw_s + 1023u) & ~1023u) - raw_s);   // 1024-aligned in the shared window
   uint8_t* stages = dyn;
   uint8_t* qbuf = dyn + NS * kTileBytes;
   uint8_t* pbuf = qbuf + 2 * kQBytes;
-  int* pre = reinterpret_cast<int*>(pbuf + 2 * kPBytes);   // pbuf: 2 buffers of [p_hi | p_lo]
+  uint8_t* raw = pbuf + 2 * kPBytes;                         // pbuf: 2 buffers of [p_hi | p_lo]
+  int* pre = reinterpret_cast<int*>(raw + (I8 ? kRaw * kRawBytes : 0));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.num_seqs, Hkv = p.num_kv_heads, bs = p.block_size;
-  const int64_t chunk_bytes = (int64_t)bs * 2 * kD * 2;
-  constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+  const int64_t chunk_bytes = I8 ? I8Layout{bs, Hkv}.chunk_bytes() : (int64_t)bs * 2 * kD * 2;
+  // Operand type of the MMAs.  8-bit caches always use fp16 operands: codes
+  // (|c| <= 127) are exact in fp16, and bf16 queries are brought into fp16 by
+  // an exact power-of-two prescale per item (undone on the scores).
+  using OpT = std::conditional_t<I8, __half, T>;
+  constexpr bool kBF16 = std::is_same<OpT, __nv_bfloat16>::value;
+  constexpr bool kQConvert = I8 && std::is_same<T, __nv_bfloat16>::value;
+  constexpr int NCW = I8 ? converter_warps(G) : 0;
 
   // ---- set-up: barriers, zeroed Q buffers (padding heads stay zero), TMEM
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&sh.full[i], 1);
+      mbar_init(&sh.full[i], I8 ? NCW : 1);   // 8-bit: the converter warps arrive
       mbar_init(&sh.empty[i], 1);
+    }
+    if (I8) {
+      for (int i = 0; i < kRaw; ++i) {
+        mbar_init(&sh.raw_full[i], 1);
+        mbar_init(&sh.raw_empty[i], 4);
+      }
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.s_full[i], 1);
@@ -136,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     sh.abort_flag = 0;
     fence_mbar_init();
   }
-  for (int i = threadIdx.x; i < 2 * kQBytes / 16; i += kThreads)
+  for (int i = threadIdx.x; i < 2 * kQBytes / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
   if (warp == 1) {
     tc::tmem_alloc(&sh.tmem_base, kTmemCols);
@@ -205,7 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     if (blockIdx.x < total) nxt = fetch(blockIdx.x);
     for (int it = blockIdx.x; it < total && !aborted; it += gridDim.x) {
       const Item cur = nxt;
-      if (it + (int)gridDim.x < total) nxt = fetch(it + gridDim.x);
+      const bool more = it + (int)gridDim.x < total;
+      if (more) nxt = fetch(it + gridDim.x);
       const int s = cur.s, kvh = cur.kvh, part = cur.part, ctx = cur.ctx, id_lane = cur.id_lane;
       const int32_t* row = p.block_tables + (int64_t)s * p.bt_stride;   // entry table_index(j) holds block j
       if (ctx_invalid(p, ctx)) {
@@ -245,15 +299,49 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         aborted = true;
         break;
       }
+      float qinv = 1.f;
       {
         uint8_t* qb = qbuf + qslot * kQBytes;
+        uint4 qw[kQChunks];
+#pragma unroll
+        for (int k = 0; k < kQChunks; ++k) qw[k] = cur.qv[k];
+        if constexpr (kQConvert) {
+          // bf16 -> fp16 times 2^e, e chosen so the item's max |q| lands in
+          // [2^14, 2^15): exact for every element within 2^28 of the max
+          float mx = 0.f;
+#pragma unroll
+          for (int k = 0; k < kQChunks; ++k) {
+            const uint32_t w[4] = {qw[k].x, qw[k].y, qw[k].z, qw[k].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = Elem<T>::to_float2(w[i]);
+              mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+          }
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o2));
+          int e = 0;
+          if (mx > 0.f) e = min(100, max(-100, 14 - ilogbf(mx)));
+          const float up = ldexpf(1.f, e);
+          qinv = ldexpf(1.f, -e);
+#pragma unroll
+          for (int k = 0; k < kQChunks; ++k) {
+            uint32_t w[4] = {qw[k].x, qw[k].y, qw[k].z, qw[k].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = Elem<T>::to_float2(w[i]);
+              w[i] = Elem<__half>::pack2(f.x * up, f.y * up);
+            }
+            qw[k] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
 #pragma unroll
         for (int k = 0; k < kQChunks; ++k) {
           const int c = lane + 32 * k;
           if (c < G * 16) {
             const int n = c >> 4, cc = c & 15, atom = cc >> 3, piece = cc & 7;
             *reinterpret_cast<uint4*>(qb + (atom * 2 + (n >> 3)) * 1024 + (n & 7) * 128 + ((piece ^ (n & 7)) << 4)) =
-                cur.qv[k];
+                qw[k];
           }
         }
         tc::fence_proxy_async_smem();
@@ -261,7 +349,51 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       }
       // ---- stream the tiles
       const int ntiles = (t1 - t0 + kTile - 1) / kTile;
-      for (int k = 0; k < ntiles; ++k) {
+      for (int k = 0; k < ntiles && I8; ++k) {
+        // 8-bit: each tile goes to the converter warps as two 64-token half tiles
+        const int valid = min(kTile, t1 - (t0 + k * kTile));
+        TileMeta m;
+        m.s = s; m.kvh = kvh; m.part = part; m.valid = valid;
+        m.last = (k == ntiles - 1); m.qslot = qslot; m.n_parts = n_parts;
+        m.lo = max(0, t_first - (t0 + k * kTile));
+        m.qinv = qinv;
+        // the tile's block ids, lane i holding blocks i + 32 c of the tile: the
+        // item's first 32 come from the prefetched id_lane, the rest are loaded
+        // here, all in flight together
+        const int nbt = (valid + bs - 1) / bs;
+        int idr[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int b = lane + 32 * c, bi = k * (kTile / bs) + b;
+          const int id_sh = __shfl_sync(kFull, id_lane, bi & 31);
+          idr[c] = b < nbt ? (bi < 32 ? id_sh : row[table_index(jb + bi, p.ring_blocks)]) : 0;
+        }
+        for (int h = 0; h < 2 && !aborted; ++h) {
+          const int q = 2 * tile_seq + h, r = q % kRaw;
+          if (q >= kRaw && !mbar_wait(&sh.raw_empty[r], ((q / kRaw) - 1) & 1)) {
+            aborted = true;
+            break;
+          }
+          const int hv = min(64, valid - 64 * h);
+          const int nbh = hv > 0 ? (hv + bs - 1) / bs : 0;
+          if (lane == 0) {
+            sh.raw_meta[r] = m;
+            mbar_arrive_expect_tx(&sh.raw_full[r], (uint32_t)(nbh * chunk_bytes));
+          }
+          __syncwarp();
+          const int hb0 = h * (64 / bs);                 // first block of the half, within the tile
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int b = lane + 32 * c - hb0;             // this lane's block c, within the half
+            if (b >= 0 && b < nbh)
+              bulk_g2s(raw + r * kRawBytes + b * chunk_bytes, p.cache + ((int64_t)idr[c] * Hkv + kvh) * chunk_bytes,
+                       (uint32_t)chunk_bytes, &sh.raw_full[r]);
+          }
+        }
+        if (aborted) break;
+        ++tile_seq;
+      }
+      for (int k = 0; k < ntiles && !I8; ++k) {
         const int slot = tile_seq % NS;
         if (tile_seq >= NS && !mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1)) {
           aborted = true;
@@ -274,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           m.s = s; m.kvh = kvh; m.part = part; m.valid = valid;
           m.last = (k == ntiles - 1); m.qslot = qslot; m.n_parts = n_parts;
           m.lo = max(0, t_first - (t0 + k * kTile));
+          m.qinv = qinv;
           sh.meta[slot] = m;
           mbar_arrive_expect_tx(&sh.full[slot], (uint32_t)(nb * chunk_bytes));
         }
@@ -289,20 +422,43 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       }
       ++item_seq;
     }
-    // ---- no more work: a stage whose metadata says so
-    const int slot = tile_seq % NS;
-    if (!aborted && tile_seq >= NS && !mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1)) aborted = true;
-    if (aborted && lane == 0) {
-      // never leave copies in flight: wait (bounded) for the latest phase of every stage
-      for (int t = max(0, tile_seq - NS); t < tile_seq; ++t) mbar_wait(&sh.full[t % NS], (t / NS) & 1);
-    }
-    if (lane == 0) {
-      if (aborted) {
-        report(p.dev_err, PA_DEVERR_TIMEOUT);
-        sh.abort_flag = 1;
+    // ---- no more work: a stage (8-bit: a raw half tile) whose metadata says so
+    if (I8) {
+      // the "no more work" mark goes into both half slots of the next tile (each
+      // converter thread watches its own half's slot)
+      for (int h = 0; h < 2; ++h) {
+        const int q = 2 * tile_seq + h, r = q % kRaw;
+        if (!aborted && q >= kRaw && !mbar_wait(&sh.raw_empty[r], ((q / kRaw) - 1) & 1)) aborted = true;
+        if (aborted && lane == 0 && h == 0) {
+          // never leave copies in flight: wait (bounded) for the latest phase of every raw slot
+          const int issued = 2 * tile_seq;
+          for (int t = max(0, issued - kRaw); t < issued; ++t) mbar_wait(&sh.raw_full[t % kRaw], (t / kRaw) & 1);
+        }
+        if (lane == 0) {
+          if (aborted && h == 0) {
+            report(p.dev_err, PA_DEVERR_TIMEOUT);
+            sh.abort_flag = 1;
+          }
+          sh.raw_meta[r].s = -1;
+          mbar_arrive(&sh.raw_full[r]);
+        }
+        __syncwarp();
       }
-      sh.meta[slot].s = -1;
-      mbar_arrive(&sh.full[slot]);
+    } else {
+      const int slot = tile_seq % NS;
+      if (!aborted && tile_seq >= NS && !mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1)) aborted = true;
+      if (aborted && lane == 0) {
+        // never leave copies in flight: wait (bounded) for the latest phase of every stage
+        for (int t = max(0, tile_seq - NS); t < tile_seq; ++t) mbar_wait(&sh.full[t % NS], (t / NS) & 1);
+      }
+      if (lane == 0) {
+        if (aborted) {
+          report(p.dev_err, PA_DEVERR_TIMEOUT);
+          sh.abort_flag = 1;
+        }
+        sh.meta[slot].s = -1;
+        mbar_arrive(&sh.full[slot]);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -411,10 +567,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.s_free[sb]);
       const bool rv = row >= mt.lo && row < mt.valid;
+      // 8-bit: K_t = sk_t * codes and V_t = sv_t * codes; sk_t scales this row's
+      // scores and sv_t its P^T row (the normaliser keeps the unscaled p)
+      const float kscale = I8 ? sh.sk[slot][row] * (p.scale_log2 * mt.qinv) : p.scale_log2;
+      const float vscale = I8 ? sh.sv[slot][row] : 1.f;
       float x[G], corr[G];
 #pragma unroll
       for (int n = 0; n < G; ++n) {
-        x[n] = rv ? sv[n] * p.scale_log2 : -INFINITY;
+        x[n] = rv ? sv[n] * kscale : -INFINITY;
         float v = x[n];
 #pragma unroll
         for (int o2 = 16; o2 > 0; o2 >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o2));
@@ -440,10 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       uint32_t pk[NPV / 2];   // [p_hi of heads 0..HG-1 | p_lo of heads 0..HG-1], two per word
 #pragma unroll
       for (int n2 = 0; n2 < HG; n2 += 2) {
-        const float a = (n2 < G) ? pr[n2] : 0.f, b = (n2 + 1 < G) ? pr[n2 + 1] : 0.f;
-        pk[n2 >> 1] = Elem<T>::pack2(a, b);
-        const float2 r = Elem<T>::to_float2(pk[n2 >> 1]);
-        pk[(HG + n2) >> 1] = Elem<T>::pack2(a - r.x, b - r.y);
+        const float a = (n2 < G) ? pr[n2] * vscale : 0.f, b = (n2 + 1 < G) ? pr[n2 + 1] * vscale : 0.f;
+        pk[n2 >> 1] = Elem<OpT>::pack2(a, b);
+        const float2 r = Elem<OpT>::to_float2(pk[n2 >> 1]);
+        pk[(HG + n2) >> 1] = Elem<OpT>::pack2(a - r.x, b - r.y);
       }
       // P^T buffer hb was last read by PV(t - 2): wait for it to complete
       if (tile_seq >= 2 && !mbar_wait(&sh.o_full[hb], ((tile_seq - 2) >> 1) & 1)) { ok = false; break; }
@@ -512,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       report(p.dev_err, PA_DEVERR_TIMEOUT);
       sh.abort_flag = 1;
     }
-  } else {
+  } else if (warp < 10) {
     // =================================================================== output warps (6-9)
     // Tile t: O^T -> acc = acc * corr_t + O_t (thread = TMEM lane = head dim);
     // at the end of an item, write out = acc / L (or the partition's partials).
@@ -577,6 +737,91 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       report(p.dev_err, PA_DEVERR_TIMEOUT);
       sh.abort_flag = 1;
     }
+  } else if (I8) {
+    // =================================================================== converter warps (8-bit)
+    // Half tile h (64 tokens) of tile t: for each token one thread turns its K
+    // code row and another its V code row into the 16-bit operand rows of the
+    // stage (the 16-bit cache layout: 8-token groups of K then V atoms, pieces
+    // swizzled by the row's index in its group) and copies the token's scale.
+    // Rows past the tile's last token become zeros (scale 0).  With 8 warps
+    // the two halves are converted side by side (threads 128-255 take half 1);
+    // with 4 warps each thread converts its row of both halves in turn.
+    constexpr int kHalvesPerThread = NCW == 8 ? 1 : 2;
+    const int ct = threadIdx.x - kThreads;                 // 0 .. 32 NCW - 1
+    const int part = (ct >> 6) & 1, u = ct & 63;
+    const int h_first = NCW == 8 ? (ct >> 7) : 0;
+    const I8Layout L8{bs, Hkv};
+    const int64_t sbytes = L8.scale_bytes();
+    int tile_seq = 0;
+    bool ok = true;
+    while (ok) {
+      const int slot = tile_seq % NS;
+      TileMeta mt;
+      mt.s = -1;
+      for (int hh = 0; hh < kHalvesPerThread; ++hh) {
+        const int h = h_first + hh;
+        const int q = 2 * tile_seq + h, r = q % kRaw;
+        if (!mbar_wait(&sh.raw_full[r], (q / kRaw) & 1)) {
+          ok = false;
+          break;
+        }
+        mt = sh.raw_meta[r];
+        if (mt.s < 0 || sh.abort_flag) break;               // no more work
+        if (hh == 0 && tile_seq >= NS && !mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const int t = 64 * h + u;                           // token row in the tile
+        uint8_t* dst = stages + slot * kTileBytes + (t >> 3) * kGroupBytes + part * 2048 + (t & 7) * 128;
+        float scale = 0.f;
+        if (t < mt.valid) {
+          const int b = u / bs, tb = u - b * bs;
+          const uint8_t* chunk = raw + r * kRawBytes + b * chunk_bytes;
+          const uint8_t* src = chunk + (int64_t)(part * bs + tb) * kD;
+          scale = *reinterpret_cast<const float*>(chunk + 2LL * bs * kD + part * sbytes + 4 * tb);
+          uint4 in[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) in[j] = *reinterpret_cast<const uint4*>(src + ((j ^ (tb & 7)) << 4));
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint32_t o[8];
+            codes_to_16bit<__half>(in[j], o);
+            uint8_t* atom = dst + (j >> 2) * 1024;
+            const int p0 = (2 * j) & 7;
+            *reinterpret_cast<uint4*>(atom + ((p0 ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(atom + (((p0 + 1) ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            *reinterpret_cast<uint4*>(dst + c * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(dst + 1024 + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        (part == 0 ? sh.sk : sh.sv)[slot][t] = scale;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.raw_empty[r]);
+      }
+      if (!ok) break;
+      if (mt.s >= 0 && sh.abort_flag) {
+        ok = false;
+        break;
+      }
+      if (mt.s < 0 && tile_seq >= NS && !mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      if (ct == 0) sh.meta[slot] = mt;                    // a real tile, or "no more work"
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.full[slot]);
+      if (mt.s < 0) break;
+      ++tile_seq;
+    }
+    if (!ok && lane == 0) {
+      report(p.dev_err, PA_DEVERR_TIMEOUT);
+      sh.abort_flag = 1;
+    }
   }
 
   // ---- tear-down: release TMEM once every role is done
@@ -588,24 +833,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   }
 }
 
-template <typename T, int G, int NS>
+template <typename T, int G, int NS, bool I8>
 cudaError_t launch_typed(const DecodeParams& p, int num_sms, cudaStream_t stream) {
-  const size_t smem = 1024 + (size_t)NS * kTileBytes + 2 * kQBytes + 2 * kPBytes + (size_t)(p.num_seqs + 1) * 4;
-  auto kern = decode_tc_kernel<T, G, NS>;
-  cudaError_t e = set_smem_attribute_once<decode_tc_kernel<T, G, NS>>(smem);
+  const size_t smem = 1024 + (size_t)NS * kTileBytes + 2 * kQBytes + 2 * kPBytes + (I8 ? (size_t)kRaw * kRawBytes : 0) +
+                      (size_t)(p.num_seqs + 1) * 4;
+  auto kern = decode_tc_kernel<T, G, NS, I8>;
+  cudaError_t e = set_smem_attribute_once<decode_tc_kernel<T, G, NS, I8>>(smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, kThreads, smem, stream>>>(p);
+  kern<<<num_sms, threads_of(I8, G), smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <typename T, int NS>
+template <typename T, int NS, bool I8>
 cudaError_t launch_group(const DecodeParams& p, int group, int num_sms, cudaStream_t stream) {
   switch (group) {
-    case 1: return launch_typed<T, 1, NS>(p, num_sms, stream);
-    case 2: return launch_typed<T, 2, NS>(p, num_sms, stream);
-    case 4: return launch_typed<T, 4, NS>(p, num_sms, stream);
-    case 8: return launch_typed<T, 8, NS>(p, num_sms, stream);
-    case 16: return launch_typed<T, 16, NS>(p, num_sms, stream);
+    case 1:
+      if constexpr (I8) return cudaErrorInvalidValue;   // 8-bit caches use the CUDA-core kernel below 4
+      else return launch_typed<T, 1, NS, false>(p, num_sms, stream);
+    case 2:
+      if constexpr (I8) return cudaErrorInvalidValue;
+      else return launch_typed<T, 2, NS, false>(p, num_sms, stream);
+    case 4: return launch_typed<T, 4, NS, I8>(p, num_sms, stream);
+    case 8: return launch_typed<T, 8, NS, I8>(p, num_sms, stream);
+    case 16:
+      if constexpr (I8) return cudaErrorInvalidValue;   // 8-bit caches serve groups up to 8
+      else return launch_typed<T, 16, NS, false>(p, num_sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -617,14 +869,28 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, int group, int nu
   const bool three = p.num_seqs <= 1024;   // shared memory: 3 stages + prefix of <= 1025 ints
   cudaError_t e;
   if (dtype == PA_F16)
-    e = three ? launch_group<__half, 3>(p, group, num_sms, stream) : launch_group<__half, 2>(p, group, num_sms, stream);
+    e = three ? launch_group<__half, 3, false>(p, group, num_sms, stream)
+              : launch_group<__half, 2, false>(p, group, num_sms, stream);
   else if (dtype == PA_BF16)
-    e = three ? launch_group<__nv_bfloat16, 3>(p, group, num_sms, stream)
-              : launch_group<__nv_bfloat16, 2>(p, group, num_sms, stream);
+    e = three ? launch_group<__nv_bfloat16, 3, false>(p, group, num_sms, stream)
+              : launch_group<__nv_bfloat16, 2, false>(p, group, num_sms, stream);
   else
     return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
   return launch_merge(p, dtype, kD, stream);
+}
+
+cudaError_t launch_decode_tc_i8(const DecodeParams& p, int act_dtype, int group, int num_sms, cudaStream_t stream) {
+  if (p.num_seqs > kTcI8MaxSeqs || group < 4 || group > 8) return cudaErrorInvalidValue;
+  cudaError_t e;
+  if (act_dtype == PA_F16)
+    e = launch_group<__half, 2, true>(p, group, num_sms, stream);
+  else if (act_dtype == PA_BF16)
+    e = launch_group<__nv_bfloat16, 2, true>(p, group, num_sms, stream);
+  else
+    return cudaErrorInvalidValue;
+  if (e != cudaSuccess) return e;
+  return launch_merge(p, act_dtype, kD, stream);
 }
 
 }  // namespace pkv

@@ -118,6 +118,12 @@ struct PrefillParams {
 };
 cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, int head_size, int group, cudaStream_t stream);
 
+// Paged decode over an 8-bit cache on the tensor cores: the same kernel with
+// converter warps that turn each staged 8-bit tile into fp16 operands.
+// group 4 or 8, at most kTcI8MaxSeqs sequences.  Launches decode and merge.
+constexpr int kTcI8MaxSeqs = 1024;
+cudaError_t launch_decode_tc_i8(const DecodeParams& p, int act_dtype, int group, int num_sms, cudaStream_t stream);
+
 // Paged decode over an 8-bit cache on CUDA cores: head_size 128, group 1/2/4/8;
 // q / out in act_dtype.  Launches the decode kernel and the merge.
 cudaError_t launch_decode_i8(const DecodeParams& p, int act_dtype, int group, cudaStream_t stream);

@@ -26,6 +26,18 @@ def _built(cuda_device):
     ensure_built()
 
 
+@pytest.fixture(params=["tc", "simt"])
+def kernel(request, monkeypatch):
+    """Which 8-bit decode runs: the default dispatch (tensor cores with converter
+    warps from 4 query heads per kv head, CUDA cores below) or the CUDA-core
+    kernel everywhere (PAGEDKV_DECODE_KERNEL=simt)."""
+    if request.param == "simt":
+        monkeypatch.setenv("PAGEDKV_DECODE_KERNEL", "simt")
+    else:
+        monkeypatch.delenv("PAGEDKV_DECODE_KERNEL", raising=False)
+    return request.param
+
+
 def i8_desc(nb, bs, hkv, dtype):
     return pkv.CacheDesc(nb, bs, hkv, 128, TORCH_DT[dtype], kv_int8=True)
 
@@ -141,7 +153,7 @@ class I8Case:
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("bs", [1, 4, 16, 32])
-def test_decode_matches_oracle(bs, G, dtype):
+def test_decode_matches_oracle(bs, G, dtype, kernel):
     rng = np.random.default_rng(520 + bs * 10 + G)
     ctx = [1, 2, 63, 64, 65, 511, 512, 513, 1100, 0, 300]
     case = I8Case(rng, len(ctx), 2 * G, 2, bs, ctx, dtype)
@@ -150,11 +162,11 @@ def test_decode_matches_oracle(bs, G, dtype):
     assert pkv.read_device_errors(err) == 0
     ref, e = case.expected()
     assert e == 0
-    assert_attention_close(out, ref, f"int8 decode bs={bs} G={G} {dtype}")
+    assert_attention_close(out, ref, f"int8 decode ({kernel}) bs={bs} G={G} {dtype}")
 
 
 @pytest.mark.parametrize("P", [128, 256, 1024])
-def test_decode_partition_sizes(P):
+def test_decode_partition_sizes(P, kernel):
     rng = np.random.default_rng(540 + P)
     ctx = [129, 3000, 1024, 1025, 7]
     case = I8Case(rng, len(ctx), 8, 2, 16, ctx, "bf16")
@@ -163,7 +175,7 @@ def test_decode_partition_sizes(P):
     assert_attention_close(case.run(P=P), ref, f"int8 decode P={P}")
 
 
-def test_decode_bad_block_id_zeroes_the_item():
+def test_decode_bad_block_id_zeroes_the_item(kernel):
     rng = np.random.default_rng(550)
     ctx = [40, 900, 200]
     case = I8Case(rng, 3, 4, 2, 16, ctx, "f16")

@@ -89,10 +89,16 @@ def measured_tensor_peak():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+# the sources the decode launch (tensor-core decode + log-sum-exp merge) is built from
+DECODE_SOURCES = ("common.cuh", "tc_common.cuh", "kernels.h", "decode_tc.cu", "decode_simt.cu")
+
+
 def source_digest() -> str:
+    """Digest of the decode kernels' sources: a recorded DRAM-traffic figure is used
+    only while it was taken on these exact sources."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_168_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in DECODE_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]

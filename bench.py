@@ -275,10 +275,38 @@ def oracle_sample(w, budget_s: float, max_items: int | None = None, start: int =
     return done_bytes / t_total / 1e9, done_seqs / t_total, desc, cores, t_total
 
 
+def run_reference_prefill(args):
+    """The fp64 oracle's prefill on the host cores, on windows of the prefill workload."""
+    from paged_kv_cache_168_gb300.workloads import make_prefill_workload
+    w = make_prefill_workload(args.workload, device="cpu")
+    cfg = w.cfg
+    per_step = max(1.0, args.reference_seconds / max(args.steps + args.warmup, 1))
+    for i in range(args.warmup):
+        prefill_oracle_sample(w, per_step / 4, start=100 + i)
+    vals, desc, cores = [], "", 1
+    for i in range(args.steps):
+        v, desc, cores = prefill_oracle_sample(w, per_step, start=i + 1)
+        vals.append(v)
+    value = float(np.median(vals))
+    line = {
+        "impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * per_step, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": PREFILL_DESCRIPTIONS[args.workload], "global_batch": cfg.num_seqs},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args):
     world, rank, local = dist_env()
     if rank != 0:
         return 0
+    if args.workload in PREFILL_DESCRIPTIONS:
+        return run_reference_prefill(args)
     from paged_kv_cache_168_gb300.workloads import make_workload
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     w = make_workload(args.workload, device=dev, num_seqs=args.seqs)

@@ -532,6 +532,8 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
     __syncwarp();
   } else if (warp < 6) {
     // =================================================================== softmax warps (2-5)
+    // (wait results are made warp-uniform in the softmax and output warps: the
+    // TMEM loads after them are warp-collective and must never run diverged)
     // Tile t: S^T -> tile maxima -> P^T (hi, lo) for the PV product; at the end
     // of an item, the normaliser.  Hands per-tile factors to the output warps.
     const int quarter = warp & 3;
@@ -547,19 +549,19 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
     bool ok = true;
     while (true) {
       const int slot = tile_seq % NS;
-      if (!mbar_wait(&sh.full[slot], (tile_seq / NS) & 1)) { ok = false; break; }
+      if (!__all_sync(kFull, mbar_wait(&sh.full[slot], (tile_seq / NS) & 1))) { ok = false; break; }
       const TileMeta mt = sh.meta[slot];
       const int hb = tile_seq & 1;
-      if (mt.s < 0 || sh.abort_flag) {
+      if (__any_sync(kFull, mt.s < 0 || sh.abort_flag)) {
         // tell the output warps there is no more work
-        if (tile_seq >= 2 && !mbar_wait(&sh.c_free[hb], ((tile_seq >> 1) - 1) & 1)) { ok = false; break; }
+        if (tile_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.c_free[hb], ((tile_seq >> 1) - 1) & 1))) { ok = false; break; }
         if (row == 0) sh.hand[hb].meta.s = -1;
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.c_full[hb]);
         break;
       }
       const int sb = tile_seq & 1;
-      if (!mbar_wait(&sh.s_full[sb], (tile_seq >> 1) & 1)) { ok = false; break; }
+      if (!__all_sync(kFull, mbar_wait(&sh.s_full[sb], (tile_seq >> 1) & 1))) { ok = false; break; }
       tc::fence_after_sync();
       float sv[16];
       tc::tmem_ld16(lane_addr + sb * 16, sv);
@@ -582,7 +584,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.max_bar[hb]);
-      if (!mbar_wait(&sh.max_bar[hb], (tile_seq >> 1) & 1)) { ok = false; break; }
+      if (!__all_sync(kFull, mbar_wait(&sh.max_bar[hb], (tile_seq >> 1) & 1))) { ok = false; break; }
 #pragma unroll
       for (int n = 0; n < G; ++n) {
         const float (*rm)[kN] = sh.red_max[hb];
@@ -606,7 +608,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
         pk[(HG + n2) >> 1] = Elem<OpT>::pack2(a - r.x, b - r.y);
       }
       // P^T buffer hb was last read by PV(t - 2): wait for it to complete
-      if (tile_seq >= 2 && !mbar_wait(&sh.o_full[hb], ((tile_seq - 2) >> 1) & 1)) { ok = false; break; }
+      if (tile_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.o_full[hb], ((tile_seq - 2) >> 1) & 1))) { ok = false; break; }
       // MN-major without swizzle: core matrix = 8 tokens x 8 columns (128 B);
       // column chunks 128 B apart, 8-token groups (NPV / 8) * 128 B apart
       uint8_t* prow = pbuf + hb * kPBytes + (row >> 3) * (NPV / 8) * 128 + (row & 7) * 16;
@@ -638,14 +640,14 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.sum_bar);
-        if (!mbar_wait(&sh.sum_bar, sum_uses & 1)) { ok = false; break; }
+        if (!__all_sync(kFull, mbar_wait(&sh.sum_bar, sum_uses & 1))) { ok = false; break; }
         ++sum_uses;
 #pragma unroll
         for (int n = 0; n < G; ++n)
           L[n] = sh.red_sum[0][n] + sh.red_sum[1][n] + sh.red_sum[2][n] + sh.red_sum[3][n];
       }
       // hand-off to the output warps
-      if (tile_seq >= 2 && !mbar_wait(&sh.c_free[hb], ((tile_seq >> 1) - 1) & 1)) { ok = false; break; }
+      if (tile_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.c_free[hb], ((tile_seq >> 1) - 1) & 1))) { ok = false; break; }
       if (row == 0) {
         sh.hand[hb].meta = mt;
 #pragma unroll
@@ -686,7 +688,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
     bool ok = true;
     while (true) {
       const int hb = tile_seq & 1;
-      if (!mbar_wait(&sh.c_full[hb], (tile_seq >> 1) & 1)) { ok = false; break; }
+      if (!__all_sync(kFull, mbar_wait(&sh.c_full[hb], (tile_seq >> 1) & 1))) { ok = false; break; }
       const TileMeta mt = sh.hand[hb].meta;
       if (mt.s < 0) break;
       float corr[G], m_fin[G], L[G];
@@ -698,7 +700,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.c_free[hb]);
-      if (!mbar_wait(&sh.o_full[hb], (tile_seq >> 1) & 1)) { ok = false; break; }
+      if (!__all_sync(kFull, mbar_wait(&sh.o_full[hb], (tile_seq >> 1) & 1))) { ok = false; break; }
       tc::fence_after_sync();
       float o[2][16];
       tc::tmem_ld16(lane_addr + 32 + hb * 32, o[0]);

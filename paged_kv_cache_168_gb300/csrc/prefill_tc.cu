@@ -11,9 +11,11 @@
 // One CTA per (query tile, kv head, sequence).  A tile is M = 128 rows: 128/G
 // consecutive query positions x the G query heads of the kv head (row =
 // position * G + head), so one pass over the KV serves all G heads.  Per
-// 128-token KV tile t:
-//     S_t = Q K_t^T        (M = 128 rows, N = 128 tokens, K = D)  -> TMEM (fp32)
-//     O  += P_t V_t        (M = 128 rows, N = D, K = 128 tokens)  -> TMEM (fp32)
+// 64-token KV tile t:
+//     S_t = Q K_t^T        (M = 128 rows, N = 64 tokens, K = D)   -> TMEM (fp32)
+//     O  += P_t V_t        (M = 128 rows, N = D, K = 64 tokens)   -> TMEM (fp32)
+// (64-token tiles keep a CTA at ~100 KB of shared memory and 256 TMEM columns,
+// so two CTAs share an SM and hide each other's softmax and set-up latency.)
 // Q (written once, 128B-swizzled K-major, shared memory) is the A operand of
 // S; the cache's 8-token groups staged by bulk copies are directly the K-major
 // B operand (K) and the MN-major B operand (V).  P is written by the softmax
@@ -29,11 +31,11 @@
 //   warp 0      bulk copies of each KV tile's (block, kv head) chunks into a
 //               2-stage ring (mbarrier transaction counts).
 //   warp 1      one lane issues S_{t+1} ahead of O += P_t V_t.
-// TMEM columns: S/P buffer 0 [0, 128), S/P buffer 1 [128, 256), O [256, 256 + D);
-// within a buffer P occupies p_hi [0, 64) and p_lo [64, 128) (tokens packed
-// two per column).
+// TMEM columns: S/P buffer 0 [0, 64), S/P buffer 1 [64, 128), O [128, 128 + D);
+// within a buffer P occupies p_hi [0, 32) and p_lo [32, 64) (tokens packed two
+// per column).
 //   warps 2-9   thread = TMEM lane = query row, in two warpgroups that own
-//               half of the tile's 128 columns (and half of O's columns)
+//               half of the tile's 64 columns (and half of O's columns)
 //               each: causal mask, online softmax in base 2 with the row
 //               maxima exchanged through shared memory.  The running max is
 //               raised only when a tile's max exceeds it by more than 8 (a
@@ -55,11 +57,11 @@ namespace pkv {
 namespace {
 
 constexpr int kRows = 128;                // MMA M: (position, head) rows of one query tile
-constexpr int kKv = 128;                  // tokens per KV tile
+constexpr int kKv = 64;                   // tokens per KV tile (two CTAs fit an SM)
 constexpr int kThreads = 320;             // producer, MMA, 8 softmax warps (two column halves)
 constexpr int kSoftmaxWarps = 8;
-constexpr uint32_t kTmemCols = 512;       // S0 [0,128) S1 [128,256) O [256, 256 + D)
-constexpr uint32_t kOCol = 256;
+constexpr uint32_t kTmemCols = 256;       // S0 [0,64) S1 [64,128) O [128, 128 + D): two CTAs per SM
+constexpr uint32_t kOCol = 2 * kKv;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr float kRescaleThreshold = 8.f;  // base-2 units
 
@@ -90,7 +92,7 @@ __device__ __forceinline__ uint32_t op_offset(int r, int piece) {
 }
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
   using C = Cfg<D>;
   constexpr int PT = kRows / G;                      // query positions per tile
   constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;

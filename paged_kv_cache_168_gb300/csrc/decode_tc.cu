@@ -35,6 +35,13 @@
 //   warps 6-9   output (thread = TMEM lane = head dim): fold O_hi + O_lo of
 //               each tile into registers with the online-softmax correction the
 //               softmax warps hand over, and write the item's result.
+// 8-bit caches (codes + one fp32 scale per token and kv head) change the
+// staging: warp 0 only plans (items, Q, block ids per tile into a descriptor
+// ring); one copy warp bulk-copies each tile's 8-bit chunks into two rings of
+// 64-token raw half tiles; converter warps turn the codes into exact fp16
+// operands -- K rows straight into TMEM (the A operand of QK is then read from
+// TMEM), V rows into a V-only stage in shared memory -- and pass the token
+// scales on; the softmax warps fold the scales into scores and weights.
 // Every wait is bounded; a timeout sets PA_DEVERR_TIMEOUT and ends the CTA.
 #include <math.h>
 
@@ -57,10 +64,23 @@ constexpr int kPBytes = kTile * 32 * 2;            // P^T operand: 128 tokens x 
 constexpr int kThreads = 320;                      // producer, MMA, 4 softmax warps, 4 output warps
 // 8-bit caches add converter warps: 8 when the registers allow it (group <= 4), else 4
 __host__ __device__ constexpr int converter_warps(int G) { return G <= 4 ? 8 : 4; }
-__host__ __device__ constexpr int threads_of(bool i8, int G) { return kThreads + (i8 ? 32 * converter_warps(G) : 0); }
+// 8-bit caches also add one copy warp (after the converters) that only issues
+// the bulk copies: a bulk copy instruction holds its warp for ~100 cycles per
+// active lane, so nothing else waits behind it.
+__host__ __device__ constexpr int threads_of(bool i8, int G) {
+  return kThreads + (i8 ? 32 * (converter_warps(G) + 1) : 0);
+}
+constexpr int kND = 4;                             // 8-bit: tile descriptors in flight (planner -> copy warp)
 constexpr int kRawBytes = 64 * (2 * kD + 32);      // one 64-token half tile of 8-bit chunks (bs 1: 288 B/token)
-constexpr int kRaw = 3;                            // raw half tiles in flight
-constexpr uint32_t kTmemCols = 128;                // S0 S1 (16 columns each) | O0 O1 (32 columns each)
+// TMEM columns: S0 S1 (16 each) | O0 O1 (32 each); 8-bit caches add the fp16 K
+// operand of each stage (128 tokens x 128 dims, two per column: 64 columns).
+constexpr uint32_t kKCol = 128;
+__host__ __device__ constexpr uint32_t tmem_cols(bool i8, int ns) {
+  return !i8 ? 128u : (kKCol + 64u * ns <= 256u ? 256u : 512u);
+}
+// A stage holds the tile's K and V operands (16-bit caches) or, for 8-bit
+// caches, only the converted V operand (K lives in TMEM).
+__host__ __device__ constexpr int stage_bytes(bool i8) { return i8 ? kTile * kD * 2 : kTileBytes; }
 constexpr uint32_t kFull = 0xffffffffu;
 
 struct TileMeta {
@@ -69,7 +89,7 @@ struct TileMeta {
   float qinv;                    // 8-bit caches with bf16 q: 2^-e undoing the exact prescale of Q to fp16
 };
 
-template <int NS, bool I8>
+template <int NS, bool I8, int NRH>
 struct Shared {
   uint64_t full[NS], empty[NS];
   uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2], q_free[2];
@@ -87,8 +107,15 @@ struct Shared {
   volatile int abort_flag;
   // 8-bit caches: producer -> converter ring of raw half tiles, and the token
   // scales of each converted stage
-  uint64_t raw_full[I8 ? kRaw : 1], raw_empty[I8 ? kRaw : 1];
-  TileMeta raw_meta[I8 ? kRaw : 1];
+  // (two rings of NRH slots, one per 64-token half: slot h * NRH + k % NRH)
+  uint64_t raw_full[I8 ? 2 * NRH : 1], raw_empty[I8 ? 2 * NRH : 1];
+  TileMeta raw_meta[I8 ? 2 * NRH : 1];
+  // planner -> copy warp: per tile its metadata and block ids
+  struct TileDesc {
+    TileMeta meta;
+    int ids[I8 ? kTile : 1];
+  } desc[I8 ? kND : 1];
+  uint64_t desc_full[I8 ? kND : 1], desc_empty[I8 ? kND : 1];
   float sk[I8 ? NS : 1][I8 ? kTile : 1];
   float sv[I8 ? NS : 1][I8 ? kTile : 1];
 };
@@ -135,21 +162,23 @@ __device__ void warp_zero_rows(const DecodeParams& p, int s, int kvh, int lane) 
   for (int i = lane * 8; i < G * kD; i += 32 * 8) *reinterpret_cast<uint4*>(out + i) = make_uint4(0, 0, 0, 0);
 }
 
-template <typename T, int G, int NS, bool I8>
+template <typename T, int G, int NS, bool I8, int NRH>
 __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
   // P^T holds p_hi for the G heads in columns [0, HG) and p_lo in [HG, 2 HG):
   // one PV product (N = 2 HG) yields both halves of O^T.
   constexpr int HG = G < 8 ? 8 : G;
   constexpr int NPV = 2 * HG;
-  __shared__ Shared<NS, I8> sh;
+  __shared__ Shared<NS, I8, NRH> sh;
+  constexpr int kStage = stage_bytes(I8);
+  constexpr uint32_t kCols = tmem_cols(I8, NS);
   extern __shared__ __align__(1024) uint8_t dyn_raw[];
   const uint32_t raw_s = smem_u32(dyn_raw);
   uint8_t* dyn = dyn_raw + (((raw_s + 1023u) & ~1023u) - raw_s);   // 1024-aligned in the shared window
   uint8_t* stages = dyn;
-  uint8_t* qbuf = dyn + NS * kTileBytes;
+  uint8_t* qbuf = dyn + NS * kStage;
   uint8_t* pbuf = qbuf + 2 * kQBytes;
   uint8_t* raw = pbuf + 2 * kPBytes;                         // pbuf: 2 buffers of [p_hi | p_lo]
-  int* pre = reinterpret_cast<int*>(raw + (I8 ? kRaw * kRawBytes : 0));
+  int* pre = reinterpret_cast<int*>(raw + (I8 ? 2 * NRH * kRawBytes : 0));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.num_seqs, Hkv = p.num_kv_heads, bs = p.block_size;
@@ -169,9 +198,13 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       mbar_init(&sh.empty[i], 1);
     }
     if (I8) {
-      for (int i = 0; i < kRaw; ++i) {
+      for (int i = 0; i < 2 * NRH; ++i) {
         mbar_init(&sh.raw_full[i], 1);
-        mbar_init(&sh.raw_empty[i], 4);
+        mbar_init(&sh.raw_empty[i], NCW / 2);   // the converter warps of the half's TMEM lane quarters
+      }
+      for (int i = 0; i < kND; ++i) {
+        mbar_init(&sh.desc_full[i], 1);
+        mbar_init(&sh.desc_empty[i], 1);
       }
     }
     for (int i = 0; i < 2; ++i) {
@@ -192,7 +225,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
   for (int i = threadIdx.x; i < 2 * kQBytes / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
   if (warp == 1) {
-    tc::tmem_alloc(&sh.tmem_base, kTmemCols);
+    tc::tmem_alloc(&sh.tmem_base, kCols);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
@@ -239,9 +272,15 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       r.s = lo;
       r.part = j - pre[lo];
       r.ctx = p.context_lens[r.s];
-      // first logical block of the partition (a window makes it depend on ctx)
-      const int jb = ((windowed ? attended_from(p, r.ctx) : 0) + r.part * P) / bs;
-      const int ti = table_index(jb + lane, p.ring_blocks);
+      // first logical block of the partition: only a window makes it depend on
+      // ctx, so without one the block-id load below does not wait for ctx
+      int ti;
+      if (windowed) {
+        const int jb = (attended_from(p, r.ctx) + r.part * P) / bs;
+        ti = table_index(jb + lane, p.ring_blocks);
+      } else {
+        ti = r.part * (P / bs) + lane;   // P is a multiple of 128, bs divides it
+      }
       r.id_lane = (lane < P / bs && ti < p.bt_stride && ti >= 0) ? p.block_tables[(int64_t)r.s * p.bt_stride + ti] : 0;
       const T* qsrc = static_cast<const T*>(p.q) + (int64_t)r.s * p.q_seq_stride + (int64_t)r.kvh * G * kD;
 #pragma unroll
@@ -350,7 +389,8 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       // ---- stream the tiles
       const int ntiles = (t1 - t0 + kTile - 1) / kTile;
       for (int k = 0; k < ntiles && I8; ++k) {
-        // 8-bit: each tile goes to the converter warps as two 64-token half tiles
+        // 8-bit: each tile goes to the copy warp as a descriptor (metadata and
+        // block ids); it stages the tile as two 64-token half tiles
         const int valid = min(kTile, t1 - (t0 + k * kTile));
         TileMeta m;
         m.s = s; m.kvh = kvh; m.part = part; m.valid = valid;
@@ -368,28 +408,18 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
           const int id_sh = __shfl_sync(kFull, id_lane, bi & 31);
           idr[c] = b < nbt ? (bi < 32 ? id_sh : row[table_index(jb + bi, p.ring_blocks)]) : 0;
         }
-        for (int h = 0; h < 2 && !aborted; ++h) {
-          const int q = 2 * tile_seq + h, r = q % kRaw;
-          if (q >= kRaw && !mbar_wait(&sh.raw_empty[r], ((q / kRaw) - 1) & 1)) {
-            aborted = true;
-            break;
-          }
-          const int hv = min(64, valid - 64 * h);
-          const int nbh = hv > 0 ? (hv + bs - 1) / bs : 0;
-          if (lane == 0) {
-            sh.raw_meta[r] = m;
-            mbar_arrive_expect_tx(&sh.raw_full[r], (uint32_t)(nbh * chunk_bytes));
-          }
-          __syncwarp();
-          const int hb0 = h * (64 / bs);                 // first block of the half, within the tile
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int b = lane + 32 * c - hb0;             // this lane's block c, within the half
-            if (b >= 0 && b < nbh)
-              bulk_g2s(raw + r * kRawBytes + b * chunk_bytes, p.cache + ((int64_t)idr[c] * Hkv + kvh) * chunk_bytes,
-                       (uint32_t)chunk_bytes, &sh.raw_full[r]);
-          }
+        // hand the tile to the copy warp
+        const int d = tile_seq % kND;
+        if (tile_seq >= kND && !mbar_wait(&sh.desc_empty[d], ((tile_seq / kND) - 1) & 1)) {
+          aborted = true;
+          break;
         }
+        if (lane == 0) sh.desc[d].meta = m;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (lane + 32 * c < nbt) sh.desc[d].ids[lane + 32 * c] = idr[c];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.desc_full[d]);
         if (aborted) break;
         ++tile_seq;
       }
@@ -415,7 +445,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
         const int id_sh = __shfl_sync(kFull, id_lane, bi & 31);
         if (lane < nb) {
           const int id = bi < 32 ? id_sh : row[table_index(jb + bi, p.ring_blocks)];
-          bulk_g2s(stages + slot * kTileBytes + lane * chunk_bytes,
+          bulk_g2s(stages + slot * kStage + lane * chunk_bytes,
                    p.cache + ((int64_t)id * Hkv + kvh) * chunk_bytes, (uint32_t)chunk_bytes, &sh.full[slot]);
         }
         ++tile_seq;
@@ -424,25 +454,16 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
     }
     // ---- no more work: a stage (8-bit: a raw half tile) whose metadata says so
     if (I8) {
-      // the "no more work" mark goes into both half slots of the next tile (each
-      // converter thread watches its own half's slot)
-      for (int h = 0; h < 2; ++h) {
-        const int q = 2 * tile_seq + h, r = q % kRaw;
-        if (!aborted && q >= kRaw && !mbar_wait(&sh.raw_empty[r], ((q / kRaw) - 1) & 1)) aborted = true;
-        if (aborted && lane == 0 && h == 0) {
-          // never leave copies in flight: wait (bounded) for the latest phase of every raw slot
-          const int issued = 2 * tile_seq;
-          for (int t = max(0, issued - kRaw); t < issued; ++t) mbar_wait(&sh.raw_full[t % kRaw], (t / kRaw) & 1);
+      // a descriptor that says so; the copy warp passes it on to both halves
+      const int d = tile_seq % kND;
+      if (!aborted && tile_seq >= kND && !mbar_wait(&sh.desc_empty[d], ((tile_seq / kND) - 1) & 1)) aborted = true;
+      if (lane == 0) {
+        if (aborted) {
+          report(p.dev_err, PA_DEVERR_TIMEOUT);
+          sh.abort_flag = 1;
         }
-        if (lane == 0) {
-          if (aborted && h == 0) {
-            report(p.dev_err, PA_DEVERR_TIMEOUT);
-            sh.abort_flag = 1;
-          }
-          sh.raw_meta[r].s = -1;
-          mbar_arrive(&sh.raw_full[r]);
-        }
-        __syncwarp();
+        sh.desc[d].meta.s = -1;
+        mbar_arrive(&sh.desc_full[d]);
       }
     } else {
       const int slot = tile_seq % NS;
@@ -465,7 +486,8 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
     // =================================================================== MMA issuer
     // Event-driven: QK(t) as soon as tile t has landed and its S buffer is free,
     // PV(t) as soon as P(t) is written and its O buffer is free -- neither waits
-    // for the other stream, so a stage is released right after its own PV.
+    // for the other stream, so a stage is released right after its own PV.  The
+    // barriers are tested without blocking, so one stream never sleeps on the other.
     if (lane == 0) {
       const uint32_t id_qk = tc::idesc_f16(128, kN, kBF16, false, false);
       const uint32_t id_pv = tc::idesc_f16(128, NPV, kBF16, true, true);
@@ -476,20 +498,24 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
         bool progressed = false;
         if (qk < end) {
           const int slot = qk % NS;
-          if (mbar_try_wait(&sh.full[slot], (qk / NS) & 1)) {
+          if (mbar_test_wait(&sh.full[slot], (qk / NS) & 1)) {
             const TileMeta m = sh.meta[slot];
             if (m.s < 0) {
               end = qk;
               progressed = true;
-            } else if (qk < 2 || mbar_try_wait(&sh.s_free[qk & 1], ((qk >> 1) - 1) & 1)) {
+            } else if (qk < 2 || mbar_test_wait(&sh.s_free[qk & 1], ((qk >> 1) - 1) & 1)) {
               tc::fence_after_sync();
-              const uint32_t st = smem_u32(stages + slot * kTileBytes), qa = smem_u32(qbuf + m.qslot * kQBytes);
+              const uint32_t st = smem_u32(stages + slot * kStage), qa = smem_u32(qbuf + m.qslot * kQBytes);
 #pragma unroll
-              for (int kk = 0; kk < kD / 16; ++kk)
-                tc::mma_f16(tmem + (qk & 1) * 16,
-                            tc::smem_desc(st + (kk >> 2) * 1024 + (kk & 3) * 32, 16, kGroupBytes, tc::kSwizzle128B),
-                            tc::smem_desc(qa + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B), id_qk,
-                            kk > 0);
+              for (int kk = 0; kk < kD / 16; ++kk) {
+                const uint64_t qd = tc::smem_desc(qa + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
+                if constexpr (I8)   // K (fp16, token = TMEM lane) converted into TMEM: 16 dims = 8 columns
+                  tc::mma_f16_ta(tmem + (qk & 1) * 16, tmem + kKCol + slot * 64 + kk * 8, qd, id_qk, kk > 0);
+                else
+                  tc::mma_f16(tmem + (qk & 1) * 16,
+                              tc::smem_desc(st + (kk >> 2) * 1024 + (kk & 3) * 32, 16, kGroupBytes, tc::kSwizzle128B),
+                              qd, id_qk, kk > 0);
+              }
               tc::commit(&sh.s_full[qk & 1]);
               if (m.last) tc::commit(&sh.q_free[m.qslot]);
               ++qk;
@@ -499,16 +525,19 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
         }
         if (pv < qk) {
           const int pb = pv & 1;
-          if (mbar_try_wait(&sh.p_full[pb], (pv >> 1) & 1) &&
-              (pv < 2 || mbar_try_wait(&sh.o_free[pb], ((pv >> 1) - 1) & 1))) {
+          if (mbar_test_wait(&sh.p_full[pb], (pv >> 1) & 1) &&
+              (pv < 2 || mbar_test_wait(&sh.o_free[pb], ((pv >> 1) - 1) & 1))) {
             tc::fence_after_sync();
             const int slot = pv % NS;
             const int valid = sh.meta[slot].valid;   // the stage is not refilled before this PV completes
-            const uint32_t st = smem_u32(stages + slot * kTileBytes), pa = smem_u32(pbuf + pb * kPBytes);
+            const uint32_t st = smem_u32(stages + slot * kStage), pa = smem_u32(pbuf + pb * kPBytes);
             const int nsteps = (valid + 15) >> 4;
+            // V of 8-token group g: at g * 4 KiB + 2 KiB among the K atoms (16-bit
+            // caches), at g * 2 KiB in a V-only stage (8-bit caches)
+            constexpr uint32_t kVGroup = I8 ? 2048 : kGroupBytes, kVOff = I8 ? 0 : 2048;
             for (int kk = 0; kk < nsteps; ++kk)
               tc::mma_f16(tmem + 32 + pb * 32,
-                          tc::smem_desc(st + kk * 8192 + 2048, 1024, kGroupBytes, tc::kSwizzle128B),
+                          tc::smem_desc(st + kk * 2 * kVGroup + kVOff, 1024, kVGroup, tc::kSwizzle128B),
                           tc::smem_desc(pa + kk * (NPV / 8) * 256, (NPV / 8) * 128, 128, tc::kSwizzleNone), id_pv,
                           kk > 0);
             tc::commit(&sh.o_full[pb]);
@@ -617,8 +646,9 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
         *reinterpret_cast<uint4*>(prow + c * 128) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       // V rows of tokens past the context inside the last 16-token MMA step
       // must not hold NaN/Inf (0 * NaN = NaN): zero them.
-      if (!rv && row < ((mt.valid + 15) & ~15)) {
-        uint8_t* vrow = stages + slot * kTileBytes + (row >> 3) * kGroupBytes + 2048 + (row & 7) * 128;
+      // (8-bit caches: the converter warps write zero rows there.)
+      if (!I8 && !rv && row < ((mt.valid + 15) & ~15)) {
+        uint8_t* vrow = stages + slot * kStage + (row >> 3) * kGroupBytes + 2048 + (row & 7) * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
@@ -739,90 +769,163 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       report(p.dev_err, PA_DEVERR_TIMEOUT);
       sh.abort_flag = 1;
     }
-  } else if (I8) {
+  } else if (I8 && warp < kThreads / 32 + NCW) {
     // =================================================================== converter warps (8-bit)
-    // Half tile h (64 tokens) of tile t: for each token one thread turns its K
-    // code row and another its V code row into the 16-bit operand rows of the
-    // stage (the 16-bit cache layout: 8-token groups of K then V atoms, pieces
-    // swizzled by the row's index in its group) and copies the token's scale.
-    // Rows past the tile's last token become zeros (scale 0).  With 8 warps
-    // the two halves are converted side by side (threads 128-255 take half 1);
-    // with 4 warps each thread converts its row of both halves in turn.
-    constexpr int kHalvesPerThread = NCW == 8 ? 1 : 2;
-    const int ct = threadIdx.x - kThreads;                 // 0 .. 32 NCW - 1
-    const int part = (ct >> 6) & 1, u = ct & 63;
-    const int h_first = NCW == 8 ? (ct >> 7) : 0;
+    // A warp may access TMEM lanes 32 (warp % 4) .. + 31, so thread `lane` owns
+    // token row t = 32 (warp % 4) + lane of every tile (in half tile t / 64).
+    // With 8 warps the two warps of a lane quarter split the 128 dims into
+    // halves; with 4, one warp converts all of them.  For its row a thread turns
+    // the K codes into fp16 pairs stored to TMEM (row t = lane t: the A operand
+    // of S^T = K Q^T), the V codes into the stage's V atoms (swizzled 128-byte
+    // rows: the MN-major A operand of O^T = V^T P^T), and copies the token's
+    // scales.  Rows past the tile's last token become zeros (scale 0).
+    constexpr int kSplit = NCW == 8 ? 2 : 1;
+    constexpr int kPc = 8 / kSplit;                       // 16-code pieces per row and thread
+    const int quarter = warp & 3;
+    const int t = quarter * 32 + lane, h = t >> 6, u = t & 63;
+    const int dh = kSplit == 2 ? ((warp - kThreads / 32) >> 2) : 0;
+    const uint32_t k_lane = tmem + ((uint32_t)(quarter * 32) << 16) + kKCol + dh * (kPc * 8);
     const I8Layout L8{bs, Hkv};
     const int64_t sbytes = L8.scale_bytes();
     int tile_seq = 0;
     bool ok = true;
-    while (ok) {
+    while (true) {
       const int slot = tile_seq % NS;
-      TileMeta mt;
-      mt.s = -1;
-      for (int hh = 0; hh < kHalvesPerThread; ++hh) {
-        const int h = h_first + hh;
-        const int q = 2 * tile_seq + h, r = q % kRaw;
-        if (!mbar_wait(&sh.raw_full[r], (q / kRaw) & 1)) {
-          ok = false;
-          break;
-        }
-        mt = sh.raw_meta[r];
-        if (mt.s < 0 || sh.abort_flag) break;               // no more work
-        if (hh == 0 && tile_seq >= NS && !mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        const int t = 64 * h + u;                           // token row in the tile
-        uint8_t* dst = stages + slot * kTileBytes + (t >> 3) * kGroupBytes + part * 2048 + (t & 7) * 128;
-        float scale = 0.f;
+      const int r = h * NRH + tile_seq % NRH;
+      if (!__all_sync(kFull, mbar_wait(&sh.raw_full[r], (tile_seq / NRH) & 1))) { ok = false; break; }
+      const TileMeta mt = sh.raw_meta[r];
+      const bool end = mt.s < 0;                             // "no more work"
+      if (__any_sync(kFull, !end && sh.abort_flag)) { ok = false; break; }
+      // the stage and its TMEM K operand were last read by PV(t - NS)
+      if (tile_seq >= NS && !__all_sync(kFull, mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      if (!end) {
+        uint4 kin[kPc], vin[kPc];
+        float skv = 0.f, svv = 0.f;
+#pragma unroll
+        for (int j = 0; j < kPc; ++j) kin[j] = vin[j] = make_uint4(0, 0, 0, 0);   // zero codes -> +0
         if (t < mt.valid) {
           const int b = u / bs, tb = u - b * bs;
           const uint8_t* chunk = raw + r * kRawBytes + b * chunk_bytes;
-          const uint8_t* src = chunk + (int64_t)(part * bs + tb) * kD;
-          scale = *reinterpret_cast<const float*>(chunk + 2LL * bs * kD + part * sbytes + 4 * tb);
-          uint4 in[8];
+          const uint8_t* ks = chunk + (int64_t)tb * kD;
+          const uint8_t* vs = chunk + (int64_t)(bs + tb) * kD;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) in[j] = *reinterpret_cast<const uint4*>(src + ((j ^ (tb & 7)) << 4));
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint32_t o[8];
-            codes_to_16bit<__half>(in[j], o);
-            uint8_t* atom = dst + (j >> 2) * 1024;
-            const int p0 = (2 * j) & 7;
-            *reinterpret_cast<uint4*>(atom + ((p0 ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(atom + (((p0 + 1) ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          for (int j = 0; j < kPc; ++j) {
+            const int off = ((dh * kPc + j) ^ (tb & 7)) << 4;
+            kin[j] = *reinterpret_cast<const uint4*>(ks + off);
+            vin[j] = *reinterpret_cast<const uint4*>(vs + off);
           }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            *reinterpret_cast<uint4*>(dst + c * 16) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(dst + 1024 + c * 16) = make_uint4(0, 0, 0, 0);
-          }
+          skv = *reinterpret_cast<const float*>(chunk + 2LL * bs * kD + 4 * tb);
+          svv = *reinterpret_cast<const float*>(chunk + 2LL * bs * kD + sbytes + 4 * tb);
         }
-        (part == 0 ? sh.sk : sh.sv)[slot][t] = scale;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.raw_empty[r]);
+        // V -> the stage's V atoms (8-token group t / 8 at 2 KiB per group)
+        uint8_t* vrow = stages + slot * kStage + (t >> 3) * 2048 + (t & 7) * 128;
+#pragma unroll
+        for (int j = 0; j < kPc; ++j) {
+          uint32_t o[8];
+          codes_to_16bit<__half>(vin[j], o);
+          const int pg = dh * kPc + j;                       // 16 dims: two 16-byte pieces of atom pg / 4
+          uint8_t* atom = vrow + (pg >> 2) * 1024;
+          const int p0 = (2 * pg) & 7;
+          *reinterpret_cast<uint4*>(atom + ((p0 ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(atom + (((p0 + 1) ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        // K -> TMEM, 32 columns (64 dims) per store
+#pragma unroll
+        for (int g = 0; g < kPc / 4; ++g) {
+          uint32_t kr[32];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t o[8];
+            codes_to_16bit<__half>(kin[4 * g + j], o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) kr[8 * j + e] = o[e];
+          }
+          tc::tmem_st32u(k_lane + slot * 64 + g * 32, kr);
+        }
+        if (dh == 0) sh.sk[slot][t] = skv;
+        if (dh == kSplit - 1) sh.sv[slot][t] = svv;
+        tc::tmem_wait_st();
       }
-      if (!ok) break;
-      if (mt.s >= 0 && sh.abort_flag) {
-        ok = false;
-        break;
-      }
-      if (mt.s < 0 && tile_seq >= NS && !mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1)) {
-        ok = false;
-        break;
-      }
-      if (ct == 0) sh.meta[slot] = mt;                    // a real tile, or "no more work"
+      if (warp == kThreads / 32 && lane == 0) sh.meta[slot] = mt;   // a real tile, or "no more work"
+      tc::fence_before_sync();
       tc::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.full[slot]);
-      if (mt.s < 0) break;
+      if (lane == 0) {
+        mbar_arrive(&sh.raw_empty[r]);
+        mbar_arrive(&sh.full[slot]);
+      }
+      if (end) break;
       ++tile_seq;
     }
     if (!ok && lane == 0) {
       report(p.dev_err, PA_DEVERR_TIMEOUT);
       sh.abort_flag = 1;
+    }
+  } else if (I8) {
+    // =================================================================== copy warp (8-bit)
+    // Tile t: wait for its descriptor and for both halves' raw slots, then one
+    // instruction issues the bulk copies of all its (block, kv head) chunks
+    // (lanes i + 32 c; blocks past the first half go to the half-1 slot).
+    const int bph = 64 / bs;                      // blocks per half tile
+    int tile = 0;
+    bool ok = true;
+    while (true) {
+      const int d = tile % kND;
+      if (!__all_sync(kFull, mbar_wait(&sh.desc_full[d], (tile / kND) & 1))) { ok = false; break; }
+      TileMeta m = sh.desc[d].meta;
+      const int r0 = tile % NRH, r1 = NRH + r0;
+      if (tile >= NRH && !__all_sync(kFull, mbar_wait(&sh.raw_empty[r0], ((tile / NRH) - 1) & 1) &&
+                                                mbar_wait(&sh.raw_empty[r1], ((tile / NRH) - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      if (__any_sync(kFull, sh.abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (m.s < 0) {
+        // no more work: the mark goes into both halves' slots (each converter
+        // warp watches its own half's ring)
+        if (lane == 0) {
+          sh.raw_meta[r0] = m;
+          sh.raw_meta[r1] = m;
+          mbar_arrive(&sh.raw_full[r0]);
+          mbar_arrive(&sh.raw_full[r1]);
+        }
+        break;
+      }
+      const int nbt = (m.valid + bs - 1) / bs;
+      const int nb0 = min(nbt, bph);
+      if (lane == 0) {
+        sh.raw_meta[r0] = m;
+        sh.raw_meta[r1] = m;
+        mbar_arrive_expect_tx(&sh.raw_full[r0], (uint32_t)(nb0 * chunk_bytes));
+        mbar_arrive_expect_tx(&sh.raw_full[r1], (uint32_t)((nbt - nb0) * chunk_bytes));
+      }
+      __syncwarp();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int b = lane + 32 * c;
+        if (b < nbt) {
+          const int h = b >= bph, r = h ? r1 : r0;
+          bulk_g2s(raw + r * kRawBytes + (b - h * bph) * chunk_bytes,
+                   p.cache + ((int64_t)sh.desc[d].ids[b] * Hkv + m.kvh) * chunk_bytes, (uint32_t)chunk_bytes,
+                   &sh.raw_full[r]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.desc_empty[d]);
+      ++tile;
+    }
+    if (!ok && lane == 0) {
+      // never leave copies in flight: wait (bounded) for the latest phase of every raw slot
+      for (int h = 0; h < 2; ++h)
+        for (int t = max(0, tile - NRH); t < tile; ++t) mbar_wait(&sh.raw_full[h * NRH + t % NRH], (t / NRH) & 1);
+      report(p.dev_err, PA_DEVERR_TIMEOUT);
+      sh.abort_flag = 1;   // the other roles see it and leave their (bounded) loops
     }
   }
 
@@ -831,38 +934,38 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, kTmemCols);
+    tc::tmem_dealloc(tmem, kCols);
   }
 }
 
-template <typename T, int G, int NS, bool I8>
+template <typename T, int G, int NS, bool I8, int NRH>
 cudaError_t launch_typed(const DecodeParams& p, int num_sms, cudaStream_t stream) {
-  const size_t smem = 1024 + (size_t)NS * kTileBytes + 2 * kQBytes + 2 * kPBytes + (I8 ? (size_t)kRaw * kRawBytes : 0) +
-                      (size_t)(p.num_seqs + 1) * 4;
-  auto kern = decode_tc_kernel<T, G, NS, I8>;
-  cudaError_t e = set_smem_attribute_once<decode_tc_kernel<T, G, NS, I8>>(smem);
+  const size_t smem = 1024 + (size_t)NS * stage_bytes(I8) + 2 * kQBytes + 2 * kPBytes +
+                      (I8 ? (size_t)2 * NRH * kRawBytes : 0) + (size_t)(p.num_seqs + 1) * 4;
+  auto kern = decode_tc_kernel<T, G, NS, I8, NRH>;
+  cudaError_t e = set_smem_attribute_once<decode_tc_kernel<T, G, NS, I8, NRH>>(smem);
   if (e != cudaSuccess) return e;
   kern<<<num_sms, threads_of(I8, G), smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <typename T, int NS, bool I8>
+template <typename T, int NS, bool I8, int NRH>
 cudaError_t launch_group(const DecodeParams& p, int group, int num_sms, cudaStream_t stream) {
   switch (group) {
-    case 1:
-      if constexpr (I8) return cudaErrorInvalidValue;   // 8-bit caches use the CUDA-core kernel below 4
-      else return launch_typed<T, 1, NS, false>(p, num_sms, stream);
-    case 2:
-      if constexpr (I8) return cudaErrorInvalidValue;
-      else return launch_typed<T, 2, NS, false>(p, num_sms, stream);
-    case 4: return launch_typed<T, 4, NS, I8>(p, num_sms, stream);
-    case 8: return launch_typed<T, 8, NS, I8>(p, num_sms, stream);
+    case 1: return launch_typed<T, 1, NS, I8, NRH>(p, num_sms, stream);
+    case 2: return launch_typed<T, 2, NS, I8, NRH>(p, num_sms, stream);
+    case 4: return launch_typed<T, 4, NS, I8, NRH>(p, num_sms, stream);
+    case 8: return launch_typed<T, 8, NS, I8, NRH>(p, num_sms, stream);
     case 16:
       if constexpr (I8) return cudaErrorInvalidValue;   // 8-bit caches serve groups up to 8
-      else return launch_typed<T, 16, NS, false>(p, num_sms, stream);
+      else return launch_typed<T, 16, NS, false, 1>(p, num_sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }
+
+// 8-bit caches: 3 converted stages (V in shared memory, K in TMEM) and 2 raw
+// 64-token half tiles of 8-bit chunks per half in flight (~74 KB)
+constexpr int kI8Stages = 3, kI8Raw = 2;
 
 }  // namespace
 
@@ -871,11 +974,11 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, int group, int nu
   const bool three = p.num_seqs <= 1024;   // shared memory: 3 stages + prefix of <= 1025 ints
   cudaError_t e;
   if (dtype == PA_F16)
-    e = three ? launch_group<__half, 3, false>(p, group, num_sms, stream)
-              : launch_group<__half, 2, false>(p, group, num_sms, stream);
+    e = three ? launch_group<__half, 3, false, 1>(p, group, num_sms, stream)
+              : launch_group<__half, 2, false, 1>(p, group, num_sms, stream);
   else if (dtype == PA_BF16)
-    e = three ? launch_group<__nv_bfloat16, 3, false>(p, group, num_sms, stream)
-              : launch_group<__nv_bfloat16, 2, false>(p, group, num_sms, stream);
+    e = three ? launch_group<__nv_bfloat16, 3, false, 1>(p, group, num_sms, stream)
+              : launch_group<__nv_bfloat16, 2, false, 1>(p, group, num_sms, stream);
   else
     return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
@@ -883,12 +986,12 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, int group, int nu
 }
 
 cudaError_t launch_decode_tc_i8(const DecodeParams& p, int act_dtype, int group, int num_sms, cudaStream_t stream) {
-  if (p.num_seqs > kTcI8MaxSeqs || group < 4 || group > 8) return cudaErrorInvalidValue;
+  if (p.num_seqs > kTcI8MaxSeqs || group < 1 || group > 8) return cudaErrorInvalidValue;
   cudaError_t e;
   if (act_dtype == PA_F16)
-    e = launch_group<__half, 2, true>(p, group, num_sms, stream);
+    e = launch_group<__half, kI8Stages, true, kI8Raw>(p, group, num_sms, stream);
   else if (act_dtype == PA_BF16)
-    e = launch_group<__nv_bfloat16, 2, true>(p, group, num_sms, stream);
+    e = launch_group<__nv_bfloat16, kI8Stages, true, kI8Raw>(p, group, num_sms, stream);
   else
     return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;

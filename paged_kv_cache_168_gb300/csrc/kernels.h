@@ -120,7 +120,7 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, int head_size, 
 
 // Paged decode over an 8-bit cache on the tensor cores: the same kernel with
 // converter warps that turn each staged 8-bit tile into fp16 operands.
-// group 4 or 8, at most kTcI8MaxSeqs sequences.  Launches decode and merge.
+// group 1, 2, 4 or 8, at most kTcI8MaxSeqs sequences.  Launches decode and merge.
 constexpr int kTcI8MaxSeqs = 1024;
 cudaError_t launch_decode_tc_i8(const DecodeParams& p, int act_dtype, int group, int num_sms, cudaStream_t stream);
 

@@ -288,10 +288,10 @@ pa_status pa_decode_window(void* out, const void* q, int64_t q_seq_stride, const
   p.dev_err = dev_err;
   cudaError_t e;
   if (is_i8(desc)) {
-    // the tensor-core kernel wins from 4 query heads per kv head on (its converter
-    // warps cost the same per token whatever the group; the CUDA-core kernel's
-    // work grows with it); below that the CUDA-core kernel is faster
-    if (group >= 4 && use_tensor_cores(desc->head_size, 8, group, num_seqs) && num_seqs <= pkv::kTcI8MaxSeqs) {
+    // tensor cores for every group (block sizes below 8 included: the converter
+    // warps repack any block size into whole 8-token atoms); the CUDA-core
+    // kernel serves more than kTcI8MaxSeqs sequences
+    if (use_tensor_cores(desc->head_size, 8, group, num_seqs) && num_seqs <= pkv::kTcI8MaxSeqs) {
       int dev = 0, sms = 0;
       e = cudaGetDevice(&dev);
       if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -162,6 +162,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
+// The same, polling with test_wait (never suspends): for a single-lane issuer
+// that must react as soon as the phase completes.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i)
+    if (mbar_test_wait(bar, parity)) return true;
+  return false;
+}
+
 // 1-D bulk copy global -> shared, completing `bytes` transactions on `bar`.
 // dst and src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

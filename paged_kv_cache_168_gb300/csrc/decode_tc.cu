@@ -67,8 +67,18 @@ __host__ __device__ constexpr int converter_warps(int G) { return G <= 4 ? 8 : 4
 // 8-bit caches also add one copy warp (after the converters) that only issues
 // the bulk copies: a bulk copy instruction holds its warp for ~100 cycles per
 // active lane, so nothing else waits behind it.
+// Two softmax warpgroups take alternate tiles (warps 2-5 the even ones, four
+// warps after all other roles the odd ones), so one tile's softmax overlaps the
+// next -- except for 16 heads per kv head (the output warps would hold 6 x 16
+// accumulators) and 8-bit caches with 8 heads (their registers are spent).
+__host__ __device__ constexpr bool ping_pong(bool i8, int G) { return !i8 && G < 16; }
+// 16-bit caches issue QK and PV from two warps (one lane each); 8-bit caches,
+// whose tiles are paced by the converter warps, keep one event-driven issuer
+// (measured faster there).
+__host__ __device__ constexpr bool split_issue(bool i8) { return !i8; }
 __host__ __device__ constexpr int threads_of(bool i8, int G) {
-  return kThreads + (i8 ? 32 * (converter_warps(G) + 1) : 0);
+  return kThreads + (i8 ? 32 * (converter_warps(G) + 1) : 0) + (ping_pong(i8, G) ? 128 : 0) +
+         (split_issue(i8) ? 32 : 0);
 }
 constexpr int kND = 4;                             // 8-bit: tile descriptors in flight (planner -> copy warp)
 constexpr int kRawBytes = 64 * (2 * kD + 32);      // one 64-token half tile of 8-bit chunks (bs 1: 288 B/token)
@@ -86,6 +96,7 @@ constexpr uint32_t kFull = 0xffffffffu;
 struct TileMeta {
   int s, kvh, part, valid;       // sequence (< 0: no more work), kv head, partition, rows < valid hold tokens
   int last, qslot, n_parts, lo;  // last tile of the item, Q buffer, partitions, rows < lo precede the window
+  int tail;                      // tiles of the item after this one
   float qinv;                    // 8-bit caches with bf16 q: 2^-e undoing the exact prescale of Q to fp16
 };
 
@@ -93,18 +104,21 @@ template <int NS, bool I8, int NRH>
 struct Shared {
   uint64_t full[NS], empty[NS];
   uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2], q_free[2];
-  uint64_t max_bar[2], sum_bar;   // softmax-warp exchanges (bounded waits, unlike bar.sync)
+  uint64_t m_full[2];             // MMA issuer -> softmax: tile t's metadata in smeta[t & 1]
+  TileMeta smeta[2];
+  uint64_t max_bar[2];            // softmax-warp exchange (bounded waits, unlike bar.sync)
   uint64_t c_full[2], c_free[2];  // softmax -> output warps: per-tile hand-off ring
   TileMeta meta[NS];
   struct Handoff {                // what the output warps need for tile t (ring slot t & 1)
     TileMeta meta;
     float corr[kN];               // 2^(m_{t-1} - m_t) per head
-    float m_fin[kN], L[kN];       // item maximum and normaliser, valid when meta.last
+    float m_fin[kN];              // the group's item maximum, on its last tile of the item
+    float Lq[4][kN];              // the group's sums per TMEM lane quarter, on the same tile
   } hand[2];
   float red_max[2][4][kN];
-  float red_sum[4][kN];
   uint32_t tmem_base;
   volatile int abort_flag;
+  volatile int end_tile;          // QK issuer -> PV issuer: tiles in this CTA (set at the end)
   // 8-bit caches: producer -> converter ring of raw half tiles, and the token
   // scales of each converted stage
   // (two rings of NRH slots, one per 64-token half: slot h * NRH + k % NRH)
@@ -190,6 +204,9 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
   constexpr bool kBF16 = std::is_same<OpT, __nv_bfloat16>::value;
   constexpr bool kQConvert = I8 && std::is_same<T, __nv_bfloat16>::value;
   constexpr int NCW = I8 ? converter_warps(G) : 0;
+  constexpr int kSoftB = kThreads / 32 + (I8 ? NCW + 1 : 0);   // first warp of softmax group 1
+  constexpr bool kSplitIssue = split_issue(I8);
+  constexpr int kPVWarp = threads_of(I8, G) / 32 - 1;           // with split issue, the PV issuer: the last warp
 
   // ---- set-up: barriers, zeroed Q buffers (padding heads stay zero), TMEM
   if (threadIdx.x == 0) {
@@ -209,6 +226,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.s_full[i], 1);
+      mbar_init(&sh.m_full[i], 1);
       mbar_init(&sh.s_free[i], 4);
       mbar_init(&sh.p_full[i], 4);
       mbar_init(&sh.o_full[i], 1);
@@ -218,12 +236,14 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       mbar_init(&sh.c_full[i], 4);
       mbar_init(&sh.c_free[i], 4);
     }
-    mbar_init(&sh.sum_bar, 4);
     sh.abort_flag = 0;
+    sh.end_tile = 0x7fffffff;
     fence_mbar_init();
   }
   for (int i = threadIdx.x; i < 2 * kQBytes / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
+  // items per sequence, all loaded at once (the producer scans them below)
+  for (int i = threadIdx.x; i < S; i += blockDim.x) pre[i + 1] = items_of(p, p.context_lens[i]);
   if (warp == 1) {
     tc::tmem_alloc(&sh.tmem_base, kCols);
     tc::tmem_relinquish();
@@ -237,7 +257,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
     // =================================================================== producer
     int carry = 0;
     for (int base = 0; base < S; base += 32) {
-      int x = (base + lane < S) ? items_of(p, p.context_lens[base + lane]) : 0;
+      int x = (base + lane < S) ? pre[base + lane + 1] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(kFull, x, o);
@@ -396,6 +416,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
         m.s = s; m.kvh = kvh; m.part = part; m.valid = valid;
         m.last = (k == ntiles - 1); m.qslot = qslot; m.n_parts = n_parts;
         m.lo = max(0, t_first - (t0 + k * kTile));
+        m.tail = ntiles - 1 - k;
         m.qinv = qinv;
         // the tile's block ids, lane i holding blocks i + 32 c of the tile: the
         // item's first 32 come from the prefetched id_lane, the rest are loaded
@@ -436,6 +457,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
           m.s = s; m.kvh = kvh; m.part = part; m.valid = valid;
           m.last = (k == ntiles - 1); m.qslot = qslot; m.n_parts = n_parts;
           m.lo = max(0, t_first - (t0 + k * kTile));
+          m.tail = ntiles - 1 - k;
           m.qinv = qinv;
           sh.meta[slot] = m;
           mbar_arrive_expect_tx(&sh.full[slot], (uint32_t)(nb * chunk_bytes));
@@ -482,12 +504,12 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // =================================================================== MMA issuer
-    // Event-driven: QK(t) as soon as tile t has landed and its S buffer is free,
-    // PV(t) as soon as P(t) is written and its O buffer is free -- neither waits
-    // for the other stream, so a stage is released right after its own PV.  The
-    // barriers are tested without blocking, so one stream never sleeps on the other.
+  } else if (warp == 1 && !kSplitIssue) {
+    // =================================================================== MMA issuer (8-bit caches)
+    // Event-driven: QK(t) as soon as tile t has landed (converted) and its S
+    // buffer is free, PV(t) as soon as P(t) is written and its O buffer is free
+    // -- neither waits for the other stream, so a stage is released right after
+    // its own PV.  The barriers are tested without blocking.
     if (lane == 0) {
       const uint32_t id_qk = tc::idesc_f16(128, kN, kBF16, false, false);
       const uint32_t id_pv = tc::idesc_f16(128, NPV, kBF16, true, true);
@@ -506,7 +528,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
             } else if (qk < 2 || mbar_test_wait(&sh.s_free[qk & 1], ((qk >> 1) - 1) & 1)) {
               tc::fence_after_sync();
               const uint32_t st = smem_u32(stages + slot * kStage), qa = smem_u32(qbuf + m.qslot * kQBytes);
-#pragma unroll
+  #pragma unroll
               for (int kk = 0; kk < kD / 16; ++kk) {
                 const uint64_t qd = tc::smem_desc(qa + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
                 if constexpr (I8)   // K (fp16, token = TMEM lane) converted into TMEM: 16 dims = 8 columns
@@ -559,12 +581,118 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       }
     }
     __syncwarp();
-  } else if (warp < 6) {
-    // =================================================================== softmax warps (2-5)
+  } else if (warp == 1) {
+    // =================================================================== QK issuer (16-bit caches)
+    // One lane: QK(t) as soon as tile t has landed and its S buffer is free.
+    // The PV products have their own issuer warp, so neither stream waits for
+    // the other's issue.  Descriptors are built once per tile and advanced by
+    // constant offsets (16-byte units in the start-address field).
+    if (lane == 0) {
+      const uint32_t id_qk = tc::idesc_f16(128, kN, kBF16, false, false);
+      int qk = 0;
+      bool ok = true;
+      while (true) {
+        const int slot = qk % NS;
+        if (!mbar_spin(&sh.full[slot], (qk / NS) & 1) || sh.abort_flag) { ok = false; break; }
+        const TileMeta m = sh.meta[slot];
+        if (m.s < 0) break;
+        if (qk >= 2 && !mbar_spin(&sh.s_free[qk & 1], ((qk >> 1) - 1) & 1)) { ok = false; break; }
+        // the softmax warps take the tile's metadata from here (smeta[b] was
+        // last read for tile qk - 2, before its S buffer was freed)
+        sh.smeta[qk & 1] = m;
+        mbar_arrive(&sh.m_full[qk & 1]);
+        tc::fence_after_sync();
+        const uint64_t qd = tc::smem_desc(smem_u32(qbuf + m.qslot * kQBytes), 16, 1024, tc::kSwizzle128B);
+        const uint64_t kd = tc::smem_desc(smem_u32(stages + slot * kStage), 16, kGroupBytes, tc::kSwizzle128B);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t q_k = qd + (uint64_t)((((kk >> 2) * 2048) + (kk & 3) * 32) >> 4);
+          if constexpr (I8)   // K (fp16, token = TMEM lane) converted into TMEM: 16 dims = 8 columns
+            tc::mma_f16_ta(tmem + (qk & 1) * 16, tmem + kKCol + slot * 64 + kk * 8, q_k, id_qk, kk > 0);
+          else
+            tc::mma_f16(tmem + (qk & 1) * 16, kd + (uint64_t)((((kk >> 2) * 1024) + (kk & 3) * 32) >> 4), q_k, id_qk,
+                        kk > 0);
+        }
+        tc::commit(&sh.s_full[qk & 1]);
+        if (m.last) tc::commit(&sh.q_free[m.qslot]);
+        ++qk;
+      }
+      sh.end_tile = qk;   // the PV issuer stops there
+      if (ok) {
+        // no more work: both metadata buffers say so (marked with the end tile,
+        // so only the softmax warps waiting for tile `end` pass it on), once
+        // the softmax warps have read the last metadata of each buffer (they
+        // release S(t) after reading smeta for tile t)
+        const int end = qk;
+        for (int u = max(0, end - 2); u < end && ok; ++u)
+          ok = mbar_wait(&sh.s_free[u & 1], (u >> 1) & 1);
+        if (ok) {
+          for (int b2 = 0; b2 < 2; ++b2) {
+            sh.smeta[b2].s = -1;
+            sh.smeta[b2].valid = end;
+            mbar_arrive(&sh.m_full[b2]);
+          }
+        }
+      }
+      if (!ok) {
+        report(p.dev_err, PA_DEVERR_TIMEOUT);
+        sh.abort_flag = 1;
+      }
+    }
+    __syncwarp();
+  } else if (kSplitIssue && warp == kPVWarp) {
+    // =================================================================== PV issuer (16-bit caches)
+    // One lane: PV(t) as soon as P(t) is written and its O buffer is free; the
+    // commit after it releases the stage (QK(t) completed before the softmax of
+    // tile t began).
+    if (lane == 0) {
+      const uint32_t id_pv = tc::idesc_f16(128, NPV, kBF16, true, true);
+      // V of 8-token group g: at g * 4 KiB + 2 KiB among the K atoms (16-bit
+      // caches), at g * 2 KiB in a V-only stage (8-bit caches)
+      constexpr uint32_t kVGroup = I8 ? 2048 : kGroupBytes, kVOff = I8 ? 0 : 2048;
+      int pv = 0;
+      uint32_t idle = 0;
+      bool ok = true;
+      while (pv < sh.end_tile) {
+        const int pb = pv & 1;
+        if (mbar_test_wait(&sh.p_full[pb], (pv >> 1) & 1) &&
+            (pv < 2 || mbar_test_wait(&sh.o_free[pb], ((pv >> 1) - 1) & 1))) {
+          tc::fence_after_sync();
+          const int slot = pv % NS;
+          const int valid = sh.meta[slot].valid;   // the stage is not refilled before this PV completes
+          const uint64_t vd = tc::smem_desc(smem_u32(stages + slot * kStage) + kVOff, 1024, kVGroup, tc::kSwizzle128B);
+          const uint64_t pd = tc::smem_desc(smem_u32(pbuf + pb * kPBytes), (NPV / 8) * 128, 128, tc::kSwizzleNone);
+          const int nsteps = (valid + 15) >> 4;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            if (kk < nsteps)
+              tc::mma_f16(tmem + 32 + pb * 32, vd + (uint64_t)((kk * 2 * kVGroup) >> 4),
+                          pd + (uint64_t)((kk * (NPV / 8) * 256) >> 4), id_pv, kk > 0);
+          tc::commit(&sh.o_full[pb]);
+          tc::commit(&sh.empty[slot]);
+          ++pv;
+          idle = 0;
+        } else if (++idle > kSpinLimit || sh.abort_flag) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) {
+        report(p.dev_err, PA_DEVERR_TIMEOUT);
+        sh.abort_flag = 1;
+      }
+    }
+    __syncwarp();
+  } else if ((warp >= 2 && warp < 6) || (ping_pong(I8, G) && warp >= kSoftB && warp < kSoftB + 4)) {
+    // =================================================================== softmax warps (2-5, group 1)
     // (wait results are made warp-uniform in the softmax and output warps: the
     // TMEM loads after them are warp-collective and must never run diverged)
     // Tile t: S^T -> tile maxima -> P^T (hi, lo) for the PV product; at the end
     // of an item, the normaliser.  Hands per-tile factors to the output warps.
+    // With two warpgroups, group g takes tiles t = g mod 2 and keeps its own
+    // running maximum and sums for the item; the output warps merge the two.
+    constexpr bool PP = ping_pong(I8, G);
+    const int grp = (PP && warp >= kSoftB) ? 1 : 0;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;   // TMEM lane = token row of S^T
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
@@ -574,21 +702,35 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       m[n] = -INFINITY;
       lp[n] = 0.f;
     }
-    int tile_seq = 0, sum_uses = 0;
+    int tile_seq = grp;
     bool ok = true;
     while (true) {
       const int slot = tile_seq % NS;
-      if (!__all_sync(kFull, mbar_wait(&sh.full[slot], (tile_seq / NS) & 1))) { ok = false; break; }
-      const TileMeta mt = sh.meta[slot];
       const int hb = tile_seq & 1;
+      // the tile's metadata: with one group straight from the stage (it comes
+      // with the stage's barrier); with two, forwarded by the QK issuer per S
+      // buffer, so each group only ever waits on its own buffer's phases
+      TileMeta mt;
+      if constexpr (PP) {
+        if (!__all_sync(kFull, mbar_wait(&sh.m_full[hb], (tile_seq >> 1) & 1))) { ok = false; break; }
+        mt = sh.smeta[hb];
+      } else {
+        if (!__all_sync(kFull, mbar_wait(&sh.full[slot], (tile_seq / NS) & 1))) { ok = false; break; }
+        mt = sh.meta[slot];
+      }
       if (__any_sync(kFull, mt.s < 0 || sh.abort_flag)) {
-        // tell the output warps there is no more work
-        if (tile_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.c_free[hb], ((tile_seq >> 1) - 1) & 1))) { ok = false; break; }
-        if (row == 0) sh.hand[hb].meta.s = -1;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.c_full[hb]);
+        // tell the output warps there is no more work (the group whose turn
+        // the end tile is; the forwarded end mark carries the end tile in valid)
+        if (mt.s < 0 && (!PP || mt.valid == tile_seq)) {
+          if (tile_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.c_free[hb], ((tile_seq >> 1) - 1) & 1))) { ok = false; break; }
+          if (lane == 0 && quarter == 0) sh.hand[hb].meta.s = -1;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.c_full[hb]);
+        }
         break;
       }
+      // this group's last tile of the item: it hands over its maximum and sums
+      const bool fin = mt.tail == 0 || (PP && mt.tail == 1);
       const int sb = tile_seq & 1;
       if (!__all_sync(kFull, mbar_wait(&sh.s_full[sb], (tile_seq >> 1) & 1))) { ok = false; break; }
       tc::fence_after_sync();
@@ -658,47 +800,42 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.p_full[hb]);
-      // item end: normaliser L = sum over the 128 rows of the running sums
-      float L[G];
-      if (mt.last) {
+      // this group's part of the normaliser from this quarter's 32 rows; the
+      // output warps add the quarters (and the groups)
+      float Lq[G];
+      if (fin) {
 #pragma unroll
         for (int n = 0; n < G; ++n) {
           float v = lp[n];
 #pragma unroll
           for (int o2 = 16; o2 > 0; o2 >>= 1) v += __shfl_xor_sync(kFull, v, o2);
-          if (lane == 0) sh.red_sum[quarter][n] = v;
+          Lq[n] = v;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.sum_bar);
-        if (!__all_sync(kFull, mbar_wait(&sh.sum_bar, sum_uses & 1))) { ok = false; break; }
-        ++sum_uses;
-#pragma unroll
-        for (int n = 0; n < G; ++n)
-          L[n] = sh.red_sum[0][n] + sh.red_sum[1][n] + sh.red_sum[2][n] + sh.red_sum[3][n];
       }
       // hand-off to the output warps
       if (tile_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.c_free[hb], ((tile_seq >> 1) - 1) & 1))) { ok = false; break; }
-      if (row == 0) {
+      if (lane == 0 && quarter == 0) {
         sh.hand[hb].meta = mt;
 #pragma unroll
         for (int n = 0; n < G; ++n) {
           sh.hand[hb].corr[n] = corr[n];
-          if (mt.last) {
-            sh.hand[hb].m_fin[n] = m[n];
-            sh.hand[hb].L[n] = L[n];
-          }
+          if (fin) sh.hand[hb].m_fin[n] = m[n];
         }
+      }
+      if (fin && lane == 0) {
+#pragma unroll
+        for (int n = 0; n < G; ++n) sh.hand[hb].Lq[quarter][n] = Lq[n];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.c_full[hb]);
-      if (mt.last) {
+      if (fin) {
 #pragma unroll
         for (int n = 0; n < G; ++n) {
           m[n] = -INFINITY;
           lp[n] = 0.f;
         }
       }
-      ++tile_seq;
+      tile_seq += PP ? 2 : 1;
     }
     if (!ok && lane == 0) {
       report(p.dev_err, PA_DEVERR_TIMEOUT);
@@ -706,27 +843,46 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
     }
   } else if (warp < 10) {
     // =================================================================== output warps (6-9)
-    // Tile t: O^T -> acc = acc * corr_t + O_t (thread = TMEM lane = head dim);
-    // at the end of an item, write out = acc / L (or the partition's partials).
+    // Tile t: O^T -> acc = acc * corr_t + O_t (thread = TMEM lane = head dim),
+    // one accumulator per softmax warpgroup; at the end of an item the groups'
+    // (maximum, sum, acc) merge exactly (log-sum-exp) into out = acc / L, or
+    // into the partition's partial results.
+    constexpr bool PP = ping_pong(I8, G);
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-    float acc[G];
+    float acc0[G], acc1[G], mg0[G], mg1[G], Lg0[G], Lg1[G];
 #pragma unroll
-    for (int n = 0; n < G; ++n) acc[n] = 0.f;
+    for (int n = 0; n < G; ++n) {
+      acc0[n] = acc1[n] = 0.f;
+      mg0[n] = mg1[n] = -INFINITY;
+      Lg0[n] = Lg1[n] = 0.f;
+    }
     int tile_seq = 0;
     bool ok = true;
     while (true) {
       const int hb = tile_seq & 1;
+      const bool g1 = PP && hb == 1;   // a tile of softmax group 1
       if (!__all_sync(kFull, mbar_wait(&sh.c_full[hb], (tile_seq >> 1) & 1))) { ok = false; break; }
       const TileMeta mt = sh.hand[hb].meta;
       if (mt.s < 0) break;
-      float corr[G], m_fin[G], L[G];
+      const bool fin = mt.tail == 0 || (PP && mt.tail == 1);
+      float corr[G];
 #pragma unroll
-      for (int n = 0; n < G; ++n) {
-        corr[n] = sh.hand[hb].corr[n];
-        m_fin[n] = sh.hand[hb].m_fin[n];
-        L[n] = sh.hand[hb].L[n];
+      for (int n = 0; n < G; ++n) corr[n] = sh.hand[hb].corr[n];
+      if (fin) {
+#pragma unroll
+        for (int n = 0; n < G; ++n) {
+          const float mf = sh.hand[hb].m_fin[n];
+          const float Lf = (sh.hand[hb].Lq[0][n] + sh.hand[hb].Lq[1][n]) + (sh.hand[hb].Lq[2][n] + sh.hand[hb].Lq[3][n]);
+          if (g1) {
+            mg1[n] = mf;
+            Lg1[n] = Lf;
+          } else {
+            mg0[n] = mf;
+            Lg0[n] = Lf;
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.c_free[hb]);
@@ -740,28 +896,35 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       if (lane == 0) mbar_arrive(&sh.o_free[hb]);
 #pragma unroll
       for (int n = 0; n < G; ++n) {
-        const float hi_part = o[n >> 4][n & 15], lo_part = o[(HG + n) >> 4][(HG + n) & 15];
-        acc[n] = fmaf(acc[n], corr[n], hi_part + lo_part);
+        const float x = o[n >> 4][n & 15] + o[(HG + n) >> 4][(HG + n) & 15];   // O_hi + O_lo
+        if (g1) acc1[n] = fmaf(acc1[n], corr[n], x);
+        else acc0[n] = fmaf(acc0[n], corr[n], x);
       }
       if (mt.last) {
         const int64_t h0 = (int64_t)mt.s * p.num_q_heads + mt.kvh * G;
-        if (mt.n_parts == 1) {
-          T* out = static_cast<T*>(p.out);
+        T* out = static_cast<T*>(p.out);
 #pragma unroll
-          for (int n = 0; n < G; ++n) out[(h0 + n) * kD + row] = Elem<T>::from_float(acc[n] / L[n]);
-        } else {
-#pragma unroll
-          for (int n = 0; n < G; ++n) {
+        for (int n = 0; n < G; ++n) {
+          // merge the groups: a group without a tile in this item has m = -inf
+          const float M = PP ? fmaxf(mg0[n], mg1[n]) : mg0[n];
+          const float f0 = (mg0[n] == -INFINITY) ? 0.f : exp2f(mg0[n] - M);
+          const float f1 = (!PP || mg1[n] == -INFINITY) ? 0.f : exp2f(mg1[n] - M);
+          const float O = PP ? fmaf(acc0[n], f0, acc1[n] * f1) : acc0[n];
+          const float L = PP ? fmaf(Lg0[n], f0, Lg1[n] * f1) : Lg0[n];
+          if (mt.n_parts == 1) {
+            out[(h0 + n) * kD + row] = Elem<T>::from_float(O / L);
+          } else {
             const int64_t r = (h0 + n) * p.max_parts + mt.part;
-            p.ws_o[r * kD + row] = acc[n];
+            p.ws_o[r * kD + row] = O;
             if (row == 0) {
-              p.ws_ml[r * 2 + 0] = m_fin[n];
-              p.ws_ml[r * 2 + 1] = L[n];
+              p.ws_ml[r * 2 + 0] = M;
+              p.ws_ml[r * 2 + 1] = L;
             }
           }
+          acc0[n] = acc1[n] = 0.f;
+          mg0[n] = mg1[n] = -INFINITY;
+          Lg0[n] = Lg1[n] = 0.f;
         }
-#pragma unroll
-        for (int n = 0; n < G; ++n) acc[n] = 0.f;
       }
       ++tile_seq;
     }
@@ -769,7 +932,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       report(p.dev_err, PA_DEVERR_TIMEOUT);
       sh.abort_flag = 1;
     }
-  } else if (I8 && warp < kThreads / 32 + NCW) {
+  } else if (I8 && warp >= kThreads / 32 && warp < kThreads / 32 + NCW) {
     // =================================================================== converter warps (8-bit)
     // A warp may access TMEM lanes 32 (warp % 4) .. + 31, so thread `lane` owns
     // token row t = 32 (warp % 4) + lane of every tile (in half tile t / 64).
@@ -864,7 +1027,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       report(p.dev_err, PA_DEVERR_TIMEOUT);
       sh.abort_flag = 1;
     }
-  } else if (I8) {
+  } else if (I8 && warp == kThreads / 32 + NCW) {
     // =================================================================== copy warp (8-bit)
     // Tile t: wait for its descriptor and for both halves' raw slots, then one
     // instruction issues the bulk copies of all its (block, kv head) chunks

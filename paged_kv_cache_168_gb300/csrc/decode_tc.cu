@@ -23,18 +23,25 @@
 //   warp 0      producer: item walk, block-id validation, Q staging, one bulk
 //               copy per (block, kv head) chunk into a ring of NS 64 KiB stages;
 //               per-stage metadata travels with the stage's mbarrier.
-//   warp 1      MMA issuer (one lane): QK(t) and PV(t) each issued as soon as
-//               their inputs are ready (polled, bounded).
+//   warp 1      MMA issue (one lane): QK(t) as soon as tile t is staged and its
+//               S buffer is free, PV(t) as soon as P(t) is written and its O
+//               buffer is free.  16-bit caches give PV its own issuer (the last
+//               warp), since one lane issuing all 16 MMAs of a tile is the limit.
 //   warps 2-5   softmax (thread = TMEM lane = token row): tile max across the
 //               128 rows, p = 2^(s - m) in fp32, written in the cache type as
 //               p_hi = round(p) and p_lo = round(p - p_hi) side by side in one
 //               P^T operand (N = 16, or 32 at 16 heads), so one PV product gives
 //               O_hi and O_lo and the weights reach the tensor core with ~16
-//               significant bits even for bf16.  At an item's end they also
-//               reduce the normaliser.
+//               significant bits even for bf16.  For 16-bit caches (up to 8
+//               heads per kv head) a second softmax warpgroup (warps 10-13)
+//               takes the odd tiles, each group with its own running maximum
+//               and sums; the tile metadata reaches each group through the QK
+//               issuer, one buffer per S buffer.
 //   warps 6-9   output (thread = TMEM lane = head dim): fold O_hi + O_lo of
 //               each tile into registers with the online-softmax correction the
-//               softmax warps hand over, and write the item's result.
+//               softmax warps hand over (one accumulator per softmax group),
+//               merge the groups by log-sum-exp at the item's end and write the
+//               item's result (or the partition's partial results).
 // 8-bit caches (codes + one fp32 scale per token and kv head) change the
 // staging: warp 0 only plans (items, Q, block ids per tile into a descriptor
 // ring); one copy warp bulk-copies each tile's 8-bit chunks into two rings of
@@ -61,7 +68,7 @@ constexpr int kGroupBytes = 8 * 2 * kD * 2;        // one 8-token group: 4 KiB
 constexpr int kN = 16;                             // MMA N: query heads, zero-padded
 constexpr int kQBytes = kN * kD * 2;               // 4 KiB
 constexpr int kPBytes = kTile * 32 * 2;            // P^T operand: 128 tokens x up to 32 columns (8 KiB)
-constexpr int kThreads = 320;                      // producer, MMA, 4 softmax warps, 4 output warps
+constexpr int kThreads = 320;                      // producer, MMA issue, 4 softmax warps, 4 output warps
 // 8-bit caches add converter warps: 8 when the registers allow it (group <= 4), else 4
 __host__ __device__ constexpr int converter_warps(int G) { return G <= 4 ? 8 : 4; }
 // 8-bit caches also add one copy warp (after the converters) that only issues

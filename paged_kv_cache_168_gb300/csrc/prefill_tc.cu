@@ -85,6 +85,13 @@ struct Shared {
   volatile int abort_flag;
 };
 
+// 2^x by the MUFU instruction (relative error about 2^-22; -inf -> +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Offset of the 16-byte piece `piece` (8 elements) of row r in a 128B-swizzled
 // K-major operand of 128 rows whose 64-element column blocks are kQAtomBytes apart.
 __device__ __forceinline__ uint32_t op_offset(int r, int piece) {
@@ -317,14 +324,25 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.s_free[sb]);
       const int lim = (row_ok ? min(kKv, pos + 1 - j * kKv) : 0) - wg * kCols;   // columns of this half attended
+      // x stays in raw score units (the scale, > 0, is folded into the exponent
+      // below); masked columns become -inf.  Tiles wholly below the diagonal
+      // skip the mask.
       float mt = -INFINITY;
+      if (lim >= kCols) {
 #pragma unroll
-      for (int c = 0; c < kCols / 16; ++c)
+        for (int c = 0; c < kCols / 16; ++c)
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          x[c][e] = (c * 16 + e < lim) ? x[c][e] * p.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[c][e]);
-        }
+          for (int e = 0; e < 16; ++e) mt = fmaxf(mt, x[c][e]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < kCols / 16; ++c)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            x[c][e] = (c * 16 + e < lim) ? x[c][e] : -INFINITY;
+            mt = fmaxf(mt, x[c][e]);
+          }
+      }
+      mt *= p.scale_log2;   // base-2 units
       // after the exchange both halves have read their S columns, so P may be
       // written over them
       mt = fmaxf(mt, exchange(j, mt));
@@ -358,14 +376,17 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
       }
       // p = 2^(x - m) in fp32; P (in TMEM, two tokens per column) gets round(p)
       // and, for bf16, round(p - round(p))
+      // (a row with every column so far masked has m = -inf: its x are all -inf
+      // and with nm = 0 its p come out 0)
+      const float nm = (m == -INFINITY) ? 0.f : -m;
 #pragma unroll
       for (int h = 0; h < kCols / 32; ++h) {
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int c = h * 32 + 2 * e;
-          const float a = (m == -INFINITY) ? 0.f : exp2f(x[c >> 4][c & 15] - m);
-          const float b = (m == -INFINITY) ? 0.f : exp2f(x[c >> 4][(c & 15) + 1] - m);
+          const float a = ex2_approx(fmaf(x[c >> 4][c & 15], p.scale_log2, nm));
+          const float b = ex2_approx(fmaf(x[c >> 4][(c & 15) + 1], p.scale_log2, nm));
           l += a + b;
           hi[e] = Elem<T>::pack2(a, b);
           if (kLo) {

@@ -77,7 +77,7 @@ struct Cfg {
 };
 
 struct Shared {
-  uint64_t full[2], empty[2], s_full[2], s_free[2], p_full, pv_done;
+  uint64_t full[2], empty[2], s_full[2], s_free[2], p_full[2], pv_done;
   uint64_t xbar;                  // the two softmax warpgroups' per-row exchanges
   float red[2][2][kRows];         // [exchange parity][warpgroup][row]
   uint32_t tmem_base;
@@ -167,7 +167,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.s_free[i], kSoftmaxWarps);
     }
-    mbar_init(&sh.p_full, kSoftmaxWarps);
+    mbar_init(&sh.p_full[0], kSoftmaxWarps);
+    mbar_init(&sh.p_full[1], kSoftmaxWarps);
     mbar_init(&sh.pv_done, 1);
     mbar_init(&sh.xbar, kSoftmaxWarps);
     sh.abort_flag = 0;
@@ -235,45 +236,63 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
       const uint32_t id_qk = tc::idesc_f16(kRows, kKv, kBF16, false, false);
       const uint32_t id_pv = tc::idesc_f16(kRows, D, kBF16, false, true);
       const uint32_t qa = smem_u32(qbuf);
-      auto issue_qk = [&](int j) -> bool {
-        const int slot = j & 1;
-        if (!mbar_wait(&sh.full[slot], (j >> 1) & 1)) return false;
-        if (j >= 2 && !mbar_wait(&sh.s_free[slot], ((j >> 1) - 1) & 1)) return false;
-        tc::fence_after_sync();
-        const uint32_t st = smem_u32(stages + slot * C::kStageBytes);
+      // Event-driven: QK(j) as soon as tile j has landed (and P(j - 2), which it
+      // overwrites in TMEM, has gone to PV(j - 2)); PV(j) as soon as P(j) is
+      // written -- so PV(j), and with it the release of tile j's stage, never
+      // waits for the next tile's data.  Barriers are tested without blocking.
+      // (tcgen05 operations of this thread execute in issue order, so S(j + 2)
+      // overwrites P(j) only after PV(j) has read it.)
+      const uint64_t qd0 = tc::smem_desc(qa, 16, 1024, tc::kSwizzle128B);
+      int qk = 0, pv = 0;
+      uint32_t idle = 0;
+      bool ok = true;
+      while (pv < n_kv) {
+        bool progressed = false;
+        if (qk < n_kv && pv >= qk - 1) {
+          const int slot = qk & 1;
+          if (mbar_test_wait(&sh.full[slot], (qk >> 1) & 1) &&
+              (qk < 2 || mbar_test_wait(&sh.s_free[slot], ((qk >> 1) - 1) & 1))) {
+            tc::fence_after_sync();
+            const uint64_t kd0 = tc::smem_desc(smem_u32(stages + slot * C::kStageBytes), 16, C::kGroupBytes,
+                                               tc::kSwizzle128B);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_f16(tmem + slot * kKv,
-                      tc::smem_desc(qa + (kk >> 2) * C::kQAtomBytes + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B),
-                      tc::smem_desc(st + (kk >> 2) * 1024 + (kk & 3) * 32, 16, C::kGroupBytes, tc::kSwizzle128B),
-                      id_qk, kk > 0);
-        tc::commit(&sh.s_full[slot]);
-        return true;
-      };
-      bool ok = !sh.abort_flag && issue_qk(0);
-      for (int j = 0; j < n_kv && ok; ++j) {
-        if (j + 1 < n_kv && !issue_qk(j + 1)) {
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc::mma_f16(tmem + slot * kKv, qd0 + (uint64_t)((((kk >> 2) * C::kQAtomBytes) + (kk & 3) * 32) >> 4),
+                          kd0 + (uint64_t)((((kk >> 2) * 1024) + (kk & 3) * 32) >> 4), id_qk, kk > 0);
+            tc::commit(&sh.s_full[slot]);
+            ++qk;
+            progressed = true;
+          }
+        }
+        if (pv < qk) {
+          const int slot = pv & 1;
+          if (mbar_test_wait(&sh.p_full[slot], (pv >> 1) & 1)) {
+            tc::fence_after_sync();
+            const uint64_t vd0 = tc::smem_desc(smem_u32(stages + slot * C::kStageBytes) + C::kAtoms * 1024, 1024,
+                                               C::kGroupBytes, tc::kSwizzle128B);
+            const int valid = min(kKv, kv_len - pv * kKv);
+            const int nsteps = (valid + 15) >> 4;
+#pragma unroll
+            for (int kk = 0; kk < kKv / 16; ++kk) {
+              if (kk < nsteps) {
+                const uint64_t vdesc = vd0 + (uint64_t)((kk * 2 * C::kGroupBytes) >> 4);
+                const uint32_t pa = tmem + slot * kKv + kk * 8;      // 16 tokens = 8 packed columns
+                tc::mma_f16_ta(tmem + kOCol, pa, vdesc, id_pv, (pv > 0 || kk > 0) ? 1u : 0u);
+                if (kLo) tc::mma_f16_ta(tmem + kOCol, pa + kKv / 2, vdesc, id_pv, 1u);
+              }
+            }
+            tc::commit(&sh.pv_done);
+            tc::commit(&sh.empty[slot]);
+            ++pv;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          idle = 0;
+        } else if (++idle > kSpinLimit || sh.abort_flag) {
           ok = false;
           break;
         }
-        if (!mbar_wait(&sh.p_full, j & 1) || sh.abort_flag) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
-        const int slot = j & 1;
-        const uint32_t st = smem_u32(stages + slot * C::kStageBytes);
-        const int valid = min(kKv, kv_len - j * kKv);
-        const int nsteps = (valid + 15) >> 4;
-        for (int kk = 0; kk < nsteps; ++kk) {
-          const uint64_t vdesc =
-              tc::smem_desc(st + kk * 2 * C::kGroupBytes + C::kAtoms * 1024, 1024, C::kGroupBytes, tc::kSwizzle128B);
-          const uint32_t pa = tmem + slot * kKv + kk * 8;      // 16 tokens = 8 packed columns
-          tc::mma_f16_ta(tmem + kOCol, pa, vdesc, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          if (kLo) tc::mma_f16_ta(tmem + kOCol, pa + kKv / 2, vdesc, id_pv, 1u);
-        }
-        tc::commit(&sh.pv_done);
-        tc::commit(&sh.empty[slot]);
       }
       if (!ok) {
         report(p.dev_err, PA_DEVERR_TIMEOUT);
@@ -422,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.p_full);
+      if (lane == 0) mbar_arrive(&sh.p_full[sb]);
     }
     if (ok && n_kv > 0) ok = __all_sync(kFull, mbar_wait(&sh.pv_done, (n_kv - 1) & 1));
     float l_tot = 0.f;

@@ -30,7 +30,8 @@
 // Roles:
 //   warp 0      bulk copies of each KV tile's (block, kv head) chunks into a
 //               2-stage ring (mbarrier transaction counts).
-//   warp 1      one lane issues S_{t+1} ahead of O += P_t V_t.
+//   warp 1      one lane, event-driven: S_t as soon as tile t has landed (and
+//               PV_{t-2} has been issued), O += P_t V_t as soon as P_t is written.
 // TMEM columns: S/P buffer 0 [0, 64), S/P buffer 1 [64, 128), O [128, 128 + D);
 // within a buffer P occupies p_hi [0, 32) and p_lo [32, 64) (tokens packed two
 // per column).
@@ -77,7 +78,10 @@ struct Cfg {
 };
 
 struct Shared {
-  uint64_t full[2], empty[2], s_full[2], s_free[2], p_full[2], pv_done;
+  // pv_done[b]: PV of the tiles using S/P buffer b (j & 1 == b) completed.  A
+  // barrier that a waiter may trail by a tile is kept per buffer, so a waiter is
+  // never two phases behind (the parity it waits for would then alias).
+  uint64_t full[2], empty[2], s_full[2], s_free[2], p_full[2], pv_done[2];
   uint64_t xbar;                  // the two softmax warpgroups' per-row exchanges
   float red[2][2][kRows];         // [exchange parity][warpgroup][row]
   uint32_t tmem_base;
@@ -169,7 +173,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
     }
     mbar_init(&sh.p_full[0], kSoftmaxWarps);
     mbar_init(&sh.p_full[1], kSoftmaxWarps);
-    mbar_init(&sh.pv_done, 1);
+    mbar_init(&sh.pv_done[0], 1);
+    mbar_init(&sh.pv_done[1], 1);
     mbar_init(&sh.xbar, kSoftmaxWarps);
     sh.abort_flag = 0;
     fence_mbar_init();
@@ -281,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
                 if (kLo) tc::mma_f16_ta(tmem + kOCol, pa + kKv / 2, vdesc, id_pv, 1u);
               }
             }
-            tc::commit(&sh.pv_done);
+            tc::commit(&sh.pv_done[slot]);
             tc::commit(&sh.empty[slot]);
             ++pv;
             progressed = true;
@@ -374,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
         // O holds exactly tiles < j once PV_{j-1} has completed (PV_j waits for
         // this warp's P).  The whole warp takes the O round trip; rows that keep
         // their max scale by 1.
-        if (!__all_sync(kFull, mbar_wait(&sh.pv_done, (j - 1) & 1))) {
+        if (!__all_sync(kFull, mbar_wait(&sh.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1))) {
           ok = false;
           break;
         }
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.p_full[sb]);
     }
-    if (ok && n_kv > 0) ok = __all_sync(kFull, mbar_wait(&sh.pv_done, (n_kv - 1) & 1));
+    if (ok && n_kv > 0) ok = __all_sync(kFull, mbar_wait(&sh.pv_done[(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1));
     float l_tot = 0.f;
     if (ok) l_tot = l + exchange(n_kv, l);
     if (ok) {

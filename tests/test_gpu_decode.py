@@ -178,3 +178,20 @@ def test_entries_past_the_context_are_never_read(D, kernel):
     p = Paged(rng, S=2, Hq=4, Hkv=4, D=D, bs=16, ctx=[17, 100], dtype="f16", width=12)
     p.tables[0, 2:] = 10 ** 6
     check(p, P=128)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (32, 8), (64, 8)])
+def test_decode_tiles_with_far_apart_maxima(dtype, Hq, Hkv, kernel):
+    # keys of every other 128-token tile scaled by 8 (exact in fp16/bf16): the
+    # score maxima of consecutive tiles differ by tens of base-2 units, so the
+    # running maximum jumps between tiles and, with two softmax groups taking
+    # alternate tiles, one group's share of an item all but vanishes in the merge
+    rng = np.random.default_rng(zlib.crc32(repr(("far", dtype, Hq, Hkv)).encode()))
+    ctx = [128 * 5 + 17, 300, 129, 1000, 384, 2048]
+    p = Paged(rng, S=len(ctx), Hq=Hq, Hkv=Hkv, D=128, bs=16, ctx=ctx, dtype=dtype)
+    for s, c in enumerate(ctx):
+        hot = (np.arange(c) // 128) % 2 == s % 2
+        p.K[s][hot] *= 8.0
+    p.write_all()
+    check(p, P=512, what=f"{kernel} far-apart maxima {dtype} {Hq}/{Hkv}")

@@ -126,6 +126,7 @@ struct Shared {
   uint32_t tmem_base;
   volatile int abort_flag;
   volatile int end_tile;          // QK issuer -> PV issuer: tiles in this CTA (set at the end)
+  int cls_cnt[64], cls_cur[64];   // item ordering: remainder partitions per class, placement cursors
   // 8-bit caches: producer -> converter ring of raw half tiles, and the token
   // scales of each converted stage
   // (two rings of NRH slots, one per 64-token half: slot h * NRH + k % NRH)
@@ -172,9 +173,20 @@ __device__ __forceinline__ void codes_to_16bit(const uint4 w4, uint32_t (&o)[8])
 __device__ __forceinline__ bool ctx_invalid(const DecodeParams& p, int ctx) { return !context_ok(p, ctx); }
 
 // Work items of one sequence: its partitions, or one item that only writes zeros.
-__device__ __forceinline__ int items_of(const DecodeParams& p, int ctx) {
-  if (ctx <= 0 || ctx_invalid(p, ctx)) return 1;
-  return (ctx - attended_from(p, ctx) + p.partition_size - 1) / p.partition_size;
+// A sequence's work: F full partitions (P / 128 tiles each) and, if the
+// attended length is not a multiple of P, one remainder partition of
+// ceil(rem / 128) tiles (its "class", 1 .. P / 128 - 1).  A sequence with no
+// (or an invalid) context is one remainder item of class 1 that writes zeros.
+__device__ __forceinline__ void work_of(const DecodeParams& p, int ctx, int& full, int& cls) {
+  if (ctx <= 0 || ctx_invalid(p, ctx)) {
+    full = 0;
+    cls = 1;
+    return;
+  }
+  const int len = ctx - attended_from(p, ctx);
+  full = len / p.partition_size;
+  const int rem = len - full * p.partition_size;
+  cls = (rem + kTile - 1) / kTile;
 }
 
 template <typename T, int G>
@@ -199,7 +211,9 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
   uint8_t* qbuf = dyn + NS * kStage;
   uint8_t* pbuf = qbuf + 2 * kQBytes;
   uint8_t* raw = pbuf + 2 * kPBytes;                         // pbuf: 2 buffers of [p_hi | p_lo]
-  int* pre = reinterpret_cast<int*>(raw + (I8 ? 2 * NRH * kRawBytes : 0));
+  int* pre = reinterpret_cast<int*>(raw + (I8 ? 2 * NRH * kRawBytes : 0));   // [S + 1]
+  int16_t* rseq = reinterpret_cast<int16_t*>(pre + p.num_seqs + 1);              // [S]
+  uint8_t* rcls = reinterpret_cast<uint8_t*>(rseq + p.num_seqs);                 // [S]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.num_seqs, Hkv = p.num_kv_heads, bs = p.block_size;
@@ -249,8 +263,15 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
   }
   for (int i = threadIdx.x; i < 2 * kQBytes / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
-  // items per sequence, all loaded at once (the producer scans them below)
-  for (int i = threadIdx.x; i < S; i += blockDim.x) pre[i + 1] = items_of(p, p.context_lens[i]);
+  // per sequence its full partitions and its remainder's class, all loaded at
+  // once (the producer orders the items below)
+  for (int i = threadIdx.x; i < S; i += blockDim.x) {
+    int full, cls;
+    work_of(p, p.context_lens[i], full, cls);
+    pre[i + 1] = full;
+    rcls[i] = (uint8_t)cls;
+  }
+  for (int i = threadIdx.x; i < 64; i += blockDim.x) sh.cls_cnt[i] = 0;
   if (warp == 1) {
     tc::tmem_alloc(&sh.tmem_base, kCols);
     tc::tmem_relinquish();
@@ -275,8 +296,39 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
     }
     if (lane == 0) pre[0] = 0;
     __syncwarp();
-    const int total = carry * Hkv;
+    // Item order (identical in every CTA): all full partitions in (sequence,
+    // partition) order, then the remainder partitions from the most tiles down,
+    // stably by sequence; kv heads innermost.  CTAs take the items round by
+    // round in snake order (c, then 151 - c, ...), so every CTA gets about the
+    // same number of tiles (longest first).
+    const int n_full = carry;
+    for (int i = lane; i < S; i += 32) atomicAdd(&sh.cls_cnt[rcls[i]], 1);
+    __syncwarp();
+    if (lane == 0) {
+      int at = 0;
+      for (int c = 63; c >= 1; --c) {
+        sh.cls_cur[c] = at;
+        at += sh.cls_cnt[c];
+      }
+      sh.cls_cnt[0] = at;   // remainder partitions in all
+    }
+    __syncwarp();
+    for (int base = 0; base < S; base += 32) {
+      const int i = base + lane;
+      const int cls = i < S ? rcls[i] : 0;
+      const uint32_t same = __match_any_sync(kFull, cls);
+      const int slot_in = __popc(same & ((1u << lane) - 1u));
+      if (cls > 0) rseq[sh.cls_cur[cls] + slot_in] = (int16_t)i;
+      __syncwarp();
+      if (cls > 0 && slot_in == 0) sh.cls_cur[cls] += __popc(same);
+      __syncwarp();
+    }
+    const int total = (n_full + sh.cls_cnt[0]) * Hkv;
     const int P = p.partition_size;
+    // the item a CTA takes in round k (snake order); >= total: none
+    auto item_of_round = [&](int k) {
+      return k * (int)gridDim.x + ((k & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x);
+    };
     const bool windowed = p.window > 0 || p.ring_blocks > 0;
     constexpr int kQChunks = (G * 16 + 31) / 32;
     // The next item's independent loads (context length, its first 32 block ids,
@@ -290,14 +342,19 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       Item r;
       const int j = it / Hkv;
       r.kvh = it - j * Hkv;
-      int lo = 0, hi = S - 1;   // last sequence whose first item index is <= j
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (pre[mid] <= j) lo = mid;
-        else hi = mid - 1;
+      if (j < n_full) {
+        int lo = 0, hi = S - 1;   // last sequence whose first full partition is <= j
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (pre[mid] <= j) lo = mid;
+          else hi = mid - 1;
+        }
+        r.s = lo;
+        r.part = j - pre[lo];
+      } else {
+        r.s = rseq[j - n_full];
+        r.part = pre[r.s + 1] - pre[r.s];   // the remainder follows the full partitions
       }
-      r.s = lo;
-      r.part = j - pre[lo];
       r.ctx = p.context_lens[r.s];
       // first logical block of the partition: only a window makes it depend on
       // ctx, so without one the block-id load below does not wait for ctx
@@ -321,11 +378,11 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
     int tile_seq = 0, item_seq = 0;
     bool aborted = false;
     Item nxt;
-    if (blockIdx.x < total) nxt = fetch(blockIdx.x);
-    for (int it = blockIdx.x; it < total && !aborted; it += gridDim.x) {
+    if (item_of_round(0) < total) nxt = fetch(item_of_round(0));
+    for (int round = 0; item_of_round(round) < total && !aborted; ++round) {
       const Item cur = nxt;
-      const bool more = it + (int)gridDim.x < total;
-      if (more) nxt = fetch(it + gridDim.x);
+      const bool more = item_of_round(round + 1) < total;
+      if (more) nxt = fetch(item_of_round(round + 1));
       const int s = cur.s, kvh = cur.kvh, part = cur.part, ctx = cur.ctx, id_lane = cur.id_lane;
       const int32_t* row = p.block_tables + (int64_t)s * p.bt_stride;   // entry table_index(j) holds block j
       if (ctx_invalid(p, ctx)) {
@@ -1111,7 +1168,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
 template <typename T, int G, int NS, bool I8, int NRH>
 cudaError_t launch_typed(const DecodeParams& p, int num_sms, cudaStream_t stream) {
   const size_t smem = 1024 + (size_t)NS * stage_bytes(I8) + 2 * kQBytes + 2 * kPBytes +
-                      (I8 ? (size_t)2 * NRH * kRawBytes : 0) + (size_t)(p.num_seqs + 1) * 4;
+                      (I8 ? (size_t)2 * NRH * kRawBytes : 0) + (size_t)(p.num_seqs + 1) * 4 + (size_t)p.num_seqs * 3;
   auto kern = decode_tc_kernel<T, G, NS, I8, NRH>;
   cudaError_t e = set_smem_attribute_once<decode_tc_kernel<T, G, NS, I8, NRH>>(smem);
   if (e != cudaSuccess) return e;
@@ -1141,7 +1198,7 @@ constexpr int kI8Stages = 3, kI8Raw = 2;
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, int group, int num_sms, cudaStream_t stream) {
   if (p.num_seqs > kTcMaxSeqs) return cudaErrorInvalidValue;
-  const bool three = p.num_seqs <= 1024;   // shared memory: 3 stages + prefix of <= 1025 ints
+  const bool three = p.num_seqs <= 512;    // shared memory: 3 stages + item ordering of <= 512 sequences
   cudaError_t e;
   if (dtype == PA_F16)
     e = three ? launch_group<__half, 3, false, 1>(p, group, num_sms, stream)

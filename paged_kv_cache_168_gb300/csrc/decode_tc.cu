@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
   constexpr int NCW = I8 ? converter_warps(G) : 0;
   constexpr int kSoftB = kThreads / 32 + (I8 ? NCW + 1 : 0);   // first warp of softmax group 1
   constexpr bool kSplitIssue = split_issue(I8);
+  static_assert(!ping_pong(I8, G) || kSplitIssue, "two softmax groups take their tile metadata from the QK issuer");
   constexpr int kPVWarp = threads_of(I8, G) / 32 - 1;           // with split issue, the PV issuer: the last warp
 
   // ---- set-up: barriers, zeroed Q buffers (padding heads stay zero), TMEM

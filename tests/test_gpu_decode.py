@@ -195,3 +195,16 @@ def test_decode_tiles_with_far_apart_maxima(dtype, Hq, Hkv, kernel):
         p.K[s][hot] *= 8.0
     p.write_all()
     check(p, P=512, what=f"{kernel} far-apart maxima {dtype} {Hq}/{Hkv}")
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,dtype", [(700, 8, 2, "bf16"), (1100, 4, 4, "f16")])
+def test_decode_many_sequences_item_order(S, Hq, Hkv, dtype):
+    # more than 512 sequences (the tensor-core decode's 2-stage ring) with
+    # contexts of every partition class, zeros included: every item of the
+    # longest-first, snake-ordered walk must be served exactly once
+    rng = np.random.default_rng(300 + S)
+    ctx = rng.integers(0, 600, size=S)
+    ctx[::97] = 0
+    ctx[5::89] = 128 * rng.integers(1, 5, size=len(ctx[5::89]))   # whole partitions, no remainder
+    p = Paged(rng, S=S, Hq=Hq, Hkv=Hkv, D=128, bs=16, ctx=list(ctx), dtype=dtype)
+    check(p, P=128, what=f"many sequences S={S}")

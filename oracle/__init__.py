@@ -120,6 +120,8 @@ def _load():
     lib.oracle_reshape_and_cache_i8.restype = ctypes.c_int
     lib.oracle_decode_i8.argtypes = [P, P, i64, P, G, P, i32, P, i32, i32, i32, dbl, i32]
     lib.oracle_decode_i8.restype = ctypes.c_int
+    lib.oracle_decode_i8_window.argtypes = [P, P, i64, P, G, P, i32, P, i32, i32, i32, dbl, i32, i32, i32]
+    lib.oracle_decode_i8_window.restype = ctypes.c_int
     lib.oracle_copy_blocks_bytes.argtypes = [P, i64, i32, i32, i64, P, i32]
     lib.oracle_copy_blocks_bytes.restype = ctypes.c_int
     lib.oracle_prefill.argtypes = [P, P, i64, P, G, P, i32, P, P, i32, i32, dbl, i32]
@@ -297,8 +299,10 @@ def reshape_and_cache_i8(layer: np.ndarray, geom: Geom, key: np.ndarray, value: 
 
 
 def decode_i8(q: np.ndarray, layer: np.ndarray, geom: Geom, block_tables: np.ndarray, context_lens: np.ndarray,
-              scale: float, max_context_len: int | None = None, nthreads: int = 0):
-    """Paged decode over an 8-bit cache (values = code * scale), in fp64."""
+              scale: float, max_context_len: int | None = None, nthreads: int = 0, window: int = 0, ring: int = 0):
+    """Paged decode over an 8-bit cache (values = code * scale), in fp64; window /
+    ring as for ``decode`` (attended positions window_start(...) .. ctx - 1, block
+    j of a ring table at entry j % ring)."""
     assert layer.dtype == np.uint8 and geom.head_size == 128
     q = _u16(q)
     S, Hq, D = q.shape
@@ -307,8 +311,9 @@ def decode_i8(q: np.ndarray, layer: np.ndarray, geom: Geom, block_tables: np.nda
     if max_context_len is None:
         max_context_len = int(cl.max()) if cl.size else 0
     out = np.zeros((S, Hq, D))
-    err = _load().oracle_decode_i8(_ptr(out), _ptr(q), Hq * D, _ptr(layer), ctypes.byref(geom.c()), _ptr(bt),
-                                   bt.shape[1], _ptr(cl), S, Hq, max_context_len, scale, nthreads)
+    err = _load().oracle_decode_i8_window(_ptr(out), _ptr(q), Hq * D, _ptr(layer), ctypes.byref(geom.c()), _ptr(bt),
+                                          bt.shape[1], _ptr(cl), S, Hq, max_context_len, scale, window, ring,
+                                          nthreads)
     return out, err
 
 

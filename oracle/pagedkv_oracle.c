@@ -402,10 +402,13 @@ int oracle_reshape_and_cache_i8(uint8_t* layer, const oracle_geom* g, const uint
     return err;
 }
 
-int oracle_decode_i8(double* out, const uint16_t* q, int64_t q_seq_stride, const uint8_t* layer,
-                     const oracle_geom* g, const int32_t* block_tables, int32_t bt_stride,
-                     const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
-                     double scale, int32_t nthreads) {
+/* The 8-bit decode with the same attended set as oracle_decode_window:
+ * positions oracle_window_start(ctx, bs, window, ring) .. ctx - 1, logical
+ * block j found at table entry j % ring when ring > 0. */
+int oracle_decode_i8_window(double* out, const uint16_t* q, int64_t q_seq_stride, const uint8_t* layer,
+                            const oracle_geom* g, const int32_t* block_tables, int32_t bt_stride,
+                            const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t max_context_len, double scale, int32_t window, int32_t ring, int32_t nthreads) {
     const int32_t D = g->head_size;
     const int32_t G = num_q_heads / g->num_kv_heads;
     int err = 0;
@@ -419,20 +422,23 @@ int oracle_decode_i8(double* out, const uint16_t* q, int64_t q_seq_stride, const
         for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
         const int32_t ctx = context_lens[s];
         if (ctx <= 0) continue;
-        if ((int64_t)ctx > (int64_t)bt_stride * g->block_size || ctx > max_context_len) {
+        if ((ring <= 0 && (int64_t)ctx > (int64_t)bt_stride * g->block_size) || ctx > max_context_len) {
             err |= ORC_ERR_CONTEXT;
             continue;
         }
-        double* K = (double*)malloc(sizeof(double) * (size_t)ctx * D);
-        double* V = (double*)malloc(sizeof(double) * (size_t)ctx * D);
+        const int32_t t0 = oracle_window_start(ctx, g->block_size, window, ring);
+        const int32_t n = ctx - t0;
+        double* K = (double*)malloc(sizeof(double) * (size_t)n * D);
+        double* V = (double*)malloc(sizeof(double) * (size_t)n * D);
         double* qd = (double*)malloc(sizeof(double) * (size_t)D);
         int bad = 0;
-        for (int32_t t = 0; t < ctx && !bad; ++t) {
-            const int32_t block = block_tables[(int64_t)s * bt_stride + t / g->block_size];
+        for (int32_t t = t0; t < ctx && !bad; ++t) {
+            const int32_t j = t / g->block_size;
+            const int32_t block = block_tables[(int64_t)s * bt_stride + (ring > 0 ? j % ring : j)];
             if (block < 0 || block >= g->num_blocks) { bad = 1; break; }
             for (int32_t d = 0; d < D; ++d) {
-                K[(int64_t)t * D + d] = i8_value(layer, g, block, h / G, 0, t % g->block_size, d);
-                V[(int64_t)t * D + d] = i8_value(layer, g, block, h / G, 1, t % g->block_size, d);
+                K[(int64_t)(t - t0) * D + d] = i8_value(layer, g, block, h / G, 0, t % g->block_size, d);
+                V[(int64_t)(t - t0) * D + d] = i8_value(layer, g, block, h / G, 1, t % g->block_size, d);
             }
         }
         if (bad) {
@@ -440,13 +446,21 @@ int oracle_decode_i8(double* out, const uint16_t* q, int64_t q_seq_stride, const
         } else {
             for (int32_t d = 0; d < D; ++d)
                 qd[d] = elem_to_double(q[(int64_t)s * q_seq_stride + (int64_t)h * D + d], g->dtype);
-            oracle_contiguous_attention(qd, K, V, ctx, D, scale, o);
+            oracle_contiguous_attention(qd, K, V, n, D, scale, o);
         }
         free(K);
         free(V);
         free(qd);
     }
     return err;
+}
+
+int oracle_decode_i8(double* out, const uint16_t* q, int64_t q_seq_stride, const uint8_t* layer,
+                     const oracle_geom* g, const int32_t* block_tables, int32_t bt_stride,
+                     const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                     double scale, int32_t nthreads) {
+    return oracle_decode_i8_window(out, q, q_seq_stride, layer, g, block_tables, bt_stride, context_lens, num_seqs,
+                                   num_q_heads, max_context_len, scale, 0, 0, nthreads);
 }
 
 int oracle_copy_blocks_bytes(uint8_t* pool, int64_t block_bytes, int32_t num_blocks, int32_t num_layers,

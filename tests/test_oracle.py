@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from paged_helpers import NAN_BITS, Paged, bits_to_f64, to_bits
+from paged_helpers import NAN_BITS, Paged, RingPaged, bits_to_f64, to_bits
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -545,3 +545,35 @@ def test_prefill_error_cases():
     # a sequence with no new tokens contributes no rows
     got, err = oracle.prefill(qb[:5], p.pool, p.geom, p.tables[:2], p.ctx[:2], np.array([0, 5, 5], np.int32), 0.1)
     assert err == 0 and got.shape == (5, 4, 64)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("bs,W,exact", [(16, 40, True), (16, 40, False), (8, 100, True), (4, 9, True)])
+def test_i8_window_on_grid_values_equals_16bit_window(dtype, bs, W, exact):
+    # ring tables written token by token (older blocks overwritten): on values the
+    # 8-bit cache stores exactly, its window decode equals the pinned 16-bit window
+    # decode, and with an exact ring both equal attention over the last W tokens
+    rng = np.random.default_rng(33 + bs + W)
+    ring = -(-(W - 1) // bs) + 1 if exact else -(-W // bs)
+    ctx = [1, W - 1, W, W + 1, 3 * W + 5]
+    p = RingPaged(rng, S=len(ctx), Hq=8, Hkv=2, D=128, bs=bs, ctx=ctx, ring=ring, dtype=dtype)
+    g8 = oracle.Geom(p.num_blocks, bs, 2, 128, dtype)
+    pool8 = _i8_pool(g8, p.num_blocks)
+    p.pool[:] = 0
+    for s, c in enumerate(ctx):
+        codes = rng.integers(-127, 128, (2, c, 2, 128))
+        codes[:, :, :, 0] = 127
+        vals = codes * 2.0 ** -6
+        p.K[s], p.V[s] = vals[0], vals[1]
+        t = np.arange(c)
+        slots = p.tables[s, (t // bs) % ring].astype(np.int64) * bs + t % bs
+        kb, vb = to_bits(vals[0], dtype), to_bits(vals[1], dtype)
+        assert oracle.reshape_and_cache(p.pool, p.geom, kb, vb, slots) == 0
+        assert oracle.reshape_and_cache_i8(pool8, g8, kb, vb, slots) == 0
+    scale = 1 / math.sqrt(128)
+    ref, e1 = oracle.decode(p.q_bits, p.pool, p.geom, p.tables, p.ctx, scale, window=W, ring=ring)
+    got, e2 = oracle.decode_i8(p.q_bits, pool8, g8, p.tables, p.ctx, scale, window=W, ring=ring)
+    assert e1 == 0 and e2 == 0
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+    if exact:
+        assert np.allclose(got, p.expected_window(scale, W), rtol=1e-12, atol=1e-12)

@@ -196,8 +196,8 @@ int32_t pa_decode_partition_size(int32_t partition_size, int32_t max_context_len
  * multiple of num_kv_heads with group size 1, 2, 4 or 8, and 16 at head_size 128
  * with block_size >= 8 (PA_ERR_UNSUPPORTED otherwise).  An 8-bit cache
  * (PA_INT8_F16 / PA_INT8_BF16) attends over code * scale: head_size 128, group
- * size 1, 2, 4 or 8, any supported block_size; q and out are the dtype's 16-bit
- * type; pa_decode_window with window or ring_blocks > 0 is PA_ERR_UNSUPPORTED. */
+ * size 1, 2, 4 or 8, any supported block_size (windows and ring tables
+ * included); q and out are the dtype's 16-bit type. */
 pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,
                     const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
                     int32_t block_table_stride, const int32_t* context_lens, int32_t num_seqs,

@@ -235,8 +235,6 @@ pa_status pa_decode_window(void* out, const void* q, int64_t q_seq_stride, const
   if (desc->num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads > 65535");
   if (is_i8(desc) && group > 8)
     return fail(PA_ERR_UNSUPPORTED, "8-bit cache with %d query heads per kv head (supported: 1, 2, 4, 8)", group);
-  if (is_i8(desc) && (window > 0 || ring_blocks > 0))
-    return fail(PA_ERR_UNSUPPORTED, "8-bit cache with a window or ring tables");
   if (!out || !q || !kv_cache || !block_tables || !context_lens)
     return fail(PA_ERR_INVALID_ARG, "out, q, kv_cache, block_tables and context_lens must be non-NULL");
   if (!aligned16(out) || !aligned16(q) || !aligned16(kv_cache))

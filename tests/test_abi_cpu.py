@@ -194,8 +194,9 @@ def test_int8_decode_limits(lib):
     assert _decode(lib, desc=_desc(kv_int8=True, head_size=64)) == _lib.PA_ERR_UNSUPPORTED
     st = lib.pa_decode_window(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 4 * 128, ctypes.c_void_p(FAKE),
                               ctypes.byref(d8), 0, ctypes.c_void_p(FAKE), 8, ctypes.c_void_p(FAKE), 2, 4, 100,
-                              0.1, 64, 0, 0, None, 0, None, None)
-    assert st == _lib.PA_ERR_UNSUPPORTED                                    # no window over 8-bit caches
+                              0.1, -1, 0, 0, None, 0, None, None)
+    assert st == _lib.PA_ERR_INVALID_ARG                                    # windows over 8-bit caches are
+    #                                                                         validated like 16-bit ones
     # an 8-bit pool and a 16-bit pool are different geometries for swapping
     arr = np.array([[0, 1]], np.int64)
     st = lib.pa_swap_blocks(ctypes.c_void_p(FAKE), ctypes.byref(_desc()), ctypes.c_void_p(FAKE),

@@ -258,3 +258,41 @@ def test_full_size_step_matches_oracle(name):
                               max_context_len=w.max_context_len)
     assert e == 0
     assert_attention_close(out[torch.from_numpy(sel).cuda()], ref, name)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("bs,W,exact", [(16, 40, True), (16, 200, False), (8, 100, True), (1, 30, True)])
+def test_window_ring_decode_matches_oracle(bs, W, exact, G, dtype, kernel):
+    # sliding-window decode over an 8-bit cache whose ring tables were written
+    # token by token (older blocks overwritten; the pool starts as random bytes)
+    rng = np.random.default_rng(570 + bs * 10 + W + G)
+    ring = -(-(W - 1) // bs) + 1 if exact else -(-W // bs)
+    ctx = np.asarray([1, W - 1, W, W + 1, 3 * W + 5, 700, 0], np.int32)
+    S, Hkv = len(ctx), 2
+    nb = S * ring + 3
+    geom = oracle.Geom(nb, bs, Hkv, 128, dtype)
+    pool = rng.integers(0, 256, nb * oracle.i8_block_bytes(geom), dtype=np.uint8)
+    tables = rng.permutation(nb)[:S * ring].reshape(S, ring).astype(np.int32)
+    for s, c in enumerate(ctx):
+        if c == 0:
+            continue
+        t = np.arange(c)
+        slots = tables[s, (t // bs) % ring].astype(np.int64) * bs + t % bs
+        x = rng.standard_normal((2, c, Hkv, 128))
+        assert oracle.reshape_and_cache_i8(pool, geom, to_bits(x[0], dtype), to_bits(x[1], dtype), slots) == 0
+    q_bits = to_bits(rng.standard_normal((S, G * Hkv, 128)), dtype)
+    mx = int(ctx.max())
+    ref, e = oracle.decode_i8(q_bits, pool, geom, tables, ctx, 1 / math.sqrt(128), max_context_len=mx,
+                              window=W, ring=ring)
+    assert e == 0
+    q = u16_to_dev(q_bits, dtype)
+    out = torch.full_like(q, float("nan"))
+    span = pkv.decode_window_span(mx, bs, W, ring)
+    ws = torch.empty(max(pkv.decode_workspace_bytes(S, G * Hkv, 128, span, 128) // 4, 4), dtype=torch.float32,
+                     device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.decode_window(out, q, pool_to_dev(pool), i8_desc(nb, bs, Hkv, dtype), torch.from_numpy(tables).cuda(),
+                      torch.from_numpy(ctx).cuda(), mx, 1 / math.sqrt(128), W, ring, ws, 128, dev_err=err)
+    assert pkv.read_device_errors(err) == 0
+    assert_attention_close(out, ref, f"int8 window ({kernel}) bs={bs} W={W} ring={ring} G={G} {dtype}")

@@ -16,10 +16,11 @@
 // swizzle, written by the softmax warps) are the B operands; S^T and O^T
 // accumulate in fp32 in tensor memory (TMEM), double-buffered.
 //
-// One persistent CTA per SM walks a static round-robin share of the work items
-// (sequence, kv head, partition); the list of items is built in shared memory
-// from a prefix sum of partitions per sequence, so no CTA is spent on empty
-// partitions.  Roles:
+// One persistent CTA per SM walks a static share of the work items (sequence,
+// kv head, partition): every CTA builds the same list in shared memory -- full
+// partitions first, then the remainder partitions from the most tiles down --
+// and takes one item per round in snake order, so the CTAs get about the same
+// number of tiles and none is spent on empty partitions.  Roles:
 //   warp 0      producer: item walk, block-id validation, Q staging, one bulk
 //               copy per (block, kv head) chunk into a ring of NS 64 KiB stages;
 //               per-stage metadata travels with the stage's mbarrier.

@@ -104,16 +104,17 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, partition_size: int):
     """DRAM bytes per decode launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+    on the current kernel sources at this partition size (else None)."""
     path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_src = re.search(r"source_digest:\s*([0-9a-f]+)", text)
     m_val = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not (m_src and m_val) or m_src.group(1) != source_digest():
+    m_part = re.search(r"partition_size:\s*([0-9]+)", text)
+    if not (m_src and m_val and m_part) or m_src.group(1) != source_digest() or int(m_part.group(1)) != partition_size:
         return None
     return float(m_val.group(1))
 
@@ -429,6 +430,7 @@ def run_gpu(args):
     dec_ms = float(np.mean(decode_ms))
     achieved = nbytes["decode"] / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
+    part = _lib.decode_partition_size(step.desc, w.cfg.num_seqs, w.max_context_len, args.partition_size)
 
     line = None
     if rank == 0:
@@ -445,7 +447,7 @@ def run_gpu(args):
             "config": {"workload": DESCRIPTIONS[args.workload] + (f" (first {args.seqs} sequences)" if args.seqs else ""),
                        "global_batch": w.cfg.num_seqs * world,
                        "max_context_len": w.max_context_len, "tokens_in_context": int(w.context_lens_np.sum()),
-                       "partition_size": _lib.decode_partition_size(args.partition_size, w.max_context_len),
+                       "partition_size": part,
                        "parallelism": f"replicas{world}",
                        "l2": f"inputs larger than L2: {step.kv_cache.numel() * step.kv_cache.element_size() / 1e9:.2f} GB pool, "
                              f"{nbytes['decode_kv'] / 1e9:.2f} GB of KV read per step"},
@@ -456,7 +458,7 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "kernel": "pa_decode (decode + log-sum-exp merge)",
                          "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                         "traffic": recorded_traffic(args.workload),
+                         "traffic": recorded_traffic(args.workload, part),
                          "decode_ms": round(dec_ms, 4)},
             "cpu_baseline": cpu,
             "e2e": {"value": round(world * nbytes["total"] / (e2e_ms / K * 1e-3) / 1e9, 2), "unit": "GB/s",

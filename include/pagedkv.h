@@ -160,14 +160,28 @@ pa_status pa_reshape_and_cache(void* kv_cache, const pa_cache_desc* desc, int32_
                                int32_t num_tokens, uint32_t* dev_err, void* stream);
 
 /* Workspace bytes pa_decode needs for these shapes (0 when no sequence can span
- * more than one partition).  partition_size 0 selects the default
- * (pa_decode_partition_size). */
-size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
+ * more than one partition, or desc is NULL).  partition_size 0 selects the
+ * default (pa_decode_partition_size with the same desc, num_seqs and
+ * max_context_len). */
+size_t pa_decode_workspace_bytes(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_q_heads,
                                  int32_t max_context_len, int32_t partition_size);
 
-/* The partition size pa_decode uses: `partition_size` itself when > 0, else the
- * default for this max_context_len (512 tokens, or 1024 above 32768 tokens). */
-int32_t pa_decode_partition_size(int32_t partition_size, int32_t max_context_len);
+/* The partition size pa_decode uses: `partition_size` itself when > 0, else a
+ * default that depends on the kernel these shapes get.
+ *   Tensor-core kernel (head_size 128 and either a 16-bit cache with
+ *   block_size >= 8 and at most 8192 sequences, or an 8-bit cache with at most
+ *   1024 sequences): it walks work items of one (sequence, kv head, partition),
+ *   and the default is the longest of 4096, 2048, 1024 and 512 tokens (8192
+ *   first when max_context_len > 32768) for which
+ *     num_seqs * num_kv_heads * ceil(max_context_len / P) >= 912
+ *   (six items per SM of a 152-SM GPU), else 512.  Longer partitions write and
+ *   merge fewer partial results; shorter ones split the work finely enough to
+ *   keep every SM busy to the end.
+ *   CUDA-core kernel (the other shapes): 512, or 1024 when max_context_len >
+ *   32768.
+ * desc NULL gives 512. */
+int32_t pa_decode_partition_size(const pa_cache_desc* desc, int32_t num_seqs, int32_t max_context_len,
+                                 int32_t partition_size);
 
 /* Paged decode attention: one query token per sequence.
  * For sequence s and query head h (kv head = h / (num_q_heads / num_kv_heads)):
@@ -250,7 +264,7 @@ pa_status pa_prefill(void* out, const void* q, int64_t q_token_stride, const voi
  *                The window is exact when ring_blocks >= ceil((window-1)/bs) + 1.
  *                0: linear rows (then ctx must fit the row, as in pa_decode).
  * Other arguments as pa_decode; size the workspace with
- * pa_decode_workspace_bytes(num_seqs, num_q_heads, head_size,
+ * pa_decode_workspace_bytes(desc, num_seqs, num_q_heads,
  * pa_decode_window_span(max_context_len, block_size, window, ring_blocks),
  * partition_size).  pa_decode is this call with window = ring_blocks = 0. */
 pa_status pa_decode_window(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,

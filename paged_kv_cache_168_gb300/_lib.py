@@ -90,9 +90,9 @@ def load():
     lib.pa_cache_scale_offset.restype = i64
     lib.pa_reshape_and_cache.argtypes = [P, D, i32, P, i64, P, i64, P, i32, P, P]
     lib.pa_reshape_and_cache.restype = ctypes.c_int
-    lib.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    lib.pa_decode_workspace_bytes.argtypes = [D, i32, i32, i32, i32]
     lib.pa_decode_workspace_bytes.restype = sz
-    lib.pa_decode_partition_size.argtypes = [i32, i32]
+    lib.pa_decode_partition_size.argtypes = [D, i32, i32, i32]
     lib.pa_decode_partition_size.restype = i32
     lib.pa_decode.argtypes = [P, P, i64, P, D, i32, P, i32, P, i32, i32, i32, ctypes.c_float, i32, P, sz, P, P]
     lib.pa_decode.restype = ctypes.c_int
@@ -194,13 +194,14 @@ def reshape_and_cache(kv_cache: torch.Tensor, desc: CacheDesc, key: torch.Tensor
                                        _stream(stream)))
 
 
-def decode_partition_size(partition_size: int = 0, max_context_len: int = 0) -> int:
-    return load().pa_decode_partition_size(partition_size, max_context_len)
+def decode_partition_size(desc: CacheDesc, num_seqs: int, max_context_len: int, partition_size: int = 0) -> int:
+    return load().pa_decode_partition_size(ctypes.byref(desc.c()), num_seqs, max_context_len, partition_size)
 
 
-def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_size: int, max_context_len: int,
+def decode_workspace_bytes(desc: CacheDesc, num_seqs: int, num_q_heads: int, max_context_len: int,
                            partition_size: int = 0) -> int:
-    return load().pa_decode_workspace_bytes(num_seqs, num_q_heads, head_size, max_context_len, partition_size)
+    return load().pa_decode_workspace_bytes(ctypes.byref(desc.c()), num_seqs, num_q_heads, max_context_len,
+                                            partition_size)
 
 
 def decode(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor, desc: CacheDesc,

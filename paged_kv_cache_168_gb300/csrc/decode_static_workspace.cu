@@ -58,9 +58,7 @@ extern "C" pa_status pa_decode_static_workspace(void* out, const void* q, int64_
                                                 const int32_t* context_lens, int32_t num_seqs,
                                                 int32_t num_q_heads, int32_t max_context_len, float scale,
                                                 int32_t partition_size, uint32_t* dev_err, void* stream) {
-  const int32_t head_size = desc ? desc->head_size : 0;
-  const size_t need =
-      pa_decode_workspace_bytes(num_seqs, num_q_heads, head_size, max_context_len, partition_size);
+  const size_t need = pa_decode_workspace_bytes(desc, num_seqs, num_q_heads, max_context_len, partition_size);
   if (need > (size_t)PA_STATIC_WORKSPACE_BYTES) {
     // Same status as pa_decode with a too-small workspace; nothing is launched.
     pkv::set_last_error(

@@ -64,6 +64,9 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kTile = 128;                         // tokens per tile
+// Remainder-partition classes (tiles in the remainder): 1 .. P / kTile, and P is
+// at most 8192 tokens; a larger class (only a larger P) shares the top slot.
+constexpr int kClasses = 8192 / kTile + 1;
 constexpr int kTileBytes = kTile * 2 * kD * 2;     // K + V of 128 tokens: 64 KiB
 constexpr int kGroupBytes = 8 * 2 * kD * 2;        // one 8-token group: 4 KiB
 constexpr int kN = 16;                             // MMA N: query heads, zero-padded
@@ -127,7 +130,7 @@ struct Shared {
   uint32_t tmem_base;
   volatile int abort_flag;
   volatile int end_tile;          // QK issuer -> PV issuer: tiles in this CTA (set at the end)
-  int cls_cnt[64], cls_cur[64];   // item ordering: remainder partitions per class, placement cursors
+  int cls_cnt[kClasses], cls_cur[kClasses];   // item ordering: remainder partitions per class, cursors
   // 8-bit caches: producer -> converter ring of raw half tiles, and the token
   // scales of each converted stage
   // (two rings of NRH slots, one per 64-token half: slot h * NRH + k % NRH)
@@ -176,8 +179,9 @@ __device__ __forceinline__ bool ctx_invalid(const DecodeParams& p, int ctx) { re
 // Work items of one sequence: its partitions, or one item that only writes zeros.
 // A sequence's work: F full partitions (P / 128 tiles each) and, if the
 // attended length is not a multiple of P, one remainder partition of
-// ceil(rem / 128) tiles (its "class", 1 .. P / 128 - 1).  A sequence with no
-// (or an invalid) context is one remainder item of class 1 that writes zeros.
+// ceil(rem / 128) tiles (its "class", 1 .. P / 128: a remainder of P - 1 tokens
+// has P / 128 tiles).  A sequence with no (or an invalid) context is one
+// remainder item of class 1 that writes zeros.
 __device__ __forceinline__ void work_of(const DecodeParams& p, int ctx, int& full, int& cls) {
   if (ctx <= 0 || ctx_invalid(p, ctx)) {
     full = 0;
@@ -187,7 +191,7 @@ __device__ __forceinline__ void work_of(const DecodeParams& p, int ctx, int& ful
   const int len = ctx - attended_from(p, ctx);
   full = len / p.partition_size;
   const int rem = len - full * p.partition_size;
-  cls = (rem + kTile - 1) / kTile;
+  cls = min((rem + kTile - 1) / kTile, kClasses - 1);
 }
 
 template <typename T, int G>
@@ -273,7 +277,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
     pre[i + 1] = full;
     rcls[i] = (uint8_t)cls;
   }
-  for (int i = threadIdx.x; i < 64; i += blockDim.x) sh.cls_cnt[i] = 0;
+  for (int i = threadIdx.x; i < kClasses; i += blockDim.x) sh.cls_cnt[i] = 0;
   if (warp == 1) {
     tc::tmem_alloc(&sh.tmem_base, kCols);
     tc::tmem_relinquish();
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
     __syncwarp();
     if (lane == 0) {
       int at = 0;
-      for (int c = 63; c >= 1; --c) {
+      for (int c = kClasses - 1; c >= 1; --c) {
         sh.cls_cur[c] = at;
         at += sh.cls_cnt[c];
       }

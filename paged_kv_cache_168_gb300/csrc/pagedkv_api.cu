@@ -32,7 +32,18 @@ pa_status cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-constexpr int kDefaultPartition = 512;
+// Default partition sizes for the tensor-core kernels: the shortest, the longest
+// for contexts up to kLongContext tokens, the longest beyond, and the work items
+// (sequence, kv head, partition) wanted before a longer partition is taken -- six
+// per SM of a 152-SM GB300, below which the persistent kernels' last wave leaves
+// SMs idle (a sweep of 512..8192 tokens on the 7B, 8B, 70B and beam decode
+// shapes, 16- and 8-bit).  The CUDA-core kernel, one CTA per item, keeps 512
+// (1024 past kLongContext): longer partitions leave it too few CTAs.
+constexpr int kMinPartition = 512;
+constexpr int kMaxPartition = 4096;
+constexpr int kMaxLongPartition = 8192;
+constexpr int kLongContext = 32768;
+constexpr int64_t kMinItems = 6 * 152;
 
 // Kernel choice: the tensor-core kernel serves head_size 128 (group sizes 1-16,
 // up to pkv::kTcMaxSeqs sequences); the CUDA-core kernel serves the rest.  The
@@ -47,6 +58,14 @@ bool use_tensor_cores(int head_size, int block_size, int group, int num_seqs) {
 }
 
 bool is_i8(const pa_cache_desc* d) { return d->dtype == PA_INT8_F16 || d->dtype == PA_INT8_BF16; }
+
+// Whether these shapes get a tensor-core kernel by default (the environment
+// switch aside): 16-bit caches as use_tensor_cores; 8-bit caches at head_size
+// 128 up to pkv::kTcI8MaxSeqs sequences, any block size.
+bool tc_by_default(const pa_cache_desc* d, int num_seqs) {
+  if (d->head_size != 128) return false;
+  return is_i8(d) ? num_seqs <= pkv::kTcI8MaxSeqs : d->block_size >= 8 && num_seqs <= pkv::kTcMaxSeqs;
+}
 
 // 16-bit type of q, key, value and out (and of a 16-bit cache).
 int act_dtype(const pa_cache_desc* d) { return d->dtype == PA_INT8_BF16 || d->dtype == PA_BF16 ? PA_BF16 : PA_F16; }
@@ -190,16 +209,28 @@ pa_status pa_reshape_and_cache(void* kv_cache, const pa_cache_desc* desc, int32_
   return e == cudaSuccess ? PA_OK : cuda_fail(e, "reshape_and_cache launch");
 }
 
-int32_t pa_decode_partition_size(int32_t partition_size, int32_t max_context_len) {
+int32_t pa_decode_partition_size(const pa_cache_desc* desc, int32_t num_seqs, int32_t max_context_len,
+                                 int32_t partition_size) {
   if (partition_size > 0) return partition_size;
-  // Long contexts use longer partitions: each partition writes (D + 2) floats per
-  // query head, which at 8 query heads per kv head is 2G/P of the KV bytes.
-  return max_context_len > 32768 ? 2 * kDefaultPartition : kDefaultPartition;
+  if (!desc || !tc_by_default(desc, num_seqs))
+    return desc && max_context_len > kLongContext ? 2 * kMinPartition : kMinPartition;
+  // Each partition writes (D + 2) floats per query head and the merge reads them
+  // back, so longer partitions cost less -- until one item is so long that the
+  // kernel's tail runs on a few SMs.  Long contexts have the per-SM work to
+  // hide an 8192-token item; with contexts of at most 32768 tokens an item
+  // stays at most 4096 tokens long.
+  const int64_t pairs = (int64_t)(num_seqs > 0 ? num_seqs : 0) * (desc->num_kv_heads > 0 ? desc->num_kv_heads : 0);
+  const int64_t ctx = max_context_len > 0 ? max_context_len : 0;
+  for (int P = max_context_len > kLongContext ? kMaxLongPartition : kMaxPartition; P > kMinPartition; P /= 2)
+    if (pairs * ((ctx + P - 1) / P) >= kMinItems) return P;
+  return kMinPartition;
 }
 
-size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
+size_t pa_decode_workspace_bytes(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_q_heads,
                                  int32_t max_context_len, int32_t partition_size) {
-  const int64_t P = pa_decode_partition_size(partition_size, max_context_len);
+  if (!desc) return 0;
+  const int64_t P = pa_decode_partition_size(desc, num_seqs, max_context_len, partition_size);
+  const int64_t head_size = desc->head_size;
   if (num_seqs <= 0 || num_q_heads <= 0 || head_size <= 0 || max_context_len <= 0 || P <= 0) return 0;
   const int64_t parts = (max_context_len + P - 1) / P;
   if (parts <= 1) return 0;
@@ -250,11 +281,11 @@ pa_status pa_decode_window(void* out, const void* q, int64_t q_seq_stride, const
     return fail(PA_ERR_INVALID_ARG, "ring_blocks %d not in [0, block_table_stride %d]", ring_blocks,
                 block_table_stride);
   const int32_t span = pa_decode_window_span(max_context_len, desc->block_size, window, ring_blocks);
-  const int32_t P = pa_decode_partition_size(partition_size, span);
+  const int32_t P = pa_decode_partition_size(desc, num_seqs, span, partition_size);
   if (P % 128 || P < 128 || P > 8192)
     return fail(PA_ERR_INVALID_ARG, "partition_size %d must be a multiple of 128 in [128, 8192]", P);
   if (!(scale > 0.f) || scale != scale) return fail(PA_ERR_INVALID_ARG, "scale must be a positive number");
-  const size_t need = pa_decode_workspace_bytes(num_seqs, num_q_heads, desc->head_size, span, P);
+  const size_t need = pa_decode_workspace_bytes(desc, num_seqs, num_q_heads, span, P);
   if (workspace_bytes < need)
     return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", workspace_bytes, need);
   if (need && (!workspace || !aligned16(workspace)))

@@ -35,7 +35,7 @@ class DecodeStep:
             self.kv_cache = w.kv_cache
         self.partition_size = partition_size
         self.out = torch.empty_like(w.q)
-        nbytes = _lib.decode_workspace_bytes(cfg.num_seqs, cfg.num_q_heads, cfg.head_size, w.max_context_len,
+        nbytes = _lib.decode_workspace_bytes(self.desc, cfg.num_seqs, cfg.num_q_heads, w.max_context_len,
                                              partition_size)
         self.workspace = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device=dev)
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -86,7 +86,7 @@ class DecodeStep:
             n += -(-w.swap_out_pairs.shape[0] // per) + -(-w.swap_in_pairs.shape[0] // per)
         if w.copy_pairs.shape[0]:
             n += -(-w.copy_pairs.shape[0] // per)
-        P = _lib.decode_partition_size(self.partition_size, w.max_context_len)
+        P = _lib.decode_partition_size(self.desc, cfg.num_seqs, w.max_context_len, self.partition_size)
         n += 1 + (1 if -(-w.max_context_len // P) > 1 else 0)   # decode (+ merge)
         return n
 

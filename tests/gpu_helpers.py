@@ -50,7 +50,7 @@ def desc_of(num_blocks, bs, Hkv, D, dtype, num_layers=1, layer_stride_bytes=0):
 def run_decode(q, pool, desc, tables, ctx, max_ctx, scale, P=0, dev_err=None):
     S, Hq, D = q.shape
     out = torch.full_like(q, float("nan"))
-    nbytes = pkv.decode_workspace_bytes(S, Hq, D, max_ctx, P)
+    nbytes = pkv.decode_workspace_bytes(desc, S, Hq, max_ctx, P)
     ws = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device=q.device)
     pkv.decode(out, q, pool, desc, tables, ctx, max_ctx, scale, ws, P, dev_err=dev_err)
     return out

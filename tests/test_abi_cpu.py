@@ -63,13 +63,40 @@ def test_library_layout_agrees_with_oracle_layout(lib, bs, D, dtype):
     assert _lib.cache_element_offset(d, 0, 0, 2, 0, 0) == -1
 
 
+def test_default_partition_size(lib):
+    def ps(num_seqs, num_kv_heads, max_ctx, P=0, bs=16, D=128, kv_int8=False):
+        return _lib.decode_partition_size(CacheDesc(100, bs, num_kv_heads, D, kv_int8=kv_int8), num_seqs, max_ctx, P)
+    assert ps(8, 8, 131072, P=256) == 256                 # an explicit size is kept
+    # tensor-core shapes: the longest partition that still gives >= 912
+    # (sequence, kv head, partition) items
+    assert ps(64, 32, 4096) == 4096                       # 2048 pairs: one partition each
+    assert ps(128, 8, 2304) == 4096                       # 1024 pairs
+    assert ps(256, 8, 8192) == 4096                       # capped at 4096 up to 32768 tokens
+    assert ps(8, 8, 131072) == 8192                       # 64 pairs x 16 partitions
+    assert ps(8, 8, 120000) == 8192                       # 64 x 15 = 960
+    assert ps(8, 8, 16384) == 1024                        # 64 x 16 = 1024; 2048 gives 512
+    assert ps(8, 8, 32768) == 2048                        # not long: the cap stays 4096
+    assert ps(1, 8, 4096) == 512                          # too few items at any size: the shortest
+    assert ps(0, 8, 4096) == 512 and ps(64, 8, 0) == 512
+    assert ps(256, 8, 8192, bs=1, kv_int8=True) == 4096   # 8-bit caches: tensor cores at any block size
+    assert ps(2000, 8, 8192, kv_int8=True) == 512         # beyond 1024 sequences: CUDA-core kernel
+    # CUDA-core shapes keep 512 (1024 past 32768 tokens)
+    assert ps(64, 32, 4096, bs=1) == 512 and ps(64, 32, 4096, D=64) == 512
+    assert ps(8, 8, 131072, bs=4) == 1024
+    assert _lib.load().pa_decode_partition_size(None, 64, 4096, 0) == 512
+
+
 def test_workspace_sizing(lib):
-    assert _lib.decode_partition_size(0, 4096) == 512 and _lib.decode_partition_size(0, 131072) == 1024
-    assert _lib.decode_partition_size(256, 131072) == 256
-    assert _lib.decode_workspace_bytes(64, 32, 128, 512) == 0        # one partition: no workspace
-    assert _lib.decode_workspace_bytes(64, 32, 128, 4096) == 64 * 32 * 8 * 130 * 4
-    assert _lib.decode_workspace_bytes(8, 64, 128, 131072, 1024) == 8 * 64 * 128 * 130 * 4
-    assert _lib.decode_workspace_bytes(8, 64, 128, 131072) == 8 * 64 * 128 * 130 * 4
+    def wb(S, Hq, Hkv, D, max_ctx, P=0, bs=16):
+        return _lib.decode_workspace_bytes(CacheDesc(100, bs, Hkv, D), S, Hq, max_ctx, P)
+    assert wb(64, 32, 32, 128, 512, 512) == 0             # one partition: no workspace
+    assert wb(64, 32, 32, 128, 4096) == 0                  # the default is one 4096-token partition here
+    assert wb(64, 32, 32, 128, 4096, bs=1) == 64 * 32 * 8 * 130 * 4   # CUDA-core kernel: 512
+    assert wb(64, 32, 32, 128, 4096, 512) == 64 * 32 * 8 * 130 * 4
+    assert wb(8, 64, 8, 128, 131072, 1024) == 8 * 64 * 128 * 130 * 4
+    assert wb(8, 64, 8, 128, 131072) == 8 * 64 * 16 * 130 * 4
+    assert wb(8, 64, 8, 64, 16384) == 8 * 64 * 32 * 66 * 4
+    assert _lib.load().pa_decode_workspace_bytes(None, 8, 64, 16384, 512) == 0
 
 
 def test_status_strings(lib):

@@ -35,11 +35,12 @@ def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "source_digest", lambda: "abc123")
     (tmp_path / "profiles" / "decode_7b_traffic.md").write_text(
-        "traffic_bytes_per_launch: 2.5e9\nsource_digest: abc123\n")
-    assert bench.recorded_traffic("7b") == 2.5e9
+        "traffic_bytes_per_launch: 2.5e9\nsource_digest: abc123\npartition_size: 4096\n")
+    assert bench.recorded_traffic("7b", 4096) == 2.5e9
+    assert bench.recorded_traffic("7b", 512) is None            # taken at another partition size
     monkeypatch.setattr(bench, "source_digest", lambda: "changed")
-    assert bench.recorded_traffic("7b") is None
-    assert bench.recorded_traffic("8b") is None
+    assert bench.recorded_traffic("7b", 4096) is None
+    assert bench.recorded_traffic("8b", 4096) is None
 
 
 def test_oracle_baseline_on_tiny_workload():

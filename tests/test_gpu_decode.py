@@ -86,6 +86,16 @@ def test_partition_size_does_not_change_the_result(P, kernel):
     check(p, P=P, what=f"P={P}")
 
 
+@pytest.mark.parametrize("P", [4096, 8192])
+def test_remainders_of_every_length_class(P, kernel):
+    # remainder partitions of P - 1 tokens have P / 128 tiles: the top class of
+    # the tensor-core kernel's longest-first item order
+    rng = np.random.default_rng(230 + P // 1024)
+    ctx = [P - 1, 2 * P - 1, P - 127, P - 128, P - 129, P + 1, 1, P, 3 * P - 5]
+    p = Paged(rng, S=len(ctx), Hq=8, Hkv=2, D=128, bs=16, ctx=ctx, dtype="bf16")
+    check(p, P=P, what=f"remainder classes P={P}")
+
+
 def test_tiny_config_end_to_end():
     w = pytest.importorskip("paged_kv_cache_168_gb300.workloads").make_workload("tiny", device="cuda",
                                                                                 nan_unused=True)

@@ -84,8 +84,8 @@ class Engine:
         out = torch.empty((len(sids), HQ, D), dtype=torch.bfloat16, device="cuda")
         mx = int(ctx.max())
         span = pkv.decode_window_span(mx, BS, window, ring)
-        ws = torch.empty(max(pkv.decode_workspace_bytes(len(sids), HQ, D, span, 128) // 4, 4), dtype=torch.float32,
-                         device="cuda")
+        nbytes = pkv.decode_workspace_bytes(self.desc, len(sids), HQ, span, 128)
+        ws = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device="cuda")
         pkv.decode_window(out, u16_to_dev(q, DT), self.dev_pool, self.desc, torch.from_numpy(tables).cuda(),
                           torch.from_numpy(ctx).cuda(), mx, scale, window, ring, ws, 128)
         assert_attention_close(out, ref, "engine step")

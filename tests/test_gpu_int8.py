@@ -137,9 +137,10 @@ class I8Case:
         mx = max(int(self.ctx.max()), 1)
         q = u16_to_dev(self.q_bits, self.dtype)
         out = torch.full_like(q, float("nan"))
-        ws = torch.empty(max(pkv.decode_workspace_bytes(self.S, self.Hq, 128, mx, P) // 4, 4), dtype=torch.float32,
-                         device="cuda")
-        pkv.decode(out, q, pool_to_dev(self.pool), i8_desc(self.nb, self.bs, self.Hkv, self.dtype),
+        desc = i8_desc(self.nb, self.bs, self.Hkv, self.dtype)
+        nbytes = pkv.decode_workspace_bytes(desc, self.S, self.Hq, mx, P)
+        ws = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device="cuda")
+        pkv.decode(out, q, pool_to_dev(self.pool), desc,
                    torch.from_numpy(tables).cuda(), torch.from_numpy(self.ctx).cuda(), mx, 1 / math.sqrt(128), ws, P,
                    dev_err=err)
         return out
@@ -165,14 +166,25 @@ def test_decode_matches_oracle(bs, G, dtype, kernel):
     assert_attention_close(out, ref, f"int8 decode ({kernel}) bs={bs} G={G} {dtype}")
 
 
-@pytest.mark.parametrize("P", [128, 256, 1024])
+@pytest.mark.parametrize("P", [128, 256, 1024, 4096, 8192])
 def test_decode_partition_sizes(P, kernel):
     rng = np.random.default_rng(540 + P)
-    ctx = [129, 3000, 1024, 1025, 7]
+    ctx = [129, 3000, 1024, 1025, 7, 9000]
     case = I8Case(rng, len(ctx), 8, 2, 16, ctx, "bf16")
     ref, e = case.expected()
     assert e == 0
     assert_attention_close(case.run(P=P), ref, f"int8 decode P={P}")
+
+
+def test_decode_remainders_of_every_length_class(kernel):
+    # a remainder of P - 1 tokens has P / 128 tiles: the top ordering class
+    P = 8192
+    rng = np.random.default_rng(545)
+    ctx = [P - 1, 2 * P - 1, P - 127, P - 129, 3, P]
+    case = I8Case(rng, len(ctx), 8, 2, 16, ctx, "f16")
+    ref, e = case.expected()
+    assert e == 0
+    assert_attention_close(case.run(P=P), ref, "int8 decode, remainder classes")
 
 
 def test_decode_bad_block_id_zeroes_the_item(kernel):
@@ -289,8 +301,8 @@ def test_window_ring_decode_matches_oracle(bs, W, exact, G, dtype, kernel):
     q = u16_to_dev(q_bits, dtype)
     out = torch.full_like(q, float("nan"))
     span = pkv.decode_window_span(mx, bs, W, ring)
-    ws = torch.empty(max(pkv.decode_workspace_bytes(S, G * Hkv, 128, span, 128) // 4, 4), dtype=torch.float32,
-                     device="cuda")
+    nbytes = pkv.decode_workspace_bytes(i8_desc(nb, bs, Hkv, dtype), S, G * Hkv, span, 128)
+    ws = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     pkv.decode_window(out, q, pool_to_dev(pool), i8_desc(nb, bs, Hkv, dtype), torch.from_numpy(tables).cuda(),
                       torch.from_numpy(ctx).cuda(), mx, 1 / math.sqrt(128), W, ring, ws, 128, dev_err=err)

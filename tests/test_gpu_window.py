@@ -38,7 +38,7 @@ def run_window(p, window, ring, P=0, max_ctx=None, dev_err=None):
     ctx = torch.from_numpy(p.ctx).cuda()
     desc = desc_of(p.num_blocks, p.bs, p.Hkv, p.D, p.dtype)
     span = pkv.decode_window_span(max_ctx, p.bs, window, ring)
-    nbytes = pkv.decode_workspace_bytes(p.S, p.Hq, p.D, span, P)
+    nbytes = pkv.decode_workspace_bytes(desc, p.S, p.Hq, span, P)
     ws = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device="cuda")
     out = torch.full_like(q, float("nan"))
     pkv.decode_window(out, q, pool, desc, tables, ctx, max_ctx, 1 / math.sqrt(p.D), window, ring, ws, P,

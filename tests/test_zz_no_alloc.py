@@ -41,7 +41,7 @@ def test_static_workspace_matches_caller_workspace_on_two_calls():
     for p, (q, pool, tables, ctx, desc) in cases:          # two calls in a row, different data
         max_ctx = int(p.ctx.max())
         scale = 1 / math.sqrt(p.D)
-        need = pkv.decode_workspace_bytes(p.S, p.Hq, p.D, max_ctx, P)
+        need = pkv.decode_workspace_bytes(desc, p.S, p.Hq, max_ctx, P)
         assert 0 < need <= pkv._lib.STATIC_WORKSPACE_BYTES     # the shared array is really used
         ref = run_decode(q, pool, desc, tables, ctx, max_ctx, scale, P)
         out = torch.full_like(q, float("nan"))
@@ -54,13 +54,13 @@ def test_static_workspace_matches_caller_workspace_on_two_calls():
 
 def test_static_workspace_refuses_shapes_beyond_its_size():
     S, Hq, D, max_ctx, P = 2048, 64, 128, 8192, 128
-    assert pkv.decode_workspace_bytes(S, Hq, D, max_ctx, P) > pkv._lib.STATIC_WORKSPACE_BYTES
+    desc = pkv.CacheDesc(1, 16, 8, D, torch.float16)
+    assert pkv.decode_workspace_bytes(desc, S, Hq, max_ctx, P) > pkv._lib.STATIC_WORKSPACE_BYTES
     q = torch.zeros((S, Hq, D), dtype=torch.float16, device="cuda")
     out = torch.zeros_like(q)
     pool = torch.zeros(8 * 2 * 16 * D, dtype=torch.float16, device="cuda")
     tables = torch.zeros((S, 1), dtype=torch.int32, device="cuda")
     ctx = torch.zeros(S, dtype=torch.int32, device="cuda")     # even if launched, nothing would be read
-    desc = pkv.CacheDesc(1, 16, 8, D, torch.float16)
     with pytest.raises(pkv.PagedKVError) as e:
         pkv._lib.decode_static_workspace(out, q, pool, desc, tables, ctx, max_ctx, 0.088, P)
     assert e.value.status == pkv.PA_ERR_WORKSPACE_TOO_SMALL

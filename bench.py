@@ -10,7 +10,7 @@ already in HBM when the timed region starts.  Prints one JSON line.
 value  = algorithmic bytes of the step / device time of the step, GB/s (whole job).
 e2e    = the same, through the C ABI with host buffers: every step copies the
          step's inputs (q, new K/V, block tables, context lengths, slot mapping)
-         from pinned host memory and the output back, inside the timed region.
+         from one pinned host buffer and the output back, inside the timed region.
 roofline = the decode launch (pa_decode: decode kernel + merge kernel) against the
          measured HBM copy bandwidth.
 --impl reference times the fp64 CPU oracle (the correctness reference) on a
@@ -199,6 +199,32 @@ def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+class HostInputs:
+    """A step's inputs packed into one pinned host buffer, so each end-to-end step
+    moves them with one host->device copy (small copies each pay the link's
+    latency); on the device each input is a view of one staging buffer, every
+    view 256-byte aligned."""
+
+    def __init__(self, w, names, device):
+        offs, at = {}, 0
+        for k in names:
+            t = getattr(w, k)
+            offs[k] = at
+            at += -(-t.numel() * t.element_size() // 256) * 256
+        self.host = torch.zeros(at, dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(at, dtype=torch.uint8, device=device)
+        self.views = {}
+        for k in names:
+            t = getattr(w, k).contiguous()
+            n = t.numel() * t.element_size()
+            self.host[offs[k]:offs[k] + n].copy_(t.reshape(-1).view(torch.uint8).cpu())
+            self.views[k] = self.dev[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
+        self.nbytes = at
+
+    def upload(self):
+        self.dev.copy_(self.host, non_blocking=True)
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -393,19 +419,17 @@ def run_gpu(args):
     assert _lib.read_device_errors(step.dev_err, stream=stream) == 0, "device error during timed steps"
 
     # ---- end to end through the C ABI with host buffers
-    host_in = {k: getattr(w, k).cpu().pin_memory() for k in
-               ("q", "key", "value", "block_tables", "context_lens", "slot_mapping")}
-    dev_in = {k: torch.empty_like(getattr(w, k)) for k in host_in}
+    names = ("q", "key", "value", "block_tables", "context_lens", "slot_mapping")
+    staged = HostInputs(w, names, device)
     host_out = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d = staged.nbytes
     d2h = host_out.numel() * host_out.element_size()
-    saved = {k: getattr(w, k) for k in host_in}
-    for k in host_in:
-        setattr(w, k, dev_in[k])
+    saved = {k: getattr(w, k) for k in names}
+    for k in names:
+        setattr(w, k, staged.views[k])
 
     def e2e_step():
-        for k in host_in:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
+        staged.upload()
         step()
         host_out.copy_(step.out, non_blocking=True)
 
@@ -557,18 +581,16 @@ def run_gpu_prefill(args):
 
     # end to end with host buffers: inputs in, output back, every step
     names = ("q", "key", "value", "block_tables", "context_lens", "query_start_loc", "slot_mapping")
-    host_in = {k: getattr(w, k).cpu().pin_memory() for k in names}
-    dev_in = {k: torch.empty_like(getattr(w, k)) for k in names}
+    staged = HostInputs(w, names, device)
     host_out = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d = staged.nbytes
     d2h = host_out.numel() * host_out.element_size()
     saved = {k: getattr(w, k) for k in names}
     for k in names:
-        setattr(w, k, dev_in[k])
+        setattr(w, k, staged.views[k])
 
     def e2e_step():
-        for k in names:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
+        staged.upload()
         step()
         host_out.copy_(step.out, non_blocking=True)
 

@@ -407,7 +407,8 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       const int jb = t0 / bs;
       const int nblk = (t1 - t0 + bs - 1) / bs;
       bool bad = lane < nblk && (id_lane < 0 || id_lane >= p.num_blocks);
-      for (int b = lane + 32; b < nblk; b += 32) {
+#pragma unroll 4
+      for (int b = lane + 32; b < nblk; b += 32) {   // unrolled: several loads in flight
         const int id = row[table_index(jb + b, p.ring_blocks)];
         bad |= (id < 0 || id >= p.num_blocks);
       }
@@ -514,6 +515,16 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
         if (aborted) break;
         ++tile_seq;
       }
+      // 16-bit: the block id of this lane's chunk of tile k.  The item's first 32
+      // come from the prefetched id_lane; a later one is loaded a tile ahead, so
+      // the load overlaps the wait for a free stage instead of delaying the copy.
+      auto tile_id = [&](int k) {
+        const int bi = k * (kTile / bs) + lane;
+        const int nbk = (min(kTile, t1 - (t0 + k * kTile)) + bs - 1) / bs;
+        const int id_sh = __shfl_sync(kFull, id_lane, bi & 31);
+        return lane < nbk ? (bi < 32 ? id_sh : row[table_index(jb + bi, p.ring_blocks)]) : 0;
+      };
+      int id_k = (!I8 && ntiles > 0) ? tile_id(0) : 0;
       for (int k = 0; k < ntiles && !I8; ++k) {
         const int slot = tile_seq % NS;
         if (tile_seq >= NS && !mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1)) {
@@ -533,13 +544,10 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
           mbar_arrive_expect_tx(&sh.full[slot], (uint32_t)(nb * chunk_bytes));
         }
         __syncwarp();
-        const int bi = k * (kTile / bs) + lane;             // block of this lane's copy
-        const int id_sh = __shfl_sync(kFull, id_lane, bi & 31);
-        if (lane < nb) {
-          const int id = bi < 32 ? id_sh : row[table_index(jb + bi, p.ring_blocks)];
+        if (lane < nb)
           bulk_g2s(stages + slot * kStage + lane * chunk_bytes,
-                   p.cache + ((int64_t)id * Hkv + kvh) * chunk_bytes, (uint32_t)chunk_bytes, &sh.full[slot]);
-        }
+                   p.cache + ((int64_t)id_k * Hkv + kvh) * chunk_bytes, (uint32_t)chunk_bytes, &sh.full[slot]);
+        if (k + 1 < ntiles) id_k = tile_id(k + 1);
         ++tile_seq;
       }
       ++item_seq;

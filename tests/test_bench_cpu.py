@@ -43,6 +43,22 @@ def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
     assert bench.recorded_traffic("8b", 4096) is None
 
 
+def test_host_inputs_pack_every_input_into_one_buffer(monkeypatch):
+    import torch
+    from paged_kv_cache_168_gb300.workloads import make_workload
+    monkeypatch.setattr(torch.Tensor, "pin_memory", lambda self: self)   # no GPU here: pageable stands in
+    w = make_workload("tiny", device="cpu")
+    names = ("q", "key", "value", "block_tables", "context_lens", "slot_mapping")
+    h = bench.HostInputs(w, names, "cpu")
+    h.dev.fill_(0xAB)
+    h.upload()                                    # one copy brings every input
+    for k in names:
+        a, b = getattr(w, k), h.views[k]
+        assert a.dtype == b.dtype and a.shape == b.shape and torch.equal(a, b), k
+        assert (b.data_ptr() - h.dev.data_ptr()) % 256 == 0
+    assert h.nbytes == sum(-(-getattr(w, k).numel() * getattr(w, k).element_size() // 256) * 256 for k in names)
+
+
 def test_oracle_baseline_on_tiny_workload():
     from paged_kv_cache_168_gb300.workloads import make_workload
     w = make_workload("tiny")

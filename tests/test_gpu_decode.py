@@ -207,6 +207,17 @@ def test_decode_tiles_with_far_apart_maxima(dtype, Hq, Hkv, kernel):
     check(p, P=512, what=f"{kernel} far-apart maxima {dtype} {Hq}/{Hkv}")
 
 
+@pytest.mark.parametrize("S", [8192, 8193])
+def test_decode_at_the_tensor_core_sequence_limit(S):
+    # 8192 sequences is the most the tensor-core decode takes (its item-order
+    # tables live in shared memory); one more goes to the CUDA-core kernel
+    rng = np.random.default_rng(320 + S)
+    ctx = rng.integers(0, 48, size=S)
+    ctx[::501] = 0
+    p = Paged(rng, S=S, Hq=2, Hkv=1, D=128, bs=16, ctx=list(ctx), dtype="f16")
+    check(p, what=f"S={S} at the tensor-core limit")
+
+
 @pytest.mark.parametrize("S,Hq,Hkv,dtype", [(700, 8, 2, "bf16"), (1100, 4, 4, "f16")])
 def test_decode_many_sequences_item_order(S, Hq, Hkv, dtype):
     # more than 512 sequences (the tensor-core decode's 2-stage ring) with

@@ -187,6 +187,19 @@ def test_decode_remainders_of_every_length_class(kernel):
     assert_attention_close(case.run(P=P), ref, "int8 decode, remainder classes")
 
 
+@pytest.mark.parametrize("S", [1024, 1025])
+def test_decode_at_the_tensor_core_sequence_limit(S):
+    # 1024 sequences is the most the 8-bit tensor-core decode takes; one more
+    # goes to the CUDA-core 8-bit kernel
+    rng = np.random.default_rng(548 + S)
+    ctx = rng.integers(0, 40, size=S)
+    ctx[::97] = 0
+    case = I8Case(rng, S, 2, 1, 16, list(ctx), "bf16")
+    ref, e = case.expected()
+    assert e == 0
+    assert_attention_close(case.run(), ref, f"int8 decode, S={S} at the tensor-core limit")
+
+
 def test_decode_bad_block_id_zeroes_the_item(kernel):
     rng = np.random.default_rng(550)
     ctx = [40, 900, 200]

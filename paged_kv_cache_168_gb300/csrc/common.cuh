@@ -141,6 +141,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// A hint: bring the 128-byte line that holds *ptr into L2; nothing is returned.
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 // Non-blocking test of phase `parity` (try_wait may suspend the thread for a
 // while; a loop that polls several barriers in turn must not sleep on one).
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {

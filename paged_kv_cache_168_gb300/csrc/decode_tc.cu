@@ -370,6 +370,16 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
         ti = table_index(jb + lane, p.ring_blocks);
       } else {
         ti = r.part * (P / bs) + lane;   // P is a multiple of 128, bs divides it
+        // the partition's later block ids, checked when the item starts: into L2
+        // now, a whole item ahead, so that check waits for L2, not HBM (lane i
+        // covers ids 32 (i + 1) .. 32 (i + 1) + 31; P / bs <= 1024)
+        const int row_end = min(p.bt_stride, r.part * (P / bs) + P / bs);
+        const int t = r.part * (P / bs) + 32 * (lane + 1);
+        if (t < row_end) {
+          const int32_t* rp = p.block_tables + (int64_t)r.s * p.bt_stride;
+          prefetch_l2(rp + t);
+          prefetch_l2(rp + min(t + 31, row_end - 1));
+        }
       }
       r.id_lane = (lane < P / bs && ti < p.bt_stride && ti >= 0) ? p.block_tables[(int64_t)r.s * p.bt_stride + ti] : 0;
       const T* qsrc = static_cast<const T*>(p.q) + (int64_t)r.s * p.q_seq_stride + (int64_t)r.kvh * G * kD;

@@ -148,6 +148,35 @@ def test_shared_prefix_blocks_equal_unshared_copies(kernel):
     assert torch.equal(a, b)
 
 
+def test_bad_block_ids_among_many_items(kernel):
+    # several items per persistent CTA, so an item's ids are checked while the
+    # item before it streams: bad ids in first, middle and last partitions
+    rng = np.random.default_rng(206)
+    S = 300
+    ctx = rng.integers(1, 600, size=S)
+    bad = {7: 0, 55: None, 123: None, 250: 0, 299: None}     # sequence -> table entry (None: the last)
+    for s_ in bad:
+        ctx[s_] = max(int(ctx[s_]), 300)
+    p = Paged(rng, S=S, Hq=4, Hkv=2, D=128, bs=16, ctx=list(ctx), dtype="f16")
+    scale = 1 / math.sqrt(128)
+    mx = int(p.ctx.max())
+    ref, _ = oracle.decode(p.q_bits, p.pool, p.geom, p.tables, p.ctx, scale, max_context_len=mx)
+    q, pool, tables, ctx_d, desc = paged_to_dev(p)
+    bad_tables = tables.clone()
+    for i, (s_, e) in enumerate(bad.items()):
+        e = (int(p.ctx[s_]) - 1) // 16 if e is None else e
+        if s_ == 55:
+            e = 10                                            # a middle partition (P = 128: 8 blocks each)
+        bad_tables[s_, e] = -1 - i if i % 2 else p.num_blocks + i
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run_decode(q, pool, desc, bad_tables, ctx_d, mx, scale, P=128, dev_err=err)
+    assert pkv.read_device_errors(err) == pkv.DEVERR_BLOCK_ID
+    rows = sorted(bad)
+    assert torch.all(out[rows] == 0)
+    good = [s_ for s_ in range(S) if s_ not in bad]
+    assert_attention_close(out[good], ref[good], f"{kernel}: sequences beside bad ones")
+
+
 @pytest.mark.parametrize("D", [64, 128])
 def test_zero_context_rows_are_zero(D, kernel):
     rng = np.random.default_rng(204)

@@ -270,10 +270,11 @@ def oracle_build_blocks(w, s):
     built[blocks] = True
 
 
-def oracle_sample(w, budget_s: float, max_items: int | None = None, start: int = 0):
+def oracle_sample(w, budget_s: float, max_items: int | None = None, start: int = 0, threads: int = 0):
     """Time the fp64 oracle on the workload sequence by sequence (all query heads
-    of a sequence together) until ~budget_s seconds of wall time.  Returns
-    (GB/s of algorithmic KV bytes, seq-steps/s, description, cores, seconds)."""
+    of a sequence together) until ~budget_s seconds of wall time, on `threads`
+    OpenMP threads (0: all).  Returns (GB/s of algorithmic KV bytes, seq-steps/s,
+    description, cores, seconds)."""
     import oracle
     cfg = w.cfg
     g, pool, q, _ = oracle_inputs(w)
@@ -285,18 +286,18 @@ def oracle_sample(w, budget_s: float, max_items: int | None = None, start: int =
             oracle_build_blocks(w, s)           # cache construction, not timed
             t0 = time.perf_counter()
             oracle.decode_i8(q[s:s + 1], pool, g, w.block_tables_np[s:s + 1], w.context_lens_np[s:s + 1],
-                             w.scale, max_context_len=w.max_context_len)
+                             w.scale, max_context_len=w.max_context_len, nthreads=threads)
         else:
             sel = np.array([[s, h] for h in range(cfg.num_q_heads)], dtype=np.int32)
             t0 = time.perf_counter()
             oracle.decode(q, pool, g, w.block_tables_np, w.context_lens_np, w.scale,
-                          max_context_len=w.max_context_len, sel=sel)
+                          max_context_len=w.max_context_len, sel=sel, nthreads=threads)
         t_total += time.perf_counter() - t0
         done_bytes += int(w.context_lens_np[s]) * kv_tok
         done_seqs += 1
         if t_total >= budget_s or (max_items and done_seqs >= max_items):
             break
-    cores = oracle.max_threads()
+    cores = threads or oracle.max_threads()
     desc = (f"{done_seqs} of {cfg.num_seqs} sequences (all {cfg.num_q_heads} query heads each, "
             f"{done_bytes / 1e9:.3f} GB of KV) of the {cfg.name} workload, fp64 oracle, {cores} OpenMP threads")
     return done_bytes / t_total / 1e9, done_seqs / t_total, desc, cores, t_total
@@ -461,8 +462,11 @@ def run_gpu(args):
         cpu = None
         if args.cpu_baseline_seconds > 0:
             v, sps, desc, cores, _ = oracle_sample(w, args.cpu_baseline_seconds)
+            v1, sps1, desc1, _, _ = oracle_sample(w, args.cpu_baseline_seconds / 3, start=7, threads=1)
             cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc,
-                   "seq_steps_per_s": round(sps, 4)}
+                   "seq_steps_per_s": round(sps, 4),
+                   "single_thread": {"value": round(v1, 4), "unit": "GB/s", "cores": 1, "sample": desc1,
+                                     "seq_steps_per_s": round(sps1, 4)}}
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
@@ -477,6 +481,7 @@ def run_gpu(args):
                              f"{nbytes['decode_kv'] / 1e9:.2f} GB of KV read per step"},
             "seq_steps_per_s": round(world * w.cfg.num_seqs / (ms * 1e-3), 1),
             "decode_kv_gbs": round(nbytes["decode_kv"] / (dec_ms * 1e-3) / 1e9, 2),
+            "decode_ms_p10_p50_p90": [round(float(np.percentile(decode_ms, x)), 4) for x in (10, 50, 90)],
             "frac_of_spec_8tbs": round(achieved / SPEC_HBM_GBS, 4),
             "bytes_per_step": nbytes,
             "roofline": {"bound": "hbm", "kernel": "pa_decode (decode + log-sum-exp merge)",
@@ -501,11 +506,11 @@ def run_gpu(args):
 
 # ------------------------------------------------------------------ prefill / extend
 
-def prefill_oracle_sample(w, budget_s: float, start: int = 0):
+def prefill_oracle_sample(w, budget_s: float, start: int = 0, threads: int = 0):
     """Time the fp64 oracle's prefill on 64-query-token windows of the workload
     (all heads; a window at a random offset of a random sequence, attending
-    everything before it) until ~budget_s seconds: (TFLOP/s of causal FLOPs,
-    description, cores)."""
+    everything before it) until ~budget_s seconds, on `threads` OpenMP threads
+    (0: all): (TFLOP/s of causal FLOPs, description, cores)."""
     import oracle
     from paged_kv_cache_168_gb300.workloads import as_u16
     cfg = w.cfg
@@ -523,11 +528,11 @@ def prefill_oracle_sample(w, budget_s: float, start: int = 0):
         c = int(ctx[s]) - q_len + j0 + n                     # the context the window's last token sees
         t0 = time.perf_counter()
         oracle.prefill(q[qsl[s] + j0:qsl[s] + j0 + n], pool, g, w.block_tables_np[s:s + 1],
-                       np.array([c], np.int32), np.array([0, n], np.int32), w.scale)
+                       np.array([c], np.int32), np.array([0, n], np.int32), w.scale, nthreads=threads)
         t_total += time.perf_counter() - t0
         flops += 4 * cfg.head_size * cfg.num_q_heads * (n * (c - n) + n * (n + 1) // 2)
         windows += 1
-    cores = oracle.max_threads()
+    cores = threads or oracle.max_threads()
     desc = (f"{windows} windows of 64 query tokens (all {cfg.num_q_heads} heads, random sequence and offset) "
             f"of the {cfg.name} workload, fp64 oracle, {cores} OpenMP threads")
     return flops / t_total / 1e12, desc, cores
@@ -617,7 +622,9 @@ def run_gpu_prefill(args):
         cpu = None
         if args.cpu_baseline_seconds > 0:
             v, desc, cores = prefill_oracle_sample(w, args.cpu_baseline_seconds)
-            cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+            v1, desc1, _ = prefill_oracle_sample(w, args.cpu_baseline_seconds / 3, start=7, threads=1)
+            cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
+                   "single_thread": {"value": round(v1, 6), "unit": "TFLOP/s", "cores": 1, "sample": desc1}}
         line = {
             "metric": PREFILL_METRIC, "value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),

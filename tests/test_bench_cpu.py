@@ -64,6 +64,8 @@ def test_oracle_baseline_on_tiny_workload():
     w = make_workload("tiny")
     gbs, sps, desc, cores, secs = bench.oracle_sample(w, 0.05)
     assert gbs > 0 and sps > 0 and cores >= 1 and "tiny" in desc
+    gbs1, _, desc1, cores1, _ = bench.oracle_sample(w, 0.05, threads=1)
+    assert gbs1 > 0 and cores1 == 1 and "1 OpenMP threads" in desc1
 
 
 def _rank(rank, world, port, out):

@@ -380,6 +380,22 @@ pa_status pa_bm_swap_out(pa_block_manager* bm, const int64_t* seq_ids, int32_t n
 pa_status pa_bm_swap_in(pa_block_manager* bm, const int64_t* seq_ids, int32_t n, int64_t* pairs, int32_t capacity,
                         int32_t* num_pairs);
 
+/* Whether num_running sequences can each take one more token now: 1 when
+ * num_running <= the free device blocks (each may need a new block, or a copy
+ * of a shared last block), else 0 -- the vLLM block manager's can_append_slots
+ * ("推理框架知识点" page, running/swapped queues). */
+int32_t pa_bm_can_append_slots(pa_block_manager* bm, int32_t num_running);
+
+/* Admission of pa_bm_swap_in for the n (swapped-out) sequences: their distinct
+ * blocks (a shared block counted once) against the free device blocks and the
+ * watermark, as pa_bm_can_allocate: a pa_alloc_status, or -1 for an unknown or
+ * not swapped-out sequence (pa_last_error_message says which). */
+int32_t pa_bm_can_swap_in(pa_block_manager* bm, const int64_t* seq_ids, int32_t n);
+
+/* Whether the host pool has room for pa_bm_swap_out of the n (device-resident)
+ * sequences: 1 or 0, or -1 for an unknown or swapped-out sequence. */
+int32_t pa_bm_can_swap_out(pa_block_manager* bm, const int64_t* seq_ids, int32_t n);
+
 /* Free blocks (the evictor's cached blocks included) on the device (0) or host (1) side. */
 int32_t pa_bm_num_free_blocks(pa_block_manager* bm, int32_t on_host);
 

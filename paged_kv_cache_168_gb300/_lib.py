@@ -31,7 +31,7 @@ EXPORTED = [
     "pa_status_string", "pa_last_error_message",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_can_allocate", "pa_bm_allocate", "pa_bm_append_slot", "pa_bm_fork",
     "pa_bm_free", "pa_bm_block_table", "pa_bm_swap_out", "pa_bm_swap_in", "pa_bm_num_free_blocks",
-    "pa_bm_ref_count",
+    "pa_bm_ref_count", "pa_bm_can_append_slots", "pa_bm_can_swap_in", "pa_bm_can_swap_out",
 ]
 
 
@@ -138,6 +138,12 @@ def load():
     lib.pa_bm_num_free_blocks.restype = i32
     lib.pa_bm_ref_count.argtypes = [B, i32, i32]
     lib.pa_bm_ref_count.restype = i32
+    lib.pa_bm_can_append_slots.argtypes = [B, i32]
+    lib.pa_bm_can_append_slots.restype = i32
+    lib.pa_bm_can_swap_in.argtypes = [B, P, i32]
+    lib.pa_bm_can_swap_in.restype = i32
+    lib.pa_bm_can_swap_out.argtypes = [B, P, i32]
+    lib.pa_bm_can_swap_out.restype = i32
     lib.pa_status_string.argtypes = [ctypes.c_int]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_last_error_message.argtypes = []
@@ -357,6 +363,23 @@ class BlockManager:
     def swap_in(self, seq_ids):
         """Move the sequences' blocks back to the device pool; (host, device) pairs."""
         return self._swap(self._lib.pa_bm_swap_in, seq_ids)
+
+    def can_append_slots(self, num_running: int) -> bool:
+        return self._lib.pa_bm_can_append_slots(self._h, num_running) == 1
+
+    def _can_swap(self, fn, seq_ids) -> int:
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        r = fn(self._h, ids.ctypes.data_as(ctypes.c_void_p), ids.size)
+        if r < 0:
+            _check(PA_ERR_INVALID_ARG)
+        return r
+
+    def can_swap_in(self, seq_ids) -> int:
+        """Admission of swap_in (an alloc status: OK, LATER or NEVER)."""
+        return self._can_swap(self._lib.pa_bm_can_swap_in, seq_ids)
+
+    def can_swap_out(self, seq_ids) -> bool:
+        return self._can_swap(self._lib.pa_bm_can_swap_out, seq_ids) == 1
 
     def num_free(self, on_host: bool = False) -> int:
         return self._lib.pa_bm_num_free_blocks(self._h, int(on_host))

@@ -393,6 +393,44 @@ static pa_status bm_swap(pa_block_manager* bm, const int64_t* seq_ids, int32_t n
   return PA_OK;
 }
 
+// Distinct blocks of the n sequences, all on the side given (-1: an unknown
+// sequence, or one on the other side).
+static int32_t bm_distinct_blocks(pa_block_manager* bm, const int64_t* seq_ids, int32_t n, bool swapped) {
+  if (n < 0 || (n > 0 && !seq_ids)) {
+    bm_fail(PA_ERR_INVALID_ARG, "NULL argument");
+    return -1;
+  }
+  std::set<int32_t> need;
+  for (int32_t i = 0; i < n; ++i) {
+    Seq* s = bm->find(seq_ids[i]);
+    if (!s || s->swapped != swapped) {
+      bm_fail(PA_ERR_INVALID_ARG, "unknown sequence or wrong side");
+      return -1;
+    }
+    need.insert(s->table.begin(), s->table.end());
+  }
+  return (int32_t)need.size();
+}
+
+int32_t pa_bm_can_append_slots(pa_block_manager* bm, int32_t num_running) {
+  // each running sequence may need one new block (or a copy of a shared last block)
+  return num_running >= 0 && num_running <= bm->gpu.num_free() ? 1 : 0;
+}
+
+int32_t pa_bm_can_swap_in(pa_block_manager* bm, const int64_t* seq_ids, int32_t n) {
+  const int32_t need = bm_distinct_blocks(bm, seq_ids, n, true);
+  if (need < 0) return -1;
+  if (bm->gpu.total() - need < bm->watermark_blocks) return PA_ALLOC_NEVER;
+  if (bm->gpu.num_free() - need >= bm->watermark_blocks) return PA_ALLOC_OK;
+  return PA_ALLOC_LATER;
+}
+
+int32_t pa_bm_can_swap_out(pa_block_manager* bm, const int64_t* seq_ids, int32_t n) {
+  const int32_t need = bm_distinct_blocks(bm, seq_ids, n, false);
+  if (need < 0) return -1;
+  return need <= bm->cpu.num_free() ? 1 : 0;
+}
+
 pa_status pa_bm_swap_out(pa_block_manager* bm, const int64_t* seq_ids, int32_t n, int64_t* pairs, int32_t capacity,
                          int32_t* num_pairs) {
   return bm_swap(bm, seq_ids, n, pairs, capacity, num_pairs, true);

@@ -169,6 +169,28 @@ class RefBlockManager:
             s["swapped"] = out
         return sorted(mapping.items())
 
+    def can_append_slots(self, num_running):
+        return num_running <= self.gpu.num_free()
+
+    def _distinct(self, sids, swapped):
+        need = set()
+        for sid in sids:
+            s = self.seqs[sid]
+            assert s["swapped"] == swapped
+            need.update(s["table"])
+        return len(need)
+
+    def can_swap_in(self, sids):
+        need = self._distinct(sids, True)
+        if self.ngpu - need < self.watermark_blocks:
+            return NEVER
+        if self.gpu.num_free() - need >= self.watermark_blocks:
+            return OK
+        return LATER
+
+    def can_swap_out(self, sids):
+        return self._distinct(sids, False) <= self.cpu.num_free()
+
     def swap_out(self, sids):
         return self._swap(sids, True)
 

@@ -135,6 +135,7 @@ def test_random_operations_match_the_model(seed, caching, window):
         elif op < 0.93 and alive and ncpu and not caching:
             sid = rnd.choice(alive)
             need = len(set(ref.block_table(sid)[0]))
+            assert cpp.can_swap_out([sid]) == ref.can_swap_out([sid]) == (ref.cpu.num_free() >= need)
             if ref.cpu.num_free() >= need:
                 assert cpp.swap_out([sid]).tolist() == [list(p) for p in ref.swap_out([sid])]
                 alive.remove(sid)
@@ -142,6 +143,7 @@ def test_random_operations_match_the_model(seed, caching, window):
         elif swapped:
             sid = swapped.pop(0)
             need = len(set(ref.block_table(sid)[0]))
+            assert cpp.can_swap_in([sid]) == ref.can_swap_in([sid])
             if ref.gpu.num_free() >= need:
                 assert cpp.swap_in([sid]).tolist() == [list(p) for p in ref.swap_in([sid])]
                 alive.append(sid)
@@ -153,6 +155,45 @@ def test_random_operations_match_the_model(seed, caching, window):
             assert t.tolist() == rt and n == rn, (step, sid)
         assert cpp.num_free() == ref.gpu.num_free()
         assert [cpp.ref_count(b) for b in range(ngpu)] == ref.gpu.ref
+        k = rnd.randint(0, len(alive) + 3)
+        assert cpp.can_append_slots(k) == ref.can_append_slots(k)
+
+
+def test_swap_and_append_admission():
+    # two sequences share both blocks of a prompt (a fork): swapping them
+    # together needs those two blocks once on the other side
+    bm = BlockManager(4, 6, 2, watermark=0.0)
+    bm.allocate(0, list(range(8)))                  # 2 full blocks
+    bm.fork(0, 1)
+    assert bm.can_swap_out([0, 1]) and bm.can_swap_out([0])
+    bm.allocate(2, [1])                             # 1 block
+    assert not bm.can_swap_out([0, 1, 2])           # 3 distinct blocks, 2 host blocks
+    assert bm.can_append_slots(3) and bm.can_append_slots(bm.num_free())
+    assert not bm.can_append_slots(bm.num_free() + 1)
+    pairs = bm.swap_out([0, 1])
+    assert len(pairs) == 2 and bm.num_free(on_host=True) == 0
+    assert bm.can_swap_in([0, 1]) == OK    # 5 device blocks free, 2 needed
+    bm.allocate(3, list(range(16)))                 # 4 blocks: 1 left
+    assert bm.can_swap_in([0, 1]) == LATER
+    bm.free(3)
+    with pytest.raises(PagedKVError):
+        bm.can_swap_in([2])                         # not swapped out
+    with pytest.raises(PagedKVError):
+        bm.can_swap_out([0])                        # swapped out
+    with pytest.raises(PagedKVError):
+        bm.can_swap_in([99])                        # unknown
+    # the watermark keeps admission from taking the last free blocks; a request
+    # larger than the pool less the watermark can never be admitted
+    wm = BlockManager(4, 10, 10, watermark=0.2)     # 2 blocks held back
+    wm.allocate(0, list(range(36)))                 # 9 blocks
+    wm.swap_out([0])
+    assert wm.can_swap_in([0]) == NEVER    # 10 - 9 < 2
+    wm2 = BlockManager(4, 10, 10, watermark=0.2)
+    wm2.allocate(0, list(range(32)))                # 8 blocks
+    wm2.swap_out([0])
+    assert wm2.can_swap_in([0]) == OK      # 10 free - 8 >= 2
+    wm2.allocate(1, [5])
+    assert wm2.can_swap_in([0]) == LATER   # 9 free - 8 < 2
 
 
 def test_errors_leave_state_unchanged():

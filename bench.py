@@ -481,6 +481,7 @@ def run_gpu(args):
                              f"{nbytes['decode_kv'] / 1e9:.2f} GB of KV read per step"},
             "seq_steps_per_s": round(world * w.cfg.num_seqs / (ms * 1e-3), 1),
             "decode_kv_gbs": round(nbytes["decode_kv"] / (dec_ms * 1e-3) / 1e9, 2),
+            "decode_unique_kv_gbs": round(nbytes["decode_kv_unique"] / (dec_ms * 1e-3) / 1e9, 2),
             "decode_ms_p10_p50_p90": [round(float(np.percentile(decode_ms, x)), 4) for x in (10, 50, 90)],
             "frac_of_spec_8tbs": round(achieved / SPEC_HBM_GBS, 4),
             "bytes_per_step": nbytes,

@@ -15,6 +15,24 @@ from . import _lib
 from .workloads import Workload
 
 
+def unique_kv_tokens(block_tables: np.ndarray, context_lens: np.ndarray, block_size: int) -> int:
+    """Distinct cache slots one decode step reads: for each physical block, the
+    most tokens any sequence attends in it.  Blocks that several sequences share
+    (a beam group's prompt) count once, which is what HBM must deliver when the
+    other readers hit L2."""
+    ctx = context_lens.astype(np.int64)
+    nblk = -(-ctx // block_size)
+    j = np.arange(block_tables.shape[1])[None, :]
+    valid = j < nblk[:, None]
+    tokens = np.clip(ctx[:, None] - j * block_size, 0, block_size)[valid]
+    phys = block_tables[valid].astype(np.int64)
+    if phys.size == 0:
+        return 0
+    best = np.zeros(int(phys.max()) + 1, np.int64)
+    np.maximum.at(best, phys, tokens)
+    return int(best.sum())
+
+
 class DecodeStep:
     """One decode step over a workload.  For an 8-bit cache the pool is built
     here (outside any timed step) by writing the workload's logical history into
@@ -105,8 +123,9 @@ class DecodeStep:
         block_bytes = self.block_bytes
         copy = 2 * w.copy_pairs.shape[0] * block_bytes
         swap = (w.swap_out_pairs.shape[0] + w.swap_in_pairs.shape[0]) * block_bytes * 2
-        return {"decode": decode, "decode_kv": int(ctx.sum()) * kv_tok, "reshape": reshape, "copy": copy,
-                "swap": swap, "total": decode + reshape + copy + swap}
+        unique = unique_kv_tokens(w.block_tables_np, w.context_lens_np, cfg.block_size) * kv_tok
+        return {"decode": decode, "decode_kv": int(ctx.sum()) * kv_tok, "decode_kv_unique": unique,
+                "reshape": reshape, "copy": copy, "swap": swap, "total": decode + reshape + copy + swap}
 
 
 class PrefillStep:

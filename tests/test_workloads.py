@@ -64,3 +64,24 @@ def test_prefill_workloads_are_seeded_and_consistent():
             assert np.array_equal(a.slot_mapping_np[qsl[s]:qsl[s + 1]], want)
         used = a.block_tables_np[a.block_tables_np >= 0]
         assert np.unique(used).size == used.size and used.max() < a.num_blocks
+
+
+def test_unique_kv_tokens_counts_a_shared_block_once():
+    from paged_kv_cache_168_gb300.step import unique_kv_tokens
+    bs = 4
+    # seqs 0 and 1 share blocks 5 and 6 (8 tokens); seq 0 then has 3 tokens in
+    # block 1, seq 1 has 4 in block 2 and 1 in block 3; seq 2 is empty
+    tables = np.array([[5, 6, 1, -1], [5, 6, 2, 3], [-1, -1, -1, -1]], np.int32)
+    ctx = np.array([11, 13, 0], np.int32)
+    assert unique_kv_tokens(tables, ctx, bs) == 8 + 3 + 4 + 1
+    # a block that two sequences fill to different depths counts its deeper use
+    tables2 = np.array([[7, -1], [7, 8]], np.int32)
+    assert unique_kv_tokens(tables2, np.array([3, 5], np.int32), bs) == 4 + 1
+    # without sharing, unique equals the logical count
+    w = make_workload("tiny")
+    assert unique_kv_tokens(w.block_tables_np, w.context_lens_np, w.cfg.block_size) == int(w.context_lens_np.sum())
+    beam = make_workload("beam")
+    u = unique_kv_tokens(beam.block_tables_np, beam.context_lens_np, beam.cfg.block_size)
+    groups = beam.cfg.num_seqs // beam.cfg.beams
+    assert u < int(beam.context_lens_np.sum())
+    assert u >= groups * beam.cfg.ctx[1]          # every group's shared prompt, once

@@ -234,7 +234,11 @@ size_t pa_decode_workspace_bytes(const pa_cache_desc* desc, int32_t num_seqs, in
   if (num_seqs <= 0 || num_q_heads <= 0 || head_size <= 0 || max_context_len <= 0 || P <= 0) return 0;
   const int64_t parts = (max_context_len + P - 1) / P;
   if (parts <= 1) return 0;
-  return (size_t)((int64_t)num_seqs * num_q_heads * parts * (head_size + 2) * 4);
+  // saturate instead of wrapping: a wrapped (small) size would let a too-small
+  // workspace pass pa_decode's check
+  const unsigned __int128 need = (unsigned __int128)num_seqs * (unsigned __int128)num_q_heads *
+                                 (unsigned __int128)parts * (unsigned __int128)((head_size + 2) * 4);
+  return need > (unsigned __int128)(SIZE_MAX / 2) ? SIZE_MAX : (size_t)need;
 }
 
 int32_t pa_decode_window_span(int32_t max_context_len, int32_t block_size, int32_t window, int32_t ring_blocks) {

@@ -97,6 +97,9 @@ def test_workspace_sizing(lib):
     assert wb(8, 64, 8, 128, 131072) == 8 * 64 * 16 * 130 * 4
     assert wb(8, 64, 8, 64, 16384) == 8 * 64 * 32 * 66 * 4
     assert _lib.load().pa_decode_workspace_bytes(None, 8, 64, 16384, 512) == 0
+    # sizes that do not fit saturate (a wrapped, small size would pass as enough)
+    huge = _lib.decode_workspace_bytes(CacheDesc(100, 16, 65535, 128), 65535, 65535 * 16, 2**31 - 1, 128)
+    assert huge == 2**64 - 1
 
 
 def test_status_strings(lib):

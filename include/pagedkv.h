@@ -160,9 +160,9 @@ pa_status pa_reshape_and_cache(void* kv_cache, const pa_cache_desc* desc, int32_
                                int32_t num_tokens, uint32_t* dev_err, void* stream);
 
 /* Workspace bytes pa_decode needs for these shapes (0 when no sequence can span
- * more than one partition, or desc is NULL).  partition_size 0 selects the
- * default (pa_decode_partition_size with the same desc, num_seqs and
- * max_context_len). */
+ * more than one partition, or desc is NULL; SIZE_MAX when the size does not fit
+ * in half the address space).  partition_size 0 selects the default
+ * (pa_decode_partition_size with the same desc, num_seqs and max_context_len). */
 size_t pa_decode_workspace_bytes(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_q_heads,
                                  int32_t max_context_len, int32_t partition_size);
 

@@ -57,6 +57,14 @@ def test_host_inputs_pack_every_input_into_one_buffer(monkeypatch):
         assert a.dtype == b.dtype and a.shape == b.shape and torch.equal(a, b), k
         assert (b.data_ptr() - h.dev.data_ptr()) % 256 == 0
     assert h.nbytes == sum(-(-getattr(w, k).numel() * getattr(w, k).element_size() // 256) * 256 for k in names)
+    # the prefill step's inputs (query_start_loc among them) travel the same way
+    from paged_kv_cache_168_gb300.workloads import make_prefill_workload
+    pw = make_prefill_workload("prefill_8b", device="cpu")
+    pnames = ("q", "key", "value", "block_tables", "context_lens", "query_start_loc", "slot_mapping")
+    ph = bench.HostInputs(pw, pnames, "cpu")
+    ph.upload()
+    for k in pnames:
+        assert torch.equal(getattr(pw, k), ph.views[k]), k
 
 
 def test_oracle_baseline_on_tiny_workload():

@@ -425,6 +425,104 @@ def test_i8_quantisation_properties(dtype):
                 assert np.all(np.abs(vec - codes * scale) <= scale * 0.5 * (1 + 1e-5))
 
 
+def _np_i8_quantise(vec: np.ndarray):
+    """numpy binary32 restatement of the 8-bit reading (FAQ page, TurboMind
+    section, "8bit KV Cache"): amax = max|x|; the quotient 127 / amax is rounded
+    to binary32 first, each x is multiplied by it (binary32) and rounded half to
+    even (np.rint), then clipped to +-127; scale = amax / 127 in binary32."""
+    v = vec.astype(np.float32)
+    amax = np.float32(np.max(np.abs(v)))
+    if amax == 0:
+        return np.zeros(v.shape, np.int8), np.float32(0)
+    inv = np.float32(127) / amax
+    return np.clip(np.rint(v * inv), -127, 127).astype(np.int8), np.float32(amax / np.float32(127))
+
+
+def _i8_discriminating_vectors(dtype, want=24):
+    """Vectors (exactly representable in `dtype`) on which the plausible wrong
+    arrangements of the quantiser give other bytes than the reading:
+      * exact ties x * (127 / amax) = k + 1/2 of both signs (amax = 127 / 2^j
+        makes the quotient a power of two): half-away-from-zero rounding differs;
+      * pairs (amax, x) where (x * 127) / amax and x * (127 / amax) round to
+        different integers (a one-ulp difference across a half-integer);
+      * maxima where amax * (1 / 127) is not amax / 127."""
+    tdt = TORCH_DT16[dtype]
+
+    def rep(a):
+        return torch.from_numpy(np.asarray(a, np.float32)).to(tdt).to(torch.float32).numpy()
+
+    vecs = []
+    for j in range(4):
+        amax = np.float32(127.0 / 2 ** j)
+        half = np.float32(0.5 / 2 ** j)                  # x * 2^j = k + 1/2  for x = (2k + 1) * half
+        ks = np.array([0, 1, 2, 3, 10, 41, 100, 125, 126])
+        xs = ((2 * ks + 1) * half).astype(np.float32)
+        xs = xs[xs < amax]
+        v = np.zeros(128, np.float32)
+        v[0] = amax
+        v[1:1 + xs.size] = xs
+        v[64:64 + xs.size] = -xs
+        vecs.append(rep(v))
+    rng = np.random.default_rng(7)
+    amax = rep(rng.uniform(0.01, 1000, 40000))
+    k = rng.integers(0, 127, amax.size)
+    x0 = torch.from_numpy(((k + 0.5) * amax.astype(np.float64) / 127).astype(np.float32)).to(tdt)
+    order_pairs = []
+    for d in range(-3, 4):                               # neighbours of the tie point, in ulps of dtype
+        x = (x0.view(torch.int16) + d).view(tdt).to(torch.float32).numpy()
+        ok = np.isfinite(x) & (np.abs(x) <= amax)
+        inv = np.float32(127) / amax
+        diff = ok & (np.rint(x * inv) != np.rint((x * np.float32(127)) / amax))
+        order_pairs += list(zip(amax[diff], x[diff]))
+    for a, x in order_pairs[:want]:
+        v = np.zeros(128, np.float32)
+        v[0], v[1], v[2] = a, x, -x
+        v[3:] = rep(rng.uniform(-1, 1, 125) * a)
+        vecs.append(rep(v))
+    scale_diff = amax[(amax / np.float32(127)) != (amax * (np.float32(1) / np.float32(127)))]
+    for a in scale_diff[:want]:
+        v = rep(rng.uniform(-1, 1, 128) * a)
+        v[5] = -a
+        vecs.append(rep(v))
+    return np.stack(vecs)
+
+
+TORCH_DT16 = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_i8_quantiser_bytes_equal_numpy_binary32(dtype):
+    """The oracle's 8-bit writer stores exactly the codes and scales of an
+    independent numpy binary32 computation of the reading, on inputs chosen so
+    that half-away-from-zero rounding, the order x * 127 / amax, or a scale of
+    amax * (1 / 127) would each change some byte."""
+    vecs = _i8_discriminating_vectors(dtype)
+    n = vecs.shape[0]
+    bs, hkv = 16, 1
+    nb = -(-n // bs)
+    g = oracle.Geom(nb, bs, hkv, 128, dtype)
+    pool = _i8_pool(g, nb)
+    bits = to_bits(vecs.reshape(n, 1, 128), dtype)
+    assert np.array_equal(bits_to_f64(bits, dtype).reshape(n, 128), vecs.astype(np.float64))   # exact inputs
+    slots = np.arange(n, dtype=np.int64)
+    assert oracle.reshape_and_cache_i8(pool, g, bits, bits, slots) == 0
+    half_away = order = scale_mul = 0
+    for i in range(n):
+        want_codes, want_scale = _np_i8_quantise(vecs[i])
+        for part in (0, 1):
+            codes, scale = _read_i8(pool, g, i // bs, 0, part, i % bs)
+            assert np.array_equal(codes, want_codes), (i, part)
+            assert np.float32(scale).view(np.uint32) == want_scale.view(np.uint32), (i, part)
+        # the fixture discriminates: count the elements each wrong arrangement changes
+        v = vecs[i].astype(np.float32)
+        amax = np.float32(np.max(np.abs(v)))
+        y = v * (np.float32(127) / amax)
+        half_away += int(np.sum(np.clip(np.trunc(y + np.copysign(np.float32(0.5), y)), -127, 127) != want_codes))
+        order += int(np.sum(np.clip(np.rint((v * np.float32(127)) / amax), -127, 127) != want_codes))
+        scale_mul += int(amax * (np.float32(1) / np.float32(127)) != want_scale)
+    assert half_away > 0 and order > 0 and scale_mul > 0, (half_away, order, scale_mul)
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_i8_decode_on_grid_values_equals_16bit_decode(dtype):
     # values code * 2^-6 with one code of +-127 per vector are stored exactly by

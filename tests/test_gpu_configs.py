@@ -1,10 +1,8 @@
 """Full-size parity on the five workloads, in the launch configuration the
 benchmark times (DecodeStep, default partition size).
 
-Cache operations are compared bit for bit on the whole pool.  Attention is
-compared on a sample of (sequence, query head) pairs the oracle computes one by
-one (the longest and shortest contexts, every query head of one kv head, and a
-seeded random sample)."""
+Cache operations are compared bit for bit on the whole pool, and attention on
+every (sequence, query head) output row against the fp64 oracle."""
 import numpy as np
 import pytest
 import torch
@@ -21,23 +19,6 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(scope="module", autouse=True)
 def _built(cuda_device):
     ensure_built()
-
-
-def sample_pairs(w, n_random=24, seed=0):
-    cfg = w.cfg
-    ctx = w.context_lens_np
-    G = cfg.num_q_heads // cfg.num_kv_heads
-    rng = np.random.default_rng(seed)
-    pairs = set()
-    for s in (int(ctx.argmax()), int(ctx.argmin())):
-        for h in range(0, cfg.num_q_heads, max(1, cfg.num_q_heads // 4)):
-            pairs.add((s, h))
-    s = int(rng.integers(cfg.num_seqs))
-    for h in range(G):                           # every query head of kv head 0
-        pairs.add((s, h))
-    for _ in range(n_random):
-        pairs.add((int(rng.integers(cfg.num_seqs)), int(rng.integers(cfg.num_q_heads))))
-    return np.array(sorted(pairs), dtype=np.int32)
 
 
 @pytest.mark.parametrize("name", ["tiny", "7b", "8b", "70b", "beam"])
@@ -63,12 +44,9 @@ def test_full_size_step_matches_oracle(name):
     assert oracle.reshape_and_cache(pool, g, as_u16(w.key), as_u16(w.value), w.slot_mapping_np) == 0
     assert np.array_equal(dev_to_u16(w.kv_cache).reshape(-1), pool)
 
-    sel = sample_pairs(w) if name != "tiny" else None
     ref, err = oracle.decode(as_u16(w.q), pool, g, w.block_tables_np, w.context_lens_np, w.scale,
-                             max_context_len=w.max_context_len, sel=sel)
+                             max_context_len=w.max_context_len)
     assert err == 0
-    got = out if sel is None else out[torch.from_numpy(sel[:, 0]).long().cuda(),
-                                      torch.from_numpy(sel[:, 1]).long().cuda()]
-    assert_attention_close(got, ref, name)
+    assert_attention_close(out, ref, f"full-size {name}")
     # every output row is finite (NaN-filled unused blocks were never read)
     assert bool(torch.isfinite(out).all())

@@ -173,8 +173,9 @@ size_t pa_decode_workspace_bytes(const pa_cache_desc* desc, int32_t num_seqs, in
  *   1024 sequences): it walks work items of one (sequence, kv head, partition),
  *   and the default is the longest of 4096, 2048, 1024 and 512 tokens (8192
  *   first when max_context_len > 32768) for which
- *     num_seqs * num_kv_heads * ceil(max_context_len / P) >= 912
- *   (six items per SM of a 152-SM GPU), else 512.  Longer partitions write and
+ *     num_seqs * num_kv_heads * ceil(max_context_len / P) >= 6 * SMs
+ *   (six items per SM of the current device: 912 on a 152-SM GB300; 152 is
+ *   assumed when no device can be queried), else 512.  Longer partitions write and
  *   merge fewer partial results; shorter ones split the work finely enough to
  *   keep every SM busy to the end.
  *   CUDA-core kernel (the other shapes): 512, or 1024 when max_context_len >
@@ -292,9 +293,15 @@ int32_t pa_decode_window_span(int32_t max_context_len, int32_t block_size, int32
  *     PA_STATIC_WORKSPACE_BYTES are rejected with PA_ERR_WORKSPACE_TOO_SMALL
  *     (pa_last_error_message explains); nothing is launched.  A larger
  *     partition_size shrinks the need.
- *   - It allocates nothing.  The first call on a device that needs the array
- *     looks up its device address (cudaGetSymbolAddress) with that device
- *     current and caches it; make that first call before any stream capture.
+ *   - Every argument is checked as pa_decode checks it before the size test,
+ *     so a bad argument returns its own status (PA_ERR_INVALID_ARG or
+ *     PA_ERR_UNSUPPORTED), not PA_ERR_WORKSPACE_TOO_SMALL.
+ *   - It allocates nothing.  The first call in a CUDA context that needs the
+ *     array looks up its device address (cudaGetSymbolAddress) with the device
+ *     current and caches it for that context; make that first call before any
+ *     stream capture.  After cudaDeviceReset the device's new context gets a
+ *     fresh lookup (the array may then sit at another address), so the first
+ *     call after a reset must also come before any capture.
  *   - The array is shared by every call on a device and keeps the last call's
  *     contents (decode needs none of it zeroed).  Calls that may overlap on the
  *     GPU -- on different streams, or from different threads -- race on it:

@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <vector>
 
 #include "common.cuh"
@@ -34,16 +35,41 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 // Default partition sizes for the tensor-core kernels: the shortest, the longest
 // for contexts up to kLongContext tokens, the longest beyond, and the work items
-// (sequence, kv head, partition) wanted before a longer partition is taken -- six
-// per SM of a 152-SM GB300, below which the persistent kernels' last wave leaves
-// SMs idle (a sweep of 512..8192 tokens on the 7B, 8B, 70B and beam decode
-// shapes, 16- and 8-bit).  The CUDA-core kernel, one CTA per item, keeps 512
-// (1024 past kLongContext): longer partitions leave it too few CTAs.
+// (sequence, kv head, partition) wanted before a longer partition is taken --
+// kItemsPerSm per SM of the current device (912 on a 152-SM GB300), below which
+// the persistent kernels' last wave leaves SMs idle (a sweep of 512..8192 tokens
+// on the 7B, 8B, 70B and beam decode shapes, 16- and 8-bit).  The CUDA-core
+// kernel, one CTA per item, keeps 512 (1024 past kLongContext): longer
+// partitions leave it too few CTAs.
 constexpr int kMinPartition = 512;
 constexpr int kMaxPartition = 4096;
 constexpr int kMaxLongPartition = 8192;
 constexpr int kLongContext = 32768;
-constexpr int64_t kMinItems = 6 * 152;
+constexpr int64_t kItemsPerSm = 6;
+constexpr int kDefaultSms = 152;   // GB300; used where no device can be queried (host-only callers)
+
+// SMs of the current device (looked up once per device), or kDefaultSms when no
+// device is present.  The persistent decode kernels launch one CTA per SM, so
+// their default partition size follows this count.
+int device_sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    (void)cudaGetLastError();
+    return kDefaultSms;
+  }
+  if (dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    (void)cudaGetLastError();
+    return kDefaultSms;
+  }
+  if (dev < 64) cached[dev].store(sms, std::memory_order_relaxed);
+  return sms;
+}
 
 // Kernel choice: the tensor-core kernel serves head_size 128 (group sizes 1-16,
 // up to pkv::kTcMaxSeqs sequences); the CUDA-core kernel serves the rest.  The
@@ -147,6 +173,56 @@ namespace pkv {
 // Record a message for pa_last_error_message() (used by entry points defined in
 // other translation units).
 void set_last_error(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
+
+// Every host-side check of pa_decode_window's arguments except the workspace
+// (shared with pa_decode_static_workspace, whose workspace is the library's
+// own): PA_OK with *need = the workspace bytes these shapes use, or the first
+// failing check's status (message recorded).  num_seqs == 0 passes with
+// *need = 0 (nothing to launch).
+pa_status check_decode_args(const void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,
+                            const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
+                            int32_t block_table_stride, const int32_t* context_lens, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t max_context_len, float scale, int32_t window,
+                            int32_t ring_blocks, int32_t partition_size, size_t* need) {
+  *need = 0;
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (layer < 0 || layer >= desc->num_layers) return fail(PA_ERR_INVALID_ARG, "layer %d", layer);
+  if (num_seqs < 0 || num_seqs > 65535) return fail(PA_ERR_INVALID_ARG, "num_seqs %d not in [0, 65535]", num_seqs);
+  if (num_seqs == 0) return PA_OK;
+  if (num_q_heads <= 0 || num_q_heads % desc->num_kv_heads)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
+                num_q_heads, desc->num_kv_heads);
+  const int group = num_q_heads / desc->num_kv_heads;
+  if (group != 1 && group != 2 && group != 4 && group != 8 &&
+      !(group == 16 && desc->head_size == 128 && desc->block_size >= 8))
+    return fail(PA_ERR_UNSUPPORTED,
+                "query heads per kv head %d (supported: 1, 2, 4, 8; 16 at head_size 128 with block_size >= 8)", group);
+  if (desc->num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads > 65535");
+  if (is_i8(desc) && group > 8)
+    return fail(PA_ERR_UNSUPPORTED, "8-bit cache with %d query heads per kv head (supported: 1, 2, 4, 8)", group);
+  if (!out || !q || !kv_cache || !block_tables || !context_lens)
+    return fail(PA_ERR_INVALID_ARG, "out, q, kv_cache, block_tables and context_lens must be non-NULL");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(kv_cache))
+    return fail(PA_ERR_INVALID_ARG, "out, q and kv_cache must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3) || (reinterpret_cast<uintptr_t>(context_lens) & 3))
+    return fail(PA_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
+  if (q_seq_stride < (int64_t)num_q_heads * desc->head_size || q_seq_stride % 8)
+    return fail(PA_ERR_INVALID_ARG, "q_seq_stride must be >= num_q_heads*head_size and a multiple of 8");
+  if (block_table_stride <= 0) return fail(PA_ERR_INVALID_ARG, "block_table_stride %d", block_table_stride);
+  if (max_context_len <= 0) return fail(PA_ERR_INVALID_ARG, "max_context_len %d", max_context_len);
+  if (window < 0) return fail(PA_ERR_INVALID_ARG, "window %d < 0", window);
+  if (ring_blocks < 0 || ring_blocks > block_table_stride)
+    return fail(PA_ERR_INVALID_ARG, "ring_blocks %d not in [0, block_table_stride %d]", ring_blocks,
+                block_table_stride);
+  const int32_t span = pa_decode_window_span(max_context_len, desc->block_size, window, ring_blocks);
+  const int32_t P = pa_decode_partition_size(desc, num_seqs, span, partition_size);
+  if (P % 128 || P < 128 || P > 8192)
+    return fail(PA_ERR_INVALID_ARG, "partition_size %d must be a multiple of 128 in [128, 8192]", P);
+  if (!(scale > 0.f) || scale != scale) return fail(PA_ERR_INVALID_ARG, "scale must be a positive number");
+  *need = pa_decode_workspace_bytes(desc, num_seqs, num_q_heads, span, P);
+  return PA_OK;
+}
 }  // namespace pkv
 
 extern "C" {
@@ -222,7 +298,7 @@ int32_t pa_decode_partition_size(const pa_cache_desc* desc, int32_t num_seqs, in
   const int64_t pairs = (int64_t)(num_seqs > 0 ? num_seqs : 0) * (desc->num_kv_heads > 0 ? desc->num_kv_heads : 0);
   const int64_t ctx = max_context_len > 0 ? max_context_len : 0;
   for (int P = max_context_len > kLongContext ? kMaxLongPartition : kMaxPartition; P > kMinPartition; P /= 2)
-    if (pairs * ((ctx + P - 1) / P) >= kMinItems) return P;
+    if (pairs * ((ctx + P - 1) / P) >= kItemsPerSm * device_sm_count()) return P;
   return kMinPartition;
 }
 
@@ -254,46 +330,18 @@ pa_status pa_decode_window(void* out, const void* q, int64_t q_seq_stride, const
                            int32_t num_q_heads, int32_t max_context_len, float scale, int32_t window,
                            int32_t ring_blocks, int32_t partition_size, void* workspace, size_t workspace_bytes,
                            uint32_t* dev_err, void* stream) {
-  pa_status st = check_desc(desc);
-  if (st != PA_OK) return st;
-  if (layer < 0 || layer >= desc->num_layers) return fail(PA_ERR_INVALID_ARG, "layer %d", layer);
-  if (num_seqs < 0 || num_seqs > 65535) return fail(PA_ERR_INVALID_ARG, "num_seqs %d not in [0, 65535]", num_seqs);
-  if (num_seqs == 0) return PA_OK;
-  if (num_q_heads <= 0 || num_q_heads % desc->num_kv_heads)
-    return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
-                num_q_heads, desc->num_kv_heads);
-  const int group = num_q_heads / desc->num_kv_heads;
-  if (group != 1 && group != 2 && group != 4 && group != 8 &&
-      !(group == 16 && desc->head_size == 128 && desc->block_size >= 8))
-    return fail(PA_ERR_UNSUPPORTED,
-                "query heads per kv head %d (supported: 1, 2, 4, 8; 16 at head_size 128 with block_size >= 8)", group);
-  if (desc->num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads > 65535");
-  if (is_i8(desc) && group > 8)
-    return fail(PA_ERR_UNSUPPORTED, "8-bit cache with %d query heads per kv head (supported: 1, 2, 4, 8)", group);
-  if (!out || !q || !kv_cache || !block_tables || !context_lens)
-    return fail(PA_ERR_INVALID_ARG, "out, q, kv_cache, block_tables and context_lens must be non-NULL");
-  if (!aligned16(out) || !aligned16(q) || !aligned16(kv_cache))
-    return fail(PA_ERR_INVALID_ARG, "out, q and kv_cache must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(block_tables) & 3) || (reinterpret_cast<uintptr_t>(context_lens) & 3))
-    return fail(PA_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
-  if (q_seq_stride < (int64_t)num_q_heads * desc->head_size || q_seq_stride % 8)
-    return fail(PA_ERR_INVALID_ARG, "q_seq_stride must be >= num_q_heads*head_size and a multiple of 8");
-  if (block_table_stride <= 0) return fail(PA_ERR_INVALID_ARG, "block_table_stride %d", block_table_stride);
-  if (max_context_len <= 0) return fail(PA_ERR_INVALID_ARG, "max_context_len %d", max_context_len);
-  if (window < 0) return fail(PA_ERR_INVALID_ARG, "window %d < 0", window);
-  if (ring_blocks < 0 || ring_blocks > block_table_stride)
-    return fail(PA_ERR_INVALID_ARG, "ring_blocks %d not in [0, block_table_stride %d]", ring_blocks,
-                block_table_stride);
-  const int32_t span = pa_decode_window_span(max_context_len, desc->block_size, window, ring_blocks);
-  const int32_t P = pa_decode_partition_size(desc, num_seqs, span, partition_size);
-  if (P % 128 || P < 128 || P > 8192)
-    return fail(PA_ERR_INVALID_ARG, "partition_size %d must be a multiple of 128 in [128, 8192]", P);
-  if (!(scale > 0.f) || scale != scale) return fail(PA_ERR_INVALID_ARG, "scale must be a positive number");
-  const size_t need = pa_decode_workspace_bytes(desc, num_seqs, num_q_heads, span, P);
+  size_t need = 0;
+  pa_status st = pkv::check_decode_args(out, q, q_seq_stride, kv_cache, desc, layer, block_tables,
+                                        block_table_stride, context_lens, num_seqs, num_q_heads, max_context_len,
+                                        scale, window, ring_blocks, partition_size, &need);
+  if (st != PA_OK || num_seqs == 0) return st;
   if (workspace_bytes < need)
     return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", workspace_bytes, need);
   if (need && (!workspace || !aligned16(workspace)))
     return fail(PA_ERR_INVALID_ARG, "workspace must be non-NULL and 16-byte aligned");
+  const int group = num_q_heads / desc->num_kv_heads;
+  const int32_t span = pa_decode_window_span(max_context_len, desc->block_size, window, ring_blocks);
+  const int32_t P = pa_decode_partition_size(desc, num_seqs, span, partition_size);
 
   pkv::DecodeParams p{};
   p.out = out;

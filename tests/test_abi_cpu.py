@@ -153,6 +153,38 @@ def test_decode_rejects_bad_arguments(lib):
     assert _decode(lib, S=0) == _lib.PA_OK                                 # nothing to do
 
 
+def _decode_static(lib, desc=None, S=2, Hq=4, max_ctx=100, P=0, scale=0.1):
+    return lib.pa_decode_static_workspace(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), Hq * 128,
+                                          ctypes.c_void_p(FAKE), ctypes.byref(desc or _desc()), 0,
+                                          ctypes.c_void_p(FAKE), 8, ctypes.c_void_p(FAKE), S, Hq, max_ctx, scale, P,
+                                          None, None)
+
+
+def test_static_workspace_checks_arguments_before_its_size(lib):
+    # a bad argument is reported as such, even where the shapes would also be
+    # too large for the library's fixed workspace
+    assert _decode_static(lib, P=100) == _lib.PA_ERR_INVALID_ARG
+    assert _decode_static(lib, S=4096, Hq=64, desc=_desc(num_kv_heads=8), max_ctx=8192, P=64) == _lib.PA_ERR_INVALID_ARG
+    assert b"partition_size" in lib.pa_last_error_message()
+    assert _decode_static(lib, Hq=6) == _lib.PA_ERR_UNSUPPORTED
+    assert _decode_static(lib, scale=0.0) == _lib.PA_ERR_INVALID_ARG
+    # valid arguments, too large a workspace: refused before any launch
+    assert _decode_static(lib, S=4096, Hq=64, desc=_desc(num_kv_heads=8), max_ctx=8192, P=128) == \
+        _lib.PA_ERR_WORKSPACE_TOO_SMALL
+    assert b"PA_STATIC_WORKSPACE_BYTES" in lib.pa_last_error_message()
+    assert _decode_static(lib, S=0) == _lib.PA_OK
+
+
+def test_static_workspace_size_matches_the_header():
+    src = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    m = re.search(r"#define\s+PA_STATIC_WORKSPACE_BYTES\s+\(([0-9u\s*]+)\)", src)
+    assert m, "PA_STATIC_WORKSPACE_BYTES not found in pagedkv.h"
+    value = 1
+    for f in m.group(1).split("*"):
+        value *= int(f.strip().rstrip("u"))
+    assert value == _lib.STATIC_WORKSPACE_BYTES
+
+
 def test_reshape_rejects_bad_arguments(lib):
     call = lambda stride, n=4, key=FAKE, layer=0: lib.pa_reshape_and_cache(
         ctypes.c_void_p(FAKE), ctypes.byref(_desc()), layer, ctypes.c_void_p(key), stride,

@@ -6,9 +6,11 @@ that forbids allocation once it is running, a binding from another language that
 cannot keep a device buffer alive between calls.  For them the library offers an
 entry point that takes no workspace and uses a fixed array in its own device
 memory instead.  These tests call it through the C ABI and check that it gives
-the same output as pa_decode with a caller-allocated workspace, on two calls in
-a row (the second call must not be disturbed by what the first left in the
-shared array), and that shapes too large for the array are refused.
+the same output as pa_decode with a caller-allocated workspace (and the fp64
+oracle's within the attention tolerance), on two calls in a row (the second
+call must not be disturbed by what the first left in the shared array), for
+16-bit and 8-bit caches and the default partition size, and that shapes too
+large for the array are refused.
 
 This file is named so that pytest collects it last."""
 import math
@@ -17,9 +19,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_168_gb300 as pkv
-from gpu_helpers import assert_attention_close, ensure_built, paged_to_dev, run_decode
-from paged_helpers import Paged
+from gpu_helpers import TORCH_DT, assert_attention_close, ensure_built, paged_to_dev, run_decode, u16_to_dev
+from paged_helpers import Paged, to_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -34,22 +37,86 @@ def _case(seed, ctx, Hq=8, Hkv=2, D=128, bs=16, dtype="bf16"):
     return p, paged_to_dev(p)
 
 
-def test_static_workspace_matches_caller_workspace_on_two_calls():
+def _i8_case(seed, ctx, Hq=8, Hkv=2, bs=16, dtype="bf16"):
+    """An 8-bit pool the oracle writes from random K/V, random block placement."""
+    rng = np.random.default_rng(seed)
+    ctx = np.asarray(ctx, np.int32)
+    nblk = -(-ctx // bs)
+    nb = int(nblk.sum()) + 3
+    g = oracle.Geom(nb, bs, Hkv, 128, dtype)
+    pool = np.zeros(nb * oracle.i8_block_bytes(g), np.uint8)
+    width = int(nblk.max())
+    tables = np.full((len(ctx), width), -1, np.int32)
+    perm = rng.permutation(nb)
+    at = 0
+    for s, c in enumerate(ctx):
+        tables[s, :nblk[s]] = perm[at:at + nblk[s]]
+        at += nblk[s]
+        t = np.arange(c)
+        slots = tables[s, t // bs].astype(np.int64) * bs + t % bs
+        x = rng.standard_normal((2, c, Hkv, 128))
+        assert oracle.reshape_and_cache_i8(pool, g, to_bits(x[0], dtype), to_bits(x[1], dtype), slots) == 0
+    q_bits = to_bits(rng.standard_normal((len(ctx), Hq, 128)), dtype)
+    desc = pkv.CacheDesc(nb, bs, Hkv, 128, TORCH_DT[dtype], kv_int8=True)
+    dev = (u16_to_dev(q_bits, dtype), torch.from_numpy(pool).cuda(), torch.from_numpy(tables).cuda(),
+           torch.from_numpy(ctx).cuda(), desc)
+    return (q_bits, pool, g, tables, ctx), dev
+
+
+def _static(q, pool, desc, tables, ctx, max_ctx, scale, P):
+    out = torch.full_like(q, float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv._lib.decode_static_workspace(out, q, pool, desc, tables, ctx, max_ctx, scale, P, dev_err=err)
+    torch.cuda.synchronize()
+    assert pkv.read_device_errors(err) == 0
+    return out
+
+
+def test_static_workspace_matches_caller_workspace_and_oracle_on_two_calls():
+    """Two calls in a row with different data (the second must not be disturbed
+    by what the first left in the shared array), each equal to pa_decode with a
+    caller workspace and within the attention tolerance of the fp64 oracle."""
     P = 128
     cases = [_case(300, [1, 127, 129, 700, 2049, 3000]),
              _case(301, [3000, 5, 1500, 256, 257, 999], Hq=16, Hkv=16, D=64, bs=8, dtype="f16")]
-    for p, (q, pool, tables, ctx, desc) in cases:          # two calls in a row, different data
+    for p, (q, pool, tables, ctx, desc) in cases:
         max_ctx = int(p.ctx.max())
         scale = 1 / math.sqrt(p.D)
         need = pkv.decode_workspace_bytes(desc, p.S, p.Hq, max_ctx, P)
         assert 0 < need <= pkv._lib.STATIC_WORKSPACE_BYTES     # the shared array is really used
         ref = run_decode(q, pool, desc, tables, ctx, max_ctx, scale, P)
-        out = torch.full_like(q, float("nan"))
-        err = torch.zeros(1, dtype=torch.int32, device="cuda")
-        pkv._lib.decode_static_workspace(out, q, pool, desc, tables, ctx, max_ctx, scale, P, dev_err=err)
-        torch.cuda.synchronize()
-        assert pkv.read_device_errors(err) == 0
+        out = _static(q, pool, desc, tables, ctx, max_ctx, scale, P)
         assert_attention_close(out, ref.to(torch.float64).cpu().numpy(), "static workspace vs caller workspace")
+        want, e = oracle.decode(p.q_bits, p.pool, p.geom, p.tables, p.ctx, scale, max_context_len=max_ctx)
+        assert e == 0
+        assert_attention_close(out, want, "static workspace vs oracle")
+
+
+def test_static_workspace_default_partition_and_8bit_cache():
+    """The default partition size (here still several partitions per sequence)
+    and an 8-bit cache, whose kernels lay out their partial results differently;
+    two calls in a row, against pa_decode with a caller workspace and the oracle."""
+    scale = 1 / math.sqrt(128)
+    p, (q, pool, tables, ctx, desc) = _case(302, [5000, 1, 4097, 640, 2500])
+    max_ctx = int(p.ctx.max())
+    assert pkv.decode_partition_size(desc, p.S, max_ctx, 0) < max_ctx            # more than one partition
+    assert pkv.decode_workspace_bytes(desc, p.S, p.Hq, max_ctx, 0) > 0
+    (qb, hpool, g, htables, hctx), (q8, pool8, tables8, ctx8, desc8) = _i8_case(303, [3000, 17, 1029, 2049])
+    max8 = int(hctx.max())
+    assert pkv.decode_workspace_bytes(desc8, len(hctx), 8, max8, 512) > 0
+    for _ in range(2):
+        out = _static(q, pool, desc, tables, ctx, max_ctx, scale, 0)
+        ref = run_decode(q, pool, desc, tables, ctx, max_ctx, scale, 0)
+        assert_attention_close(out, ref.to(torch.float64).cpu().numpy(), "static workspace, default partition")
+        want, e = oracle.decode(p.q_bits, p.pool, p.geom, p.tables, p.ctx, scale, max_context_len=max_ctx)
+        assert e == 0
+        assert_attention_close(out, want, "static workspace, default partition, vs oracle")
+        out8 = _static(q8, pool8, desc8, tables8, ctx8, max8, scale, 512)
+        ref8 = run_decode(q8, pool8, desc8, tables8, ctx8, max8, scale, 512)
+        assert_attention_close(out8, ref8.to(torch.float64).cpu().numpy(), "static workspace, 8-bit cache")
+        want8, e = oracle.decode_i8(qb, hpool, g, htables, hctx, scale, max_context_len=max8)
+        assert e == 0
+        assert_attention_close(out8, want8, "static workspace, 8-bit cache, vs oracle")
 
 
 def test_static_workspace_refuses_shapes_beyond_its_size():

@@ -129,7 +129,7 @@ class ClockSampler:
 
     def __init__(self, index: int, interval_ms: int = 50):
         self.index, self.interval_ms, self.proc, self.lines = index, interval_ms, None, []
-        self.t0 = self.t1 = None
+        self.t0 = self.t1 = self.tt = None
 
     def __enter__(self):
         try:
@@ -144,6 +144,9 @@ class ClockSampler:
 
     def mark_start(self):
         self.t0 = time.time()
+
+    def mark_timed(self):
+        self.tt = time.time()
 
     def mark_end(self):
         self.t1 = time.time()
@@ -167,15 +170,19 @@ class ClockSampler:
         except ValueError:
             return None
 
-    def summary(self):
+    def summary(self, soak_steps: int = 0):
+        """Median SM clock and throttle reasons over the samples taken between
+        mark_start and mark_end (the pre-timing soak and the timed steps)."""
         samples = [x for x in (self._parse(ln) for ln in self.lines) if x]
         if not samples:
             return None
         inside = [x for x in samples if self.t0 is not None and self.t0 <= x[0] <= (self.t1 or x[0])]
+        timed = [x for x in inside if self.tt is None or x[0] >= self.tt]
         used = inside or [min(samples, key=lambda x: abs(x[0] - (self.t0 or x[0])))]
         reasons = sorted({name for x in used for name, v in zip(self.REASONS, x[3]) if v.lower() == "active"})
         return {"sm_mhz": float(np.median([x[1] for x in used])), "sm_max_mhz": max(x[2] for x in used),
-                "reasons": reasons, "samples": len(used), "samples_in_timed_region": len(inside)}
+                "reasons": reasons, "samples": len(used), "samples_in_timed_region": len(timed),
+                "window": f"{soak_steps} untimed steps right before the timed ones, then the timed steps"}
 
 
 def dist_env():
@@ -225,6 +232,24 @@ class HostInputs:
 
     def upload(self):
         self.dev.copy_(self.host, non_blocking=True)
+
+
+def decode_config(w, args, world: int) -> dict:
+    """The `config` object of a decode line, identical in both arms: the workload,
+    its batch and context sizes, the partition size pa_decode takes for it, the
+    parallelism, and how the step compares with the L2."""
+    from paged_kv_cache_168_gb300 import _lib
+    cfg = w.cfg
+    desc = _lib.CacheDesc(w.num_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_size, w.dtype,
+                          kv_int8=cfg.kv_int8)
+    part = _lib.decode_partition_size(desc, cfg.num_seqs, w.max_context_len, args.partition_size)
+    ctx = w.context_lens_np.astype(np.int64)
+    kv_tok = cfg.num_kv_heads * (2 * cfg.head_size + 8) if cfg.kv_int8 else 2 * cfg.num_kv_heads * cfg.head_size * 2
+    return {"workload": DESCRIPTIONS[args.workload] + (f" (first {args.seqs} sequences)" if args.seqs else ""),
+            "global_batch": cfg.num_seqs * world, "max_context_len": w.max_context_len,
+            "tokens_in_context": int(ctx.sum()), "partition_size": part, "parallelism": f"replicas{world}",
+            "l2": f"inputs larger than L2: {_lib.cache_bytes(desc) / 1e9:.2f} GB pool, "
+                  f"{int(ctx.sum()) * kv_tok / 1e9:.2f} GB of KV read per step"}
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -335,7 +360,9 @@ def run_reference(args):
         return 0
     if args.workload in PREFILL_DESCRIPTIONS:
         return run_reference_prefill(args)
+    from paged_kv_cache_168_gb300.build import build
     from paged_kv_cache_168_gb300.workloads import make_workload
+    build()                                   # host-side sizes (the partition size in `config`)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     w = make_workload(args.workload, device=dev, num_seqs=args.seqs)
     cfg = w.cfg
@@ -354,8 +381,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * float(np.median(secs)), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": DESCRIPTIONS[args.workload], "global_batch": cfg.num_seqs,
-                   "max_context_len": w.max_context_len},
+        "config": decode_config(w, args, world),
         "seq_steps_per_s": round(float(np.median(seqs)), 4),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": "each step: " + desc},
@@ -387,7 +413,7 @@ def run_gpu(args):
     cfg = CONFIGS[args.workload]
     w = make_workload(args.workload, device=device, seed=cfg.seed + 1000 * rank, num_seqs=args.seqs)
     stream = torch.cuda.Stream(device)
-    step = DecodeStep(w, partition_size=args.partition_size, stream=stream)
+    step = DecodeStep(w, partition_size=args.partition_size, stream=stream, nvtx=True)
     nbytes = step.algorithmic_bytes()
     torch.cuda.synchronize()
 
@@ -402,7 +428,13 @@ def run_gpu(args):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        # the clock record covers the timed steps and, right before them, the same
+        # step repeated for ~soak seconds (untimed): a timed region of a few ms is
+        # shorter than nvidia-smi's sampling interval
         clocks.mark_start()
+        soak_steps = soak(step, stream, args.clock_soak_seconds)
+        torch.cuda.synchronize()
+        clocks.mark_timed()
         with torch.cuda.stream(stream):
             for i in range(K):
                 ev[i][0].record(stream)
@@ -453,9 +485,13 @@ def run_gpu(args):
     ms = total_ms / K
     value = world * nbytes["total"] / (ms * 1e-3) / 1e9
     dec_ms = float(np.mean(decode_ms))
-    achieved = nbytes["decode"] / (dec_ms * 1e-3) / 1e9
+    achieved = nbytes["decode_unique"] / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
     part = _lib.decode_partition_size(step.desc, w.cfg.num_seqs, w.max_context_len, args.partition_size)
+    del step
+    extras = {}
+    for name in [x for x in args.extra_workloads.split(",") if x and x != args.workload]:
+        extras[name] = measure_workload(name, args, device, stream, peak, rank)
 
     line = None
     if rank == 0:
@@ -472,13 +508,7 @@ def run_gpu(args):
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.cfg.dtype + ("+int8 cache" if w.cfg.kv_int8 else ""),
             "data": "synthetic",
-            "config": {"workload": DESCRIPTIONS[args.workload] + (f" (first {args.seqs} sequences)" if args.seqs else ""),
-                       "global_batch": w.cfg.num_seqs * world,
-                       "max_context_len": w.max_context_len, "tokens_in_context": int(w.context_lens_np.sum()),
-                       "partition_size": part,
-                       "parallelism": f"replicas{world}",
-                       "l2": f"inputs larger than L2: {step.kv_cache.numel() * step.kv_cache.element_size() / 1e9:.2f} GB pool, "
-                             f"{nbytes['decode_kv'] / 1e9:.2f} GB of KV read per step"},
+            "config": decode_config(w, args, world),
             "seq_steps_per_s": round(world * w.cfg.num_seqs / (ms * 1e-3), 1),
             "decode_kv_gbs": round(nbytes["decode_kv"] / (dec_ms * 1e-3) / 1e9, 2),
             "decode_unique_kv_gbs": round(nbytes["decode_kv_unique"] / (dec_ms * 1e-3) / 1e9, 2),
@@ -488,14 +518,16 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "kernel": "pa_decode (decode + log-sum-exp merge)",
                          "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                         "bytes": "algorithmic decode bytes, a shared physical block's tokens counted once",
                          "traffic": recorded_traffic(args.workload, part),
                          "decode_ms": round(dec_ms, 4)},
+            "workloads": extras,
             "cpu_baseline": cpu,
             "e2e": {"value": round(world * nbytes["total"] / (e2e_ms / K * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_ms / K, 4)},
             "gpu_launches": K * step.kernel_launches() * world,
-            "clocks": clocks.summary(),
+            "clocks": clocks.summary(soak_steps),
             "source_digest": source_digest(),
         }
         print(json.dumps(line), flush=True)
@@ -503,6 +535,87 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def soak(step, stream, seconds: float) -> int:
+    """Run the step back to back for about `seconds` (untimed); returns the count."""
+    if seconds <= 0:
+        return 0
+    with torch.cuda.stream(stream):
+        step()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        step()
+        torch.cuda.synchronize()
+        per = max(time.perf_counter() - t0, 1e-5)
+        n = max(1, int(seconds / per))
+        for _ in range(n):
+            step()
+    return n + 2
+
+
+def measure_workload(name: str, args, device, stream, peak: float, rank: int) -> dict:
+    """Decode of another workload in the same run, under the same warm-up and
+    step count as the headline: mean decode time (pa_decode launch), KV GB/s
+    (logical and unique bytes) and the roofline fraction on unique bytes.  For a
+    workload whose sequences share physical blocks it is also timed with a
+    buffer of twice the L2 written between steps, so no step finds the previous
+    one's blocks in L2."""
+    from paged_kv_cache_168_gb300.step import DecodeStep
+    from paged_kv_cache_168_gb300.workloads import CONFIGS, make_workload
+    from paged_kv_cache_168_gb300 import _lib
+    cfg = CONFIGS[name]
+    w = make_workload(name, device=device, seed=cfg.seed + 1000 * rank)
+    step = DecodeStep(w, stream=stream, nvtx=True)
+    nb = step.algorithmic_bytes()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    K = args.steps
+
+    def timed(flush=None):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                if flush is not None:
+                    flush.add_(1)
+                ev[i][0].record(stream)
+                step.cache_ops()
+                ev[i][1].record(stream)
+                step.attention()
+                ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        return [e[1].elapsed_time(e[2]) for e in ev], [e[0].elapsed_time(e[2]) for e in ev]
+
+    dec, tot = timed()
+    assert _lib.read_device_errors(step.dev_err, stream=stream) == 0, f"device error in {name}"
+    dec_ms, step_ms = float(np.mean(dec)), float(np.mean(tot))
+    uniq = nb["decode_unique"] / (dec_ms * 1e-3) / 1e9
+    part = _lib.decode_partition_size(step.desc, cfg.num_seqs, w.max_context_len, 0)
+    r = {"workload": DESCRIPTIONS[name], "partition_size": part, "decode_ms": round(dec_ms, 4),
+         "decode_ms_p10_p50_p90": [round(float(np.percentile(dec, x)), 4) for x in (10, 50, 90)],
+         "decode_kv_gbs": round(nb["decode_kv"] / (dec_ms * 1e-3) / 1e9, 2),
+         "decode_unique_kv_gbs": round(nb["decode_kv_unique"] / (dec_ms * 1e-3) / 1e9, 2),
+         "roofline": {"bound": "hbm", "achieved": round(uniq, 2), "peak": peak, "unit": "GB/s",
+                      "frac": round(uniq / peak, 4), "bytes": "algorithmic decode bytes, shared blocks once"},
+         "frac_of_spec_8tbs": round(nb["decode_kv_unique"] / (dec_ms * 1e-3) / 1e9 / SPEC_HBM_GBS, 4),
+         "seq_steps_per_s": round(cfg.num_seqs / (step_ms * 1e-3), 1),
+         "step_ms": round(step_ms, 4), "step_gbs": round(nb["total"] / (step_ms * 1e-3) / 1e9, 2),
+         "bytes_per_step": nb, "gpu_launches": K * step.kernel_launches()}
+    if nb["decode_kv_unique"] != nb["decode_kv"]:
+        props = torch.cuda.get_device_properties(device)
+        l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 132 * 1024 * 1024
+        flush = torch.zeros(2 * l2 // 4, dtype=torch.int32, device=device)
+        dec_f, _ = timed(flush)
+        fl_ms = float(np.mean(dec_f))
+        r["l2_flushed"] = {"flush_bytes": 2 * l2, "decode_ms": round(fl_ms, 4),
+                           "decode_unique_kv_gbs": round(nb["decode_kv_unique"] / (fl_ms * 1e-3) / 1e9, 2),
+                           "frac": round(nb["decode_unique"] / (fl_ms * 1e-3) / 1e9 / peak, 4)}
+        del flush
+    del step, w
+    torch.cuda.empty_cache()
+    return r
 
 
 # ------------------------------------------------------------------ prefill / extend
@@ -668,6 +781,10 @@ def main(argv=None):
     ap.add_argument("--seqs", type=int, default=None, help="use only the first N sequences (small profiling runs)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
+    ap.add_argument("--extra-workloads", default="8b,70b,beam",
+                    help="decode workloads also measured in the same run (the line's `workloads`); '' for none")
+    ap.add_argument("--clock-soak-seconds", type=float, default=1.0,
+                    help="untimed back-to-back steps before the timed ones, inside the clock record")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

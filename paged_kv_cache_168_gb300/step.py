@@ -38,11 +38,13 @@ class DecodeStep:
     here (outside any timed step) by writing the workload's logical history into
     every slot of every block with pa_reshape_and_cache, which quantises it."""
 
-    def __init__(self, w: Workload, partition_size: int = 0, stream: torch.cuda.Stream | None = None):
+    def __init__(self, w: Workload, partition_size: int = 0, stream: torch.cuda.Stream | None = None,
+                 nvtx: bool = False):
         cfg = w.cfg
         dev = w.q.device
         self.w = w
         self.stream = stream or torch.cuda.current_stream(dev)
+        self.nvtx = nvtx                 # an NVTX range around every library call (for profilers)
         self.desc = _lib.CacheDesc(w.num_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_size, w.dtype,
                                    kv_int8=cfg.kv_int8)
         self.block_bytes = _lib.cache_bytes(self.desc) // w.num_blocks
@@ -74,21 +76,39 @@ class DecodeStep:
             slots = torch.arange(b0 * bs, b0 * bs + n, dtype=torch.int64, device=logical.device)
             _lib.reshape_and_cache(self.kv_cache, self.desc, key, value, slots, stream=self.stream)
 
+    def _range(self, name):
+        if self.nvtx:
+            torch.cuda.nvtx.range_push(name)
+
+    def _end(self):
+        if self.nvtx:
+            torch.cuda.nvtx.range_pop()
+
     def cache_ops(self):
         w, s = self.w, self.stream
         if self.host_pool is not None:
+            self._range("pa_swap_blocks out")
             _lib.swap_blocks(self.host_pool, self.host_desc, self.kv_cache, self.desc, 0, w.swap_out_pairs, stream=s)
+            self._end()
+            self._range("pa_swap_blocks in")
             _lib.swap_blocks(self.kv_cache, self.desc, self.host_pool, self.host_desc, 1, w.swap_in_pairs, stream=s)
+            self._end()
         if w.copy_pairs.shape[0]:
+            self._range("pa_copy_blocks")
             _lib.copy_blocks(self.kv_cache, self.desc, w.copy_pairs, stream=s)
+            self._end()
+        self._range("pa_reshape_and_cache")
         _lib.reshape_and_cache(self.kv_cache, self.desc, w.key, w.value, w.slot_mapping, dev_err=self.dev_err,
                                stream=s)
+        self._end()
 
     def attention(self, q=None, out=None):
         w = self.w
+        self._range("pa_decode")
         _lib.decode(self.out if out is None else out, w.q if q is None else q, self.kv_cache, self.desc,
                     w.block_tables, w.context_lens, w.max_context_len, w.scale, self.workspace,
                     self.partition_size, dev_err=self.dev_err, stream=self.stream)
+        self._end()
 
     def __call__(self):
         self.cache_ops()
@@ -124,8 +144,12 @@ class DecodeStep:
         copy = 2 * w.copy_pairs.shape[0] * block_bytes
         swap = (w.swap_out_pairs.shape[0] + w.swap_in_pairs.shape[0]) * block_bytes * 2
         unique = unique_kv_tokens(w.block_tables_np, w.context_lens_np, cfg.block_size) * kv_tok
-        return {"decode": decode, "decode_kv": int(ctx.sum()) * kv_tok, "decode_kv_unique": unique,
-                "reshape": reshape, "copy": copy, "swap": swap, "total": decode + reshape + copy + swap}
+        # the same decode bytes with each shared physical block's tokens counted
+        # once (what HBM must deliver; equal to `decode` when nothing is shared)
+        decode_unique = decode - int(ctx.sum()) * kv_tok + unique
+        return {"decode": decode, "decode_unique": decode_unique, "decode_kv": int(ctx.sum()) * kv_tok,
+                "decode_kv_unique": unique, "reshape": reshape, "copy": copy, "swap": swap,
+                "total": decode_unique + reshape + copy + swap}
 
 
 class PrefillStep:

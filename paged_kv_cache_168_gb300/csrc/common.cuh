@@ -175,6 +175,19 @@ __device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
+// An ordinary wait of a kernel whose launch carries a poll limit: polls == 0
+// is mbar_wait (the default limit); otherwise at most `polls` non-suspending
+// polls (try_wait may sleep until the phase completes, so only test_wait makes
+// a small limit run out for certain).  Waits that drain a CTA's own copies or
+// tensor-core operations before it exits never take a caller's limit: they
+// always use mbar_wait, so a CTA never leaves work in flight.
+__device__ __forceinline__ bool mbar_wait_polls(uint64_t* bar, uint32_t parity, uint32_t polls) {
+  if (polls == 0) return mbar_wait(bar, parity);
+  for (uint32_t i = 0; i < polls; ++i)
+    if (mbar_test_wait(bar, parity)) return true;
+  return false;
+}
+
 // 1-D bulk copy global -> shared, completing `bytes` transactions on `bar`.
 // dst and src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(I8Cfg<G>::kThreads, 3)
     bool aborted = false;
     for (int st = 0; st < n_stages && !aborted; ++st) {
       const int slot = st % C::kStages;
-      if (st >= C::kStages && !mbar_wait(&empty_bar[slot], ((st / C::kStages) - 1) & 1)) {
+      if (st >= C::kStages && !mbar_wait_polls(&empty_bar[slot], ((st / C::kStages) - 1) & 1, p.wait_polls)) {
         aborted = true;
         break;
       }
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(I8Cfg<G>::kThreads, 3)
   bool aborted = false;
   for (int st = 0; st < n_stages; ++st) {
     const int slot = st % C::kStages;
-    if (!mbar_wait(&full_bar[slot], (st / C::kStages) & 1)) {
+    if (!mbar_wait_polls(&full_bar[slot], (st / C::kStages) & 1, p.wait_polls)) {
       if (lane == 0) report(p.dev_err, PA_DEVERR_TIMEOUT);
       flag_abort = 1;
       aborted = true;

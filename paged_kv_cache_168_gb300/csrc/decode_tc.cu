@@ -116,6 +116,7 @@ struct Shared {
   uint64_t full[NS], empty[NS];
   uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2], q_free[2];
   uint64_t m_full[2];             // MMA issuer -> softmax: tile t's metadata in smeta[t & 1]
+  uint64_t mma_drain[2];          // each MMA-issuing lane's own MMAs, waited for before TMEM is freed
   TileMeta smeta[2];
   uint64_t max_bar[2];            // softmax-warp exchange (bounded waits, unlike bar.sync)
   uint64_t c_full[2], c_free[2];  // softmax -> output warps: per-tile hand-off ring
@@ -262,6 +263,7 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       mbar_init(&sh.max_bar[i], 4);
       mbar_init(&sh.c_full[i], 4);
       mbar_init(&sh.c_free[i], 4);
+      mbar_init(&sh.mma_drain[i], 1);
     }
     sh.abort_flag = 0;
     sh.end_tile = 0x7fffffff;
@@ -578,8 +580,11 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
     } else {
       const int slot = tile_seq % NS;
       if (!aborted && tile_seq >= NS && !mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1)) aborted = true;
-      if (aborted && lane == 0) {
-        // never leave copies in flight: wait (bounded) for the latest phase of every stage
+      if (lane == 0) {
+        // never leave copies in flight, whether or not another role gave up:
+        // wait (bounded) for the latest phase of every stage.  Normally they
+        // have landed or are about to, and the end mark below is only read
+        // after the last tile anyway.
         for (int t = max(0, tile_seq - NS); t < tile_seq; ++t) mbar_wait(&sh.full[t % NS], (t / NS) & 1);
       }
       if (lane == 0) {
@@ -667,6 +672,9 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
         report(p.dev_err, PA_DEVERR_TIMEOUT);
         sh.abort_flag = 1;
       }
+      // every MMA this lane issued completes before TMEM can be freed
+      tc::commit(&sh.mma_drain[0]);
+      mbar_wait(&sh.mma_drain[0], 0);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -726,6 +734,9 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
         report(p.dev_err, PA_DEVERR_TIMEOUT);
         sh.abort_flag = 1;
       }
+      // every MMA this lane issued completes before TMEM can be freed
+      tc::commit(&sh.mma_drain[0]);
+      mbar_wait(&sh.mma_drain[0], 0);
     }
     __syncwarp();
   } else if (kSplitIssue && warp == kPVWarp) {
@@ -769,6 +780,8 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
         report(p.dev_err, PA_DEVERR_TIMEOUT);
         sh.abort_flag = 1;
       }
+      tc::commit(&sh.mma_drain[1]);
+      mbar_wait(&sh.mma_drain[1], 0);
     }
     __syncwarp();
   } else if ((warp >= 2 && warp < 6) || (ping_pong(I8, G) && warp >= kSoftB && warp < kSoftB + 4)) {
@@ -1171,12 +1184,15 @@ __global__ void __launch_bounds__(threads_of(I8, G), 1) decode_tc_kernel(const _
       if (lane == 0) mbar_arrive(&sh.desc_empty[d]);
       ++tile;
     }
-    if (!ok && lane == 0) {
-      // never leave copies in flight: wait (bounded) for the latest phase of every raw slot
+    if (lane == 0) {
+      // never leave copies in flight, whether or not another role gave up:
+      // wait (bounded) for the latest phase of every raw slot
       for (int h = 0; h < 2; ++h)
         for (int t = max(0, tile - NRH); t < tile; ++t) mbar_wait(&sh.raw_full[h * NRH + t % NRH], (t / NRH) & 1);
-      report(p.dev_err, PA_DEVERR_TIMEOUT);
-      sh.abort_flag = 1;   // the other roles see it and leave their (bounded) loops
+      if (!ok) {
+        report(p.dev_err, PA_DEVERR_TIMEOUT);
+        sh.abort_flag = 1;   // the other roles see it and leave their (bounded) loops
+      }
     }
   }
 

@@ -36,6 +36,8 @@ struct DecodeParams {
   uint32_t* dev_err;
   int32_t window;             // > 0: attend only positions >= ctx - window
   int32_t ring_blocks;        // > 0: table rows are rings; logical block j at entry j % ring_blocks
+  uint32_t wait_polls;        // 0: default bounded waits; > 0: ordinary waits give up after this many
+                              // polls (tests of the timeout path; CUDA-core kernels)
 };
 
 // First position a decode attends for context length ctx: inside the window

@@ -85,6 +85,19 @@ bool use_tensor_cores(int head_size, int block_size, int group, int num_seqs) {
 
 bool is_i8(const pa_cache_desc* d) { return d->dtype == PA_INT8_F16 || d->dtype == PA_INT8_BF16; }
 
+// Test hook for the timeout path: PAGEDKV_WAIT_POLLS=n (n >= 1) makes the
+// ordinary waits of the CUDA-core decode kernels give up after n
+// non-suspending polls instead of the default bound, so a test can make them
+// run out and check PA_DEVERR_TIMEOUT and the abandoned items' zeroed rows.
+// Unset (or invalid): 0, the default.
+uint32_t test_wait_polls() {
+  const char* env = getenv("PAGEDKV_WAIT_POLLS");
+  if (!env || !*env) return 0;
+  char* end = nullptr;
+  const unsigned long v = strtoul(env, &end, 10);
+  return (end && *end == 0 && v > 0 && v < (1ul << 24)) ? (uint32_t)v : 0;
+}
+
 // Whether these shapes get a tensor-core kernel by default (the environment
 // switch aside): 16-bit caches as use_tensor_cores; 8-bit caches at head_size
 // 128 up to pkv::kTcI8MaxSeqs sequences, any block size.
@@ -362,6 +375,7 @@ pa_status pa_decode_window(void* out, const void* q, int64_t q_seq_stride, const
   p.window = window;
   p.ring_blocks = ring_blocks;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_polls = test_wait_polls();
   const int64_t parts = p.max_parts;
   p.ws_o = need ? static_cast<float*>(workspace) : nullptr;
   p.ws_ml = need ? static_cast<float*>(workspace) + (int64_t)num_seqs * num_q_heads * parts * desc->head_size

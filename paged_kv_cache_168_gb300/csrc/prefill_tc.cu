@@ -83,6 +83,7 @@ struct Shared {
   // never two phases behind (the parity it waits for would then alias).
   uint64_t full[2], empty[2], s_full[2], s_free[2], p_full[2], pv_done[2];
   uint64_t xbar;                  // the two softmax warpgroups' per-row exchanges
+  uint64_t mma_drain;             // the issuer's own MMAs, waited for before TMEM is freed
   float red[2][2][kRows];         // [exchange parity][warpgroup][row]
   uint32_t tmem_base;
   int bad;
@@ -176,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
     mbar_init(&sh.pv_done[0], 1);
     mbar_init(&sh.pv_done[1], 1);
     mbar_init(&sh.xbar, kSoftmaxWarps);
+    mbar_init(&sh.mma_drain, 1);
     sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -231,8 +233,9 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
       if (aborted) {
         report(p.dev_err, PA_DEVERR_TIMEOUT);
         sh.abort_flag = 1;
-        for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(&sh.full[j & 1], (j >> 1) & 1);
       }
+      // never leave copies in flight, whether or not another role gave up
+      for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(&sh.full[j & 1], (j >> 1) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -303,6 +306,9 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
         report(p.dev_err, PA_DEVERR_TIMEOUT);
         sh.abort_flag = 1;
       }
+      // every MMA this lane issued completes before TMEM can be freed
+      tc::commit(&sh.mma_drain);
+      mbar_wait(&sh.mma_drain, 0);
     }
     __syncwarp();
   } else {

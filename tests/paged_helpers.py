@@ -114,3 +114,28 @@ class RingPaged:
             V = torch.from_numpy(self.V[s][lo:c]).permute(1, 0, 2).repeat_interleave(G, 0)
             out[s] = torch.nn.functional.scaled_dot_product_attention(q, K, V, scale=scale)[:, 0, :].numpy()
         return out
+
+
+def i8_pool_case(rng, ctx, Hq, Hkv, bs, dtype):
+    """An 8-bit pool the oracle writes from random N(0,1) K/V of each sequence
+    (head_size 128), blocks placed by a random permutation; unused blocks stay
+    zero.  Returns (q_bits [S, Hq, 128], pool bytes, geom, tables, ctx)."""
+    ctx = np.asarray(ctx, np.int32)
+    nblk = -(-ctx // bs)
+    nb = int(nblk.sum()) + 3
+    g = oracle.Geom(nb, bs, Hkv, 128, dtype)
+    pool = np.zeros(nb * oracle.i8_block_bytes(g), np.uint8)
+    tables = np.full((len(ctx), max(int(nblk.max()), 1)), -1, np.int32)
+    perm = rng.permutation(nb)
+    at = 0
+    for s, c in enumerate(ctx):
+        tables[s, :nblk[s]] = perm[at:at + nblk[s]]
+        at += nblk[s]
+        if c == 0:
+            continue
+        t = np.arange(c)
+        slots = tables[s, t // bs].astype(np.int64) * bs + t % bs
+        x = rng.standard_normal((2, c, Hkv, 128))
+        assert oracle.reshape_and_cache_i8(pool, g, to_bits(x[0], dtype), to_bits(x[1], dtype), slots) == 0
+    q_bits = to_bits(rng.standard_normal((len(ctx), Hq, 128)), dtype)
+    return q_bits, pool, g, tables, ctx

@@ -22,7 +22,7 @@ import torch
 import oracle
 import paged_kv_cache_168_gb300 as pkv
 from gpu_helpers import TORCH_DT, assert_attention_close, ensure_built, paged_to_dev, run_decode, u16_to_dev
-from paged_helpers import Paged, to_bits
+from paged_helpers import Paged, i8_pool_case
 
 pytestmark = pytest.mark.gpu
 
@@ -39,25 +39,8 @@ def _case(seed, ctx, Hq=8, Hkv=2, D=128, bs=16, dtype="bf16"):
 
 def _i8_case(seed, ctx, Hq=8, Hkv=2, bs=16, dtype="bf16"):
     """An 8-bit pool the oracle writes from random K/V, random block placement."""
-    rng = np.random.default_rng(seed)
-    ctx = np.asarray(ctx, np.int32)
-    nblk = -(-ctx // bs)
-    nb = int(nblk.sum()) + 3
-    g = oracle.Geom(nb, bs, Hkv, 128, dtype)
-    pool = np.zeros(nb * oracle.i8_block_bytes(g), np.uint8)
-    width = int(nblk.max())
-    tables = np.full((len(ctx), width), -1, np.int32)
-    perm = rng.permutation(nb)
-    at = 0
-    for s, c in enumerate(ctx):
-        tables[s, :nblk[s]] = perm[at:at + nblk[s]]
-        at += nblk[s]
-        t = np.arange(c)
-        slots = tables[s, t // bs].astype(np.int64) * bs + t % bs
-        x = rng.standard_normal((2, c, Hkv, 128))
-        assert oracle.reshape_and_cache_i8(pool, g, to_bits(x[0], dtype), to_bits(x[1], dtype), slots) == 0
-    q_bits = to_bits(rng.standard_normal((len(ctx), Hq, 128)), dtype)
-    desc = pkv.CacheDesc(nb, bs, Hkv, 128, TORCH_DT[dtype], kv_int8=True)
+    q_bits, pool, g, tables, ctx = i8_pool_case(np.random.default_rng(seed), ctx, Hq, Hkv, bs, dtype)
+    desc = pkv.CacheDesc(g.num_blocks, bs, Hkv, 128, TORCH_DT[dtype], kv_int8=True)
     dev = (u16_to_dev(q_bits, dtype), torch.from_numpy(pool).cuda(), torch.from_numpy(tables).cuda(),
            torch.from_numpy(ctx).cuda(), desc)
     return (q_bits, pool, g, tables, ctx), dev

@@ -488,6 +488,7 @@ def run_gpu(args):
     achieved = nbytes["decode_unique"] / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
     part = _lib.decode_partition_size(step.desc, w.cfg.num_seqs, w.max_context_len, args.partition_size)
+    launches = K * step.kernel_launches() * world
     del step
     extras = {}
     for name in [x for x in args.extra_workloads.split(",") if x and x != args.workload]:
@@ -526,7 +527,7 @@ def run_gpu(args):
             "e2e": {"value": round(world * nbytes["total"] / (e2e_ms / K * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_ms / K, 4)},
-            "gpu_launches": K * step.kernel_launches() * world,
+            "gpu_launches": launches,
             "clocks": clocks.summary(soak_steps),
             "source_digest": source_digest(),
         }

@@ -12,10 +12,17 @@ import torch
 
 import oracle
 import paged_kv_cache_168_gb300 as pkv
-from gpu_helpers import assert_attention_close, ensure_built, paged_to_dev, u16_to_dev
+import gpu_helpers
+from gpu_helpers import ensure_built, paged_to_dev, u16_to_dev
 from paged_helpers import Paged, to_bits
 
 pytestmark = pytest.mark.gpu
+
+
+def assert_attention_close(got, ref, what=""):
+    """The combined attention bound only (no separate fp16 max-rel bound): the
+    fp16 PV product takes the weights as one fp16 operand."""
+    return gpu_helpers.assert_attention_close(got, ref, what, strict_fp16=False)
 
 
 @pytest.fixture(scope="module", autouse=True)

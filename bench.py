@@ -90,7 +90,7 @@ def measured_tensor_peak():
 
 
 # the sources the decode launch (tensor-core decode + log-sum-exp merge) is built from
-DECODE_SOURCES = ("common.cuh", "tc_common.cuh", "kernels.h", "decode_tc.cu", "decode_simt.cu")
+DECODE_SOURCES = ("common.cuh", "tc_common.cuh", "kernels.h", "decode_tc.cuh", "decode_tc.cu", "decode_simt.cu")
 
 
 def source_digest() -> str:
@@ -242,7 +242,11 @@ def decode_config(w, args, world: int) -> dict:
     cfg = w.cfg
     desc = _lib.CacheDesc(w.num_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_size, w.dtype,
                           kv_int8=cfg.kv_int8)
-    part = _lib.decode_partition_size(desc, cfg.num_seqs, w.max_context_len, args.partition_size)
+    if w.group_start is not None:      # shared prompt blocks: pa_decode_shared_prefix's partition
+        part = _lib.decode_shared_prefix_partition_size(desc, cfg.num_seqs, cfg.num_q_heads, len(w.prefix_lens_np),
+                                                        w.max_context_len, args.partition_size)
+    else:
+        part = _lib.decode_partition_size(desc, cfg.num_seqs, w.max_context_len, args.partition_size)
     ctx = w.context_lens_np.astype(np.int64)
     kv_tok = cfg.num_kv_heads * (2 * cfg.head_size + 8) if cfg.kv_int8 else 2 * cfg.num_kv_heads * cfg.head_size * 2
     return {"workload": DESCRIPTIONS[args.workload] + (f" (first {args.seqs} sequences)" if args.seqs else ""),
@@ -487,7 +491,8 @@ def run_gpu(args):
     dec_ms = float(np.mean(decode_ms))
     achieved = nbytes["decode_unique"] / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
-    part = _lib.decode_partition_size(step.desc, w.cfg.num_seqs, w.max_context_len, args.partition_size)
+    part = step.partition()
+    step_sp = step.shared_prefix
     launches = K * step.kernel_launches() * world
     del step
     extras = {}
@@ -516,7 +521,8 @@ def run_gpu(args):
             "decode_ms_p10_p50_p90": [round(float(np.percentile(decode_ms, x)), 4) for x in (10, 50, 90)],
             "frac_of_spec_8tbs": round(achieved / SPEC_HBM_GBS, 4),
             "bytes_per_step": nbytes,
-            "roofline": {"bound": "hbm", "kernel": "pa_decode (decode + log-sum-exp merge)",
+            "roofline": {"bound": "hbm", "kernel": ("pa_decode_shared_prefix" if step_sp else "pa_decode")
+                                                   + " (decode + log-sum-exp merge)",
                          "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                          "bytes": "algorithmic decode bytes, a shared physical block's tokens counted once",
@@ -593,8 +599,9 @@ def measure_workload(name: str, args, device, stream, peak: float, rank: int) ->
     assert _lib.read_device_errors(step.dev_err, stream=stream) == 0, f"device error in {name}"
     dec_ms, step_ms = float(np.mean(dec)), float(np.mean(tot))
     uniq = nb["decode_unique"] / (dec_ms * 1e-3) / 1e9
-    part = _lib.decode_partition_size(step.desc, cfg.num_seqs, w.max_context_len, 0)
-    r = {"workload": DESCRIPTIONS[name], "partition_size": part, "decode_ms": round(dec_ms, 4),
+    part = step.partition()
+    r = {"workload": DESCRIPTIONS[name], "partition_size": part,
+         "call": "pa_decode_shared_prefix" if step.shared_prefix else "pa_decode", "decode_ms": round(dec_ms, 4),
          "decode_ms_p10_p50_p90": [round(float(np.percentile(dec, x)), 4) for x in (10, 50, 90)],
          "decode_kv_gbs": round(nb["decode_kv"] / (dec_ms * 1e-3) / 1e9, 2),
          "decode_unique_kv_gbs": round(nb["decode_kv_unique"] / (dec_ms * 1e-3) / 1e9, 2),

@@ -105,6 +105,9 @@ typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1, PA_INT8_F16 = 2, PA_INT8_BF16 =
 #define PA_DEVERR_SLOT 0x2u      /* a slot_mapping entry is not -1 and not in [0, num_blocks*block_size) */
 #define PA_DEVERR_CONTEXT 0x4u   /* context_lens[s] > block_table_stride*block_size or > max_context_len */
 #define PA_DEVERR_TIMEOUT 0x8u   /* a bounded wait inside a kernel ran out (the item was abandoned) */
+#define PA_DEVERR_PREFIX 0x10u   /* pa_decode_shared_prefix: a member's block ids differ from its group's
+                                    inside the shared prefix (its rows are zeroed), or the group
+                                    starts are out of order (sharing is then ignored) */
 
 /* Geometry of a cache pool.  head_size in {64, 128}; block_size in {1, 2, 4, 8, 16, 32}
  * (block_size 1 is token-granular paging);
@@ -247,6 +250,59 @@ pa_status pa_prefill(void* out, const void* q, int64_t q_token_stride, const voi
                      int32_t block_table_stride, const int32_t* context_lens,
                      const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads,
                      int32_t max_query_len, float scale, uint32_t* dev_err, void* stream);
+
+/* Paged decode where groups of sequences share the first tokens of their
+ * context physically: beams of one prompt, or parallel samples, whose prompt
+ * blocks are the same physical blocks in every member's block table (the
+ * mlqm.cn article's copy-on-write example, section 二.2.2: samples of one
+ * request share the prompt's blocks until one writes; the "vLLM" page's
+ * CacheEngine copies a block only when a beam writes into it).  The result is
+ * pa_decode's; the shared blocks are read from memory once per group and kv
+ * head instead of once per member.
+ *   group_start  device int32 [num_groups + 1], non-decreasing in [0, num_seqs]:
+ *                group g is sequences group_start[g] .. group_start[g+1] - 1
+ *                (consecutive; sequences outside every group are decoded alone).
+ *   prefix_lens  device int32 [num_groups]: tokens at the start of every member's
+ *                context whose block-table entries are the same in all members.
+ *                The kernel uses the largest whole number of blocks <= both
+ *                prefix_lens[g] and the group's shortest context, so any value is
+ *                safe; a group of one sequence shares nothing.
+ *   num_groups   0 .. num_seqs (0: plain pa_decode).
+ * The prefix is read through the table row of the first member of each chunk
+ * of 16 / (num_q_heads / num_kv_heads) members (one tensor-core item serves a
+ * chunk's query heads together).  A member whose table entries differ from
+ * that row inside the prefix gets zero output rows and PA_DEVERR_PREFIX; group
+ * starts out of order make the call ignore the groups (each sequence read
+ * through its own row) and also set PA_DEVERR_PREFIX.
+ * Other arguments as pa_decode; size the workspace with
+ * pa_decode_shared_prefix_workspace_bytes and take the default partition size
+ * from pa_decode_shared_prefix_partition_size (the same arguments).  Served by
+ * a dedicated tensor-core kernel for a 16-bit cache, head_size 128,
+ * block_size >= 8, 1, 2, 4 or 8 query heads per kv head and at most 192
+ * sequences; other shapes run pa_decode (the same result, without the sharing).
+ * No windows or ring tables. */
+pa_status pa_decode_shared_prefix(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,
+                                  const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
+                                  int32_t block_table_stride, const int32_t* context_lens, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t max_context_len, float scale,
+                                  const int32_t* group_start, const int32_t* prefix_lens, int32_t num_groups,
+                                  int32_t partition_size, void* workspace, size_t workspace_bytes,
+                                  uint32_t* dev_err, void* stream);
+
+/* The partition size pa_decode_shared_prefix uses: partition_size when > 0;
+ * else, where its dedicated kernel serves the shapes and num_groups > 0, the
+ * tensor-core rule of pa_decode_partition_size applied to the groups' prefixes
+ * (num_groups * num_kv_heads * ceil(max_context_len / P) >= 6 items per SM);
+ * otherwise pa_decode_partition_size(desc, num_seqs, max_context_len, 0). */
+int32_t pa_decode_shared_prefix_partition_size(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_q_heads,
+                                               int32_t num_groups, int32_t max_context_len, int32_t partition_size);
+
+/* Workspace bytes pa_decode_shared_prefix needs (partition_size 0: the default
+ * above).  Where the dedicated kernel serves the shapes: num_seqs *
+ * num_q_heads * (ceil(max_context_len / P) + 1) * (head_size + 2) floats plus
+ * 3 * num_seqs ints, rounded up to 16 bytes; otherwise pa_decode's. */
+size_t pa_decode_shared_prefix_workspace_bytes(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_q_heads,
+                                               int32_t num_groups, int32_t max_context_len, int32_t partition_size);
 
 /* Size of the workspace the library carries for pa_decode_static_workspace
  * (32 MiB on every device that loads the library, held until the process exits). */

@@ -21,13 +21,14 @@ _lib = None
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_WORKSPACE_TOO_SMALL, PA_ERR_OUT_OF_BLOCKS = range(6)
 PA_ALLOC_OK, PA_ALLOC_LATER, PA_ALLOC_NEVER = range(3)
 PA_F16, PA_BF16, PA_INT8_F16, PA_INT8_BF16 = 0, 1, 2, 3
-DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_CONTEXT, DEVERR_TIMEOUT = 1, 2, 4, 8
+DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_CONTEXT, DEVERR_TIMEOUT, DEVERR_PREFIX = 1, 2, 4, 8, 16
 DTYPE_CODE = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 
 EXPORTED = [
     "pa_cache_bytes", "pa_cache_element_offset", "pa_cache_scale_offset", "pa_reshape_and_cache", "pa_decode_workspace_bytes",
     "pa_decode_partition_size", "pa_decode", "pa_decode_window", "pa_decode_window_span", "pa_prefill",
-    "pa_decode_static_workspace", "pa_copy_blocks", "pa_swap_blocks", "pa_read_device_errors",
+    "pa_decode_static_workspace", "pa_decode_shared_prefix", "pa_decode_shared_prefix_partition_size",
+    "pa_decode_shared_prefix_workspace_bytes", "pa_copy_blocks", "pa_swap_blocks", "pa_read_device_errors",
     "pa_status_string", "pa_last_error_message",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_can_allocate", "pa_bm_allocate", "pa_bm_append_slot", "pa_bm_fork",
     "pa_bm_free", "pa_bm_block_table", "pa_bm_swap_out", "pa_bm_swap_in", "pa_bm_num_free_blocks",
@@ -106,6 +107,13 @@ def load():
     lib.pa_decode_static_workspace.argtypes = [P, P, i64, P, D, i32, P, i32, P, i32, i32, i32, ctypes.c_float,
                                                i32, P, P]
     lib.pa_decode_static_workspace.restype = ctypes.c_int
+    lib.pa_decode_shared_prefix.argtypes = [P, P, i64, P, D, i32, P, i32, P, i32, i32, i32, ctypes.c_float, P, P,
+                                            i32, i32, P, sz, P, P]
+    lib.pa_decode_shared_prefix.restype = ctypes.c_int
+    lib.pa_decode_shared_prefix_partition_size.argtypes = [D, i32, i32, i32, i32, i32]
+    lib.pa_decode_shared_prefix_partition_size.restype = i32
+    lib.pa_decode_shared_prefix_workspace_bytes.argtypes = [D, i32, i32, i32, i32, i32]
+    lib.pa_decode_shared_prefix_workspace_bytes.restype = sz
     lib.pa_copy_blocks.argtypes = [P, D, P, i32, P]
     lib.pa_copy_blocks.restype = ctypes.c_int
     lib.pa_swap_blocks.argtypes = [P, D, P, D, i32, P, i32, P]
@@ -221,6 +229,35 @@ def decode(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor, desc: Cac
                             _ptr(block_tables), block_tables.stride(0), _ptr(context_lens), S, Hq,
                             max_context_len, scale, partition_size, _ptr(workspace), ws_bytes, _ptr(dev_err),
                             _stream(stream)))
+
+
+def decode_shared_prefix_partition_size(desc: CacheDesc, num_seqs: int, num_q_heads: int, num_groups: int,
+                                        max_context_len: int, partition_size: int = 0) -> int:
+    return load().pa_decode_shared_prefix_partition_size(ctypes.byref(desc.c()), num_seqs, num_q_heads, num_groups,
+                                                         max_context_len, partition_size)
+
+
+def decode_shared_prefix_workspace_bytes(desc: CacheDesc, num_seqs: int, num_q_heads: int, num_groups: int,
+                                         max_context_len: int, partition_size: int = 0) -> int:
+    return load().pa_decode_shared_prefix_workspace_bytes(ctypes.byref(desc.c()), num_seqs, num_q_heads, num_groups,
+                                                          max_context_len, partition_size)
+
+
+def decode_shared_prefix(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor, desc: CacheDesc,
+                         block_tables: torch.Tensor, context_lens: torch.Tensor, max_context_len: int, scale: float,
+                         group_start: torch.Tensor, prefix_lens: torch.Tensor, workspace: torch.Tensor | None = None,
+                         partition_size: int = 0, layer: int = 0, dev_err: torch.Tensor | None = None,
+                         stream=None) -> None:
+    """pa_decode_shared_prefix: pa_decode where groups of consecutive sequences
+    (group_start int32 [G + 1]) share their first prefix_lens[g] tokens' blocks."""
+    S, Hq = q.shape[0], q.shape[1]
+    G = prefix_lens.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pa_decode_shared_prefix(_ptr(out), _ptr(q), q.stride(0), _ptr(kv_cache), ctypes.byref(desc.c()),
+                                          layer, _ptr(block_tables), block_tables.stride(0), _ptr(context_lens), S,
+                                          Hq, max_context_len, scale, _ptr(group_start), _ptr(prefix_lens), G,
+                                          partition_size, _ptr(workspace), ws_bytes, _ptr(dev_err),
+                                          _stream(stream)))
 
 
 def decode_window(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor, desc: CacheDesc,

@@ -369,14 +369,37 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
 // out = sum_p 2^(m_p - M) o~_p / sum_p 2^(m_p - M) l_p  (scores in base-2 units).
 // grid = (Hq, S), block = D threads.  Items with a single partition were
 // written by the decode kernel and are skipped here.
-template <typename T, int D>
+// Shared prefix (SP): the partitions of a row are its group's prefix
+// partitions, then its own; the decode kernel recorded their number, the
+// effective prefix and the first member of the sequence's prefix item, whose
+// table row the prefix was read through.  A member whose block ids differ from
+// that row inside the prefix gets zero rows and PA_DEVERR_PREFIX.
+template <typename T, int D, bool SP>
 __global__ void __launch_bounds__(D) merge_partitions_kernel(const __grid_constant__ DecodeParams p) {
   const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
   const int ctx = p.context_lens[s];
   const int P = p.partition_size;
   if (ctx <= 0 || !context_ok(p, ctx)) return;
-  const int n = (ctx - attended_from(p, ctx) + P - 1) / P;
-  if (n <= 1) return;
+  int n;
+  if constexpr (SP) {
+    n = p.ws_seq[s];
+    const int eff = p.ws_seq[p.num_seqs + s], lead = p.ws_seq[2 * p.num_seqs + s];
+    if (n == 0 || (eff == 0 && n <= 1)) return;   // zero rows, or written by the decode kernel
+    if (eff > 0 && lead != s) {
+      const int32_t* mine = p.block_tables + (int64_t)s * p.bt_stride;
+      const int32_t* theirs = p.block_tables + (int64_t)lead * p.bt_stride;
+      bool differ = false;
+      for (int j = d; j < eff / p.block_size; j += D) differ |= mine[j] != theirs[j];
+      if (__syncthreads_or(differ)) {
+        static_cast<T*>(p.out)[((int64_t)s * p.num_q_heads + h) * D + d] = Elem<T>::from_float(0.f);
+        if (d == 0 && h == 0) report(p.dev_err, PA_DEVERR_PREFIX);
+        return;
+      }
+    }
+  } else {
+    n = (ctx - attended_from(p, ctx) + P - 1) / P;
+    if (n <= 1) return;
+  }
   const int64_t row0 = ((int64_t)s * p.num_q_heads + h) * p.max_parts;
   __shared__ float sm_w[256];
   float M = -INFINITY;
@@ -418,17 +441,28 @@ static cudaError_t launch_typed(const DecodeParams& p, cudaStream_t stream) {
   kern<<<grid, C::kThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.max_parts <= 1) return e;
-  merge_partitions_kernel<T, D><<<dim3((unsigned)p.num_q_heads, (unsigned)p.num_seqs), D, 0, stream>>>(p);
+  merge_partitions_kernel<T, D, false><<<dim3((unsigned)p.num_q_heads, (unsigned)p.num_seqs), D, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_merge(const DecodeParams& p, int dtype, int head_size, cudaStream_t stream) {
   if (p.max_parts <= 1) return cudaSuccess;
   const dim3 grid((unsigned)p.num_q_heads, (unsigned)p.num_seqs);
-  if (dtype == PA_F16 && head_size == 128) merge_partitions_kernel<__half, 128><<<grid, 128, 0, stream>>>(p);
-  else if (dtype == PA_F16 && head_size == 64) merge_partitions_kernel<__half, 64><<<grid, 64, 0, stream>>>(p);
-  else if (dtype == PA_BF16 && head_size == 128) merge_partitions_kernel<__nv_bfloat16, 128><<<grid, 128, 0, stream>>>(p);
-  else if (dtype == PA_BF16 && head_size == 64) merge_partitions_kernel<__nv_bfloat16, 64><<<grid, 64, 0, stream>>>(p);
+  if (dtype == PA_F16 && head_size == 128) merge_partitions_kernel<__half, 128, false><<<grid, 128, 0, stream>>>(p);
+  else if (dtype == PA_F16 && head_size == 64) merge_partitions_kernel<__half, 64, false><<<grid, 64, 0, stream>>>(p);
+  else if (dtype == PA_BF16 && head_size == 128)
+    merge_partitions_kernel<__nv_bfloat16, 128, false><<<grid, 128, 0, stream>>>(p);
+  else if (dtype == PA_BF16 && head_size == 64)
+    merge_partitions_kernel<__nv_bfloat16, 64, false><<<grid, 64, 0, stream>>>(p);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_sp(const DecodeParams& p, int dtype, int head_size, cudaStream_t stream) {
+  const dim3 grid((unsigned)p.num_q_heads, (unsigned)p.num_seqs);
+  if (dtype == PA_F16 && head_size == 128) merge_partitions_kernel<__half, 128, true><<<grid, 128, 0, stream>>>(p);
+  else if (dtype == PA_BF16 && head_size == 128)
+    merge_partitions_kernel<__nv_bfloat16, 128, true><<<grid, 128, 0, stream>>>(p);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }

@@ -38,6 +38,13 @@ struct DecodeParams {
   int32_t ring_blocks;        // > 0: table rows are rings; logical block j at entry j % ring_blocks
   uint32_t wait_polls;        // 0: default bounded waits; > 0: ordinary waits give up after this many
                               // polls (tests of the timeout path; CUDA-core kernels)
+  // shared-prefix decode: group g = sequences group_start[g] .. group_start[g + 1] - 1,
+  // whose first prefix_lens[g] tokens are the same physical blocks
+  const int32_t* group_start; // [num_groups + 1]
+  const int32_t* prefix_lens; // [num_groups]
+  int32_t num_groups;
+  int32_t* ws_seq;            // workspace [3][num_seqs]: partitions in all, effective prefix,
+                              // first member of the sequence's prefix item (for the merge)
 };
 
 // First position a decode attends for context length ctx: inside the window
@@ -125,6 +132,14 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, int head_size, 
 // group 1, 2, 4 or 8, at most kTcI8MaxSeqs sequences.  Launches decode and merge.
 constexpr int kTcI8MaxSeqs = 1024;
 cudaError_t launch_decode_tc_i8(const DecodeParams& p, int act_dtype, int group, int num_sms, cudaStream_t stream);
+
+// Paged decode with shared prefixes on the tensor cores (16-bit cache, head_size
+// 128, block_size >= 8, group 1, 2, 4 or 8, at most kTcSpMaxSeqs sequences): a
+// group's prefix is streamed once for all its members.  Launches the decode
+// kernel and the merge (which also checks the members' prefix block ids).
+constexpr int kTcSpMaxSeqs = 192;
+cudaError_t launch_decode_tc_sp(const DecodeParams& p, int dtype, int group, int num_sms, cudaStream_t stream);
+cudaError_t launch_merge_sp(const DecodeParams& p, int dtype, int head_size, cudaStream_t stream);
 
 // Paged decode over an 8-bit cache on CUDA cores: head_size 128, group 1/2/4/8;
 // q / out in act_dtype.  Launches the decode kernel and the merge.

@@ -85,6 +85,23 @@ bool use_tensor_cores(int head_size, int block_size, int group, int num_seqs) {
 
 bool is_i8(const pa_cache_desc* d) { return d->dtype == PA_INT8_F16 || d->dtype == PA_INT8_BF16; }
 
+// Default partition of the persistent tensor-core kernels for `units` long
+// pieces of work per kv head (sequences, or shared prefixes) of up to
+// max_context_len tokens: the longest of 4096..512 (8192 first past
+// kLongContext) that still gives six items per SM.
+int32_t persistent_partition(const pa_cache_desc* desc, int64_t units, int32_t max_context_len) {
+  // Each partition writes (D + 2) floats per query head and the merge reads them
+  // back, so longer partitions cost less -- until one item is so long that the
+  // kernel's tail runs on a few SMs.  Long contexts have the per-SM work to
+  // hide an 8192-token item; with contexts of at most 32768 tokens an item
+  // stays at most 4096 tokens long.
+  const int64_t pairs = (units > 0 ? units : 0) * (desc->num_kv_heads > 0 ? desc->num_kv_heads : 0);
+  const int64_t ctx = max_context_len > 0 ? max_context_len : 0;
+  for (int P = max_context_len > kLongContext ? kMaxLongPartition : kMaxPartition; P > kMinPartition; P /= 2)
+    if (pairs * ((ctx + P - 1) / P) >= kItemsPerSm * device_sm_count()) return P;
+  return kMinPartition;
+}
+
 // Test hook for the timeout path: PAGEDKV_WAIT_POLLS=n (n >= 1) makes the
 // ordinary waits of the CUDA-core decode kernels give up after n
 // non-suspending polls instead of the default bound, so a test can make them
@@ -308,11 +325,7 @@ int32_t pa_decode_partition_size(const pa_cache_desc* desc, int32_t num_seqs, in
   // kernel's tail runs on a few SMs.  Long contexts have the per-SM work to
   // hide an 8192-token item; with contexts of at most 32768 tokens an item
   // stays at most 4096 tokens long.
-  const int64_t pairs = (int64_t)(num_seqs > 0 ? num_seqs : 0) * (desc->num_kv_heads > 0 ? desc->num_kv_heads : 0);
-  const int64_t ctx = max_context_len > 0 ? max_context_len : 0;
-  for (int P = max_context_len > kLongContext ? kMaxLongPartition : kMaxPartition; P > kMinPartition; P /= 2)
-    if (pairs * ((ctx + P - 1) / P) >= kItemsPerSm * device_sm_count()) return P;
-  return kMinPartition;
+  return persistent_partition(desc, num_seqs, max_context_len);
 }
 
 size_t pa_decode_workspace_bytes(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_q_heads,
@@ -406,6 +419,114 @@ pa_status pa_decode_window(void* out, const void* q, int64_t q_seq_stride, const
   return e == cudaSuccess ? PA_OK : cuda_fail(e, "decode launch");
 }
 
+
+// Whether the shared-prefix tensor-core kernel serves these shapes (else
+// pa_decode_shared_prefix runs pa_decode, which gives the same result).
+static bool shared_prefix_kernel_serves(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_q_heads) {
+  if (!desc || is_i8(desc) || desc->head_size != 128 || desc->block_size < 8 || desc->num_kv_heads <= 0) return false;
+  if (num_seqs <= 0 || num_seqs > pkv::kTcSpMaxSeqs || num_q_heads <= 0 || num_q_heads % desc->num_kv_heads) return false;
+  const int group = num_q_heads / desc->num_kv_heads;
+  if (group != 1 && group != 2 && group != 4 && group != 8) return false;
+  return use_tensor_cores(desc->head_size, desc->block_size, group, num_seqs);
+}
+
+// Whether pa_decode_shared_prefix takes its dedicated kernel: served shapes,
+// some groups, and partition counts that fit its 16-bit per-sequence tables.
+static bool shared_prefix_path(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_q_heads, int32_t num_groups,
+                               int32_t max_context_len, int64_t P) {
+  return num_groups > 0 && P > 0 && shared_prefix_kernel_serves(desc, num_seqs, num_q_heads) &&
+         ((int64_t)max_context_len + P - 1) / P + 1 <= 32767;
+}
+
+int32_t pa_decode_shared_prefix_partition_size(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_q_heads,
+                                               int32_t num_groups, int32_t max_context_len, int32_t partition_size) {
+  if (partition_size > 0) return partition_size;
+  if (!shared_prefix_kernel_serves(desc, num_seqs, num_q_heads) || num_groups <= 0)
+    return pa_decode_partition_size(desc, num_seqs, max_context_len, 0);
+  // the groups' prefixes are the long items: size the partitions by them
+  return persistent_partition(desc, num_groups, max_context_len);
+}
+
+size_t pa_decode_shared_prefix_workspace_bytes(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_q_heads,
+                                               int32_t num_groups, int32_t max_context_len, int32_t partition_size) {
+  if (!desc) return 0;
+  const int64_t P =
+      pa_decode_shared_prefix_partition_size(desc, num_seqs, num_q_heads, num_groups, max_context_len, partition_size);
+  if (!shared_prefix_path(desc, num_seqs, num_q_heads, num_groups, max_context_len, P))
+    return pa_decode_workspace_bytes(desc, num_seqs, num_q_heads, max_context_len, (int32_t)P);
+  if (max_context_len <= 0) return 0;
+  // a sequence's prefix and its tail split into at most ceil(ctx / P) + 1
+  // partitions; then three ints per sequence for the merge
+  const int64_t parts = (max_context_len + P - 1) / P + 1;
+  const int64_t floats = (int64_t)num_seqs * num_q_heads * parts * (desc->head_size + 2);
+  return (size_t)((floats * 4 + 3 * (int64_t)num_seqs * 4 + 15) / 16 * 16);
+}
+
+pa_status pa_decode_shared_prefix(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,
+                                  const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,
+                                  int32_t block_table_stride, const int32_t* context_lens, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t max_context_len, float scale,
+                                  const int32_t* group_start, const int32_t* prefix_lens, int32_t num_groups,
+                                  int32_t partition_size, void* workspace, size_t workspace_bytes, uint32_t* dev_err,
+                                  void* stream) {
+  size_t need = 0;
+  const int32_t P = desc ? pa_decode_shared_prefix_partition_size(desc, num_seqs, num_q_heads, num_groups,
+                                                                   max_context_len, partition_size)
+                         : partition_size;
+  pa_status st = pkv::check_decode_args(out, q, q_seq_stride, kv_cache, desc, layer, block_tables,
+                                        block_table_stride, context_lens, num_seqs, num_q_heads, max_context_len,
+                                        scale, 0, 0, P, &need);
+  if (st != PA_OK || num_seqs == 0) return st;
+  if (num_groups < 0 || num_groups > num_seqs)
+    return fail(PA_ERR_INVALID_ARG, "num_groups %d not in [0, num_seqs %d]", num_groups, num_seqs);
+  if (num_groups > 0 && (!group_start || !prefix_lens))
+    return fail(PA_ERR_INVALID_ARG, "group_start and prefix_lens must be non-NULL when num_groups > 0");
+  if ((reinterpret_cast<uintptr_t>(group_start) & 3) || (reinterpret_cast<uintptr_t>(prefix_lens) & 3))
+    return fail(PA_ERR_INVALID_ARG, "group_start and prefix_lens must be 4-byte aligned");
+  if (!shared_prefix_path(desc, num_seqs, num_q_heads, num_groups, max_context_len, P))
+    return pa_decode_window(out, q, q_seq_stride, kv_cache, desc, layer, block_tables, block_table_stride,
+                            context_lens, num_seqs, num_q_heads, max_context_len, scale, 0, 0, P, workspace,
+                            workspace_bytes, dev_err, stream);
+  need = pa_decode_shared_prefix_workspace_bytes(desc, num_seqs, num_q_heads, num_groups, max_context_len, P);
+  if (workspace_bytes < need)
+    return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+  if (!workspace || !aligned16(workspace))
+    return fail(PA_ERR_INVALID_ARG, "workspace must be non-NULL and 16-byte aligned");
+
+  pkv::DecodeParams p{};
+  p.out = out;
+  p.q = q;
+  p.q_seq_stride = q_seq_stride;
+  p.cache = static_cast<const uint8_t*>(kv_cache) + layer * layer_stride(desc);
+  p.num_blocks = desc->num_blocks;
+  p.block_size = desc->block_size;
+  p.num_kv_heads = desc->num_kv_heads;
+  p.block_tables = block_tables;
+  p.bt_stride = block_table_stride;
+  p.context_lens = context_lens;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.max_context_len = max_context_len;
+  p.partition_size = P;
+  p.max_parts = (max_context_len + P - 1) / P + 1;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_polls = test_wait_polls();
+  const int64_t rows = (int64_t)num_seqs * num_q_heads * p.max_parts;
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_ml = p.ws_o + rows * desc->head_size;
+  p.ws_seq = reinterpret_cast<int32_t*>(p.ws_ml + rows * 2);
+  p.group_start = group_start;
+  p.prefix_lens = prefix_lens;
+  p.num_groups = num_groups;
+  p.dev_err = dev_err;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = pkv::launch_decode_tc_sp(p, desc->dtype, num_q_heads / desc->num_kv_heads, sms,
+                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e, "shared-prefix decode launch");
+}
 
 pa_status pa_decode(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,
                     const pa_cache_desc* desc, int32_t layer, const int32_t* block_tables,

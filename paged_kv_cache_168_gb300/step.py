@@ -39,7 +39,7 @@ class DecodeStep:
     every slot of every block with pa_reshape_and_cache, which quantises it."""
 
     def __init__(self, w: Workload, partition_size: int = 0, stream: torch.cuda.Stream | None = None,
-                 nvtx: bool = False):
+                 nvtx: bool = False, shared_prefix: bool | None = None):
         cfg = w.cfg
         dev = w.q.device
         self.w = w
@@ -55,8 +55,15 @@ class DecodeStep:
             self.kv_cache = w.kv_cache
         self.partition_size = partition_size
         self.out = torch.empty_like(w.q)
-        nbytes = _lib.decode_workspace_bytes(self.desc, cfg.num_seqs, cfg.num_q_heads, w.max_context_len,
-                                             partition_size)
+        # a workload whose sequences share their first blocks (beam groups) is
+        # decoded with pa_decode_shared_prefix, which reads those blocks once
+        self.shared_prefix = (w.group_start is not None) if shared_prefix is None else shared_prefix
+        if self.shared_prefix:
+            nbytes = _lib.decode_shared_prefix_workspace_bytes(self.desc, cfg.num_seqs, cfg.num_q_heads,
+                                                               self.num_groups, w.max_context_len, partition_size)
+        else:
+            nbytes = _lib.decode_workspace_bytes(self.desc, cfg.num_seqs, cfg.num_q_heads, w.max_context_len,
+                                                 partition_size)
         self.workspace = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device=dev)
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.host_pool = None
@@ -75,6 +82,18 @@ class DecodeStep:
             value = part[:, :, 1].permute(0, 2, 1, 3).reshape(n, Hkv, D).contiguous()
             slots = torch.arange(b0 * bs, b0 * bs + n, dtype=torch.int64, device=logical.device)
             _lib.reshape_and_cache(self.kv_cache, self.desc, key, value, slots, stream=self.stream)
+
+    @property
+    def num_groups(self) -> int:
+        return 0 if self.w.group_start is None else int(self.w.prefix_lens.shape[0])
+
+    def partition(self) -> int:
+        """The partition size the decode call takes."""
+        cfg = self.w.cfg
+        if self.shared_prefix:
+            return _lib.decode_shared_prefix_partition_size(self.desc, cfg.num_seqs, cfg.num_q_heads, self.num_groups,
+                                                            self.w.max_context_len, self.partition_size)
+        return _lib.decode_partition_size(self.desc, cfg.num_seqs, self.w.max_context_len, self.partition_size)
 
     def _range(self, name):
         if self.nvtx:
@@ -104,10 +123,17 @@ class DecodeStep:
 
     def attention(self, q=None, out=None):
         w = self.w
-        self._range("pa_decode")
-        _lib.decode(self.out if out is None else out, w.q if q is None else q, self.kv_cache, self.desc,
-                    w.block_tables, w.context_lens, w.max_context_len, w.scale, self.workspace,
-                    self.partition_size, dev_err=self.dev_err, stream=self.stream)
+        if self.shared_prefix:
+            self._range("pa_decode_shared_prefix")
+            _lib.decode_shared_prefix(self.out if out is None else out, w.q if q is None else q, self.kv_cache,
+                                      self.desc, w.block_tables, w.context_lens, w.max_context_len, w.scale,
+                                      w.group_start, w.prefix_lens, self.workspace, self.partition_size,
+                                      dev_err=self.dev_err, stream=self.stream)
+        else:
+            self._range("pa_decode")
+            _lib.decode(self.out if out is None else out, w.q if q is None else q, self.kv_cache, self.desc,
+                        w.block_tables, w.context_lens, w.max_context_len, w.scale, self.workspace,
+                        self.partition_size, dev_err=self.dev_err, stream=self.stream)
         self._end()
 
     def __call__(self):
@@ -124,7 +150,9 @@ class DecodeStep:
             n += -(-w.swap_out_pairs.shape[0] // per) + -(-w.swap_in_pairs.shape[0] // per)
         if w.copy_pairs.shape[0]:
             n += -(-w.copy_pairs.shape[0] // per)
-        P = _lib.decode_partition_size(self.desc, cfg.num_seqs, w.max_context_len, self.partition_size)
+        if self.shared_prefix and self.num_groups > 0:
+            return n + 2                                        # decode + merge
+        P = self.partition()
         n += 1 + (1 if -(-w.max_context_len // P) > 1 else 0)   # decode (+ merge)
         return n
 

@@ -101,6 +101,13 @@ class Workload:
     swap_out_pairs: np.ndarray = field(default_factory=lambda: np.zeros((0, 2), np.int64))
     swap_in_pairs: np.ndarray = field(default_factory=lambda: np.zeros((0, 2), np.int64))
     host_blocks: int = 0
+    # sequences sharing their first blocks physically (beam groups): group g is
+    # sequences group_start[g] .. group_start[g+1]-1, whose first prefix_lens[g]
+    # tokens sit in the same blocks (device int32 tensors; None: no groups)
+    group_start: torch.Tensor = None
+    prefix_lens: torch.Tensor = None
+    group_start_np: np.ndarray = None
+    prefix_lens_np: np.ndarray = None
     # 8-bit caches: the history as logical 16-bit values [NB, Hkv, 2 (K, V), bs, D];
     # every slot of every block holds a drawn vector, quantised by whichever side
     # builds the cache from it
@@ -234,6 +241,10 @@ def make_workload(name_or_cfg, device="cpu", seed: int | None = None, nan_unused
         if unused.numel():
             pool[unused] = float("nan")
 
+    group_start = prefix_lens = None
+    if cfg.ctx[0] == "beam":
+        group_start = np.arange(0, S + 1, cfg.beams, dtype=np.int32)
+        prefix_lens = np.full(S // cfg.beams, cfg.ctx[1], dtype=np.int32)   # the shared prompt blocks
     return Workload(
         cfg=cfg, num_blocks=NB, q=q, key=key, value=value, kv_cache=pool,
         block_tables=torch.from_numpy(tables).to(dev),
@@ -243,6 +254,9 @@ def make_workload(name_or_cfg, device="cpu", seed: int | None = None, nan_unused
         block_tables_np=tables, context_lens_np=ctx, slot_mapping_np=slots, used_blocks=used,
         block_tables_before_cow_np=before, copy_pairs=copy_pairs,
         swap_out_pairs=swap_out, swap_in_pairs=swap_in, host_blocks=host_blocks, kv_logical=logical,
+        group_start=None if group_start is None else torch.from_numpy(group_start).to(dev),
+        prefix_lens=None if prefix_lens is None else torch.from_numpy(prefix_lens).to(dev),
+        group_start_np=group_start, prefix_lens_np=prefix_lens,
     )
 
 

@@ -139,3 +139,55 @@ def i8_pool_case(rng, ctx, Hq, Hkv, bs, dtype):
         assert oracle.reshape_and_cache_i8(pool, g, to_bits(x[0], dtype), to_bits(x[1], dtype), slots) == 0
     q_bits = to_bits(rng.standard_normal((len(ctx), Hq, 128)), dtype)
     return q_bits, pool, g, tables, ctx
+
+
+class SharedPaged:
+    """Groups of sequences whose first blocks are the same physical blocks, as
+    beams of one prompt after copy-on-write: group g has a prompt of prompt_len
+    tokens; its floor(prompt_len / bs) whole blocks appear at the start of every
+    member's table row, and the rest of each member's context (a partial prompt
+    block included, as a copy) sits in the member's own blocks.  Every member's
+    context holds the prompt's tokens first (as far as its length goes), then
+    its own.  `groups` is a list of (prompt_len, [member context lengths]);
+    all sequences are consecutive, group after group.  The pool is written by
+    the oracle into NaN-filled memory."""
+
+    def __init__(self, rng, groups, Hq, Hkv, D, bs, dtype="bf16"):
+        self.Hq, self.Hkv, self.D, self.bs, self.dtype = Hq, Hkv, D, bs, dtype
+        ctx = [c for _, members in groups for c in members]
+        self.S = len(ctx)
+        self.ctx = np.asarray(ctx, np.int32)
+        self.group_start = np.cumsum([0] + [len(m) for _, m in groups]).astype(np.int32)
+        self.prompt_lens = np.asarray([p for p, _ in groups], np.int32)
+        nblk = -(-self.ctx // bs)
+        shared = [p // bs for p, _ in groups]
+        need = sum(shared) + int(sum(max(0, int(n) - 0) for n in nblk))
+        self.num_blocks = need + 3
+        self.width = max(int(nblk.max()), 1)
+        self.geom = oracle.Geom(self.num_blocks, bs, Hkv, D, dtype)
+        perm = iter(rng.permutation(self.num_blocks).tolist())
+        self.tables = np.full((self.S, self.width), -1, np.int32)
+        draw = lambda *s: bits_to_f64(to_bits(rng.standard_normal(s), dtype), dtype)
+        self.K, self.V = [None] * self.S, [None] * self.S
+        s = 0
+        for (plen, members), nsh in zip(groups, shared):
+            pk, pv = draw(plen, Hkv, D), draw(plen, Hkv, D)
+            ids = [next(perm) for _ in range(nsh)]
+            for c in members:
+                own = max(0, c - plen)
+                self.K[s] = np.concatenate([pk[:min(c, plen)], draw(own, Hkv, D)])
+                self.V[s] = np.concatenate([pv[:min(c, plen)], draw(own, Hkv, D)])
+                nb = -(-c // bs)
+                row = ids[:min(nsh, nb)] + [next(perm) for _ in range(nb - min(nsh, nb))]
+                self.tables[s, :nb] = row
+                s += 1
+        self.q_bits = to_bits(rng.standard_normal((self.S, Hq, D)), dtype)
+        self.pool = np.full(self.geom.layer_elems, NAN_BITS[dtype], dtype=np.uint16)
+        for s in range(self.S):
+            c = int(self.ctx[s])
+            if c == 0:
+                continue
+            t = np.arange(c)
+            slots = self.tables[s, t // bs].astype(np.int64) * bs + t % bs
+            assert oracle.reshape_and_cache(self.pool, self.geom, to_bits(self.K[s], dtype),
+                                            to_bits(self.V[s], dtype), slots) == 0

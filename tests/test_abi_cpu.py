@@ -185,6 +185,36 @@ def test_static_workspace_size_matches_the_header():
     assert value == _lib.STATIC_WORKSPACE_BYTES
 
 
+def test_shared_prefix_sizes_and_checks(lib):
+    d = CacheDesc(100, 16, 8, 128, torch.bfloat16)
+    # beam-shaped: 32 groups x 4 beams, 32/8 heads, contexts up to 2305 tokens: the
+    # prefixes are the long items, 32 x 8 x ceil(2305 / 512) = 1280 >= 912 at 512
+    assert _lib.decode_shared_prefix_partition_size(d, 128, 32, 32, 2305) == 512
+    assert _lib.decode_shared_prefix_partition_size(d, 128, 32, 32, 2305, 1024) == 1024
+    assert _lib.decode_shared_prefix_partition_size(d, 128, 32, 0, 2305) == _lib.decode_partition_size(d, 128, 2305)
+    # workspace: (ceil(ctx / P) + 1) partitions per row, plus three ints per sequence
+    want = 128 * 32 * (5 + 1) * 130 * 4 + 3 * 128 * 4
+    assert _lib.decode_shared_prefix_workspace_bytes(d, 128, 32, 32, 2305) == -(-want // 16) * 16
+    # shapes the dedicated kernel does not serve size as pa_decode does
+    d64 = CacheDesc(100, 16, 8, 64, torch.bfloat16)
+    assert _lib.decode_shared_prefix_workspace_bytes(d64, 128, 32, 32, 2305, 512) == \
+        _lib.decode_workspace_bytes(d64, 128, 32, 2305, 512)
+    assert _lib.decode_shared_prefix_workspace_bytes(d, 300, 32, 32, 2305, 512) == \
+        _lib.decode_workspace_bytes(d, 300, 32, 2305, 512)
+
+    def call(num_groups=2, gs=FAKE, pl=FAKE, ws=1 << 30, P=256):
+        return lib.pa_decode_shared_prefix(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 4 * 128,
+                                           ctypes.c_void_p(FAKE), ctypes.byref(_desc()), 0, ctypes.c_void_p(FAKE), 8,
+                                           ctypes.c_void_p(FAKE), 4, 4, 100, 0.1, ctypes.c_void_p(gs),
+                                           ctypes.c_void_p(pl), num_groups, P, ctypes.c_void_p(FAKE), ws, None, None)
+    assert call(num_groups=5) == _lib.PA_ERR_INVALID_ARG                   # more groups than sequences
+    assert call(num_groups=-1) == _lib.PA_ERR_INVALID_ARG
+    assert call(gs=0) == _lib.PA_ERR_INVALID_ARG                            # NULL group starts
+    assert call(pl=FAKE + 2) == _lib.PA_ERR_INVALID_ARG                     # misaligned prefix lengths
+    assert call(P=100) == _lib.PA_ERR_INVALID_ARG                           # bad partition size first
+    assert call(ws=16) == _lib.PA_ERR_WORKSPACE_TOO_SMALL
+
+
 def test_reshape_rejects_bad_arguments(lib):
     call = lambda stride, n=4, key=FAKE, layer=0: lib.pa_reshape_and_cache(
         ctypes.c_void_p(FAKE), ctypes.byref(_desc()), layer, ctypes.c_void_p(key), stride,

@@ -291,9 +291,11 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, int64_t q_seq_stride
 
 /* The partition size pa_decode_shared_prefix uses: partition_size when > 0;
  * else, where its dedicated kernel serves the shapes and num_groups > 0, the
- * tensor-core rule of pa_decode_partition_size applied to the groups' prefixes
- * (num_groups * num_kv_heads * ceil(max_context_len / P) >= 6 items per SM);
- * otherwise pa_decode_partition_size(desc, num_seqs, max_context_len, 0). */
+ * longest of 4096, 2048, 1024, 512 tokens (8192 first past 32768) for which
+ * the groups' prefixes alone still give 1.5 items per SM
+ * (num_groups * num_kv_heads * ceil(max_context_len / P) >= 1.5 * SMs; each
+ * sequence adds its own tail item), else 512; otherwise
+ * pa_decode_partition_size(desc, num_seqs, max_context_len, 0). */
 int32_t pa_decode_shared_prefix_partition_size(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_q_heads,
                                                int32_t num_groups, int32_t max_context_len, int32_t partition_size);
 

@@ -367,19 +367,23 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
 
 // Log-sum-exp merge of partition results: M = max_p m_p,
 // out = sum_p 2^(m_p - M) o~_p / sum_p 2^(m_p - M) l_p  (scores in base-2 units).
-// grid = (Hq, S), block = D threads.  Items with a single partition were
-// written by the decode kernel and are skipped here.
+// grid = (num_q_heads / GB, sequences), block = GB x D threads: GB query
+// heads of one kv head per CTA.  Rows with a single partition were written by the
+// decode kernel and are skipped here; a row with an invalid partition (l < 0)
+// gets zeros.
 // Shared prefix (SP): the partitions of a row are its group's prefix
 // partitions, then its own; the decode kernel recorded their number, the
 // effective prefix and the first member of the sequence's prefix item, whose
 // table row the prefix was read through.  A member whose block ids differ from
 // that row inside the prefix gets zero rows and PA_DEVERR_PREFIX.
-template <typename T, int D, bool SP>
-__global__ void __launch_bounds__(D) merge_partitions_kernel(const __grid_constant__ DecodeParams p) {
-  const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
+template <typename T, int D, bool SP, int GB>
+__global__ void __launch_bounds__(D * GB) merge_partitions_kernel(const __grid_constant__ DecodeParams p) {
+  const int s = blockIdx.y, d = threadIdx.x % D, sub = threadIdx.x / D;
+  const int h = blockIdx.x * GB + sub;             // this thread's query head
   const int ctx = p.context_lens[s];
   const int P = p.partition_size;
   if (ctx <= 0 || !context_ok(p, ctx)) return;
+  T* out_s = static_cast<T*>(p.out) + (int64_t)s * p.num_q_heads * D;
   int n;
   if constexpr (SP) {
     n = p.ws_seq[s];
@@ -389,10 +393,10 @@ __global__ void __launch_bounds__(D) merge_partitions_kernel(const __grid_consta
       const int32_t* mine = p.block_tables + (int64_t)s * p.bt_stride;
       const int32_t* theirs = p.block_tables + (int64_t)lead * p.bt_stride;
       bool differ = false;
-      for (int j = d; j < eff / p.block_size; j += D) differ |= mine[j] != theirs[j];
+      for (int j = threadIdx.x; j < eff / p.block_size; j += D * GB) differ |= mine[j] != theirs[j];
       if (__syncthreads_or(differ)) {
-        static_cast<T*>(p.out)[((int64_t)s * p.num_q_heads + h) * D + d] = Elem<T>::from_float(0.f);
-        if (d == 0 && h == 0) report(p.dev_err, PA_DEVERR_PREFIX);
+        out_s[h * D + d] = Elem<T>::from_float(0.f);
+        if (threadIdx.x == 0 && blockIdx.x == 0) report(p.dev_err, PA_DEVERR_PREFIX);
         return;
       }
     }
@@ -400,33 +404,46 @@ __global__ void __launch_bounds__(D) merge_partitions_kernel(const __grid_consta
     n = (ctx - attended_from(p, ctx) + P - 1) / P;
     if (n <= 1) return;
   }
-  const int64_t row0 = ((int64_t)s * p.num_q_heads + h) * p.max_parts;
-  __shared__ float sm_w[256];
-  float M = -INFINITY;
-  bool bad = false;
-  for (int i = 0; i < n; ++i) {
-    const float l = p.ws_ml[(row0 + i) * 2 + 1];
-    bad |= l < 0.f;
-    M = fmaxf(M, p.ws_ml[(row0 + i) * 2 + 0]);
-  }
-  T* out = static_cast<T*>(p.out) + ((int64_t)s * p.num_q_heads + h) * D;
-  if (bad) {
-    out[d] = Elem<T>::from_float(0.f);
-    return;
-  }
-  float L = 0.f, O = 0.f;
-  for (int i0 = 0; i0 < n; i0 += 256) {
-    const int cnt = min(256, n - i0);
-    __syncthreads();
-    for (int i = d; i < cnt; i += D) sm_w[i] = exp2f(p.ws_ml[(row0 + i0 + i) * 2 + 0] - M);
-    __syncthreads();
-    for (int i = 0; i < cnt; ++i) {
-      const float w = sm_w[i];
-      L = fmaf(w, p.ws_ml[(row0 + i0 + i) * 2 + 1], L);
-      O = fmaf(w, p.ws_o[(row0 + i0 + i) * D + d], O);
+  __shared__ float sm_w[GB][256];
+  // every thread runs the same iterations (the same n), so the barriers below
+  // are reached uniformly
+  {
+    const int64_t row0 = ((int64_t)s * p.num_q_heads + h) * p.max_parts;
+    float M = -INFINITY;
+    bool bad = false;
+    for (int i = 0; i < n; ++i) {
+      bad |= p.ws_ml[(row0 + i) * 2 + 1] < 0.f;
+      M = fmaxf(M, p.ws_ml[(row0 + i) * 2 + 0]);
     }
+    float L = 0.f, O = 0.f;
+    for (int i0 = 0; i0 < n; i0 += 256) {
+      const int cnt = min(256, n - i0);
+      __syncthreads();
+      for (int i = d; i < cnt; i += D) sm_w[sub][i] = exp2f(p.ws_ml[(row0 + i0 + i) * 2 + 0] - M);
+      __syncthreads();
+      for (int i = 0; i < cnt; ++i) {
+        const float w = sm_w[sub][i];
+        L = fmaf(w, p.ws_ml[(row0 + i0 + i) * 2 + 1], L);
+        O = fmaf(w, p.ws_o[(row0 + i0 + i) * D + d], O);
+      }
+    }
+    out_s[h * D + d] = Elem<T>::from_float(bad ? 0.f : O / L);
   }
-  out[d] = Elem<T>::from_float(O / L);
+}
+
+// Launches the merge over every sequence, GB query heads of one kv head per
+// CTA: the most (up to 4) that still leave two CTAs per SM of a 152-SM GPU.
+template <typename T, int D, bool SP>
+static cudaError_t launch_merge_typed(const DecodeParams& p, cudaStream_t stream) {
+  const int G = p.num_q_heads / p.num_kv_heads;
+  const int64_t rows = (int64_t)p.num_seqs * p.num_q_heads;
+  int gb = 1;
+  while (gb < 4 && G % (2 * gb) == 0 && rows / (2 * gb) >= 2 * 152) gb *= 2;
+  const dim3 grid((unsigned)(p.num_q_heads / gb), (unsigned)p.num_seqs);
+  if (gb == 1) merge_partitions_kernel<T, D, SP, 1><<<grid, D, 0, stream>>>(p);
+  else if (gb == 2) merge_partitions_kernel<T, D, SP, 2><<<grid, 2 * D, 0, stream>>>(p);
+  else merge_partitions_kernel<T, D, SP, 4><<<grid, 4 * D, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 template <typename T, int D, int G>
@@ -441,30 +458,22 @@ static cudaError_t launch_typed(const DecodeParams& p, cudaStream_t stream) {
   kern<<<grid, C::kThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.max_parts <= 1) return e;
-  merge_partitions_kernel<T, D, false><<<dim3((unsigned)p.num_q_heads, (unsigned)p.num_seqs), D, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_merge_typed<T, D, false>(p, stream);
 }
 
 cudaError_t launch_merge(const DecodeParams& p, int dtype, int head_size, cudaStream_t stream) {
   if (p.max_parts <= 1) return cudaSuccess;
-  const dim3 grid((unsigned)p.num_q_heads, (unsigned)p.num_seqs);
-  if (dtype == PA_F16 && head_size == 128) merge_partitions_kernel<__half, 128, false><<<grid, 128, 0, stream>>>(p);
-  else if (dtype == PA_F16 && head_size == 64) merge_partitions_kernel<__half, 64, false><<<grid, 64, 0, stream>>>(p);
-  else if (dtype == PA_BF16 && head_size == 128)
-    merge_partitions_kernel<__nv_bfloat16, 128, false><<<grid, 128, 0, stream>>>(p);
-  else if (dtype == PA_BF16 && head_size == 64)
-    merge_partitions_kernel<__nv_bfloat16, 64, false><<<grid, 64, 0, stream>>>(p);
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (dtype == PA_F16 && head_size == 128) return launch_merge_typed<__half, 128, false>(p, stream);
+  if (dtype == PA_F16 && head_size == 64) return launch_merge_typed<__half, 64, false>(p, stream);
+  if (dtype == PA_BF16 && head_size == 128) return launch_merge_typed<__nv_bfloat16, 128, false>(p, stream);
+  if (dtype == PA_BF16 && head_size == 64) return launch_merge_typed<__nv_bfloat16, 64, false>(p, stream);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_merge_sp(const DecodeParams& p, int dtype, int head_size, cudaStream_t stream) {
-  const dim3 grid((unsigned)p.num_q_heads, (unsigned)p.num_seqs);
-  if (dtype == PA_F16 && head_size == 128) merge_partitions_kernel<__half, 128, true><<<grid, 128, 0, stream>>>(p);
-  else if (dtype == PA_BF16 && head_size == 128)
-    merge_partitions_kernel<__nv_bfloat16, 128, true><<<grid, 128, 0, stream>>>(p);
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (dtype == PA_F16 && head_size == 128) return launch_merge_typed<__half, 128, true>(p, stream);
+  if (dtype == PA_BF16 && head_size == 128) return launch_merge_typed<__nv_bfloat16, 128, true>(p, stream);
+  return cudaErrorInvalidValue;
 }
 
 template <typename T, int D>

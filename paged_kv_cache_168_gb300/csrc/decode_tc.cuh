@@ -138,11 +138,15 @@ __host__ __device__ constexpr int threads_of(bool i8, int G) {
 }
 constexpr int kND = 4;                             // 8-bit: tile descriptors in flight (planner -> copy warp)
 constexpr int kRawBytes = 64 * (2 * kD + 32);      // one 64-token half tile of 8-bit chunks (bs 1: 288 B/token)
-// TMEM columns: S0 S1 (16 each) | O0 O1 (32 each); 8-bit caches add the fp16 K
-// operand of each stage (128 tokens x 128 dims, two per column: 64 columns).
+// TMEM columns: S0 S1 (16 each) | the O accumulators, 32 columns each, one per
+// (item parity, softmax group): O^T of an item accumulates across its tiles,
+// so the output warps read it once per item; 8-bit caches (one softmax group)
+// add the fp16 K operand of each stage (128 tokens x 128 dims, two per column:
+// 64 columns) from column kKCol.
 constexpr uint32_t kKCol = 128;
+constexpr uint32_t kOCol = 32;
 __host__ __device__ constexpr uint32_t tmem_cols(bool i8, int ns) {
-  return !i8 ? 128u : (kKCol + 64u * ns <= 256u ? 256u : 512u);
+  return !i8 ? 256u : (kKCol + 64u * ns <= 256u ? 256u : 512u);
 }
 // A stage holds the tile's K and V operands (16-bit caches) or, for 8-bit
 // caches, only the converted V operand (K lives in TMEM).
@@ -156,23 +160,28 @@ struct TileMeta {
   float qinv;                    // 8-bit caches with bf16 q: 2^-e undoing the exact prescale of Q to fp16
   int seq0, ncol, pbase;         // column n: sequence seq0 + n / G, head kvh * G + n % G (ncol real columns);
                                  // the workspace partition of partition `part` is pbase + part
+  int head, item;                // tiles of the item before this one; the item's index in this CTA
+  int bad;                       // 16-bit caches: a block id of the item so far was out of range (block 0 read
+                                 // instead); the item's last tile has the item's verdict
 };
 
 template <int NS, bool I8, int NRH>
 struct Shared {
   uint64_t full[NS], empty[NS];
-  uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2], q_free[2];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], q_free[2];
+  // O accumulator slot o = item parity * groups + group: the PV of the group's
+  // last tile of an item completed (ofin), the output warps read it (ofree)
+  uint64_t ofin[4], ofree[4];
   uint64_t m_full[2];             // MMA issuer -> softmax: tile t's metadata in smeta[t & 1]
   uint64_t mma_drain[2];          // each MMA-issuing lane's own MMAs, waited for before TMEM is freed
   TileMeta smeta[2];
   uint64_t max_bar[2];            // softmax-warp exchange (bounded waits, unlike bar.sync)
-  uint64_t c_full[2], c_free[2];  // softmax -> output warps: per-tile hand-off ring
+  uint64_t c_full[2], c_free[2];  // softmax -> output warps: per-item hand-off, by item parity
   TileMeta meta[NS];
-  struct Handoff {                // what the output warps need for tile t (ring slot t & 1)
-    TileMeta meta;
-    int rescale;                  // the group's maximum rose on this tile: corr holds the factors
-    float corr[kN];               // 2^(m_{t-1} - m_t) per column
-  } hand[2];
+  struct ItemHand {                // an item's metadata for the output warps (slot: item parity)
+    TileMeta meta;                // its last tile's
+    int ntiles, first_grp;        // its tiles, and the softmax group of its first tile
+  } ihand[2];
   struct Final {                  // a softmax group's maximum and sums per TMEM lane quarter
     float m[kN];                  // at the end of an item: [item parity][group]
     float Lq[4][kN];
@@ -182,7 +191,6 @@ struct Shared {
   // every warp of its group arrived for tile t + 1... which follows its reads of t
   float red_max[2][2][4][kN];
   int red_up[2][2][4];
-  float corr_st[2][kN];           // a softmax group's latest correction factors, until its hand-off
   uint32_t tmem_base;
   volatile int abort_flag;
   volatile int end_tile;          // QK issuer -> PV issuer: tiles in this CTA (set at the end)
@@ -364,13 +372,18 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       mbar_init(&sh.m_full[i], 1);
       mbar_init(&sh.s_free[i], 4);
       mbar_init(&sh.p_full[i], 4);
-      mbar_init(&sh.o_full[i], 1);
-      mbar_init(&sh.o_free[i], 4);
+      mbar_init(&sh.pv_done[i], 1);
       mbar_init(&sh.q_free[i], 1);
       mbar_init(&sh.max_bar[i], 4);
-      mbar_init(&sh.c_full[i], 4);
+      // every warp of each softmax group that had a tile in the item (the group
+      // of a one-tile item arrives for both)
+      mbar_init(&sh.c_full[i], ping_pong(I8, CN) ? 8 : 4);
       mbar_init(&sh.c_free[i], 4);
       mbar_init(&sh.mma_drain[i], 1);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&sh.ofin[i], 1);
+      mbar_init(&sh.ofree[i], 4);
     }
     sh.abort_flag = 0;
     sh.end_tile = 0x7fffffff;
@@ -641,11 +654,17 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       const int t0 = t_base + part * P, t1 = min(ctx, t0 + P);
       const int jb = t0 / bs;
       const int nblk = (t1 - t0 + bs - 1) / bs;
-      bool bad = lane < nblk && (id_lane < 0 || id_lane >= p.num_blocks);
+      // 8-bit caches check the item's block ids before it starts; 16-bit
+      // caches check each tile's ids as they are issued (no round trip before
+      // the item's first copy) and mark the item bad instead
+      bool bad = false;
+      if constexpr (I8) {
+        bad = lane < nblk && (id_lane < 0 || id_lane >= p.num_blocks);
 #pragma unroll 4
-      for (int b = lane + 32; b < nblk; b += 32) {   // unrolled: several loads in flight
-        const int id = row[table_index(jb + b, p.ring_blocks)];
-        bad |= (id < 0 || id >= p.num_blocks);
+        for (int b = lane + 32; b < nblk; b += 32) {   // unrolled: several loads in flight
+          const int id = row[table_index(jb + b, p.ring_blocks)];
+          bad |= (id < 0 || id >= p.num_blocks);
+        }
       }
       if (__any_sync(kFull, bad)) {
         if (lane == 0) report(p.dev_err, PA_DEVERR_BLOCK_ID);
@@ -740,6 +759,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         m.tail = ntiles - 1 - k;
         m.qinv = qinv;
         m.seq0 = cur.seq0; m.ncol = cur.ncol; m.pbase = cur.pbase;
+        m.head = k; m.item = item_seq; m.bad = 0;
         // the tile's block ids, lane i holding blocks i + 32 c of the tile: the
         // item's first 32 come from the prefetched id_lane, the rest are loaded
         // here, all in flight together
@@ -776,6 +796,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         return lane < nbk ? (bi < 32 ? id_sh : row[table_index(jb + bi, p.ring_blocks)]) : 0;
       };
       int id_k = (!I8 && ntiles > 0) ? tile_id(0) : 0;
+      bool item_bad = false;
       for (int k = 0; k < ntiles && !I8; ++k) {
         const int slot = tile_seq % NS;
         if (tile_seq >= NS && !mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1)) {
@@ -784,6 +805,14 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         }
         const int valid = min(kTile, t1 - (t0 + k * kTile));
         const int nb = (valid + bs - 1) / bs;
+        // an id out of range is never read: block 0 stands in, the item's
+        // result is discarded (zero rows) and the error reported once per item
+        const bool id_bad = lane < nb && (id_k < 0 || id_k >= p.num_blocks);
+        if (__any_sync(kFull, id_bad)) {
+          if (lane == 0 && !item_bad) report(p.dev_err, PA_DEVERR_BLOCK_ID);
+          item_bad = true;
+        }
+        if (id_bad) id_k = 0;
         if (lane == 0) {
           TileMeta m;
           m.s = s; m.kvh = kvh; m.part = part; m.valid = valid;
@@ -792,6 +821,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
           m.tail = ntiles - 1 - k;
           m.qinv = qinv;
           m.seq0 = cur.seq0; m.ncol = cur.ncol; m.pbase = cur.pbase;
+          m.head = k; m.item = item_seq; m.bad = item_bad ? 1 : 0;
           sh.meta[slot] = m;
           mbar_arrive_expect_tx(&sh.full[slot], (uint32_t)(nb * chunk_bytes));
         }
@@ -815,6 +845,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
           sh.abort_flag = 1;
         }
         sh.desc[d].meta.s = -1;
+        sh.desc[d].meta.item = item_seq;   // the index the next item would have
         mbar_arrive(&sh.desc_full[d]);
       }
     } else {
@@ -833,6 +864,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
           sh.abort_flag = 1;
         }
         sh.meta[slot].s = -1;
+        sh.meta[slot].item = item_seq;     // the index the next item would have
         mbar_arrive(&sh.full[slot]);
       }
     }
@@ -846,6 +878,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
     if (lane == 0) {
       const uint32_t id_qk = tc::idesc_f16(128, kN, kBF16, false, false);
       const uint32_t id_pv = tc::idesc_f16(128, NPV, kBF16, true, true);
+      uint32_t used = 0, par = 0;   // per O slot: used by an item yet, parity of its uses
       int qk = 0, pv = 0, end = 0x7fffffff;
       uint32_t idle = 0;
       bool ok = true;
@@ -879,26 +912,37 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
           }
         }
         if (pv < qk) {
+          // PV(pv) accumulates into the O slot of its item (one softmax group):
+          // the item's first tile overwrites it once the output warps have read
+          // the slot's previous item; its last tile signals the output warps
           const int pb = pv & 1;
-          if (mbar_test_wait(&sh.p_full[pb], (pv >> 1) & 1) &&
-              (pv < 2 || mbar_test_wait(&sh.o_free[pb], ((pv >> 1) - 1) & 1))) {
-            tc::fence_after_sync();
+          if (mbar_test_wait(&sh.p_full[pb], (pv >> 1) & 1)) {
             const int slot = pv % NS;
-            const int valid = sh.meta[slot].valid;   // the stage is not refilled before this PV completes
-            const uint32_t st = smem_u32(stages + slot * kStage), pa = smem_u32(pbuf + pb * kPBytes);
-            const int nsteps = (valid + 15) >> 4;
-            // V of 8-token group g: at g * 4 KiB + 2 KiB among the K atoms (16-bit
-            // caches), at g * 2 KiB in a V-only stage (8-bit caches)
-            constexpr uint32_t kVGroup = I8 ? 2048 : kGroupBytes, kVOff = I8 ? 0 : 2048;
-            for (int kk = 0; kk < nsteps; ++kk)
-              tc::mma_f16(tmem + 32 + pb * 32,
-                          tc::smem_desc(st + kk * 2 * kVGroup + kVOff, 1024, kVGroup, tc::kSwizzle128B),
-                          tc::smem_desc(pa + kk * (NPV / 8) * 256, (NPV / 8) * 128, 128, tc::kSwizzleNone), id_pv,
-                          kk > 0);
-            tc::commit(&sh.o_full[pb]);
-            tc::commit(&sh.empty[slot]);
-            ++pv;
-            progressed = true;
+            const TileMeta& mr = sh.meta[slot];     // the stage is not refilled before this PV completes
+            const int valid = mr.valid, os = mr.qslot;
+            const bool first = mr.head == 0, lastg = mr.tail == 0;
+            if (!first || !((used >> os) & 1) || mbar_test_wait(&sh.ofree[os], ((par >> os) & 1) ^ 1)) {
+              tc::fence_after_sync();
+              const uint32_t st = smem_u32(stages + slot * kStage), pa = smem_u32(pbuf + pb * kPBytes);
+              const int nsteps = (valid + 15) >> 4;
+              // V of 8-token group g: at g * 4 KiB + 2 KiB among the K atoms (16-bit
+              // caches), at g * 2 KiB in a V-only stage (8-bit caches)
+              constexpr uint32_t kVGroup = I8 ? 2048 : kGroupBytes, kVOff = I8 ? 0 : 2048;
+              for (int kk = 0; kk < nsteps; ++kk)
+                tc::mma_f16(tmem + kOCol + os * 32,
+                            tc::smem_desc(st + kk * 2 * kVGroup + kVOff, 1024, kVGroup, tc::kSwizzle128B),
+                            tc::smem_desc(pa + kk * (NPV / 8) * 256, (NPV / 8) * 128, 128, tc::kSwizzleNone), id_pv,
+                            (kk > 0 || !first) ? 1u : 0u);
+              tc::commit(&sh.pv_done[pb]);
+              tc::commit(&sh.empty[slot]);
+              if (lastg) tc::commit(&sh.ofin[os]);
+              if (first) {
+                used |= 1u << os;
+                par ^= 1u << os;
+              }
+              ++pv;
+              progressed = true;
+            }
           }
         }
         if (progressed) {
@@ -954,6 +998,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         ++qk;
       }
       sh.end_tile = qk;   // the PV issuer stops there
+      const int end_item = sh.meta[qk % NS].item;   // the end mark's (valid when ok)
       if (ok) {
         // no more work: both metadata buffers say so (marked with the end tile,
         // so only the softmax warps waiting for tile `end` pass it on), once
@@ -966,6 +1011,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
           for (int b2 = 0; b2 < 2; ++b2) {
             sh.smeta[b2].s = -1;
             sh.smeta[b2].valid = end;
+            sh.smeta[b2].item = end_item;
             mbar_arrive(&sh.m_full[b2]);
           }
         }
@@ -989,27 +1035,47 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       // V of 8-token group g: at g * 4 KiB + 2 KiB among the K atoms (16-bit
       // caches), at g * 2 KiB in a V-only stage (8-bit caches)
       constexpr uint32_t kVGroup = I8 ? 2048 : kGroupBytes, kVOff = I8 ? 0 : 2048;
+      constexpr bool PP = ping_pong(I8, CN);
+      // PV(pv) accumulates into the O slot of (its item's parity, its softmax
+      // group): a group's first tile of an item overwrites the slot once the
+      // output warps have read the slot's previous item; its last tile
+      // signals the output warps
+      uint32_t used = 0, par = 0;   // per O slot: used by an item yet, parity of its uses
       int pv = 0;
       uint32_t idle = 0;
       bool ok = true;
       while (pv < sh.end_tile) {
         const int pb = pv & 1;
-        if (mbar_test_wait(&sh.p_full[pb], (pv >> 1) & 1) &&
-            (pv < 2 || mbar_test_wait(&sh.o_free[pb], ((pv >> 1) - 1) & 1))) {
-          tc::fence_after_sync();
+        bool issued = false;
+        if (mbar_test_wait(&sh.p_full[pb], (pv >> 1) & 1)) {
           const int slot = pv % NS;
-          const int valid = sh.meta[slot].valid;   // the stage is not refilled before this PV completes
-          const uint64_t vd = tc::smem_desc(smem_u32(stages + slot * kStage) + kVOff, 1024, kVGroup, tc::kSwizzle128B);
-          const uint64_t pd = tc::smem_desc(smem_u32(pbuf + pb * kPBytes), (NPV / 8) * 128, 128, tc::kSwizzleNone);
-          const int nsteps = (valid + 15) >> 4;
+          const TileMeta& mr = sh.meta[slot];   // the stage is not refilled before this PV completes
+          const int valid = mr.valid;
+          const int os = mr.qslot * (PP ? 2 : 1) + (PP ? pb : 0);
+          const bool first = PP ? mr.head < 2 : mr.head == 0, lastg = PP ? mr.tail < 2 : mr.tail == 0;
+          if (!first || !((used >> os) & 1) || mbar_test_wait(&sh.ofree[os], ((par >> os) & 1) ^ 1)) {
+            tc::fence_after_sync();
+            const uint64_t vd =
+                tc::smem_desc(smem_u32(stages + slot * kStage) + kVOff, 1024, kVGroup, tc::kSwizzle128B);
+            const uint64_t pd = tc::smem_desc(smem_u32(pbuf + pb * kPBytes), (NPV / 8) * 128, 128, tc::kSwizzleNone);
+            const int nsteps = (valid + 15) >> 4;
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            if (kk < nsteps)
-              tc::mma_f16(tmem + 32 + pb * 32, vd + (uint64_t)((kk * 2 * kVGroup) >> 4),
-                          pd + (uint64_t)((kk * (NPV / 8) * 256) >> 4), id_pv, kk > 0);
-          tc::commit(&sh.o_full[pb]);
-          tc::commit(&sh.empty[slot]);
-          ++pv;
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              if (kk < nsteps)
+                tc::mma_f16(tmem + kOCol + os * 32, vd + (uint64_t)((kk * 2 * kVGroup) >> 4),
+                            pd + (uint64_t)((kk * (NPV / 8) * 256) >> 4), id_pv, (kk > 0 || !first) ? 1u : 0u);
+            tc::commit(&sh.pv_done[pb]);
+            tc::commit(&sh.empty[slot]);
+            if (lastg) tc::commit(&sh.ofin[os]);
+            if (first) {
+              used |= 1u << os;
+              par ^= 1u << os;
+            }
+            ++pv;
+            issued = true;
+          }
+        }
+        if (issued) {
           idle = 0;
         } else if (++idle > kSpinLimit || sh.abort_flag) {
           ok = false;
@@ -1061,17 +1127,26 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       }
       if (__any_sync(kFull, mt.s < 0 || sh.abort_flag)) {
         // tell the output warps there is no more work (the group whose turn
-        // the end tile is; the forwarded end mark carries the end tile in valid)
+        // the end tile is; the forwarded end mark carries the end tile in valid
+        // and the index the next item would have in item), in the hand-off slot
+        // of that item index once its previous user is done
         if (mt.s < 0 && (!PP || mt.valid == tile_seq)) {
-          if (tile_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.c_free[hb], ((tile_seq >> 1) - 1) & 1))) { ok = false; break; }
-          if (lane == 0 && quarter == 0) sh.hand[hb].meta.s = -1;
+          const int k = mt.item, q = k & 1;
+          if (k >= 2 && !__all_sync(kFull, mbar_wait(&sh.c_free[q], ((k >> 1) - 1) & 1))) { ok = false; break; }
+          if (lane == 0 && quarter == 0) sh.ihand[q].meta.s = -1;
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.c_full[hb]);
+          if (lane == 0) {
+            mbar_arrive(&sh.c_full[q]);
+            if (PP) mbar_arrive(&sh.c_full[q]);
+          }
         }
         break;
       }
-      // this group's last tile of the item: it hands over its maximum and sums
-      const bool fin = mt.tail == 0 || (PP && mt.tail == 1);
+      // this group's first and last tiles of the item: the first starts its O
+      // accumulator afresh, the last hands over its maximum and sums
+      const bool first = PP ? mt.head < 2 : mt.head == 0;
+      const bool fin = PP ? mt.tail < 2 : mt.tail == 0;
+      const int os = mt.qslot * (PP ? 2 : 1) + grp;   // this group's O slot for the item
       const int sb = tile_seq & 1;
       if (!__all_sync(kFull, mbar_wait(&sh.s_full[sb], (tile_seq >> 1) & 1))) { ok = false; break; }
       tc::fence_after_sync();
@@ -1112,18 +1187,42 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       const bool rescale = (ups[0] | ups[1] | ups[2] | ups[3]) != 0;   // the same in all four warps
       if (rescale) {
         // new maximum: the old one, or the maxima of the warps that saw a score
-        // above it (the other warps' scores are within kLazyMax of it); the
-        // factors for the output warps wait in corr_st until the hand-off
+        // above it (the other warps' scores are within kLazyMax of it); what
+        // was summed against the old one -- the row sums, and (after the
+        // group's first tile of the item) the O accumulator in TMEM -- is
+        // rescaled, the latter once the group's previous PV has completed and
+        // before this tile's PV is issued
+        float corr[CN];
 #pragma unroll
         for (int n = 0; n < CN; ++n) {
           float mx = m[n];
 #pragma unroll
           for (int w = 0; w < 4; ++w)
             if (ups[w]) mx = fmaxf(mx, sh.red_max[hb][par][w][n]);
-          const float c = (m[n] == -INFINITY) ? 0.f : exp2f(m[n] - mx);
-          if (lane == 0 && quarter == 0) sh.corr_st[grp][n] = c;
-          lp[n] *= c;
+          corr[n] = (m[n] == -INFINITY) ? 0.f : exp2f(m[n] - mx);
+          lp[n] *= corr[n];
           m[n] = mx;
+        }
+        if (!first) {
+          // thread = TMEM lane = head dim 32 quarter + lane of O^T; columns: p_hi
+          // products of the CN columns, then p_lo products at HG + n
+          const int prev = tile_seq - (PP ? 2 : 1);   // the group's previous tile (same item)
+          if (!__all_sync(kFull, mbar_wait(&sh.pv_done[prev & 1], (prev >> 1) & 1))) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t oaddr = lane_addr + kOCol + os * 32;
+#pragma unroll
+          for (int c16 = 0; c16 < NPV / 16; ++c16) {
+            float o[16];
+            tc::tmem_ld16(oaddr + c16 * 16, o);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = (c16 * 16 + j) % HG;   // the column this product belongs to
+              if (n < CN) o[j] *= corr[n];
+            }
+            tc::tmem_st16(oaddr + c16 * 16, o);
+          }
+          tc::tmem_wait_st();
+          tc::fence_before_sync();
         }
       }
       float (&pr)[CN] = x;   // the weights replace the scores
@@ -1141,7 +1240,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         pk[(HG + n2) >> 1] = Elem<OpT>::pack2(a - r.x, b - r.y);
       }
       // P^T buffer hb was last read by PV(t - 2): wait for it to complete
-      if (tile_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.o_full[hb], ((tile_seq - 2) >> 1) & 1))) { ok = false; break; }
+      if (tile_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.pv_done[hb], ((tile_seq - 2) >> 1) & 1))) { ok = false; break; }
       // MN-major without swizzle: core matrix = 8 tokens x 8 columns (128 B);
       // column chunks 128 B apart, 8-token groups (NPV / 8) * 128 B apart
       uint8_t* prow = pbuf + hb * kPBytes + (row >> 3) * (NPV / 8) * 128 + (row & 7) * 16;
@@ -1170,28 +1269,30 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         for (int n = 0; n < CN; ++n) Lq[n] = lp[n];
         transpose_reduce<CN>(Lq, lane, [](float a, float b) { return a + b; });
       }
-      // hand-off to the output warps (after c_free(t - 2), which the output
-      // warps give for an item's last tile only once they have read its final
-      // values: so fin[item parity] is free again here)
-      if (tile_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.c_free[hb], ((tile_seq >> 1) - 1) & 1))) { ok = false; break; }
-      if (lane == 0 && quarter == 0) {
-        sh.hand[hb].meta = mt;
-        sh.hand[hb].rescale = rescale ? 1 : 0;
-        if (rescale) {
-#pragma unroll
-          for (int n = 0; n < CN; ++n) sh.hand[hb].corr[n] = sh.corr_st[grp][n];
-        }
-        if (fin) {
-#pragma unroll
-          for (int n = 0; n < CN; ++n) sh.fin[mt.qslot][grp].m[n] = m[n];
-        }
-      }
+      // hand-off to the output warps at the group's last tile of the item:
+      // its maximum and sums (and, with the item's last tile, the item's
+      // metadata) into the slot of the item's parity, once the output warps
+      // are done with the item before it of the same parity
       if (fin) {
+        const int k = mt.item, q = k & 1;
+        if (k >= 2 && !__all_sync(kFull, mbar_wait(&sh.c_free[q], ((k >> 1) - 1) & 1))) { ok = false; break; }
+        if (lane == 0 && quarter == 0) {
+#pragma unroll
+          for (int n = 0; n < CN; ++n) sh.fin[q][grp].m[n] = m[n];
+          if (mt.tail == 0) {
+            sh.ihand[q].meta = mt;
+            sh.ihand[q].ntiles = mt.head + 1;
+            sh.ihand[q].first_grp = PP ? ((tile_seq - mt.head) & 1) : 0;
+          }
+        }
         constexpr int sh_ = 5 - log2_of(CN);
-        if ((lane & ((1 << sh_) - 1)) == 0) sh.fin[mt.qslot][grp].Lq[quarter][lane >> sh_] = Lq[0];
+        if ((lane & ((1 << sh_) - 1)) == 0) sh.fin[q][grp].Lq[quarter][lane >> sh_] = Lq[0];
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sh.c_full[q]);
+          if (PP && mt.head == 0 && mt.tail == 0) mbar_arrive(&sh.c_full[q]);   // a one-tile item: for both groups
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.c_full[hb]);
       if (fin) {
 #pragma unroll
         for (int n = 0; n < CN; ++n) {
@@ -1207,68 +1308,70 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
     }
   } else if (warp < 10) {
     // =================================================================== output warps (6-9)
-    // Tile t: O^T -> acc = acc * corr_t + O_t (thread = TMEM lane = head dim),
-    // one accumulator per softmax warpgroup; at the end of an item the groups'
-    // (maximum, sum, acc) merge exactly (log-sum-exp) into out = acc / L, or
-    // into the partition's partial results.
+    // Once per item: each softmax group's O^T, accumulated in its TMEM slot
+    // over the item's tiles (thread = TMEM lane = head dim), merged with the
+    // other group's exactly (log-sum-exp) into out = O / L, or into the
+    // partition's partial results.
     constexpr bool PP = ping_pong(I8, CN);
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-    float acc0[CN], acc1[CN];
-#pragma unroll
-    for (int n = 0; n < CN; ++n) acc0[n] = acc1[n] = 0.f;
-    int tile_seq = 0, item_tiles = 0;
+    uint32_t used = 0;   // per O slot: parity of the items read from it so far
     bool ok = true;
-    while (true) {
-      const int hb = tile_seq & 1;
-      const bool g1 = PP && hb == 1;   // a tile of softmax group 1
-      if (!__all_sync(kFull, mbar_wait(&sh.c_full[hb], (tile_seq >> 1) & 1))) { ok = false; break; }
-      const TileMeta mt = sh.hand[hb].meta;
+    for (int k = 0;; ++k) {
+      const int q = k & 1;
+      if (!__all_sync(kFull, mbar_wait(&sh.c_full[q], (k >> 1) & 1))) { ok = false; break; }
+      const TileMeta mt = sh.ihand[q].meta;
       if (mt.s < 0) break;
-      const bool rescale = sh.hand[hb].rescale != 0;
-      float corr[CN];
-      if (rescale) {
+      // the groups that had a tile in this item: the group of its first tile,
+      // and (two groups) the other one when it has more than one tile
+      const int ntiles = sh.ihand[q].ntiles, g_first = sh.ihand[q].first_grp;
+      const bool has0 = !PP || g_first == 0 || ntiles >= 2, has1 = PP && (g_first == 1 || ntiles >= 2);
+      // O of each group: p_hi products + p_lo products of every column
+      float x0[CN], x1[CN];
 #pragma unroll
-        for (int n = 0; n < CN; ++n) corr[n] = sh.hand[hb].corr[n];
-      }
-      // an item's last tile frees its hand-off slot only after its final
-      // values (fin[item parity]) have been read, below
-      if (!mt.last) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.c_free[hb]);
-      }
-      if (!__all_sync(kFull, mbar_wait(&sh.o_full[hb], (tile_seq >> 1) & 1))) { ok = false; break; }
-      tc::fence_after_sync();
-      float o[2][16];
-      tc::tmem_ld16(lane_addr + 32 + hb * 32, o[0]);
-      if (NPV > 16) tc::tmem_ld16(lane_addr + 32 + hb * 32 + 16, o[1]);
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.o_free[hb]);
+      for (int g = 0; g < (PP ? 2 : 1); ++g) {
+        const bool has = g == 0 ? has0 : has1;
+        const int os = q * (PP ? 2 : 1) + g;
+        if (has) {
+          if (!__all_sync(kFull, mbar_wait(&sh.ofin[os], (used >> os) & 1))) { ok = false; break; }
+          used ^= 1u << os;
+          tc::fence_after_sync();
+          float o[2][16];
+          tc::tmem_ld16(lane_addr + kOCol + os * 32, o[0]);
+          if (NPV > 16) tc::tmem_ld16(lane_addr + kOCol + os * 32 + 16, o[1]);
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.ofree[os]);
 #pragma unroll
-      for (int n = 0; n < CN; ++n) {
-        const float x = o[n >> 4][n & 15] + o[(HG + n) >> 4][(HG + n) & 15];   // O_hi + O_lo
-        if (g1) acc1[n] = rescale ? fmaf(acc1[n], corr[n], x) : acc1[n] + x;
-        else acc0[n] = rescale ? fmaf(acc0[n], corr[n], x) : acc0[n] + x;
+          for (int n = 0; n < CN; ++n) {
+            const float v = o[n >> 4][n & 15] + o[(HG + n) >> 4][(HG + n) & 15];   // O_hi + O_lo
+            if (g == 0) x0[n] = v;
+            else x1[n] = v;
+          }
+        } else {
+#pragma unroll
+          for (int n = 0; n < CN; ++n) {
+            if (g == 0) x0[n] = 0.f;
+            else x1[n] = 0.f;
+          }
+        }
       }
-      ++item_tiles;
-      if (mt.last) {
+      if (!ok) break;
+      {
         T* out = static_cast<T*>(p.out);
-        // the groups that had a tile in this item: the last tile's, and (two
-        // groups) the other one when the item has more than one tile
-        const bool has0 = !g1 || item_tiles >= 2, has1 = PP && (g1 || item_tiles >= 2);
         // Per column, the groups' exact log-sum-exp merge -- M = max(m0, m1),
         // f_g = 2^(m_g - M), L = f0 L0 + f1 L1 -- and where its row goes are the
         // same for every thread: lane n computes column n's once, and every
         // thread takes them from lane n.  dst: element offset of the row in the
-        // output (bit 0 set) or in the workspace's partial results; -1: padding.
+        // output (bit 0 set; bit 1: write zeros) or in the workspace's partial
+        // results; -1: nothing to write.
         float cf0 = 0.f, cf1 = 0.f, cL = 1.f;
         long long cdst = -1;
         if (lane < CN) {
           const int n = lane;
-          const typename Shared<NS, I8, NRH>::Final& F0 = sh.fin[mt.qslot][0];
-          const typename Shared<NS, I8, NRH>::Final& F1 = sh.fin[mt.qslot][1];
+          const typename Shared<NS, I8, NRH>::Final& F0 = sh.fin[q][0];
+          const typename Shared<NS, I8, NRH>::Final& F1 = sh.fin[q][1];
           const float mg0 = has0 ? F0.m[n] : -INFINITY, mg1 = has1 ? F1.m[n] : -INFINITY;
           const float M = fmaxf(mg0, mg1);
           cf0 = (mg0 == -INFINITY) ? 0.f : exp2f(mg0 - M);
@@ -1284,13 +1387,13 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
             const int64_t hrow = (int64_t)sq * p.num_q_heads + mt.kvh * G + n % G;
             const bool direct = SP ? (sp_eff[sq] == 0 && sp_tot[sq] == 1) : mt.n_parts == 1;
             if (direct) {
-              cdst = hrow * kD + 1;
+              cdst = hrow * kD + (mt.bad ? 3 : 1);   // bit 1: a zero row (the item read block 0 for a bad id)
             } else {
               const int64_t r = hrow * p.max_parts + mt.pbase + mt.part;
-              cdst = r * kD;
+              cdst = mt.bad ? -1 : r * kD;
               if (quarter == 0) {
-                p.ws_ml[r * 2 + 0] = M;
-                p.ws_ml[r * 2 + 1] = cL;
+                p.ws_ml[r * 2 + 0] = mt.bad ? 0.f : M;
+                p.ws_ml[r * 2 + 1] = mt.bad ? -1.f : cL;   // an invalid partition: the merge writes zeros
               }
             }
           }
@@ -1299,19 +1402,17 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         for (int n = 0; n < CN; ++n) {
           const long long dst = __shfl_sync(kFull, cdst, n);
           const float f0 = __shfl_sync(kFull, cf0, n);
-          const float O = PP ? fmaf(acc0[n], f0, acc1[n] * __shfl_sync(kFull, cf1, n)) : acc0[n];
+          const float O = PP ? fmaf(x0[n], f0, x1[n] * __shfl_sync(kFull, cf1, n)) : x0[n];
           const float L = __shfl_sync(kFull, cL, n);
           if (dst >= 0) {
-            if (dst & 1) out[(dst - 1) + row] = Elem<T>::from_float(O / L);
+            if (dst & 1) out[(dst & ~3LL) + row] = Elem<T>::from_float((dst & 2) ? 0.f : O / L);
             else p.ws_o[dst + row] = O;
           }
-          acc0[n] = acc1[n] = 0.f;
         }
-        item_tiles = 0;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.c_free[hb]);
       }
-      ++tile_seq;
+      // fin[q] and ihand[q] are free for the item after the next
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.c_free[q]);
     }
     if (!ok && lane == 0) {
       report(p.dev_err, PA_DEVERR_TIMEOUT);

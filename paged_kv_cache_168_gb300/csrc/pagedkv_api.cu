@@ -88,8 +88,9 @@ bool is_i8(const pa_cache_desc* d) { return d->dtype == PA_INT8_F16 || d->dtype 
 // Default partition of the persistent tensor-core kernels for `units` long
 // pieces of work per kv head (sequences, or shared prefixes) of up to
 // max_context_len tokens: the longest of 4096..512 (8192 first past
-// kLongContext) that still gives six items per SM.
-int32_t persistent_partition(const pa_cache_desc* desc, int64_t units, int32_t max_context_len) {
+// kLongContext) that still gives items_per_sm_x2 / 2 items per SM (six).
+int32_t persistent_partition(const pa_cache_desc* desc, int64_t units, int32_t max_context_len,
+                             int64_t items_per_sm_x2 = 2 * kItemsPerSm) {
   // Each partition writes (D + 2) floats per query head and the merge reads them
   // back, so longer partitions cost less -- until one item is so long that the
   // kernel's tail runs on a few SMs.  Long contexts have the per-SM work to
@@ -98,7 +99,7 @@ int32_t persistent_partition(const pa_cache_desc* desc, int64_t units, int32_t m
   const int64_t pairs = (units > 0 ? units : 0) * (desc->num_kv_heads > 0 ? desc->num_kv_heads : 0);
   const int64_t ctx = max_context_len > 0 ? max_context_len : 0;
   for (int P = max_context_len > kLongContext ? kMaxLongPartition : kMaxPartition; P > kMinPartition; P /= 2)
-    if (pairs * ((ctx + P - 1) / P) >= kItemsPerSm * device_sm_count()) return P;
+    if (2 * pairs * ((ctx + P - 1) / P) >= items_per_sm_x2 * device_sm_count()) return P;
   return kMinPartition;
 }
 
@@ -443,8 +444,10 @@ int32_t pa_decode_shared_prefix_partition_size(const pa_cache_desc* desc, int32_
   if (partition_size > 0) return partition_size;
   if (!shared_prefix_kernel_serves(desc, num_seqs, num_q_heads) || num_groups <= 0)
     return pa_decode_partition_size(desc, num_seqs, max_context_len, 0);
-  // the groups' prefixes are the long items: size the partitions by them
-  return persistent_partition(desc, num_groups, max_context_len);
+  // the groups' prefixes are the long items; every sequence adds a (short)
+  // tail item of its own, so 1.5 prefix items per SM keep the SMs busy to
+  // the end while items stay long (fewer partial results to merge)
+  return persistent_partition(desc, num_groups, max_context_len, 3);
 }
 
 size_t pa_decode_shared_prefix_workspace_bytes(const pa_cache_desc* desc, int32_t num_seqs, int32_t num_q_heads,

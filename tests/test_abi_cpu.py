@@ -188,12 +188,14 @@ def test_static_workspace_size_matches_the_header():
 def test_shared_prefix_sizes_and_checks(lib):
     d = CacheDesc(100, 16, 8, 128, torch.bfloat16)
     # beam-shaped: 32 groups x 4 beams, 32/8 heads, contexts up to 2305 tokens: the
-    # prefixes are the long items, 32 x 8 x ceil(2305 / 512) = 1280 >= 912 at 512
-    assert _lib.decode_shared_prefix_partition_size(d, 128, 32, 32, 2305) == 512
+    # prefixes are the long items, 32 x 8 x ceil(2305 / 4096) = 256 >= 1.5 x 152
+    assert _lib.decode_shared_prefix_partition_size(d, 128, 32, 32, 2305) == 4096
+    # 8 groups: 8 x 8 x ceil(2305 / 1024) = 192 < 228 at 1024; 320 at 512
+    assert _lib.decode_shared_prefix_partition_size(d, 128, 32, 8, 2305) == 512
     assert _lib.decode_shared_prefix_partition_size(d, 128, 32, 32, 2305, 1024) == 1024
     assert _lib.decode_shared_prefix_partition_size(d, 128, 32, 0, 2305) == _lib.decode_partition_size(d, 128, 2305)
     # workspace: (ceil(ctx / P) + 1) partitions per row, plus three ints per sequence
-    want = 128 * 32 * (5 + 1) * 130 * 4 + 3 * 128 * 4
+    want = 128 * 32 * (1 + 1) * 130 * 4 + 3 * 128 * 4
     assert _lib.decode_shared_prefix_workspace_bytes(d, 128, 32, 32, 2305) == -(-want // 16) * 16
     # shapes the dedicated kernel does not serve size as pa_decode does
     d64 = CacheDesc(100, 16, 8, 64, torch.bfloat16)

@@ -856,7 +856,8 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         // wait (bounded) for the latest phase of every stage.  Normally they
         // have landed or are about to, and the end mark below is only read
         // after the last tile anyway.
-        for (int t = max(0, tile_seq - NS); t < tile_seq; ++t) mbar_wait(&sh.full[t % NS], (t / NS) & 1);
+        for (int t = max(0, tile_seq - NS); t < tile_seq; ++t)
+          if (!mbar_wait(&sh.full[t % NS], (t / NS) & 1)) report(p.dev_err, PA_DEVERR_TIMEOUT);
       }
       if (lane == 0) {
         if (aborted) {
@@ -958,7 +959,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       }
       // every MMA this lane issued completes before TMEM can be freed
       tc::commit(&sh.mma_drain[0]);
-      mbar_wait(&sh.mma_drain[0], 0);
+      if (!mbar_wait(&sh.mma_drain[0], 0)) report(p.dev_err, PA_DEVERR_TIMEOUT);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -1022,7 +1023,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       }
       // every MMA this lane issued completes before TMEM can be freed
       tc::commit(&sh.mma_drain[0]);
-      mbar_wait(&sh.mma_drain[0], 0);
+      if (!mbar_wait(&sh.mma_drain[0], 0)) report(p.dev_err, PA_DEVERR_TIMEOUT);
     }
     __syncwarp();
   } else if (kSplitIssue && warp == kPVWarp) {
@@ -1087,7 +1088,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         sh.abort_flag = 1;
       }
       tc::commit(&sh.mma_drain[1]);
-      mbar_wait(&sh.mma_drain[1], 0);
+      if (!mbar_wait(&sh.mma_drain[1], 0)) report(p.dev_err, PA_DEVERR_TIMEOUT);
     }
     __syncwarp();
   } else if ((warp >= 2 && warp < 6) || (ping_pong(I8, CN) && warp >= kSoftB && warp < kSoftB + 4)) {
@@ -1537,8 +1538,12 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       }
       if (m.s < 0) {
         // no more work: the mark goes into both halves' slots (each converter
-        // warp watches its own half's ring)
+        // warp watches its own half's ring) -- after the drain below, whose
+        // waits on a slot's latest phase would otherwise alias the mark's
         if (lane == 0) {
+          for (int h = 0; h < 2; ++h)
+            for (int t = max(0, tile - NRH); t < tile; ++t)
+              if (!mbar_wait(&sh.raw_full[h * NRH + t % NRH], (t / NRH) & 1)) report(p.dev_err, PA_DEVERR_TIMEOUT);
           sh.raw_meta[r0] = m;
           sh.raw_meta[r1] = m;
           mbar_arrive(&sh.raw_full[r0]);
@@ -1569,15 +1574,13 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       if (lane == 0) mbar_arrive(&sh.desc_empty[d]);
       ++tile;
     }
-    if (lane == 0) {
-      // never leave copies in flight, whether or not another role gave up:
-      // wait (bounded) for the latest phase of every raw slot
+    if (!ok && lane == 0) {
+      // never leave copies in flight: wait (bounded) for the latest phase of
+      // every raw slot (the normal end drained them before posting its mark)
       for (int h = 0; h < 2; ++h)
         for (int t = max(0, tile - NRH); t < tile; ++t) mbar_wait(&sh.raw_full[h * NRH + t % NRH], (t / NRH) & 1);
-      if (!ok) {
-        report(p.dev_err, PA_DEVERR_TIMEOUT);
-        sh.abort_flag = 1;   // the other roles see it and leave their (bounded) loops
-      }
+      report(p.dev_err, PA_DEVERR_TIMEOUT);
+      sh.abort_flag = 1;   // the other roles see it and leave their (bounded) loops
     }
   }
 

@@ -235,7 +235,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
         sh.abort_flag = 1;
       }
       // never leave copies in flight, whether or not another role gave up
-      for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(&sh.full[j & 1], (j >> 1) & 1);
+      for (int j = max(0, issued - 2); j < issued; ++j)
+        if (!mbar_wait(&sh.full[j & 1], (j >> 1) & 1)) report(p.dev_err, PA_DEVERR_TIMEOUT);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
       }
       // every MMA this lane issued completes before TMEM can be freed
       tc::commit(&sh.mma_drain);
-      mbar_wait(&sh.mma_drain, 0);
+      if (!mbar_wait(&sh.mma_drain, 0)) report(p.dev_err, PA_DEVERR_TIMEOUT);
     }
     __syncwarp();
   } else {

@@ -278,7 +278,7 @@ pa_status pa_prefill(void* out, const void* q, int64_t q_token_stride, const voi
  * pa_decode_shared_prefix_workspace_bytes and take the default partition size
  * from pa_decode_shared_prefix_partition_size (the same arguments).  Served by
  * a dedicated tensor-core kernel for a 16-bit cache, head_size 128,
- * block_size >= 8, 1, 2, 4 or 8 query heads per kv head and at most 192
+ * block_size >= 8, 1, 2, 4 or 8 query heads per kv head and at most 160
  * sequences; other shapes run pa_decode (the same result, without the sharing).
  * No windows or ring tables. */
 pa_status pa_decode_shared_prefix(void* out, const void* q, int64_t q_seq_stride, const void* kv_cache,

@@ -376,39 +376,67 @@ __global__ void __launch_bounds__(SimtCfg<D, G>::kThreads, 3)
 // effective prefix and the first member of the sequence's prefix item, whose
 // table row the prefix was read through.  A member whose block ids differ from
 // that row inside the prefix gets zero rows and PA_DEVERR_PREFIX.
+constexpr int kMergeRegs = 8;   // rows with up to this many partitions merge from registers
+
 template <typename T, int D, bool SP, int GB>
 __global__ void __launch_bounds__(D * GB) merge_partitions_kernel(const __grid_constant__ DecodeParams p) {
   const int s = blockIdx.y, d = threadIdx.x % D, sub = threadIdx.x / D;
   const int h = blockIdx.x * GB + sub;             // this thread's query head
-  const int ctx = p.context_lens[s];
-  const int P = p.partition_size;
-  if (ctx <= 0 || !context_ok(p, ctx)) return;
   T* out_s = static_cast<T*>(p.out) + (int64_t)s * p.num_q_heads * D;
   int n;
+  bool differ = false, check = false;
   if constexpr (SP) {
-    n = p.ws_seq[s];
+    n = p.ws_seq[s];                               // 0 for an empty or invalid context
     const int eff = p.ws_seq[p.num_seqs + s], lead = p.ws_seq[2 * p.num_seqs + s];
     if (n == 0 || (eff == 0 && n <= 1)) return;   // zero rows, or written by the decode kernel
-    if (eff > 0 && lead != s) {
+    // the member's prefix block ids against its leader's: loaded now, decided
+    // (one barrier) after the merge's own loads
+    check = eff > 0 && lead != s;
+    if (check) {
       const int32_t* mine = p.block_tables + (int64_t)s * p.bt_stride;
       const int32_t* theirs = p.block_tables + (int64_t)lead * p.bt_stride;
-      bool differ = false;
       for (int j = threadIdx.x; j < eff / p.block_size; j += D * GB) differ |= mine[j] != theirs[j];
-      if (__syncthreads_or(differ)) {
-        out_s[h * D + d] = Elem<T>::from_float(0.f);
-        if (threadIdx.x == 0 && blockIdx.x == 0) report(p.dev_err, PA_DEVERR_PREFIX);
-        return;
-      }
     }
   } else {
-    n = (ctx - attended_from(p, ctx) + P - 1) / P;
+    const int ctx = p.context_lens[s];
+    if (ctx <= 0 || !context_ok(p, ctx)) return;
+    n = (ctx - attended_from(p, ctx) + p.partition_size - 1) / p.partition_size;
     if (n <= 1) return;
   }
-  __shared__ float sm_w[GB][256];
-  // every thread runs the same iterations (the same n), so the barriers below
-  // are reached uniformly
-  {
-    const int64_t row0 = ((int64_t)s * p.num_q_heads + h) * p.max_parts;
+  const int64_t row0 = ((int64_t)s * p.num_q_heads + h) * p.max_parts;
+  float res;
+  if (n <= kMergeRegs) {
+    // the usual case: every partition's (m, l) and o loaded at once
+    float mv[kMergeRegs], lv[kMergeRegs], ov[kMergeRegs];
+#pragma unroll
+    for (int i = 0; i < kMergeRegs; ++i) {
+      if (i < n) {
+        mv[i] = p.ws_ml[(row0 + i) * 2 + 0];
+        lv[i] = p.ws_ml[(row0 + i) * 2 + 1];
+        ov[i] = p.ws_o[(row0 + i) * D + d];
+      }
+    }
+    float M = -INFINITY;
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < kMergeRegs; ++i)
+      if (i < n) {
+        bad |= lv[i] < 0.f;
+        M = fmaxf(M, mv[i]);
+      }
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMergeRegs; ++i)
+      if (i < n) {
+        const float w = exp2f(mv[i] - M);
+        L = fmaf(w, lv[i], L);
+        O = fmaf(w, ov[i], O);
+      }
+    res = bad ? 0.f : O / L;
+  } else {
+    // every thread runs the same iterations (the same n), so the barriers
+    // below are reached uniformly
+    __shared__ float sm_w[GB][256];
     float M = -INFINITY;
     bool bad = false;
     for (int i = 0; i < n; ++i) {
@@ -427,8 +455,13 @@ __global__ void __launch_bounds__(D * GB) merge_partitions_kernel(const __grid_c
         O = fmaf(w, p.ws_o[(row0 + i0 + i) * D + d], O);
       }
     }
-    out_s[h * D + d] = Elem<T>::from_float(bad ? 0.f : O / L);
+    res = bad ? 0.f : O / L;
   }
+  if (SP && check && __syncthreads_or(differ)) {   // check is the same in every thread of the CTA
+    res = 0.f;
+    if (threadIdx.x == 0 && blockIdx.x == 0) report(p.dev_err, PA_DEVERR_PREFIX);
+  }
+  out_s[h * D + d] = Elem<T>::from_float(res);
 }
 
 // Launches the merge over every sequence, GB query heads of one kv head per

@@ -247,7 +247,7 @@ __device__ __forceinline__ bool ctx_invalid(const DecodeParams& p, int ctx) { re
 // per-sequence and per-prefix tables.  NV = virtual sequences at most: the
 // sequences, plus (shared prefix) one prefix per group chunk (<= S).
 struct ItemTables {
-  size_t pre, rseq, rcls, eff, tot, npre, pv_seq0, pv_n, pv_eff, gch, end;
+  size_t pre, rseq, rcls, eff, tot, npre, pv_seq0, pv_n, pv_eff, gch, ctx, end;
   __host__ __device__ ItemTables(int S, bool sp) {
     const size_t nv = sp ? 2 * (size_t)S : (size_t)S;
     auto a4 = [](size_t x) { return (x + 3) & ~(size_t)3; };
@@ -261,7 +261,8 @@ struct ItemTables {
     pv_n = pv_seq0 + (sp ? (size_t)S * 2 : 0);
     pv_eff = a4(pv_n + (sp ? (size_t)S : 0));
     gch = pv_eff + (sp ? (size_t)S * 4 : 0);
-    end = gch + (sp ? ((size_t)S + 1) * 4 : 0);
+    ctx = gch + (sp ? ((size_t)S + 1) * 4 : 0);
+    end = ctx + (sp ? (size_t)S * 4 : 0);
   }
 };
 
@@ -335,6 +336,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
   uint8_t* pv_n = tables + tl.pv_n;
   int* pv_eff = reinterpret_cast<int*>(tables + tl.pv_eff);
   int* gch = reinterpret_cast<int*>(tables + tl.gch);
+  int* sctx = reinterpret_cast<int*>(tables + tl.ctx);              // context lengths, staged once
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.num_seqs, Hkv = p.num_kv_heads, bs = p.block_size;
@@ -404,6 +406,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
     constexpr int MB = kN / G;
     const int NGr = p.num_groups, P = p.partition_size;
     for (int i = threadIdx.x; i < S; i += blockDim.x) {
+      sctx[i] = p.context_lens[i];
       sp_eff[i] = 0;
       sp_npre[i] = 0;
       if (blockIdx.x == 0) p.ws_seq[2 * S + i] = i;
@@ -421,7 +424,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         const int a = p.group_start[g], b = p.group_start[g + 1];
         int m = p.prefix_lens[g];
         for (int i = a; i < b && m > 0; ++i) {
-          const int c = p.context_lens[i];
+          const int c = sctx[i];
           m = (c <= 0 || ctx_invalid(p, c)) ? 0 : min(m, c);
         }
         const int eff = b - a >= 2 ? max(0, m / bs * bs) : 0;   // a group of one shares nothing
@@ -466,7 +469,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       }
     }
     for (int i = threadIdx.x; i < S; i += blockDim.x) {
-      const int c = p.context_lens[i];
+      const int c = sctx[i];
       const int tot = (c <= 0 || ctx_invalid(p, c)) ? 0 : sp_npre[i] + (c - sp_eff[i] + P - 1) / P;
       sp_tot[i] = (int16_t)tot;
       if (blockIdx.x == 0) {
@@ -483,7 +486,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
     if (SP && i >= S) {
       work_of_len(pv_eff[i - S], p.partition_size, full, cls);
     } else if (SP) {
-      const int c = p.context_lens[i];
+      const int c = sctx[i];
       if (c <= 0 || ctx_invalid(p, c)) {
         full = 0;
         cls = 1;

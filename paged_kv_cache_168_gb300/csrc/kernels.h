@@ -137,7 +137,9 @@ cudaError_t launch_decode_tc_i8(const DecodeParams& p, int act_dtype, int group,
 // 128, block_size >= 8, group 1, 2, 4 or 8, at most kTcSpMaxSeqs sequences): a
 // group's prefix is streamed once for all its members.  Launches the decode
 // kernel and the merge (which also checks the members' prefix block ids).
-constexpr int kTcSpMaxSeqs = 192;
+// (the item tables of 160 sequences keep static + dynamic shared memory within
+// the 227 KiB a CTA may have)
+constexpr int kTcSpMaxSeqs = 160;
 cudaError_t launch_decode_tc_sp(const DecodeParams& p, int dtype, int group, int num_sms, cudaStream_t stream);
 cudaError_t launch_merge_sp(const DecodeParams& p, int dtype, int head_size, cudaStream_t stream);
 

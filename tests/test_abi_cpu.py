@@ -201,8 +201,10 @@ def test_shared_prefix_sizes_and_checks(lib):
     d64 = CacheDesc(100, 16, 8, 64, torch.bfloat16)
     assert _lib.decode_shared_prefix_workspace_bytes(d64, 128, 32, 32, 2305, 512) == \
         _lib.decode_workspace_bytes(d64, 128, 32, 2305, 512)
-    assert _lib.decode_shared_prefix_workspace_bytes(d, 300, 32, 32, 2305, 512) == \
-        _lib.decode_workspace_bytes(d, 300, 32, 2305, 512)
+    assert _lib.decode_shared_prefix_workspace_bytes(d, 161, 32, 32, 2305, 512) == \
+        _lib.decode_workspace_bytes(d, 161, 32, 2305, 512)                # above 160 sequences
+    assert _lib.decode_shared_prefix_workspace_bytes(d, 160, 32, 32, 2305, 512) != \
+        _lib.decode_workspace_bytes(d, 160, 32, 2305, 512)
 
     def call(num_groups=2, gs=FAKE, pl=FAKE, ws=1 << 30, P=256):
         return lib.pa_decode_shared_prefix(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 4 * 128,

@@ -133,12 +133,24 @@ def test_shapes_outside_the_kernel_fall_back_to_plain_decode(case, monkeypatch):
     elif case == "simt":
         monkeypatch.setenv("PAGEDKV_DECODE_KERNEL", "simt")
     else:
-        groups = [(64, [70, 80])] * 100          # 200 sequences: above the kernel's limit
+        groups = [(64, [70, 80])] * 81           # 162 sequences: above the kernel's limit
     sp = SharedPaged(rng, groups, 16, 4, D, bs, "bf16")
     q, pool, desc = _dev(sp)
     out, bits = run_shared(sp, q, pool, desc, sp.tables, sp.group_start, sp.prompt_lens, 256)
     assert bits == 0
     assert_attention_close(out, oracle_ref(sp), f"fallback {case}")
+
+
+def test_the_largest_batch_the_kernel_serves():
+    # 160 sequences (40 groups of 4): the kernel's item tables at their largest
+    rng = np.random.default_rng(35)
+    groups = [(int(rng.integers(16, 400)), [int(c) for c in rng.integers(400, 700, 4)]) for _ in range(40)]
+    sp = SharedPaged(rng, groups, 32, 8, 128, 16, "bf16")
+    assert sp.S == 160
+    q, pool, desc = _dev(sp)
+    out, bits = run_shared(sp, q, pool, desc, sp.tables, sp.group_start, sp.prompt_lens, 0)
+    assert bits == 0
+    assert_attention_close(out, oracle_ref(sp), "160 sequences in groups")
 
 
 def test_beam_workload_shared_prefix_equals_plain_decode():

@@ -530,15 +530,33 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
     // round in snake order (c, then 151 - c, ...), so every CTA gets about the
     // same number of tiles (longest first).
     const int n_full = carry;
-    for (int i = lane; i < NV; i += 32) atomicAdd(&sh.cls_cnt[rcls[i]], 1);
+    // remainder partitions per class: one shared-memory atomic per distinct
+    // class per 32 virtual sequences (most share a class)
+    for (int base = 0; base < NV; base += 32) {
+      const int i = base + lane;
+      const int cls = i < NV ? rcls[i] : -1;
+      const uint32_t same = __match_any_sync(kFull, cls);
+      if (cls >= 0 && (same & ((1u << lane) - 1u)) == 0) atomicAdd(&sh.cls_cnt[cls], __popc(same));
+    }
     __syncwarp();
-    if (lane == 0) {
+    // each class's first slot: an exclusive scan over the classes from the
+    // most tiles down (class c at index kClasses - 1 - c), 32 at a time
+    {
       int at = 0;
-      for (int c = kClasses - 1; c >= 1; --c) {
-        sh.cls_cur[c] = at;
-        at += sh.cls_cnt[c];
+      for (int base = 0; base < kClasses - 1; base += 32) {
+        const int c = kClasses - 1 - (base + lane);   // classes kClasses-1 .. 1
+        const int own = c >= 1 ? sh.cls_cnt[c] : 0;
+        int x = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(kFull, x, o);
+          if (lane >= o) x += y;
+        }
+        if (c >= 1) sh.cls_cur[c] = at + x - own;
+        at += __shfl_sync(kFull, x, 31);
       }
-      sh.cls_cnt[0] = at;   // remainder partitions in all
+      __syncwarp();
+      if (lane == 0) sh.cls_cnt[0] = at;   // remainder partitions in all
     }
     __syncwarp();
     for (int base = 0; base < NV; base += 32) {

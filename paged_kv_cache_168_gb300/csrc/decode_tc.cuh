@@ -122,6 +122,14 @@ __device__ __forceinline__ void transpose_reduce(float (&v)[K], int lane, Op op)
 }
 __host__ __device__ constexpr int log2_of(int k) { return k <= 1 ? 0 : 1 + log2_of(k >> 1); }
 
+// The maximum of v over the warp, in every lane (NaN inputs are ignored, as
+// by fmaxf).
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 // 2^x on the MUFU unit (relative error about 2^-22; -inf -> +0).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -1125,12 +1133,20 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;   // TMEM lane = token row of S^T
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-    float m[CN], lp[CN];
+    // The running maxima are the same in every thread of the group.  With
+    // more than 8 columns they are held one per lane (lane l: column l mod CN)
+    // and broadcast where needed, which keeps the per-thread state small
+    // enough that nothing spills.
+    constexpr bool kDM = CN > 8;
+    float m[kDM ? 1 : CN], lp[CN];
 #pragma unroll
-    for (int n = 0; n < CN; ++n) {
-      m[n] = -INFINITY;
-      lp[n] = 0.f;
-    }
+    for (int n = 0; n < (kDM ? 1 : CN); ++n) m[n] = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < CN; ++n) lp[n] = 0.f;
+    auto m_at = [&](int n) -> float {   // column n's running maximum (every lane calls it)
+      if constexpr (kDM) return __shfl_sync(kFull, m[0], n);
+      else return m[n];
+    };
     int tile_seq = grp;
     bool ok = true;
     while (true) {
@@ -1189,17 +1205,16 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
 #pragma unroll
       for (int n = 0; n < CN; ++n) {
         x[n] = rv ? sv[n] * kscale : -INFINITY;
-        up |= x[n] > m[n] + (I8 ? 0.f : kLazyMax);   // 8-bit: the V scales ride on P, keep p <= 1
+        up |= x[n] > m_at(n) + (I8 ? 0.f : kLazyMax);   // 8-bit: the V scales ride on P, keep p <= 1
       }
       const bool wup = __any_sync(kFull, up);
       const int par = (tile_seq >> 1) & 1;   // exchange buffer of this tile (the group's tile parity)
-      if (wup) {   // this warp's column maxima over its 32 rows
-        float v[CN];
+      if (wup) {   // this warp's column maxima over its 32 rows (one warp reduction per column)
 #pragma unroll
-        for (int n = 0; n < CN; ++n) v[n] = x[n];
-        transpose_reduce<CN>(v, lane, [](float a, float b) { return fmaxf(a, b); });
-        constexpr int sh_ = 5 - log2_of(CN);
-        if ((lane & ((1 << sh_) - 1)) == 0) sh.red_max[hb][par][quarter][lane >> sh_] = v[0];
+        for (int n = 0; n < CN; ++n) {
+          const float v = warp_max(x[n]);
+          if (lane == 0) sh.red_max[hb][par][quarter][n] = v;
+        }
       }
       if (lane == 0) sh.red_up[hb][par][quarter] = wup ? 1 : 0;
       __syncwarp();
@@ -1215,15 +1230,30 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         // rescaled, the latter once the group's previous PV has completed and
         // before this tile's PV is issued
         float corr[CN];
-#pragma unroll
-        for (int n = 0; n < CN; ++n) {
-          float mx = m[n];
+        if constexpr (kDM) {
+          const int n = lane & (CN - 1);   // this lane's column
+          float mx = m[0];
 #pragma unroll
           for (int w = 0; w < 4; ++w)
             if (ups[w]) mx = fmaxf(mx, sh.red_max[hb][par][w][n]);
-          corr[n] = (m[n] == -INFINITY) ? 0.f : exp2f(m[n] - mx);
-          lp[n] *= corr[n];
-          m[n] = mx;
+          const float c = (m[0] == -INFINITY) ? 0.f : exp2f(m[0] - mx);
+          m[0] = mx;
+#pragma unroll
+          for (int k = 0; k < CN; ++k) {
+            corr[k] = __shfl_sync(kFull, c, k);
+            lp[k] *= corr[k];
+          }
+        } else {
+#pragma unroll
+          for (int n = 0; n < CN; ++n) {
+            float mx = m[n];
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+              if (ups[w]) mx = fmaxf(mx, sh.red_max[hb][par][w][n]);
+            corr[n] = (m[n] == -INFINITY) ? 0.f : exp2f(m[n] - mx);
+            lp[n] *= corr[n];
+            m[n] = mx;
+          }
         }
         if (!first) {
           // thread = TMEM lane = head dim 32 quarter + lane of O^T; columns: p_hi
@@ -1250,7 +1280,8 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       float (&pr)[CN] = x;   // the weights replace the scores
 #pragma unroll
       for (int n = 0; n < CN; ++n) {
-        pr[n] = rv ? ex2_approx(x[n] - m[n]) : 0.f;
+        const float mn = m_at(n);
+        pr[n] = rv ? ex2_approx(x[n] - mn) : 0.f;
         lp[n] += pr[n];
       }
       uint32_t pk[NPV / 2];   // [p_hi of heads 0..HG-1 | p_lo of heads 0..HG-1], two per word
@@ -1283,44 +1314,44 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.p_full[hb]);
-      // this group's part of the normaliser from this quarter's 32 rows; the
-      // output warps add the quarters (and the groups)
-      float Lq[CN];   // Lq[0]: the sum over this quarter's rows of column lane >> (5 - log2 CN)
-      if (fin) {
-#pragma unroll
-        for (int n = 0; n < CN; ++n) Lq[n] = lp[n];
-        transpose_reduce<CN>(Lq, lane, [](float a, float b) { return a + b; });
-      }
       // hand-off to the output warps at the group's last tile of the item:
       // its maximum and sums (and, with the item's last tile, the item's
       // metadata) into the slot of the item's parity, once the output warps
-      // are done with the item before it of the same parity
+      // are done with the item before it of the same parity.  The maximum is
+      // stored first, so it is dead while the sums are reduced.
       if (fin) {
         const int k = mt.item, q = k & 1;
         if (k >= 2 && !__all_sync(kFull, mbar_wait(&sh.c_free[q], ((k >> 1) - 1) & 1))) { ok = false; break; }
+        if constexpr (kDM) {
+          if (quarter == 0 && lane < CN) sh.fin[q][grp].m[lane] = m[0];
+        }
         if (lane == 0 && quarter == 0) {
+          if constexpr (!kDM) {
 #pragma unroll
-          for (int n = 0; n < CN; ++n) sh.fin[q][grp].m[n] = m[n];
+            for (int n = 0; n < CN; ++n) sh.fin[q][grp].m[n] = m[n];
+          }
           if (mt.tail == 0) {
             sh.ihand[q].meta = mt;
             sh.ihand[q].ntiles = mt.head + 1;
             sh.ihand[q].first_grp = PP ? ((tile_seq - mt.head) & 1) : 0;
           }
         }
+        // this group's part of the normaliser from this quarter's 32 rows (the
+        // output warps add the quarters and the groups), reduced in place:
+        // lp[0] becomes the sum over the quarter's rows of column
+        // lane >> (5 - log2 CN), and the sums start afresh with the next item
+        transpose_reduce<CN>(lp, lane, [](float a, float b) { return a + b; });
         constexpr int sh_ = 5 - log2_of(CN);
-        if ((lane & ((1 << sh_) - 1)) == 0) sh.fin[q][grp].Lq[quarter][lane >> sh_] = Lq[0];
+        if ((lane & ((1 << sh_) - 1)) == 0) sh.fin[q][grp].Lq[quarter][lane >> sh_] = lp[0];
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&sh.c_full[q]);
           if (PP && mt.head == 0 && mt.tail == 0) mbar_arrive(&sh.c_full[q]);   // a one-tile item: for both groups
         }
-      }
-      if (fin) {
 #pragma unroll
-        for (int n = 0; n < CN; ++n) {
-          m[n] = -INFINITY;
-          lp[n] = 0.f;
-        }
+        for (int n = 0; n < (kDM ? 1 : CN); ++n) m[n] = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < CN; ++n) lp[n] = 0.f;
       }
       tile_seq += PP ? 2 : 1;
     }

@@ -14,7 +14,7 @@
 //     K = 128 dims; 8-token groups 4 KiB apart), and
 //   * the MN-major A operand of O^T = V^T P^T (M = 128 dims, N = 16 heads,
 //     K = 128 tokens).
-// Q^T (K-major, swizzled, written by the producer warp) and P^T (MN-major, no
+// Q^T (K-major, swizzled, written by the planner warp) and P^T (MN-major, no
 // swizzle, written by the softmax warps) are the B operands; S^T and O^T
 // accumulate in fp32 in tensor memory (TMEM), double-buffered.
 //
@@ -23,9 +23,16 @@
 // partitions first, then the remainder partitions from the most tiles down --
 // and takes one item per round in snake order, so the CTAs get about the same
 // number of tiles and none is spent on empty partitions.  Roles:
-//   warp 0      producer: item walk, block-id validation, Q staging, one bulk
-//               copy per (block, kv head) chunk into a ring of NS 64 KiB stages;
-//               per-stage metadata travels with the stage's mbarrier.
+//   planner     (16-bit caches: the warp before the PV issuer; 8-bit caches:
+//               warp 0) orders the items and works out each one in turn: its
+//               place, context, first 32 block ids and query rows, written as
+//               the Q^T operand of the item's slot.  16-bit caches hand the
+//               item to the streamer through a two-slot record ring.
+//   warp 0      16-bit caches: streamer -- per item, one bulk copy per (block,
+//               kv head) chunk into a ring of NS 64 KiB stages, block ids
+//               checked per tile; per-stage metadata travels with the stage's
+//               mbarrier.  With the set-up in the planner, the next item's
+//               first copies leave as soon as a stage is free.
 //   warp 1      MMA issue (one lane): QK(t) as soon as tile t is staged and its
 //               S buffer is free, PV(t) as soon as P(t) is written and its O
 //               buffer is free.  16-bit caches give PV its own issuer (the last
@@ -40,11 +47,11 @@
 //               takes the odd tiles, each group with its own running maximum
 //               and sums; the tile metadata reaches each group through the QK
 //               issuer, one buffer per S buffer.
-//   warps 6-9   output (thread = TMEM lane = head dim): fold O_hi + O_lo of
-//               each tile into registers with the online-softmax correction the
-//               softmax warps hand over (one accumulator per softmax group),
-//               merge the groups by log-sum-exp at the item's end and write the
-//               item's result (or the partition's partial results).
+//   warps 6-9   output (thread = TMEM lane = head dim): once per item, read
+//               each softmax group's O^T = O_hi + O_lo, accumulated in TMEM over
+//               the group's tiles of the item (the softmax warps rescale it when
+//               their running maximum moves), merge the groups by log-sum-exp
+//               and write the item's result (or the partition's partial results).
 // 8-bit caches (codes + one fp32 scale per token and kv head) change the
 // staging: warp 0 only plans (items, Q, block ids per tile into a descriptor
 // ring); one copy warp bulk-copies each tile's 8-bit chunks into two rings of
@@ -76,7 +83,14 @@ constexpr int kGroupBytes = 8 * 2 * kD * 2;        // one 8-token group: 4 KiB
 constexpr int kN = 16;                             // MMA N: query heads, zero-padded
 constexpr int kQBytes = kN * kD * 2;               // 4 KiB
 constexpr int kPBytes = kTile * 32 * 2;            // P^T operand: 128 tokens x up to 32 columns (8 KiB)
-constexpr int kThreads = 320;                      // producer, MMA issue, 4 softmax warps, 4 output warps
+// Q^T slots, by item index: 16-bit caches keep four items' queries staged (the
+// planner runs up to that far ahead of the tensor core); 8-bit caches two.
+// 16-bit caches write each tile's P^T into the K atoms of the tile's own stage
+// (dead once QK(t) has completed: 512 B of each 8-token group's 2 KiB), so
+// they need no P^T buffers; 8-bit stages hold V only and keep two.
+__host__ __device__ constexpr int q_slots(bool i8) { return i8 ? 2 : 4; }
+__host__ __device__ constexpr int p_buffers(bool i8) { return i8 ? 2 : 0; }
+constexpr int kThreads = 320;                      // warp 0, MMA issue, 4 softmax warps, 4 output warps
 // 8-bit caches add converter warps: 8 when the registers allow it (group <= 4), else 4
 __host__ __device__ constexpr int converter_warps(int G) { return G <= 4 ? 8 : 4; }
 // 8-bit caches also add one copy warp (after the converters) that only issues
@@ -140,9 +154,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // whose tiles are paced by the converter warps, keep one event-driven issuer
 // (measured faster there).
 __host__ __device__ constexpr bool split_issue(bool i8) { return !i8; }
+// 16-bit caches: a planner warp works out each item (its place in the order,
+// block ids, query rows) ahead of the streaming warp, which then only issues
+// copies; 8-bit caches plan in warp 0, whose copies the copy warp issues.
+__host__ __device__ constexpr bool split_plan(bool i8) { return !i8; }
 __host__ __device__ constexpr int threads_of(bool i8, int G) {
   return kThreads + (i8 ? 32 * (converter_warps(G) + 1) : 0) + (ping_pong(i8, G) ? 128 : 0) +
-         (split_issue(i8) ? 32 : 0);
+         (split_issue(i8) ? 32 : 0) + (split_plan(i8) ? 32 : 0);
 }
 constexpr int kND = 4;                             // 8-bit: tile descriptors in flight (planner -> copy warp)
 constexpr int kRawBytes = 64 * (2 * kD + 32);      // one 64-token half tile of 8-bit chunks (bs 1: 288 B/token)
@@ -173,10 +191,17 @@ struct TileMeta {
                                  // instead); the item's last tile has the item's verdict
 };
 
+// One item as the planner hands it to the streaming warp (16-bit caches).
+struct ItemRec {
+  int s, kvh, part, n_parts, t_first, t0, t1, jb;   // table row, kv head, partition; its token range
+  int seq0, ncol, pbase, qslot, item;               // columns, Q slot, item index (-1: no more work)
+  int ids[32];                                      // its first 32 block ids
+};
+
 template <int NS, bool I8, int NRH>
 struct Shared {
   uint64_t full[NS], empty[NS];
-  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], q_free[2];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], q_free[4];
   // O accumulator slot o = item parity * groups + group: the PV of the group's
   // last tile of an item completed (ofin), the output warps read it (ofree)
   uint64_t ofin[4], ofree[4];
@@ -199,12 +224,32 @@ struct Shared {
   // every warp of its group arrived for tile t + 1... which follows its reads of t
   float red_max[2][2][4][kN];
   int red_up[2][2][4];
+  // more than 8 columns: each softmax warp's copy of its group's running
+  // maxima (double-buffered) and of the corrections of its latest rescale
+  alignas(16) float mrun[2][4][2][kN];
+  alignas(16) float mcorr[2][4][kN];
+  // each output warp's per-column table for the item it is writing: the
+  // row's place (element offset; bit 0: out, else the workspace; bit 1: a zero
+  // row; -1: nothing) and the factors of the two groups' O
+  struct alignas(16) ColOut {
+    long long dst;
+    float g0, g1;
+  };
+  ColOut colout[4][kN];
   uint32_t tmem_base;
   volatile int abort_flag;
   volatile int end_tile;          // QK issuer -> PV issuer: tiles in this CTA (set at the end)
   int sp_ok;                      // shared prefix: the group starts are ordered and in range
-  int cls_cnt[kClasses], cls_cur[kClasses];   // item ordering: remainder partitions per class, cursors
-  // 8-bit caches: producer -> converter ring of raw half tiles, and the token
+  // item ordering (set-up only): remainder partitions per class, cursors;
+  // afterwards (16-bit caches) the planner -> streamer records, by item parity
+  union {
+    struct {
+      int cnt[kClasses], cur[kClasses];
+    } ord;
+    ItemRec rec[2];
+  } u;
+  uint64_t rec_full[2], rec_empty[2];
+  // 8-bit caches: copy warp -> converter ring of raw half tiles, and the token
   // scales of each converted stage
   // (two rings of NRH slots, one per 64-token half: slot h * NRH + k % NRH)
   uint64_t raw_full[I8 ? 2 * NRH : 1], raw_empty[I8 ? 2 * NRH : 1];
@@ -327,8 +372,8 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
   uint8_t* dyn = dyn_raw + (((raw_s + 1023u) & ~1023u) - raw_s);   // 1024-aligned in the shared window
   uint8_t* stages = dyn;
   uint8_t* qbuf = dyn + NS * kStage;
-  uint8_t* pbuf = qbuf + 2 * kQBytes;
-  uint8_t* raw = pbuf + 2 * kPBytes;                         // pbuf: 2 buffers of [p_hi | p_lo]
+  uint8_t* pbuf = qbuf + q_slots(I8) * kQBytes;               // 8-bit: 2 buffers of [p_hi | p_lo]
+  uint8_t* raw = pbuf + p_buffers(I8) * kPBytes;
   uint8_t* tables = raw + (I8 ? 2 * NRH * kRawBytes : 0);
   const ItemTables tl(p.num_seqs, SP);
   int* pre = reinterpret_cast<int*>(tables + tl.pre);            // [NV + 1] full partitions, prefix sum
@@ -360,6 +405,8 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
   constexpr bool kSplitIssue = split_issue(I8);
   static_assert(!ping_pong(I8, CN) || kSplitIssue, "two softmax groups take their tile metadata from the QK issuer");
   constexpr int kPVWarp = threads_of(I8, CN) / 32 - 1;          // with split issue, the PV issuer: the last warp
+  constexpr bool kSplitPlan = split_plan(I8);
+  constexpr int kPlanWarp = kSplitPlan ? kPVWarp - 1 : 0;       // the planner: before the PV issuer, else warp 0
 
   // ---- set-up: barriers, zeroed Q buffers (padding heads stay zero), TMEM
   if (threadIdx.x == 0) {
@@ -383,7 +430,6 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       mbar_init(&sh.s_free[i], 4);
       mbar_init(&sh.p_full[i], 4);
       mbar_init(&sh.pv_done[i], 1);
-      mbar_init(&sh.q_free[i], 1);
       mbar_init(&sh.max_bar[i], 4);
       // every warp of each softmax group that had a tile in the item (the group
       // of a one-tile item arrives for both)
@@ -394,12 +440,17 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
     for (int i = 0; i < 4; ++i) {
       mbar_init(&sh.ofin[i], 1);
       mbar_init(&sh.ofree[i], 4);
+      mbar_init(&sh.q_free[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.rec_full[i], 1);
+      mbar_init(&sh.rec_empty[i], 1);
     }
     sh.abort_flag = 0;
     sh.end_tile = 0x7fffffff;
     fence_mbar_init();
   }
-  for (int i = threadIdx.x; i < 2 * kQBytes / 16; i += blockDim.x)
+  for (int i = threadIdx.x; i < q_slots(I8) * kQBytes / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
   // Shared prefix: per group (consecutive sequences group_start[g] ..
   // group_start[g + 1] - 1) the effective prefix -- the caller's prefix_lens[g]
@@ -488,7 +539,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
     __syncthreads();
   }
   // per virtual sequence its full partitions and its remainder's class, all
-  // loaded at once (the producer orders the items below)
+  // loaded at once (the planner orders the items below)
   for (int i = threadIdx.x; i < NV; i += blockDim.x) {
     int full, cls;
     if (SP && i >= S) {
@@ -507,7 +558,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
     pre[i + 1] = full;
     rcls[i] = (uint8_t)cls;
   }
-  for (int i = threadIdx.x; i < kClasses; i += blockDim.x) sh.cls_cnt[i] = 0;
+  for (int i = threadIdx.x; i < kClasses; i += blockDim.x) sh.u.ord.cnt[i] = 0;
   if (warp == 1) {
     tc::tmem_alloc(&sh.tmem_base, kCols);
     tc::tmem_relinquish();
@@ -517,8 +568,99 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
   tc::fence_after_sync();
   const uint32_t tmem = sh.tmem_base;
 
-  if (warp == 0) {
-    // =================================================================== producer
+  if (kSplitPlan && warp == 0) {
+    // =================================================================== streamer (16-bit caches)
+    // Takes the planner's items in order and streams each one's tiles: a free
+    // stage, the tile's metadata, its block copies.
+    int tile_seq = 0, item_seq = 0;
+    bool aborted = false;
+    for (;; ++item_seq) {
+      const int rs = item_seq & 1;
+      if (!__all_sync(kFull, mbar_wait(&sh.rec_full[rs], (item_seq >> 1) & 1)) || sh.abort_flag) {
+        aborted = true;
+        break;
+      }
+      const ItemRec& R = sh.u.rec[rs];
+      if (R.item < 0) break;   // no more work
+      const int s = R.s, kvh = R.kvh, part = R.part, n_parts = R.n_parts, t_first = R.t_first;
+      const int t0 = R.t0, t1 = R.t1, jb = R.jb;
+      const int seq0 = R.seq0, ncol = R.ncol, pbase = R.pbase, qslot = R.qslot;
+      const int id_lane = R.ids[lane];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.rec_empty[rs]);
+      const int32_t* row = p.block_tables + (int64_t)s * p.bt_stride;   // entry table_index(j) holds block j
+      const int ntiles = (t1 - t0 + kTile - 1) / kTile;
+      // 16-bit: the block id of this lane's chunk of tile k.  The item's first 32
+      // come from the prefetched id_lane; a later one is loaded a tile ahead, so
+      // the load overlaps the wait for a free stage instead of delaying the copy.
+      auto tile_id = [&](int k) {
+        const int bi = k * (kTile / bs) + lane;
+        const int nbk = (min(kTile, t1 - (t0 + k * kTile)) + bs - 1) / bs;
+        const int id_sh = __shfl_sync(kFull, id_lane, bi & 31);
+        return lane < nbk ? (bi < 32 ? id_sh : row[table_index(jb + bi, p.ring_blocks)]) : 0;
+      };
+      int id_k = ntiles > 0 ? tile_id(0) : 0;
+      bool item_bad = false;
+      for (int k = 0; k < ntiles; ++k) {
+        const int slot = tile_seq % NS;
+        if (tile_seq >= NS && !mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1)) {
+          aborted = true;
+          break;
+        }
+        const int valid = min(kTile, t1 - (t0 + k * kTile));
+        const int nb = (valid + bs - 1) / bs;
+        // an id out of range is never read: block 0 stands in, the item's
+        // result is discarded (zero rows) and the error reported once per item
+        const bool id_bad = lane < nb && (id_k < 0 || id_k >= p.num_blocks);
+        if (__any_sync(kFull, id_bad)) {
+          if (lane == 0 && !item_bad) report(p.dev_err, PA_DEVERR_BLOCK_ID);
+          item_bad = true;
+        }
+        if (id_bad) id_k = 0;
+        if (lane == 0) {
+          TileMeta m;
+          m.s = s; m.kvh = kvh; m.part = part; m.valid = valid;
+          m.last = (k == ntiles - 1); m.qslot = qslot; m.n_parts = n_parts;
+          m.lo = max(0, t_first - (t0 + k * kTile));
+          m.tail = ntiles - 1 - k;
+          m.qinv = 1.f;
+          m.seq0 = seq0; m.ncol = ncol; m.pbase = pbase;
+          m.head = k; m.item = item_seq; m.bad = item_bad ? 1 : 0;
+          sh.meta[slot] = m;
+          mbar_arrive_expect_tx(&sh.full[slot], (uint32_t)(nb * chunk_bytes));
+        }
+        __syncwarp();
+        if (lane < nb)
+          bulk_g2s(stages + slot * kStage + lane * chunk_bytes,
+                   p.cache + ((int64_t)id_k * Hkv + kvh) * chunk_bytes, (uint32_t)chunk_bytes, &sh.full[slot]);
+        if (k + 1 < ntiles) id_k = tile_id(k + 1);
+        ++tile_seq;
+      }
+      if (aborted) break;
+    }
+    // ---- no more work: a stage whose metadata says so
+    const int slot = tile_seq % NS;
+    if (!aborted && tile_seq >= NS && !mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1)) aborted = true;
+    if (lane == 0) {
+      // never leave copies in flight, whether or not another role gave up:
+      // wait (bounded) for the latest phase of every stage.  Normally they
+      // have landed or are about to, and the end mark below is only read
+      // after the last tile anyway.
+      for (int t = max(0, tile_seq - NS); t < tile_seq; ++t)
+        if (!mbar_wait(&sh.full[t % NS], (t / NS) & 1)) report(p.dev_err, PA_DEVERR_TIMEOUT);
+    }
+    if (lane == 0) {
+      if (aborted) {
+        report(p.dev_err, PA_DEVERR_TIMEOUT);
+        sh.abort_flag = 1;
+      }
+      sh.meta[slot].s = -1;
+      sh.meta[slot].item = item_seq;     // the index the next item would have
+      mbar_arrive(&sh.full[slot]);
+    }
+    __syncwarp();
+  } else if (warp == kPlanWarp) {
+    // =================================================================== planner
     int carry = 0;
     for (int base = 0; base < NV; base += 32) {
       int x = (base + lane < NV) ? pre[base + lane + 1] : 0;
@@ -544,7 +686,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       const int i = base + lane;
       const int cls = i < NV ? rcls[i] : -1;
       const uint32_t same = __match_any_sync(kFull, cls);
-      if (cls >= 0 && (same & ((1u << lane) - 1u)) == 0) atomicAdd(&sh.cls_cnt[cls], __popc(same));
+      if (cls >= 0 && (same & ((1u << lane) - 1u)) == 0) atomicAdd(&sh.u.ord.cnt[cls], __popc(same));
     }
     __syncwarp();
     // each class's first slot: an exclusive scan over the classes from the
@@ -553,18 +695,18 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       int at = 0;
       for (int base = 0; base < kClasses - 1; base += 32) {
         const int c = kClasses - 1 - (base + lane);   // classes kClasses-1 .. 1
-        const int own = c >= 1 ? sh.cls_cnt[c] : 0;
+        const int own = c >= 1 ? sh.u.ord.cnt[c] : 0;
         int x = own;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int y = __shfl_up_sync(kFull, x, o);
           if (lane >= o) x += y;
         }
-        if (c >= 1) sh.cls_cur[c] = at + x - own;
+        if (c >= 1) sh.u.ord.cur[c] = at + x - own;
         at += __shfl_sync(kFull, x, 31);
       }
       __syncwarp();
-      if (lane == 0) sh.cls_cnt[0] = at;   // remainder partitions in all
+      if (lane == 0) sh.u.ord.cnt[0] = at;   // remainder partitions in all
     }
     __syncwarp();
     for (int base = 0; base < NV; base += 32) {
@@ -572,12 +714,12 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       const int cls = i < NV ? rcls[i] : 0;
       const uint32_t same = __match_any_sync(kFull, cls);
       const int slot_in = __popc(same & ((1u << lane) - 1u));
-      if (cls > 0) rseq[sh.cls_cur[cls] + slot_in] = (int16_t)i;
+      if (cls > 0) rseq[sh.u.ord.cur[cls] + slot_in] = (int16_t)i;
       __syncwarp();
-      if (cls > 0 && slot_in == 0) sh.cls_cur[cls] += __popc(same);
+      if (cls > 0 && slot_in == 0) sh.u.ord.cur[cls] += __popc(same);
       __syncwarp();
     }
-    const int total = (n_full + sh.cls_cnt[0]) * Hkv;
+    const int total = (n_full + sh.u.ord.cnt[0]) * Hkv;
     const int P = p.partition_size;
     // the item a CTA takes in round k (snake order); >= total: none
     auto item_of_round = [&](int k) {
@@ -585,74 +727,120 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
     };
     const bool windowed = p.window > 0 || p.ring_blocks > 0;
     constexpr int kQChunks = (CN * 16 + 31) / 32;
-    // The next item's independent loads (context length, its first 32 block ids,
-    // the query rows) are issued while the current item streams, so an item's
-    // set-up never waits on a global-memory round trip.
+    // What an item is (virtual sequence, kv head, partition, table row, columns,
+    // context and first block) is worked out 32 rounds at a time, lane l for
+    // round rbase + l, and handed to the item by shuffles: the set-up of an item
+    // never walks the shared-memory tables or waits for its context length.
+    struct Desc {
+      int v, kvh, part, row, ctx;   // virtual sequence, kv head, partition, table row, its end
+      int t0, seq0, ncol, pbase;    // shared prefix: first position, column map, partition base
+      int fb;                       // the partition's first logical block
+    };
+    auto describe = [&](int k) {   // per lane; a round past the last item gets v = -1
+      Desc d;
+      const int it = item_of_round(k);
+      d.v = -1;
+      d.kvh = d.part = d.row = d.ctx = d.t0 = d.seq0 = d.ncol = d.pbase = d.fb = 0;
+      if (it < total) {
+        const int j = it / Hkv;
+        d.kvh = it - j * Hkv;
+        if (j < n_full) {
+          int lo = 0, hi = NV - 1;   // last virtual sequence whose first full partition is <= j
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (pre[mid] <= j) lo = mid;
+            else hi = mid - 1;
+          }
+          d.v = lo;
+          d.part = j - pre[lo];
+        } else {
+          d.v = rseq[j - n_full];
+          d.part = pre[d.v + 1] - pre[d.v];   // the remainder follows the full partitions
+        }
+        if (SP && d.v >= S) {   // a group's shared prefix, read through its first member's row
+          const int k2 = d.v - S;
+          d.row = d.seq0 = pv_seq0[k2];
+          d.ncol = pv_n[k2] * G;
+          d.ctx = pv_eff[k2];
+        } else {                // a sequence (shared prefix: its tail after the prefix)
+          d.row = d.seq0 = d.v;
+          d.ncol = G;
+          d.ctx = SP ? sctx[d.v] : p.context_lens[d.v];
+          d.t0 = SP ? sp_eff[d.v] : 0;
+          d.pbase = SP ? sp_npre[d.v] : 0;
+        }
+        d.fb = windowed ? (attended_from(p, d.ctx) + d.part * P) / bs
+                        : d.t0 / bs + d.part * (P / bs);   // P is a multiple of 128, bs divides it
+      }
+      return d;
+    };
+    int rbase = 0;
+    Desc dl = describe(lane);
+    // round k's description; every lane calls it, k never decreases, and a
+    // call for k never follows one for k + 3 or later (the window keeps the
+    // two rounds before the one that moves it)
+    auto desc_of = [&](int k) {
+      if (k >= rbase + 32) {
+        rbase = k - 2;
+        dl = describe(rbase + lane);
+      }
+      const int l = k - rbase;
+      Desc d;
+      d.v = __shfl_sync(kFull, dl.v, l);
+      d.kvh = __shfl_sync(kFull, dl.kvh, l);
+      d.part = __shfl_sync(kFull, dl.part, l);
+      d.row = __shfl_sync(kFull, dl.row, l);
+      d.ctx = __shfl_sync(kFull, dl.ctx, l);
+      d.t0 = __shfl_sync(kFull, dl.t0, l);
+      d.seq0 = __shfl_sync(kFull, dl.seq0, l);
+      d.ncol = __shfl_sync(kFull, dl.ncol, l);
+      d.pbase = __shfl_sync(kFull, dl.pbase, l);
+      d.fb = __shfl_sync(kFull, dl.fb, l);
+      return d;
+    };
+    // An item's loads (its first 32 block ids, the query rows) are issued a
+    // round ahead, while the item before it streams, and the lines they read
+    // are brought into L2 a round before that (prefetch_item), so that they
+    // have arrived when the item starts even if the item before it is short.
+    auto prefetch_item = [&](const Desc& d) {
+      // the query rows: lane l takes 128-byte line l (column l / 2, half l % 2)
+      const int n = lane >> 1;
+      if (n < d.ncol && n < CN)
+        prefetch_l2(static_cast<const T*>(p.q) + (int64_t)(d.seq0 + n / G) * p.q_seq_stride +
+                    (int64_t)(d.kvh * G + n % G) * kD + (lane & 1) * 64);
+      if (lane == 0) {
+        const int ti = windowed ? table_index(d.fb, p.ring_blocks) : d.fb;
+        if (ti >= 0 && ti < p.bt_stride) prefetch_l2(p.block_tables + (int64_t)d.row * p.bt_stride + ti);
+      }
+    };
     struct Item {
-      int v, row, kvh, part, ctx, id_lane;   // virtual sequence, table row, kv head, partition, its end
-      int t0, seq0, ncol, pbase;             // shared prefix: first position, column map, partition base
+      int id_lane;
       uint4 qv[kQChunks];
     };
-    auto fetch = [&](int it) {
+    auto fetch = [&](const Desc& d) {
       Item r;
-      const int j = it / Hkv;
-      r.kvh = it - j * Hkv;
-      if (j < n_full) {
-        int lo = 0, hi = NV - 1;   // last virtual sequence whose first full partition is <= j
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (pre[mid] <= j) lo = mid;
-          else hi = mid - 1;
-        }
-        r.v = lo;
-        r.part = j - pre[lo];
-      } else {
-        r.v = rseq[j - n_full];
-        r.part = pre[r.v + 1] - pre[r.v];   // the remainder follows the full partitions
-      }
-      if (SP && r.v >= S) {   // a group's shared prefix, read through its first member's row
-        const int k = r.v - S;
-        r.row = r.seq0 = pv_seq0[k];
-        r.ncol = pv_n[k] * G;
-        r.ctx = pv_eff[k];
-        r.t0 = 0;
-        r.pbase = 0;
-      } else {                // a sequence (shared prefix: its tail after the prefix)
-        r.row = r.seq0 = r.v;
-        r.ncol = G;
-        r.ctx = p.context_lens[r.v];
-        r.t0 = SP ? sp_eff[r.v] : 0;
-        r.pbase = SP ? sp_npre[r.v] : 0;
-      }
-      // first logical block of the partition: only a window makes it depend on
-      // ctx, so without one the block-id load below does not wait for ctx
-      int ti;
-      if (windowed) {
-        const int jb = (attended_from(p, r.ctx) + r.part * P) / bs;
-        ti = table_index(jb + lane, p.ring_blocks);
-      } else {
-        const int first = r.t0 / bs + r.part * (P / bs);   // P is a multiple of 128, bs divides it
-        ti = first + lane;
+      const int ti = windowed ? table_index(d.fb + lane, p.ring_blocks) : d.fb + lane;
+      if (!windowed) {
         // the partition's later block ids, checked when the item starts: into L2
         // now, a whole item ahead, so that check waits for L2, not HBM (lane i
         // covers ids 32 (i + 1) .. 32 (i + 1) + 31; P / bs <= 1024)
-        const int row_end = min(p.bt_stride, first + P / bs);
-        const int t = first + 32 * (lane + 1);
+        const int row_end = min(p.bt_stride, d.fb + P / bs);
+        const int t = d.fb + 32 * (lane + 1);
         if (t < row_end) {
-          const int32_t* rp = p.block_tables + (int64_t)r.row * p.bt_stride;
+          const int32_t* rp = p.block_tables + (int64_t)d.row * p.bt_stride;
           prefetch_l2(rp + t);
           prefetch_l2(rp + min(t + 31, row_end - 1));
         }
       }
       r.id_lane =
-          (lane < P / bs && ti < p.bt_stride && ti >= 0) ? p.block_tables[(int64_t)r.row * p.bt_stride + ti] : 0;
+          (lane < P / bs && ti < p.bt_stride && ti >= 0) ? p.block_tables[(int64_t)d.row * p.bt_stride + ti] : 0;
       // query rows: column n is head kvh * G + n % G of sequence seq0 + n / G
 #pragma unroll
       for (int k = 0; k < kQChunks; ++k) {
         const int c = lane + 32 * k, n = c >> 4;
-        const T* qsrc = static_cast<const T*>(p.q) + (int64_t)(r.seq0 + n / G) * p.q_seq_stride +
-                        (int64_t)(r.kvh * G + n % G) * kD;
-        r.qv[k] = (c < CN * 16 && n < r.ncol) ? *reinterpret_cast<const uint4*>(qsrc + (c & 15) * 8)
+        const T* qsrc = static_cast<const T*>(p.q) + (int64_t)(d.seq0 + n / G) * p.q_seq_stride +
+                        (int64_t)(d.kvh * G + n % G) * kD;
+        r.qv[k] = (c < CN * 16 && n < d.ncol) ? *reinterpret_cast<const uint4*>(qsrc + (c & 15) * 8)
                                                : make_uint4(0, 0, 0, 0);
       }
       return r;
@@ -660,14 +848,17 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
     int tile_seq = 0, item_seq = 0;
     bool aborted = false;
     Item nxt;
-    if (item_of_round(0) < total) nxt = fetch(item_of_round(0));
+    if (item_of_round(0) < total) nxt = fetch(desc_of(0));
+    if (item_of_round(1) < total) prefetch_item(desc_of(1));
     for (int round = 0; item_of_round(round) < total && !aborted; ++round) {
+      const Desc cd = desc_of(round);
       const Item cur = nxt;
       const bool more = item_of_round(round + 1) < total;
-      if (more) nxt = fetch(item_of_round(round + 1));
-      const int s = cur.row, kvh = cur.kvh, part = cur.part, ctx = cur.ctx, id_lane = cur.id_lane;
+      if (more) nxt = fetch(desc_of(round + 1));
+      if (item_of_round(round + 2) < total) prefetch_item(desc_of(round + 2));
+      const int s = cd.row, kvh = cd.kvh, part = cd.part, ctx = cd.ctx, id_lane = cur.id_lane;
       const int32_t* row = p.block_tables + (int64_t)s * p.bt_stride;   // entry table_index(j) holds block j
-      const bool is_prefix = SP && cur.v >= S;                          // valid by construction
+      const bool is_prefix = SP && cd.v >= S;                          // valid by construction
       if (!is_prefix && ctx_invalid(p, ctx)) {
         warp_zero_rows<T, G>(p, s, kvh, lane);
         if (lane == 0) report(p.dev_err, PA_DEVERR_CONTEXT);
@@ -677,7 +868,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         warp_zero_rows<T, G>(p, s, kvh, lane);
         continue;
       }
-      const int t_first = SP ? cur.t0 : window_start(ctx, bs, p.window, p.ring_blocks);
+      const int t_first = SP ? cd.t0 : window_start(ctx, bs, p.window, p.ring_blocks);
       const int t_base = (t_first / bs) * bs;
       const int n_parts = (ctx - t_base + P - 1) / P;
       const int t0 = t_base + part * P, t1 = min(ctx, t0 + P);
@@ -700,14 +891,14 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         if constexpr (SP) {
           // per column: a row written directly is zeroed, else the partition is
           // marked invalid and the merge writes zeros
-          for (int n = 0; n < cur.ncol; ++n) {
-            const int sq = cur.seq0 + n / G;
+          for (int n = 0; n < cd.ncol; ++n) {
+            const int sq = cd.seq0 + n / G;
             const int64_t hrow = (int64_t)sq * p.num_q_heads + kvh * G + n % G;
             if (sp_eff[sq] == 0 && sp_tot[sq] == 1) {
               if (lane < kD / 8) *reinterpret_cast<uint4*>(static_cast<T*>(p.out) + hrow * kD + lane * 8) =
                   make_uint4(0, 0, 0, 0);
             } else if (lane == 0) {
-              const int64_t r = hrow * p.max_parts + cur.pbase + part;
+              const int64_t r = hrow * p.max_parts + cd.pbase + part;
               p.ws_ml[r * 2 + 0] = 0.f;
               p.ws_ml[r * 2 + 1] = -1.f;
             }
@@ -722,8 +913,9 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         continue;
       }
       // ---- Q^T of this item into a K-major 128B-swizzled buffer
-      const int qslot = item_seq & 1;
-      if (item_seq >= 2 && !mbar_wait(&sh.q_free[qslot], ((item_seq >> 1) - 1) & 1)) {
+      constexpr int QS = q_slots(I8);
+      const int qslot = item_seq % QS;
+      if (item_seq >= QS && !mbar_wait(&sh.q_free[qslot], ((item_seq / QS) - 1) & 1)) {
         aborted = true;
         break;
       }
@@ -775,7 +967,8 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         tc::fence_proxy_async_smem();
         __syncwarp();
       }
-      // ---- stream the tiles
+      // ---- 8-bit: the tiles, as descriptors for the copy warp; 16-bit: the
+      // item, as a record for the streaming warp
       const int ntiles = (t1 - t0 + kTile - 1) / kTile;
       for (int k = 0; k < ntiles && I8; ++k) {
         // 8-bit: each tile goes to the copy warp as a descriptor (metadata and
@@ -787,7 +980,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         m.lo = max(0, t_first - (t0 + k * kTile));
         m.tail = ntiles - 1 - k;
         m.qinv = qinv;
-        m.seq0 = cur.seq0; m.ncol = cur.ncol; m.pbase = cur.pbase;
+        m.seq0 = cd.seq0; m.ncol = cd.ncol; m.pbase = cd.pbase;
         m.head = k; m.item = item_seq; m.bad = 0;
         // the tile's block ids, lane i holding blocks i + 32 c of the tile: the
         // item's first 32 come from the prefetched id_lane, the rest are loaded
@@ -815,51 +1008,23 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         if (aborted) break;
         ++tile_seq;
       }
-      // 16-bit: the block id of this lane's chunk of tile k.  The item's first 32
-      // come from the prefetched id_lane; a later one is loaded a tile ahead, so
-      // the load overlaps the wait for a free stage instead of delaying the copy.
-      auto tile_id = [&](int k) {
-        const int bi = k * (kTile / bs) + lane;
-        const int nbk = (min(kTile, t1 - (t0 + k * kTile)) + bs - 1) / bs;
-        const int id_sh = __shfl_sync(kFull, id_lane, bi & 31);
-        return lane < nbk ? (bi < 32 ? id_sh : row[table_index(jb + bi, p.ring_blocks)]) : 0;
-      };
-      int id_k = (!I8 && ntiles > 0) ? tile_id(0) : 0;
-      bool item_bad = false;
-      for (int k = 0; k < ntiles && !I8; ++k) {
-        const int slot = tile_seq % NS;
-        if (tile_seq >= NS && !mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1)) {
+      if constexpr (!I8) {
+        // hand the item to the streaming warp, in the record slot of its
+        // parity once the streamer has taken the item two before it
+        const int rs = item_seq & 1;
+        if (item_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.rec_empty[rs], ((item_seq >> 1) - 1) & 1))) {
           aborted = true;
           break;
         }
-        const int valid = min(kTile, t1 - (t0 + k * kTile));
-        const int nb = (valid + bs - 1) / bs;
-        // an id out of range is never read: block 0 stands in, the item's
-        // result is discarded (zero rows) and the error reported once per item
-        const bool id_bad = lane < nb && (id_k < 0 || id_k >= p.num_blocks);
-        if (__any_sync(kFull, id_bad)) {
-          if (lane == 0 && !item_bad) report(p.dev_err, PA_DEVERR_BLOCK_ID);
-          item_bad = true;
-        }
-        if (id_bad) id_k = 0;
+        ItemRec& R = sh.u.rec[rs];
         if (lane == 0) {
-          TileMeta m;
-          m.s = s; m.kvh = kvh; m.part = part; m.valid = valid;
-          m.last = (k == ntiles - 1); m.qslot = qslot; m.n_parts = n_parts;
-          m.lo = max(0, t_first - (t0 + k * kTile));
-          m.tail = ntiles - 1 - k;
-          m.qinv = qinv;
-          m.seq0 = cur.seq0; m.ncol = cur.ncol; m.pbase = cur.pbase;
-          m.head = k; m.item = item_seq; m.bad = item_bad ? 1 : 0;
-          sh.meta[slot] = m;
-          mbar_arrive_expect_tx(&sh.full[slot], (uint32_t)(nb * chunk_bytes));
+          R.s = s; R.kvh = kvh; R.part = part; R.n_parts = n_parts; R.t_first = t_first;
+          R.t0 = t0; R.t1 = t1; R.jb = jb;
+          R.seq0 = cd.seq0; R.ncol = cd.ncol; R.pbase = cd.pbase; R.qslot = qslot; R.item = item_seq;
         }
+        R.ids[lane] = id_lane;
         __syncwarp();
-        if (lane < nb)
-          bulk_g2s(stages + slot * kStage + lane * chunk_bytes,
-                   p.cache + ((int64_t)id_k * Hkv + kvh) * chunk_bytes, (uint32_t)chunk_bytes, &sh.full[slot]);
-        if (k + 1 < ntiles) id_k = tile_id(k + 1);
-        ++tile_seq;
+        if (lane == 0) mbar_arrive(&sh.rec_full[rs]);
       }
       ++item_seq;
     }
@@ -878,24 +1043,17 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         mbar_arrive(&sh.desc_full[d]);
       }
     } else {
-      const int slot = tile_seq % NS;
-      if (!aborted && tile_seq >= NS && !mbar_wait(&sh.empty[slot], ((tile_seq / NS) - 1) & 1)) aborted = true;
-      if (lane == 0) {
-        // never leave copies in flight, whether or not another role gave up:
-        // wait (bounded) for the latest phase of every stage.  Normally they
-        // have landed or are about to, and the end mark below is only read
-        // after the last tile anyway.
-        for (int t = max(0, tile_seq - NS); t < tile_seq; ++t)
-          if (!mbar_wait(&sh.full[t % NS], (t / NS) & 1)) report(p.dev_err, PA_DEVERR_TIMEOUT);
-      }
+      // a record that says so (once the streamer has taken the item two before)
+      const int rs = item_seq & 1;
+      if (!aborted && item_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.rec_empty[rs], ((item_seq >> 1) - 1) & 1)))
+        aborted = true;
       if (lane == 0) {
         if (aborted) {
           report(p.dev_err, PA_DEVERR_TIMEOUT);
           sh.abort_flag = 1;
         }
-        sh.meta[slot].s = -1;
-        sh.meta[slot].item = item_seq;     // the index the next item would have
-        mbar_arrive(&sh.full[slot]);
+        sh.u.rec[rs].item = -1;
+        mbar_arrive(&sh.rec_full[rs]);
       }
     }
     __syncwarp();
@@ -949,7 +1107,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
           if (mbar_test_wait(&sh.p_full[pb], (pv >> 1) & 1)) {
             const int slot = pv % NS;
             const TileMeta& mr = sh.meta[slot];     // the stage is not refilled before this PV completes
-            const int valid = mr.valid, os = mr.qslot;
+            const int valid = mr.valid, os = mr.item & 1;
             const bool first = mr.head == 0, lastg = mr.tail == 0;
             if (!first || !((used >> os) & 1) || mbar_test_wait(&sh.ofree[os], ((par >> os) & 1) ^ 1)) {
               tc::fence_after_sync();
@@ -1081,19 +1239,22 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
           const int slot = pv % NS;
           const TileMeta& mr = sh.meta[slot];   // the stage is not refilled before this PV completes
           const int valid = mr.valid;
-          const int os = mr.qslot * (PP ? 2 : 1) + (PP ? pb : 0);
+          const int os = (mr.item & 1) * (PP ? 2 : 1) + (PP ? pb : 0);
           const bool first = PP ? mr.head < 2 : mr.head == 0, lastg = PP ? mr.tail < 2 : mr.tail == 0;
           if (!first || !((used >> os) & 1) || mbar_test_wait(&sh.ofree[os], ((par >> os) & 1) ^ 1)) {
             tc::fence_after_sync();
             const uint64_t vd =
                 tc::smem_desc(smem_u32(stages + slot * kStage) + kVOff, 1024, kVGroup, tc::kSwizzle128B);
-            const uint64_t pd = tc::smem_desc(smem_u32(pbuf + pb * kPBytes), (NPV / 8) * 128, 128, tc::kSwizzleNone);
+            // P^T: 8-token groups at the start of the stage's groups (I8: in a P^T buffer)
+            const uint64_t pd = I8 ? tc::smem_desc(smem_u32(pbuf + pb * kPBytes), (NPV / 8) * 128, 128, tc::kSwizzleNone)
+                                   : tc::smem_desc(smem_u32(stages + slot * kStage), kGroupBytes, 128, tc::kSwizzleNone);
+            constexpr uint32_t kPStep = I8 ? (NPV / 8) * 256 : 2 * kGroupBytes;   // 16 tokens
             const int nsteps = (valid + 15) >> 4;
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
               if (kk < nsteps)
                 tc::mma_f16(tmem + kOCol + os * 32, vd + (uint64_t)((kk * 2 * kVGroup) >> 4),
-                            pd + (uint64_t)((kk * (NPV / 8) * 256) >> 4), id_pv, (kk > 0 || !first) ? 1u : 0u);
+                            pd + (uint64_t)((kk * kPStep) >> 4), id_pv, (kk > 0 || !first) ? 1u : 0u);
             tc::commit(&sh.pv_done[pb]);
             tc::commit(&sh.empty[slot]);
             if (lastg) tc::commit(&sh.ofin[os]);
@@ -1134,18 +1295,38 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
     const int row = quarter * 32 + lane;   // TMEM lane = token row of S^T
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     // The running maxima are the same in every thread of the group.  With
-    // more than 8 columns they are held one per lane (lane l: column l mod CN)
-    // and broadcast where needed, which keeps the per-thread state small
-    // enough that nothing spills.
-    constexpr bool kDM = CN > 8;
-    float m[kDM ? 1 : CN], lp[CN];
-#pragma unroll
-    for (int n = 0; n < (kDM ? 1 : CN); ++n) m[n] = -INFINITY;
+    // more than 8 columns each warp keeps them in shared memory (row mb of its
+    // double-buffered copy) and reads them back with broadcast vector loads
+    // where they are needed, which keeps the per-thread state small enough
+    // that nothing spills.
+    constexpr bool kSM = CN > 8;
+    float m[kSM ? 1 : CN], lp[CN];
+    float* mrow = sh.mrun[grp][quarter][0];
+    float* crow = sh.mcorr[grp][quarter];
+    int mb = 0;
 #pragma unroll
     for (int n = 0; n < CN; ++n) lp[n] = 0.f;
-    auto m_at = [&](int n) -> float {   // column n's running maximum (every lane calls it)
-      if constexpr (kDM) return __shfl_sync(kFull, m[0], n);
-      else return m[n];
+    if constexpr (kSM) {
+      if (lane < kN) mrow[lane] = -INFINITY;
+      __syncwarp();
+    } else {
+#pragma unroll
+      for (int n = 0; n < CN; ++n) m[n] = -INFINITY;
+    }
+    auto load_m = [&](float (&mv)[CN]) {   // the running maxima of the CN columns
+      if constexpr (kSM) {
+#pragma unroll
+        for (int n = 0; n < CN; n += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(mrow + mb * kN + n);
+          mv[n] = v.x;
+          mv[n + 1] = v.y;
+          mv[n + 2] = v.z;
+          mv[n + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int n = 0; n < CN; ++n) mv[n] = m[n];
+      }
     };
     int tile_seq = grp;
     bool ok = true;
@@ -1184,7 +1365,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       // accumulator afresh, the last hands over its maximum and sums
       const bool first = PP ? mt.head < 2 : mt.head == 0;
       const bool fin = PP ? mt.tail < 2 : mt.tail == 0;
-      const int os = mt.qslot * (PP ? 2 : 1) + grp;   // this group's O slot for the item
+      const int os = (mt.item & 1) * (PP ? 2 : 1) + grp;   // this group's O slot for the item
       const int sb = tile_seq & 1;
       if (!__all_sync(kFull, mbar_wait(&sh.s_full[sb], (tile_seq >> 1) & 1))) { ok = false; break; }
       tc::fence_after_sync();
@@ -1202,10 +1383,14 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       // the group's first tile of an item m = -inf, so every valid row does.)
       float x[CN];
       bool up = false;
+      {
+        float mv[CN];
+        load_m(mv);
 #pragma unroll
-      for (int n = 0; n < CN; ++n) {
-        x[n] = rv ? sv[n] * kscale : -INFINITY;
-        up |= x[n] > m_at(n) + (I8 ? 0.f : kLazyMax);   // 8-bit: the V scales ride on P, keep p <= 1
+        for (int n = 0; n < CN; ++n) {
+          x[n] = rv ? sv[n] * kscale : -INFINITY;
+          up |= x[n] > mv[n] + (I8 ? 0.f : kLazyMax);   // 8-bit: the V scales ride on P, keep p <= 1
+        }
       }
       const bool wup = __any_sync(kFull, up);
       const int par = (tile_seq >> 1) & 1;   // exchange buffer of this tile (the group's tile parity)
@@ -1230,19 +1415,31 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         // rescaled, the latter once the group's previous PV has completed and
         // before this tile's PV is issued
         float corr[CN];
-        if constexpr (kDM) {
-          const int n = lane & (CN - 1);   // this lane's column
-          float mx = m[0];
+        if constexpr (kSM) {
+          // lane n (< CN) works out column n into the other row, then every
+          // lane reads the corrections back
+          const int n = lane & (CN - 1);
+          const float mo = mrow[mb * kN + n];
+          float mx = mo;
 #pragma unroll
           for (int w = 0; w < 4; ++w)
             if (ups[w]) mx = fmaxf(mx, sh.red_max[hb][par][w][n]);
-          const float c = (m[0] == -INFINITY) ? 0.f : exp2f(m[0] - mx);
-          m[0] = mx;
-#pragma unroll
-          for (int k = 0; k < CN; ++k) {
-            corr[k] = __shfl_sync(kFull, c, k);
-            lp[k] *= corr[k];
+          if (lane < CN) {
+            mrow[(mb ^ 1) * kN + n] = mx;
+            crow[n] = (mo == -INFINITY) ? 0.f : exp2f(mo - mx);
           }
+          __syncwarp();
+          mb ^= 1;
+#pragma unroll
+          for (int k = 0; k < CN; k += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(crow + k);
+            corr[k] = v.x;
+            corr[k + 1] = v.y;
+            corr[k + 2] = v.z;
+            corr[k + 3] = v.w;
+          }
+#pragma unroll
+          for (int k = 0; k < CN; ++k) lp[k] *= corr[k];
         } else {
 #pragma unroll
           for (int n = 0; n < CN; ++n) {
@@ -1278,11 +1475,14 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         }
       }
       float (&pr)[CN] = x;   // the weights replace the scores
+      {
+        float mv[CN];
+        load_m(mv);
 #pragma unroll
-      for (int n = 0; n < CN; ++n) {
-        const float mn = m_at(n);
-        pr[n] = rv ? ex2_approx(x[n] - mn) : 0.f;
-        lp[n] += pr[n];
+        for (int n = 0; n < CN; ++n) {
+          pr[n] = rv ? ex2_approx(x[n] - mv[n]) : 0.f;
+          lp[n] += pr[n];
+        }
       }
       uint32_t pk[NPV / 2];   // [p_hi of heads 0..HG-1 | p_lo of heads 0..HG-1], two per word
 #pragma unroll
@@ -1292,11 +1492,18 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         const float2 r = Elem<OpT>::to_float2(pk[n2 >> 1]);
         pk[(HG + n2) >> 1] = Elem<OpT>::pack2(a - r.x, b - r.y);
       }
-      // P^T buffer hb was last read by PV(t - 2): wait for it to complete
-      if (tile_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.pv_done[hb], ((tile_seq - 2) >> 1) & 1))) { ok = false; break; }
+      // 8-bit: P^T buffer hb was last read by PV(t - 2): wait for it to complete.
+      // (16-bit caches write P^T into this tile's own stage, over K atoms that
+      // QK(t) has finished reading; the stage is refilled only after PV(t).)
+      if (I8 && tile_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.pv_done[hb], ((tile_seq - 2) >> 1) & 1))) {
+        ok = false;
+        break;
+      }
       // MN-major without swizzle: core matrix = 8 tokens x 8 columns (128 B);
-      // column chunks 128 B apart, 8-token groups (NPV / 8) * 128 B apart
-      uint8_t* prow = pbuf + hb * kPBytes + (row >> 3) * (NPV / 8) * 128 + (row & 7) * 16;
+      // column chunks 128 B apart, 8-token groups (NPV / 8) * 128 B apart in a
+      // P^T buffer, one stage group (4 KiB) apart in a stage
+      uint8_t* prow = I8 ? pbuf + hb * kPBytes + (row >> 3) * (NPV / 8) * 128 + (row & 7) * 16
+                         : stages + slot * kStage + (row >> 3) * kGroupBytes + (row & 7) * 16;
 #pragma unroll
       for (int c = 0; c < NPV / 8; ++c)
         *reinterpret_cast<uint4*>(prow + c * 128) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
@@ -1322,11 +1529,11 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       if (fin) {
         const int k = mt.item, q = k & 1;
         if (k >= 2 && !__all_sync(kFull, mbar_wait(&sh.c_free[q], ((k >> 1) - 1) & 1))) { ok = false; break; }
-        if constexpr (kDM) {
-          if (quarter == 0 && lane < CN) sh.fin[q][grp].m[lane] = m[0];
+        if constexpr (kSM) {
+          if (quarter == 0 && lane < CN) sh.fin[q][grp].m[lane] = mrow[mb * kN + lane];
         }
         if (lane == 0 && quarter == 0) {
-          if constexpr (!kDM) {
+          if constexpr (!kSM) {
 #pragma unroll
             for (int n = 0; n < CN; ++n) sh.fin[q][grp].m[n] = m[n];
           }
@@ -1349,9 +1556,15 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
           if (PP && mt.head == 0 && mt.tail == 0) mbar_arrive(&sh.c_full[q]);   // a one-tile item: for both groups
         }
 #pragma unroll
-        for (int n = 0; n < (kDM ? 1 : CN); ++n) m[n] = -INFINITY;
-#pragma unroll
         for (int n = 0; n < CN; ++n) lp[n] = 0.f;
+        if constexpr (kSM) {
+          __syncwarp();
+          if (lane < CN) mrow[mb * kN + lane] = -INFINITY;
+          __syncwarp();
+        } else {
+#pragma unroll
+          for (int n = 0; n < CN; ++n) m[n] = -INFINITY;
+        }
       }
       tile_seq += PP ? 2 : 1;
     }
@@ -1415,24 +1628,25 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         T* out = static_cast<T*>(p.out);
         // Per column, the groups' exact log-sum-exp merge -- M = max(m0, m1),
         // f_g = 2^(m_g - M), L = f0 L0 + f1 L1 -- and where its row goes are the
-        // same for every thread: lane n computes column n's once, and every
-        // thread takes them from lane n.  dst: element offset of the row in the
-        // output (bit 0 set; bit 1: write zeros) or in the workspace's partial
-        // results; -1: nothing to write.
-        float cf0 = 0.f, cf1 = 0.f, cL = 1.f;
-        long long cdst = -1;
+        // same for every thread: lane n works them out for column n into this
+        // warp's table, and every thread reads them back, one vector load per
+        // column.  A row written directly takes O / L as O0 (f0 / L) + O1 (f1 / L).
+        auto& tab = sh.colout[quarter];
+        const int nc = SP ? mt.ncol : CN;   // the item's columns that have a row
         if (lane < CN) {
           const int n = lane;
           const typename Shared<NS, I8, NRH>::Final& F0 = sh.fin[q][0];
           const typename Shared<NS, I8, NRH>::Final& F1 = sh.fin[q][1];
           const float mg0 = has0 ? F0.m[n] : -INFINITY, mg1 = has1 ? F1.m[n] : -INFINITY;
           const float M = fmaxf(mg0, mg1);
-          cf0 = (mg0 == -INFINITY) ? 0.f : exp2f(mg0 - M);
-          cf1 = (mg1 == -INFINITY) ? 0.f : exp2f(mg1 - M);
+          const float cf0 = (mg0 == -INFINITY) ? 0.f : exp2f(mg0 - M);
+          const float cf1 = (mg1 == -INFINITY) ? 0.f : exp2f(mg1 - M);
           const float Lg0 = has0 ? (F0.Lq[0][n] + F0.Lq[1][n]) + (F0.Lq[2][n] + F0.Lq[3][n]) : 0.f;
           const float Lg1 = has1 ? (F1.Lq[0][n] + F1.Lq[1][n]) + (F1.Lq[2][n] + F1.Lq[3][n]) : 0.f;
-          cL = PP ? fmaf(Lg0, cf0, Lg1 * cf1) : Lg0;
-          if (!SP || n < mt.ncol) {
+          const float cL = PP ? fmaf(Lg0, cf0, Lg1 * cf1) : Lg0;
+          long long cdst = -1;
+          float g0 = cf0, g1 = cf1;
+          if (n < nc) {
             // column n: head kvh * G + n % G of sequence seq0 + n / G.  A row is
             // written directly when this item is its only partition (and, for a
             // shared prefix, the sequence has none: prefix rows always merge)
@@ -1441,6 +1655,9 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
             const bool direct = SP ? (sp_eff[sq] == 0 && sp_tot[sq] == 1) : mt.n_parts == 1;
             if (direct) {
               cdst = hrow * kD + (mt.bad ? 3 : 1);   // bit 1: a zero row (the item read block 0 for a bad id)
+              const float inv = 1.f / cL;              // L >= 1: the maximum's own weight is 1
+              g0 = cf0 * inv;
+              g1 = cf1 * inv;
             } else {
               const int64_t r = hrow * p.max_parts + mt.pbase + mt.part;
               cdst = mt.bad ? -1 : r * kD;
@@ -1450,18 +1667,23 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
               }
             }
           }
+          tab[n].dst = cdst;
+          tab[n].g0 = g0;
+          tab[n].g1 = g1;
         }
+        __syncwarp();
 #pragma unroll
         for (int n = 0; n < CN; ++n) {
-          const long long dst = __shfl_sync(kFull, cdst, n);
-          const float f0 = __shfl_sync(kFull, cf0, n);
-          const float O = PP ? fmaf(x0[n], f0, x1[n] * __shfl_sync(kFull, cf1, n)) : x0[n];
-          const float L = __shfl_sync(kFull, cL, n);
-          if (dst >= 0) {
-            if (dst & 1) out[(dst & ~3LL) + row] = Elem<T>::from_float((dst & 2) ? 0.f : O / L);
-            else p.ws_o[dst + row] = O;
+          if (n < nc) {   // the same in every lane
+            const typename Shared<NS, I8, NRH>::ColOut c = tab[n];
+            if (c.dst >= 0) {
+              const float O = PP ? fmaf(x0[n], c.g0, x1[n] * c.g1) : x0[n] * c.g0;
+              if (c.dst & 1) out[(c.dst & ~3LL) + row] = Elem<T>::from_float((c.dst & 2) ? 0.f : O);
+              else p.ws_o[c.dst + row] = O;
+            }
           }
         }
+        __syncwarp();   // every lane has read the table before the next item rewrites it
       }
       // fin[q] and ihand[q] are free for the item after the next
       __syncwarp();
@@ -1648,7 +1870,8 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
 // Dynamic shared memory of one CTA: stages, Q and P^T buffers, 8-bit raw rings,
 // the item tables (1024 bytes of slack align the stages to 1024).
 __host__ __device__ inline size_t decode_tc_smem(int NS, bool I8, int NRH, bool SP, int S) {
-  return 1024 + (size_t)NS * stage_bytes(I8) + 2 * kQBytes + 2 * kPBytes + (I8 ? (size_t)2 * NRH * kRawBytes : 0) +
+  return 1024 + (size_t)NS * stage_bytes(I8) + (size_t)q_slots(I8) * kQBytes + (size_t)p_buffers(I8) * kPBytes +
+         (I8 ? (size_t)2 * NRH * kRawBytes : 0) +
          ItemTables(S, SP).end;
 }
 

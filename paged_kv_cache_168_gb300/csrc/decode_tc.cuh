@@ -89,6 +89,11 @@ constexpr int kPBytes = kTile * 32 * 2;            // P^T operand: 128 tokens x 
 // (dead once QK(t) has completed: 512 B of each 8-token group's 2 KiB), so
 // they need no P^T buffers; 8-bit stages hold V only and keep two.
 __host__ __device__ constexpr int q_slots(bool i8) { return i8 ? 2 : 4; }
+// Items in flight between the softmax and output warps (hand-off slots and O
+// accumulators in TMEM, by item index mod this): 16-bit caches four, so the
+// output warps can fall behind a run of short items without holding up the
+// tensor core; 8-bit caches two.
+__host__ __device__ constexpr int item_slots(bool i8) { return i8 ? 2 : 4; }
 __host__ __device__ constexpr int p_buffers(bool i8) { return i8 ? 2 : 0; }
 constexpr int kThreads = 320;                      // warp 0, MMA issue, 4 softmax warps, 4 output warps
 // 8-bit caches add converter warps: 8 when the registers allow it (group <= 4), else 4
@@ -165,14 +170,14 @@ __host__ __device__ constexpr int threads_of(bool i8, int G) {
 constexpr int kND = 4;                             // 8-bit: tile descriptors in flight (planner -> copy warp)
 constexpr int kRawBytes = 64 * (2 * kD + 32);      // one 64-token half tile of 8-bit chunks (bs 1: 288 B/token)
 // TMEM columns: S0 S1 (16 each) | the O accumulators, 32 columns each, one per
-// (item parity, softmax group): O^T of an item accumulates across its tiles,
+// (item slot, softmax group): O^T of an item accumulates across its tiles,
 // so the output warps read it once per item; 8-bit caches (one softmax group)
 // add the fp16 K operand of each stage (128 tokens x 128 dims, two per column:
 // 64 columns) from column kKCol.
 constexpr uint32_t kKCol = 128;
 constexpr uint32_t kOCol = 32;
 __host__ __device__ constexpr uint32_t tmem_cols(bool i8, int ns) {
-  return !i8 ? 256u : (kKCol + 64u * ns <= 256u ? 256u : 512u);
+  return !i8 ? 512u : (kKCol + 64u * ns <= 256u ? 256u : 512u);   // 16-bit: 8 O slots from kOCol
 }
 // A stage holds the tile's K and V operands (16-bit caches) or, for 8-bit
 // caches, only the converted V operand (K lives in TMEM).
@@ -202,23 +207,23 @@ template <int NS, bool I8, int NRH>
 struct Shared {
   uint64_t full[NS], empty[NS];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], q_free[4];
-  // O accumulator slot o = item parity * groups + group: the PV of the group's
+  // O accumulator slot o = item slot * groups + group: the PV of the group's
   // last tile of an item completed (ofin), the output warps read it (ofree)
-  uint64_t ofin[4], ofree[4];
+  uint64_t ofin[8], ofree[8];
   uint64_t m_full[2];             // MMA issuer -> softmax: tile t's metadata in smeta[t & 1]
   uint64_t mma_drain[2];          // each MMA-issuing lane's own MMAs, waited for before TMEM is freed
   TileMeta smeta[2];
   uint64_t max_bar[2];            // softmax-warp exchange (bounded waits, unlike bar.sync)
-  uint64_t c_full[2], c_free[2];  // softmax -> output warps: per-item hand-off, by item parity
+  uint64_t c_full[4], c_free[4];  // softmax -> output warps: per-item hand-off, by item slot
   TileMeta meta[NS];
-  struct ItemHand {                // an item's metadata for the output warps (slot: item parity)
+  struct ItemHand {                // an item's metadata for the output warps (by item slot)
     TileMeta meta;                // its last tile's
     int ntiles, first_grp;        // its tiles, and the softmax group of its first tile
-  } ihand[2];
+  } ihand[4];
   struct Final {                  // a softmax group's maximum and sums per TMEM lane quarter
-    float m[kN];                  // at the end of an item: [item parity][group]
+    float m[kN];                  // at the end of an item: [item slot][group]
     float Lq[4][kN];
-  } fin[2][2];
+  } fin[4][2];
   // the maximum exchange of a softmax group (ring slot t & 1), double-buffered
   // by the group's tile parity: a warp may write tile t + 2's values only after
   // every warp of its group arrived for tile t + 1... which follows its reads of t
@@ -228,14 +233,9 @@ struct Shared {
   // maxima (double-buffered) and of the corrections of its latest rescale
   alignas(16) float mrun[2][4][2][kN];
   alignas(16) float mcorr[2][4][kN];
-  // each output warp's per-column table for the item it is writing: the
-  // row's place (element offset; bit 0: out, else the workspace; bit 1: a zero
-  // row; -1: nothing) and the factors of the two groups' O
-  struct alignas(16) ColOut {
-    long long dst;
-    float g0, g1;
-  };
-  ColOut colout[4][kN];
+  // each output warp's per-column factors of the two groups' O for the item
+  // it is writing
+  float2 colout[4][kN];
   uint32_t tmem_base;
   volatile int abort_flag;
   volatile int end_tile;          // QK issuer -> PV issuer: tiles in this CTA (set at the end)
@@ -431,16 +431,18 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       mbar_init(&sh.p_full[i], 4);
       mbar_init(&sh.pv_done[i], 1);
       mbar_init(&sh.max_bar[i], 4);
+      mbar_init(&sh.mma_drain[i], 1);
+    }
+    for (int i = 0; i < 4; ++i) {
       // every warp of each softmax group that had a tile in the item (the group
       // of a one-tile item arrives for both)
       mbar_init(&sh.c_full[i], ping_pong(I8, CN) ? 8 : 4);
       mbar_init(&sh.c_free[i], 4);
-      mbar_init(&sh.mma_drain[i], 1);
+      mbar_init(&sh.q_free[i], 1);
     }
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 8; ++i) {
       mbar_init(&sh.ofin[i], 1);
       mbar_init(&sh.ofree[i], 4);
-      mbar_init(&sh.q_free[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.rec_full[i], 1);
@@ -1107,7 +1109,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
           if (mbar_test_wait(&sh.p_full[pb], (pv >> 1) & 1)) {
             const int slot = pv % NS;
             const TileMeta& mr = sh.meta[slot];     // the stage is not refilled before this PV completes
-            const int valid = mr.valid, os = mr.item & 1;
+            const int valid = mr.valid, os = mr.item % item_slots(I8);
             const bool first = mr.head == 0, lastg = mr.tail == 0;
             if (!first || !((used >> os) & 1) || mbar_test_wait(&sh.ofree[os], ((par >> os) & 1) ^ 1)) {
               tc::fence_after_sync();
@@ -1239,7 +1241,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
           const int slot = pv % NS;
           const TileMeta& mr = sh.meta[slot];   // the stage is not refilled before this PV completes
           const int valid = mr.valid;
-          const int os = (mr.item & 1) * (PP ? 2 : 1) + (PP ? pb : 0);
+          const int os = (mr.item % item_slots(I8)) * (PP ? 2 : 1) + (PP ? pb : 0);
           const bool first = PP ? mr.head < 2 : mr.head == 0, lastg = PP ? mr.tail < 2 : mr.tail == 0;
           if (!first || !((used >> os) & 1) || mbar_test_wait(&sh.ofree[os], ((par >> os) & 1) ^ 1)) {
             tc::fence_after_sync();
@@ -1350,8 +1352,9 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
         // and the index the next item would have in item), in the hand-off slot
         // of that item index once its previous user is done
         if (mt.s < 0 && (!PP || mt.valid == tile_seq)) {
-          const int k = mt.item, q = k & 1;
-          if (k >= 2 && !__all_sync(kFull, mbar_wait(&sh.c_free[q], ((k >> 1) - 1) & 1))) { ok = false; break; }
+          constexpr int IS = item_slots(I8);
+          const int k = mt.item, q = k % IS;
+          if (k >= IS && !__all_sync(kFull, mbar_wait(&sh.c_free[q], ((k / IS) - 1) & 1))) { ok = false; break; }
           if (lane == 0 && quarter == 0) sh.ihand[q].meta.s = -1;
           __syncwarp();
           if (lane == 0) {
@@ -1365,7 +1368,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       // accumulator afresh, the last hands over its maximum and sums
       const bool first = PP ? mt.head < 2 : mt.head == 0;
       const bool fin = PP ? mt.tail < 2 : mt.tail == 0;
-      const int os = (mt.item & 1) * (PP ? 2 : 1) + grp;   // this group's O slot for the item
+      const int os = (mt.item % item_slots(I8)) * (PP ? 2 : 1) + grp;   // this group's O slot for the item
       const int sb = tile_seq & 1;
       if (!__all_sync(kFull, mbar_wait(&sh.s_full[sb], (tile_seq >> 1) & 1))) { ok = false; break; }
       tc::fence_after_sync();
@@ -1523,12 +1526,13 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       if (lane == 0) mbar_arrive(&sh.p_full[hb]);
       // hand-off to the output warps at the group's last tile of the item:
       // its maximum and sums (and, with the item's last tile, the item's
-      // metadata) into the slot of the item's parity, once the output warps
-      // are done with the item before it of the same parity.  The maximum is
-      // stored first, so it is dead while the sums are reduced.
+      // metadata) into the item's hand-off slot, once the output warps have
+      // taken the slot's previous item.  The maximum is stored first, so it is
+      // dead while the sums are reduced.
       if (fin) {
-        const int k = mt.item, q = k & 1;
-        if (k >= 2 && !__all_sync(kFull, mbar_wait(&sh.c_free[q], ((k >> 1) - 1) & 1))) { ok = false; break; }
+        constexpr int IS = item_slots(I8);
+        const int k = mt.item, q = k % IS;
+        if (k >= IS && !__all_sync(kFull, mbar_wait(&sh.c_free[q], ((k / IS) - 1) & 1))) { ok = false; break; }
         if constexpr (kSM) {
           if (quarter == 0 && lane < CN) sh.fin[q][grp].m[lane] = mrow[mb * kN + lane];
         }
@@ -1585,14 +1589,33 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
     uint32_t used = 0;   // per O slot: parity of the items read from it so far
     bool ok = true;
     for (int k = 0;; ++k) {
-      const int q = k & 1;
-      if (!__all_sync(kFull, mbar_wait(&sh.c_full[q], (k >> 1) & 1))) { ok = false; break; }
+      constexpr int IS = item_slots(I8);
+      const int q = k % IS;
+      if (!__all_sync(kFull, mbar_wait(&sh.c_full[q], (k / IS) & 1))) { ok = false; break; }
       const TileMeta mt = sh.ihand[q].meta;
       if (mt.s < 0) break;
       // the groups that had a tile in this item: the group of its first tile,
       // and (two groups) the other one when it has more than one tile
       const int ntiles = sh.ihand[q].ntiles, g_first = sh.ihand[q].first_grp;
       const bool has0 = !PP || g_first == 0 || ntiles >= 2, has1 = PP && (g_first == 1 || ntiles >= 2);
+      // lane n (< CN): column n's maximum and sum from each group
+      float mg0 = -INFINITY, mg1 = -INFINITY, Lg0 = 0.f, Lg1 = 0.f;
+      if (lane < CN) {
+        const typename Shared<NS, I8, NRH>::Final& F0 = sh.fin[q][0];
+        const typename Shared<NS, I8, NRH>::Final& F1 = sh.fin[q][1];
+        if (has0) {
+          mg0 = F0.m[lane];
+          Lg0 = (F0.Lq[0][lane] + F0.Lq[1][lane]) + (F0.Lq[2][lane] + F0.Lq[3][lane]);
+        }
+        if (has1) {
+          mg1 = F1.m[lane];
+          Lg1 = (F1.Lq[0][lane] + F1.Lq[1][lane]) + (F1.Lq[2][lane] + F1.Lq[3][lane]);
+        }
+      }
+      // with that read, fin[q] and ihand[q] are free for the item IS later:
+      // the softmax warps need not wait for this item's rows
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.c_free[q]);
       // O of each group: p_hi products + p_lo products of every column
       float x0[CN], x1[CN];
 #pragma unroll
@@ -1626,68 +1649,64 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       if (!ok) break;
       {
         T* out = static_cast<T*>(p.out);
-        // Per column, the groups' exact log-sum-exp merge -- M = max(m0, m1),
-        // f_g = 2^(m_g - M), L = f0 L0 + f1 L1 -- and where its row goes are the
-        // same for every thread: lane n works them out for column n into this
-        // warp's table, and every thread reads them back, one vector load per
-        // column.  A row written directly takes O / L as O0 (f0 / L) + O1 (f1 / L).
-        auto& tab = sh.colout[quarter];
+        // Where the item's rows go is the same for all its columns: straight to
+        // the output when this item is their only partition (for a shared
+        // prefix: a sequence with no prefix and one partition -- a prefix item
+        // never), else to the workspace's partial results.  Column n is head
+        // kvh * G + n % G of sequence seq0 + n / G.
+        const bool direct = SP ? (sp_eff[mt.seq0] == 0 && sp_tot[mt.seq0] == 1) : mt.n_parts == 1;
+        const int64_t hbase = (int64_t)mt.seq0 * p.num_q_heads + mt.kvh * G;
         const int nc = SP ? mt.ncol : CN;   // the item's columns that have a row
+        // Per column, the groups' exact log-sum-exp merge -- M = max(m0, m1),
+        // f_g = 2^(m_g - M), L = f0 L0 + f1 L1 -- is the same for every thread:
+        // lane n works it out for column n into this warp's table, as the
+        // factors of the groups' O (f_g, or f_g / L for a row written directly),
+        // and every thread reads them back.
+        float2* tab = sh.colout[quarter];
         if (lane < CN) {
           const int n = lane;
-          const typename Shared<NS, I8, NRH>::Final& F0 = sh.fin[q][0];
-          const typename Shared<NS, I8, NRH>::Final& F1 = sh.fin[q][1];
-          const float mg0 = has0 ? F0.m[n] : -INFINITY, mg1 = has1 ? F1.m[n] : -INFINITY;
           const float M = fmaxf(mg0, mg1);
           const float cf0 = (mg0 == -INFINITY) ? 0.f : exp2f(mg0 - M);
           const float cf1 = (mg1 == -INFINITY) ? 0.f : exp2f(mg1 - M);
-          const float Lg0 = has0 ? (F0.Lq[0][n] + F0.Lq[1][n]) + (F0.Lq[2][n] + F0.Lq[3][n]) : 0.f;
-          const float Lg1 = has1 ? (F1.Lq[0][n] + F1.Lq[1][n]) + (F1.Lq[2][n] + F1.Lq[3][n]) : 0.f;
           const float cL = PP ? fmaf(Lg0, cf0, Lg1 * cf1) : Lg0;
-          long long cdst = -1;
-          float g0 = cf0, g1 = cf1;
-          if (n < nc) {
-            // column n: head kvh * G + n % G of sequence seq0 + n / G.  A row is
-            // written directly when this item is its only partition (and, for a
-            // shared prefix, the sequence has none: prefix rows always merge)
-            const int sq = mt.seq0 + n / G;
-            const int64_t hrow = (int64_t)sq * p.num_q_heads + mt.kvh * G + n % G;
-            const bool direct = SP ? (sp_eff[sq] == 0 && sp_tot[sq] == 1) : mt.n_parts == 1;
-            if (direct) {
-              cdst = hrow * kD + (mt.bad ? 3 : 1);   // bit 1: a zero row (the item read block 0 for a bad id)
-              const float inv = 1.f / cL;              // L >= 1: the maximum's own weight is 1
-              g0 = cf0 * inv;
-              g1 = cf1 * inv;
-            } else {
-              const int64_t r = hrow * p.max_parts + mt.pbase + mt.part;
-              cdst = mt.bad ? -1 : r * kD;
-              if (quarter == 0) {
-                p.ws_ml[r * 2 + 0] = mt.bad ? 0.f : M;
-                p.ws_ml[r * 2 + 1] = mt.bad ? -1.f : cL;   // an invalid partition: the merge writes zeros
-              }
+          if (direct) {
+            const float inv = 1.f / cL;   // L >= 1: the maximum's own weight is 1
+            tab[n] = make_float2(cf0 * inv, cf1 * inv);
+          } else {
+            tab[n] = make_float2(cf0, cf1);
+            if (quarter == 0 && n < nc) {
+              const int64_t r = (hbase + (n / G) * p.num_q_heads + n % G) * p.max_parts + mt.pbase + mt.part;
+              p.ws_ml[r * 2 + 0] = mt.bad ? 0.f : M;
+              p.ws_ml[r * 2 + 1] = mt.bad ? -1.f : cL;   // an invalid partition: the merge writes zeros
             }
           }
-          tab[n].dst = cdst;
-          tab[n].g0 = g0;
-          tab[n].g1 = g1;
         }
         __syncwarp();
+        // the rows: a bad item (it read block 0 for an id out of range) writes
+        // zero rows directly and nothing to the workspace
+        if (direct) {
 #pragma unroll
-        for (int n = 0; n < CN; ++n) {
-          if (n < nc) {   // the same in every lane
-            const typename Shared<NS, I8, NRH>::ColOut c = tab[n];
-            if (c.dst >= 0) {
-              const float O = PP ? fmaf(x0[n], c.g0, x1[n] * c.g1) : x0[n] * c.g0;
-              if (c.dst & 1) out[(c.dst & ~3LL) + row] = Elem<T>::from_float((c.dst & 2) ? 0.f : O);
-              else p.ws_o[c.dst + row] = O;
+          for (int n = 0; n < CN; ++n) {
+            if (n < nc) {   // the same in every lane
+              const float2 g = tab[n];
+              const float O = PP ? fmaf(x0[n], g.x, x1[n] * g.y) : x0[n] * g.x;
+              const int64_t hrow = hbase + (n / G) * p.num_q_heads + n % G;
+              out[hrow * kD + row] = Elem<T>::from_float(mt.bad ? 0.f : O);
+            }
+          }
+        } else if (!mt.bad) {
+#pragma unroll
+          for (int n = 0; n < CN; ++n) {
+            if (n < nc) {
+              const float2 g = tab[n];
+              const float O = PP ? fmaf(x0[n], g.x, x1[n] * g.y) : x0[n] * g.x;
+              const int64_t r = (hbase + (n / G) * p.num_q_heads + n % G) * p.max_parts + mt.pbase + mt.part;
+              p.ws_o[r * kD + row] = O;
             }
           }
         }
         __syncwarp();   // every lane has read the table before the next item rewrites it
       }
-      // fin[q] and ihand[q] are free for the item after the next
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.c_free[q]);
     }
     if (!ok && lane == 0) {
       report(p.dev_err, PA_DEVERR_TIMEOUT);

@@ -425,7 +425,7 @@ def run_gpu(args):
         for _ in range(args.warmup):
             step()
     torch.cuda.synchronize()
-    assert _lib.read_device_errors(step.dev_err, stream=stream) == 0, "device error during warm-up"
+    check_device_errors(_lib, step, stream, "warm-up")
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
@@ -453,7 +453,7 @@ def run_gpu(args):
     total_ms = ev[0][0].elapsed_time(ev[K - 1][3])
     decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     total_ms = reduce_max(total_ms, world, device)
-    assert _lib.read_device_errors(step.dev_err, stream=stream) == 0, "device error during timed steps"
+    check_device_errors(_lib, step, stream, "the soak and timed steps")
 
     # ---- end to end through the C ABI with host buffers
     names = ("q", "key", "value", "block_tables", "context_lens", "slot_mapping")
@@ -544,6 +544,16 @@ def run_gpu(args):
     return 0
 
 
+def check_device_errors(_lib, step, stream, where: str) -> None:
+    """Fail with the error word's bits (PA_DEVERR_*) if a kernel reported one."""
+    bits = _lib.read_device_errors(step.dev_err, stream=stream)
+    if bits:
+        names = [n for n, b in (("context", _lib.DEVERR_CONTEXT), ("block id", _lib.DEVERR_BLOCK_ID),
+                                ("slot", _lib.DEVERR_SLOT), ("timeout", _lib.DEVERR_TIMEOUT),
+                                ("prefix", _lib.DEVERR_PREFIX)) if bits & b]
+        raise AssertionError(f"device error bits {bits:#x} ({', '.join(names) or 'unknown'}) during {where}")
+
+
 def soak(step, stream, seconds: float) -> int:
     """Run the step back to back for about `seconds` (untimed); returns the count."""
     if seconds <= 0:
@@ -596,7 +606,7 @@ def measure_workload(name: str, args, device, stream, peak: float, rank: int) ->
         return [e[1].elapsed_time(e[2]) for e in ev], [e[0].elapsed_time(e[2]) for e in ev]
 
     dec, tot = timed()
-    assert _lib.read_device_errors(step.dev_err, stream=stream) == 0, f"device error in {name}"
+    check_device_errors(_lib, step, stream, name)
     dec_ms, step_ms = float(np.mean(dec)), float(np.mean(tot))
     uniq = nb["decode_unique"] / (dec_ms * 1e-3) / 1e9
     part = step.partition()
@@ -685,7 +695,7 @@ def run_gpu_prefill(args):
         for _ in range(args.warmup):
             step()
     torch.cuda.synchronize()
-    assert _lib.read_device_errors(step.dev_err, stream=stream) == 0, "device error during warm-up"
+    check_device_errors(_lib, step, stream, "warm-up")
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     barrier(world)
@@ -704,7 +714,7 @@ def run_gpu_prefill(args):
         barrier(world)
     total_ms = reduce_max(ev[0][0].elapsed_time(ev[K - 1][2]), world, device)
     attn_ms = float(np.mean([ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]))
-    assert _lib.read_device_errors(step.dev_err, stream=stream) == 0, "device error during timed steps"
+    check_device_errors(_lib, step, stream, "the soak and timed steps")
 
     # end to end with host buffers: inputs in, output back, every step
     names = ("q", "key", "value", "block_tables", "context_lens", "query_start_loc", "slot_mapping")

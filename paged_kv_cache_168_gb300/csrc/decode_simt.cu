@@ -380,9 +380,6 @@ constexpr int kMergeRegs = 8;   // rows with up to this many partitions merge fr
 
 template <typename T, int D, bool SP, int GB>
 __global__ void __launch_bounds__(D * GB) merge_partitions_kernel(const __grid_constant__ DecodeParams p) {
-  // launched as a programmatic dependent of the decode kernel: wait for that
-  // kernel to complete (and its writes to be visible) before reading its results
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int s = blockIdx.y, d = threadIdx.x % D, sub = threadIdx.x / D;
   const int h = blockIdx.x * GB + sub;             // this thread's query head
   T* out_s = static_cast<T*>(p.out) + (int64_t)s * p.num_q_heads * D;
@@ -467,24 +464,6 @@ __global__ void __launch_bounds__(D * GB) merge_partitions_kernel(const __grid_c
   out_s[h * D + d] = Elem<T>::from_float(res);
 }
 
-// A launch that may begin while the kernel before it on the stream finishes
-// (programmatic stream serialization): its CTAs can be scheduled on SMs the
-// decode kernel has left, and wait in griddepcontrol.wait for its completion.
-template <typename Kern>
-static cudaError_t launch_dependent(Kern kern, dim3 grid, unsigned threads, cudaStream_t stream, const DecodeParams& p) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
-}
-
 // Launches the merge over every sequence, GB query heads of one kv head per
 // CTA: the most (up to 4) that still leave two CTAs per SM of a 152-SM GPU.
 template <typename T, int D, bool SP>
@@ -494,9 +473,10 @@ static cudaError_t launch_merge_typed(const DecodeParams& p, cudaStream_t stream
   int gb = 1;
   while (gb < 4 && G % (2 * gb) == 0 && rows / (2 * gb) >= 2 * 152) gb *= 2;
   const dim3 grid((unsigned)(p.num_q_heads / gb), (unsigned)p.num_seqs);
-  if (gb == 1) return launch_dependent(merge_partitions_kernel<T, D, SP, 1>, grid, D, stream, p);
-  if (gb == 2) return launch_dependent(merge_partitions_kernel<T, D, SP, 2>, grid, 2 * D, stream, p);
-  return launch_dependent(merge_partitions_kernel<T, D, SP, 4>, grid, 4 * D, stream, p);
+  if (gb == 1) merge_partitions_kernel<T, D, SP, 1><<<grid, D, 0, stream>>>(p);
+  else if (gb == 2) merge_partitions_kernel<T, D, SP, 2><<<grid, 2 * D, 0, stream>>>(p);
+  else merge_partitions_kernel<T, D, SP, 4><<<grid, 4 * D, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 template <typename T, int D, int G>

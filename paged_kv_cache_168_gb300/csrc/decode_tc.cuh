@@ -569,9 +569,6 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sh.tmem_base;
-  // the merge launched after this kernel may be scheduled on SMs this grid has
-  // left (it waits for the grid's completion before it reads anything)
-  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
 
   if (kSplitPlan && warp == 0) {
     // =================================================================== streamer (16-bit caches)

@@ -90,7 +90,8 @@ def measured_tensor_peak():
 
 
 # the sources the decode launch (tensor-core decode + log-sum-exp merge) is built from
-DECODE_SOURCES = ("common.cuh", "tc_common.cuh", "kernels.h", "decode_tc.cuh", "decode_tc.cu", "decode_simt.cu")
+DECODE_SOURCES = ("common.cuh", "tc_common.cuh", "kernels.h", "decode_tc.cuh", "decode_tc.cu", "decode_tc_prefix.cu",
+                  "decode_simt.cu")
 
 
 def source_digest() -> str:
@@ -616,7 +617,8 @@ def measure_workload(name: str, args, device, stream, peak: float, rank: int) ->
          "decode_kv_gbs": round(nb["decode_kv"] / (dec_ms * 1e-3) / 1e9, 2),
          "decode_unique_kv_gbs": round(nb["decode_kv_unique"] / (dec_ms * 1e-3) / 1e9, 2),
          "roofline": {"bound": "hbm", "achieved": round(uniq, 2), "peak": peak, "unit": "GB/s",
-                      "frac": round(uniq / peak, 4), "bytes": "algorithmic decode bytes, shared blocks once"},
+                      "frac": round(uniq / peak, 4), "bytes": "algorithmic decode bytes, shared blocks once",
+                      "traffic": recorded_traffic(name, part)},
          "frac_of_spec_8tbs": round(nb["decode_kv_unique"] / (dec_ms * 1e-3) / 1e9 / SPEC_HBM_GBS, 4),
          "seq_steps_per_s": round(cfg.num_seqs / (step_ms * 1e-3), 1),
          "step_ms": round(step_ms, 4), "step_gbs": round(nb["total"] / (step_ms * 1e-3) / 1e9, 2),

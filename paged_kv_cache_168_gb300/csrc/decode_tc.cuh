@@ -1497,7 +1497,8 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       }
       // 8-bit: P^T buffer hb was last read by PV(t - 2): wait for it to complete.
       // (16-bit caches write P^T into this tile's own stage, over K atoms that
-      // QK(t) has finished reading; the stage is refilled only after PV(t).)
+      // QK(t) has finished reading; the stage is refilled only after PV(t); they
+      // wait for PV(t - 2) only before completing p_full, below.)
       if (I8 && tile_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.pv_done[hb], ((tile_seq - 2) >> 1) & 1))) {
         ok = false;
         break;
@@ -1520,6 +1521,14 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
           *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(vrow + 1024 + c * 16) = make_uint4(0, 0, 0, 0);
         }
+      }
+      // p_full[hb] may complete tile t's phase only once the PV issuer has
+      // taken tile t - 2's: it tells the phases apart by parity, and while
+      // PV(t - 2) waits for its O slot this group could otherwise finish tile t
+      // and make that phase look pending again.  (8-bit caches waited above.)
+      if (!I8 && tile_seq >= 2 && !__all_sync(kFull, mbar_wait(&sh.pv_done[hb], ((tile_seq - 2) >> 1) & 1))) {
+        ok = false;
+        break;
       }
       tc::fence_proxy_async_smem();
       __syncwarp();

@@ -1226,7 +1226,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
       // caches), at g * 2 KiB in a V-only stage (8-bit caches)
       constexpr uint32_t kVGroup = I8 ? 2048 : kGroupBytes, kVOff = I8 ? 0 : 2048;
       constexpr bool PP = ping_pong(I8, CN);
-      // PV(pv) accumulates into the O slot of (its item's parity, its softmax
+      // PV(pv) accumulates into the O slot of (its item's slot, its softmax
       // group): a group's first tile of an item overwrites the slot once the
       // output warps have read the slot's previous item; its last tile
       // signals the output warps
@@ -1895,7 +1895,7 @@ __global__ void __launch_bounds__(threads_of(I8, SP ? kN : G), 1) decode_tc_kern
   }
 }
 
-// Dynamic shared memory of one CTA: stages, Q and P^T buffers, 8-bit raw rings,
+// Dynamic shared memory of one CTA: stages, Q slots, P^T buffers (8-bit), 8-bit raw rings,
 // the item tables (1024 bytes of slack align the stages to 1024).
 __host__ __device__ inline size_t decode_tc_smem(int NS, bool I8, int NRH, bool SP, int S) {
   return 1024 + (size_t)NS * stage_bytes(I8) + (size_t)q_slots(I8) * kQBytes + (size_t)p_buffers(I8) * kPBytes +

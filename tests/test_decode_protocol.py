@@ -10,11 +10,13 @@ keeps each barrier's completed-phase count, fails the moment a role tests a
 barrier that is two or more phases past the one it waits for, and fails on a
 deadlock.  Tensor-core completions (commits) arrive in issue order at random
 times, bulk copies land in any order.  Each role takes the same steps, in the
-same order, as its code in decode_tc.cuh; the softmax warpgroups and the four
-output warps are one actor each (their own barriers between warps are not
-modelled), and the end-of-work marks are left out: the model runs a fixed list
-of items.  One test plants the mistake that once went into the kernel (no wait
-for PV(t - 2) before completing p_full) and checks that the model catches it."""
+same order, as its code in decode_tc.cuh, the end-of-work marks included
+(the planner's last record, the streamer's last stage, the QK issuer's two
+metadata buffers, the softmax group whose turn the end tile is, the output
+warps' last hand-off slot); the softmax warpgroups and the four output warps
+are one actor each (their own barriers between warps are not modelled).  One
+test plants the mistake that once went into the kernel (no wait for PV(t - 2)
+before completing p_full) and checks that the model catches it."""
 import random
 
 import pytest
@@ -77,6 +79,7 @@ class Model:
         self.copies = []       # landing copies: stage barriers
         self.progress = 0
         self.out_items = 0
+        self.end_tile = None   # set by the QK issuer when it meets the end mark
 
     # -- asynchronous completions
     def commit(self, bars):
@@ -112,6 +115,11 @@ class Model:
                 yield from self.wait(self.rec_empty[k % 2], k // 2 - 1)
             self.rec_full[k % 2].arrive()
             self.progress += 1
+        n = len(self.items)                              # the record that says "no more work"
+        if n >= 2:
+            yield from self.wait(self.rec_empty[n % 2], n // 2 - 1)
+        self.rec_full[n % 2].arrive()
+        self.progress += 1
 
     def streamer(self):
         t = 0
@@ -125,10 +133,22 @@ class Model:
                 self.progress += 1
                 t += 1
                 yield
+        n = len(self.items)
+        yield from self.wait(self.rec_full[n % 2], n // 2)   # the planner's end record
+        # no more work: the next stage, once free, carries the end mark (after
+        # the streamer's own copies of the last stages have landed)
+        if t >= NS:
+            yield from self.wait(self.empty[t % NS], t // NS - 1)
+        for u in range(max(0, t - NS), t):
+            yield from self.wait(self.full[u % NS], u // NS)
+        self.full[t % NS].arrive()
+        self.progress += 1
 
     def qk_issuer(self):
-        for t in range(self.T):
+        for t in range(self.T + 1):
             yield from self.wait(self.full[t % NS], t // NS)
+            if t == self.T:   # the end mark
+                break
             if t >= 2:
                 yield from self.wait(self.s_free[t & 1], (t >> 1) - 1)
             self.m_full[t & 1].arrive()
@@ -136,11 +156,27 @@ class Model:
             self.commit([self.s_full[t & 1]] + ([self.q_free[k % QS]] if tail == 0 else []))
             self.progress += 1
             yield
+        T = self.T
+        self.end_tile = T                                 # the PV issuer stops there
+        for u in range(max(0, T - 2), T):                 # both metadata buffers read
+            yield from self.wait(self.s_free[u & 1], u >> 1)
+        self.m_full[0].arrive()                           # end marks (valid = T, item = n)
+        self.m_full[1].arrive()
+        self.progress += 1
 
     def softmax(self, g):
-        for t in range(g, self.T, 2):
-            k, head, tail = self.tiles[t]
+        t = g
+        while True:
             yield from self.wait(self.m_full[g], t >> 1)
+            if t >= self.T:   # the end mark: the group whose turn tile T is tells the output warps
+                if t == self.T:
+                    k = len(self.items)
+                    if k >= IS:
+                        yield from self.wait(self.c_free[k % IS], k // IS - 1)
+                    self.c_full[k % IS].arrive(2)
+                    self.progress += 1
+                return
+            k, head, tail = self.tiles[t]
             yield from self.wait(self.s_full[g], t >> 1)
             self.s_free[g].arrive()
             first, fin = head < 2, tail < 2
@@ -156,6 +192,7 @@ class Model:
                     yield from self.wait(self.c_free[k % IS], k // IS - 1)
                 self.c_full[k % IS].arrive(2 if head == 0 and tail == 0 else 1)
                 self.progress += 1
+            t += 2
             yield
 
     def pv_issuer(self):
@@ -177,6 +214,9 @@ class Model:
                 uses[os] += 1
             self.progress += 1
             yield
+        while self.end_tile is None:   # polls P of tile T until the QK issuer sets the end
+            self.p_full[self.T & 1].test(self.T >> 1)
+            yield
 
     def output(self):
         reads = [0] * (2 * IS)
@@ -196,6 +236,8 @@ class Model:
             t0 += n
             self.out_items += 1
             self.progress += 1
+        n = len(self.items)
+        yield from self.wait(self.c_full[n % IS], n // IS)   # the end mark
 
     def run(self, max_steps=200000):
         roles = [self.planner(), self.streamer(), self.qk_issuer(), self.softmax(0), self.softmax(1),

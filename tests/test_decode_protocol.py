@@ -286,3 +286,223 @@ def test_the_model_catches_p_full_running_two_phases_ahead():
         except AssertionError:
             pass
     assert caught > 0
+
+
+# ---------------------------------------------------------------- 8-bit caches
+
+ND = 4       # tile descriptors in flight (planner -> copy warp)
+NRH = 2      # raw half-tile slots per half
+IS8 = 2      # items in flight between softmax and output warps
+QS8 = 2      # Q slots
+
+
+class Model8:
+    """The 8-bit cache's roles: the planner (items, Q, per-tile descriptors), the
+    copy warp (each tile's chunks into a slot of both halves' raw rings), the
+    converter warps of each half (raw -> operands, then the stage's `full`), the
+    event-driven MMA issuer (QK and PV from one lane), one softmax group, the
+    output warps."""
+
+    def __init__(self, items, rng, drain_before_end_mark=True):
+        self.rng = rng
+        self.items = items
+        self.tiles = []
+        for k, n in enumerate(items):
+            for j in range(n):
+                self.tiles.append((k, j, n - 1 - j, rng.random() < 0.7))   # (item, head, tail, half 1 has bytes)
+        self.T = len(self.tiles)
+        self.drain_first = drain_before_end_mark
+        b = Bar
+        self.desc_full = [b(f"desc_full[{i}]", 1) for i in range(ND)]
+        self.desc_empty = [b(f"desc_empty[{i}]", 1) for i in range(ND)]
+        self.raw_full = [b(f"raw_full[{i}]", 1) for i in range(2 * NRH)]
+        self.raw_empty = [b(f"raw_empty[{i}]", 1) for i in range(2 * NRH)]
+        self.full = [b(f"full[{i}]", 2) for i in range(NS)]          # both halves' converters
+        self.empty = [b(f"empty[{i}]", 1) for i in range(NS)]
+        self.s_full = [b(f"s_full[{i}]", 1) for i in range(2)]
+        self.s_free = [b(f"s_free[{i}]", 1) for i in range(2)]
+        self.p_full = [b(f"p_full[{i}]", 1) for i in range(2)]
+        self.pv_done = [b(f"pv_done[{i}]", 1) for i in range(2)]
+        self.q_free = [b(f"q_free[{i}]", 1) for i in range(QS8)]
+        self.c_full = [b(f"c_full[{i}]", 1) for i in range(IS8)]
+        self.c_free = [b(f"c_free[{i}]", 1) for i in range(IS8)]
+        self.ofin = [b(f"ofin[{i}]", 1) for i in range(IS8)]
+        self.ofree = [b(f"ofree[{i}]", 1) for i in range(IS8)]
+        self.tensor, self.copies = [], []
+        self.progress = 0
+        self.out_items = 0
+
+    commit = Model.commit
+    fire = Model.fire
+    wait = Model.wait
+
+    def planner(self):
+        tile = 0
+        for k, n in enumerate(self.items):
+            if k >= QS8:
+                yield from self.wait(self.q_free[k % QS8], k // QS8 - 1)
+            yield                                              # Q written
+            for _ in range(n):
+                if tile >= ND:
+                    yield from self.wait(self.desc_empty[tile % ND], tile // ND - 1)
+                self.desc_full[tile % ND].arrive()
+                self.progress += 1
+                tile += 1
+                yield
+        if tile >= ND:                                         # the end descriptor
+            yield from self.wait(self.desc_empty[tile % ND], tile // ND - 1)
+        self.desc_full[tile % ND].arrive()
+        self.progress += 1
+
+    def copy_warp(self):
+        for tile in range(self.T + 1):
+            yield from self.wait(self.desc_full[tile % ND], tile // ND)
+            r0, r1 = tile % NRH, NRH + tile % NRH
+            if tile >= NRH:
+                yield from self.wait(self.raw_empty[r0], tile // NRH - 1)
+                yield from self.wait(self.raw_empty[r1], tile // NRH - 1)
+            if tile == self.T:   # no more work: the mark into both halves, after the own copies landed
+                drain = [(h * NRH + t % NRH, t // NRH) for h in (0, 1) for t in range(max(0, tile - NRH), tile)]
+                if not self.drain_first:
+                    self.raw_full[r0].arrive()
+                    self.raw_full[r1].arrive()
+                for r, ph in drain:
+                    yield from self.wait(self.raw_full[r], ph)
+                if self.drain_first:
+                    self.raw_full[r0].arrive()
+                    self.raw_full[r1].arrive()
+                self.progress += 1
+                return
+            self.copies.append(self.raw_full[r0])               # half 0 always has bytes
+            if self.tiles[tile][3]:
+                self.copies.append(self.raw_full[r1])
+            else:
+                self.raw_full[r1].arrive()                       # expect_tx(0): the arrive completes it
+            self.desc_empty[tile % ND].arrive()
+            self.progress += 1
+            yield
+
+    def converter(self, h):
+        for t in range(self.T + 1):
+            r = h * NRH + t % NRH
+            yield from self.wait(self.raw_full[r], t // NRH)
+            if t >= NS:
+                yield from self.wait(self.empty[t % NS], t // NS - 1)
+            yield                                              # K into TMEM, V into the stage
+            self.raw_empty[r].arrive()
+            self.full[t % NS].arrive()
+            self.progress += 1
+            if t == self.T:
+                return
+
+    def mma_issuer(self):
+        qk = pv = 0
+        end = None
+        used = [False] * IS8
+        uses = [0] * IS8
+        while end is None or pv < end:
+            if end is None and self.full[qk % NS].test(qk // NS):
+                if qk == self.T:
+                    end = qk
+                elif qk < 2 or self.s_free[qk & 1].test((qk >> 1) - 1):
+                    k, head, tail, _ = self.tiles[qk]
+                    self.commit([self.s_full[qk & 1]] + ([self.q_free[k % QS8]] if tail == 0 else []))
+                    qk += 1
+                    self.progress += 1
+            if pv < qk and self.p_full[pv & 1].test(pv >> 1):
+                k, head, tail, _ = self.tiles[pv]
+                os = k % IS8
+                first = head == 0
+                if not first or not used[os] or self.ofree[os].test(uses[os] - 1):
+                    self.commit([self.pv_done[pv & 1], self.empty[pv % NS]] + ([self.ofin[os]] if tail == 0 else []))
+                    if first:
+                        used[os] = True
+                        uses[os] += 1
+                    pv += 1
+                    self.progress += 1
+            yield
+
+    def softmax(self):
+        for t in range(self.T + 1):
+            yield from self.wait(self.full[t % NS], t // NS)
+            if t == self.T:   # the end mark
+                n = len(self.items)
+                if n >= IS8:
+                    yield from self.wait(self.c_free[n % IS8], n // IS8 - 1)
+                self.c_full[n % IS8].arrive()
+                self.progress += 1
+                return
+            k, head, tail, _ = self.tiles[t]
+            yield from self.wait(self.s_full[t & 1], t >> 1)
+            self.s_free[t & 1].arrive()
+            if head > 0 and self.rng.random() < 0.3:            # the running maximum rose: rescale O
+                yield from self.wait(self.pv_done[(t - 1) & 1], (t - 1) >> 1)
+            if t >= 2:                                         # the P^T buffer, last read by PV(t - 2)
+                yield from self.wait(self.pv_done[t & 1], (t - 2) >> 1)
+            yield                                              # P^T written
+            self.p_full[t & 1].arrive()
+            self.progress += 1
+            if tail == 0:
+                if k >= IS8:
+                    yield from self.wait(self.c_free[k % IS8], k // IS8 - 1)
+                self.c_full[k % IS8].arrive()
+                self.progress += 1
+            yield
+
+    def output(self):
+        for k in range(len(self.items)):
+            q = k % IS8
+            yield from self.wait(self.c_full[q], k // IS8)
+            self.c_free[q].arrive()
+            yield from self.wait(self.ofin[q], k // IS8)
+            self.ofree[q].arrive()
+            for _ in range(self.rng.randrange(4)):
+                yield
+            self.out_items += 1
+            self.progress += 1
+        n = len(self.items)
+        yield from self.wait(self.c_full[n % IS8], n // IS8)
+
+    def run(self, max_steps=200000):
+        roles = [self.planner(), self.copy_warp(), self.converter(0), self.converter(1), self.mma_issuer(),
+                 self.softmax(), self.output()]
+        live = list(roles)
+        idle = 0
+        for _ in range(max_steps):
+            if not live and not self.tensor and not self.copies:
+                break
+            before = self.progress
+            if (self.tensor or self.copies) and self.rng.random() < 0.3:
+                self.fire()
+            elif live:
+                r = self.rng.choice(live)
+                try:
+                    next(r)
+                except StopIteration:
+                    live.remove(r)
+            idle = 0 if self.progress != before else idle + 1
+            if idle > 20000:
+                raise AssertionError("deadlock: no role can move")
+        assert self.out_items == len(self.items), "not every item reached the output warps"
+
+
+def test_8bit_hand_offs_never_alias_a_phase_and_never_deadlock():
+    rng = random.Random(2027)
+    for _ in range(400):
+        Model8(random_items(rng, rng.randrange(1, 40)), rng).run()
+
+
+def test_the_model_catches_the_copy_warp_draining_after_its_end_mark():
+    """The copy warp once drained its copies after posting its end mark into the
+    raw slots; the drain's wait on a slot then named the mark's phase by the
+    same parity.  The model must see that alias."""
+    rng = random.Random(8)
+    caught = 0
+    for _ in range(200):
+        try:
+            Model8(random_items(rng, rng.randrange(1, 40)), rng, drain_before_end_mark=False).run()
+        except Alias:
+            caught += 1
+        except AssertionError:
+            pass
+    assert caught > 0

@@ -1,6 +1,6 @@
 """Host-side logic of bench.py without a GPU: clock-sample parsing, the traffic
-record, the oracle CPU baseline on the tiny workload, and the cross-rank
-aggregation with two gloo ranks."""
+record, the device-error report, the oracle CPU baseline on the tiny workload,
+and the cross-rank aggregation with two gloo ranks."""
 import os
 import socket
 
@@ -41,6 +41,24 @@ def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "source_digest", lambda: "changed")
     assert bench.recorded_traffic("7b", 4096) is None
     assert bench.recorded_traffic("8b", 4096) is None
+
+
+def test_device_errors_are_named_with_their_bits():
+    class FakeLib:
+        DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_CONTEXT, DEVERR_TIMEOUT, DEVERR_PREFIX = 1, 2, 4, 8, 16
+
+        def __init__(self, bits):
+            self.bits = bits
+
+        def read_device_errors(self, dev_err, stream=None):
+            return self.bits
+
+    class Step:
+        dev_err = None
+
+    bench.check_device_errors(FakeLib(0), Step(), None, "warm-up")   # a clear word passes
+    with pytest.raises(AssertionError, match=r"0x9 \(block id, timeout\) during the timed steps"):
+        bench.check_device_errors(FakeLib(9), Step(), None, "the timed steps")
 
 
 def test_host_inputs_pack_every_input_into_one_buffer(monkeypatch):

@@ -1,5 +1,5 @@
-"""A model of the tensor-core decode kernel's hand-offs (16-bit caches), run on
-the CPU under random schedules.
+"""Models of the tensor-core kernels' hand-offs (decode with 16-bit and 8-bit
+caches, prefill), run on the CPU under random schedules.
 
 The kernel's roles -- planner, streaming warp, QK issuer, two softmax groups,
 PV issuer, output warps -- pass work through mbarriers.  A waiter names the
@@ -501,6 +501,117 @@ def test_the_model_catches_the_copy_warp_draining_after_its_end_mark():
     for _ in range(200):
         try:
             Model8(random_items(rng, rng.randrange(1, 40)), rng, drain_before_end_mark=False).run()
+        except Alias:
+            caught += 1
+        except AssertionError:
+            pass
+    assert caught > 0
+
+
+# ---------------------------------------------------------------- prefill
+
+class ModelPrefill:
+    """The prefill kernel's roles for one query tile: the producer (KV tiles into
+    two stages), the event-driven MMA issuer (QK(j) only once PV(j - 2) has been
+    issued: S(j) lands in the TMEM columns that held P(j - 2); with two stages the
+    refill of tile j's stage already waits for PV(j - 2), so this is belt and
+    braces), the softmax warps (one actor)."""
+
+    def __init__(self, n_kv, rng, producer_waits_empty=True):
+        self.rng, self.n = rng, n_kv
+        self.wait_empty = producer_waits_empty
+        b = Bar
+        self.full = [b(f"full[{i}]", 1) for i in range(2)]
+        self.empty = [b(f"empty[{i}]", 1) for i in range(2)]
+        self.s_full = [b(f"s_full[{i}]", 1) for i in range(2)]
+        self.s_free = [b(f"s_free[{i}]", 1) for i in range(2)]
+        self.p_full = [b(f"p_full[{i}]", 1) for i in range(2)]
+        self.pv_done = [b(f"pv_done[{i}]", 1) for i in range(2)]
+        self.tensor, self.copies = [], []
+        self.progress = 0
+        self.done = False
+        self.partial = [rng.random() < 0.5 for _ in range(n_kv)]   # a tile with a ragged end
+
+    commit = Model.commit
+    fire = Model.fire
+    wait = Model.wait
+
+    def producer(self):
+        for j in range(self.n):
+            if j >= 2 and self.wait_empty:
+                yield from self.wait(self.empty[j & 1], (j >> 1) - 1)
+            self.copies.append(self.full[j & 1])
+            self.progress += 1
+            yield
+        for j in range(max(0, self.n - 2), self.n):   # its own copies landed before the CTA ends
+            yield from self.wait(self.full[j & 1], j >> 1)
+
+    def mma_issuer(self):
+        qk = pv = 0
+        while pv < self.n:
+            if qk < self.n and pv >= qk - 1:
+                if self.full[qk & 1].test(qk >> 1) and (qk < 2 or self.s_free[qk & 1].test((qk >> 1) - 1)):
+                    self.commit([self.s_full[qk & 1]])
+                    qk += 1
+                    self.progress += 1
+            if pv < qk and self.p_full[pv & 1].test(pv >> 1):
+                self.commit([self.pv_done[pv & 1], self.empty[pv & 1]])
+                pv += 1
+                self.progress += 1
+            yield
+
+    def softmax(self):
+        for j in range(self.n):
+            yield from self.wait(self.s_full[j & 1], j >> 1)
+            self.s_free[j & 1].arrive()
+            if j >= 1 and self.rng.random() < 0.3:           # the row maximum rose: rescale O
+                yield from self.wait(self.pv_done[(j - 1) & 1], (j - 1) >> 1)
+            yield                                            # P into TMEM
+            if self.partial[j]:                              # zero V rows past the tile's end
+                yield from self.wait(self.full[j & 1], j >> 1)
+            self.p_full[j & 1].arrive()
+            self.progress += 1
+            yield
+        if self.n:
+            yield from self.wait(self.pv_done[(self.n - 1) & 1], (self.n - 1) >> 1)
+        self.done = True
+        self.progress += 1
+
+    def run(self, max_steps=100000):
+        live = [self.producer(), self.mma_issuer(), self.softmax()]
+        idle = 0
+        for _ in range(max_steps):
+            if not live and not self.tensor and not self.copies:
+                break
+            before = self.progress
+            if (self.tensor or self.copies) and self.rng.random() < 0.3:
+                self.fire()
+            elif live:
+                r = self.rng.choice(live)
+                try:
+                    next(r)
+                except StopIteration:
+                    live.remove(r)
+            idle = 0 if self.progress != before else idle + 1
+            if idle > 20000:
+                raise AssertionError("deadlock: no role can move")
+        assert self.done
+
+
+def test_prefill_hand_offs_never_alias_a_phase_and_never_deadlock():
+    rng = random.Random(2028)
+    for _ in range(600):
+        ModelPrefill(rng.randrange(0, 40), rng).run()
+
+
+def test_the_model_catches_a_stage_refilled_before_its_pv_in_prefill():
+    """A producer that refills a stage without waiting for the PV that last read
+    it lets the stage's `full` run two phases ahead of the MMA issuer."""
+    rng = random.Random(9)
+    caught = 0
+    for _ in range(400):
+        try:
+            ModelPrefill(rng.randrange(4, 40), rng, producer_waits_empty=False).run()
         except Alias:
             caught += 1
         except AssertionError:
